@@ -1,0 +1,110 @@
+"""Pins for the oracle's whole decode pass.
+
+* Against an independent float64 GPT-2 forward assembled from torch library
+  routines (layer_norm, scaled_dot_product_attention with a causal mask, tanh
+  gelu, matmul) on the checkpoint-layout weights.  A transposed operand, a
+  swapped gamma/beta, a wrong q/k/v split or head order, a wrong attention
+  scale or a missing residual all fail it.
+* KV-cached decode equals whole-sequence recompute with a causal mask.
+* Position handling: append-only, rewind, bad inputs.
+"""
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import oracle as orc
+from transformer_decode_token_gb300 import synth
+
+
+def torch_gpt2_logits(cfg, w, tokens):
+    """Float64 GPT-2 forward over a whole sequence, from library routines."""
+    d = lambda a: torch.from_numpy(np.asarray(a, np.float32)).double()
+    E, H, D = cfg.n_embd, cfg.n_head, cfg.head_dim
+    t = torch.as_tensor(np.asarray(tokens, np.int64))
+    n = t.numel()
+    x = d(w["wte"])[t] + d(w["wpe"])[:n]
+    for L in w["layers"]:
+        h = F.layer_norm(x, (E,), d(L["ln1_w"]), d(L["ln1_b"]), eps=cfg.ln_eps)
+        qkv = h @ d(L["attn_w"]) + d(L["attn_b"])
+        q, k, v = qkv.split(E, dim=-1)
+        q, k, v = (a.reshape(n, H, D).transpose(0, 1) for a in (q, k, v))
+        a = F.scaled_dot_product_attention(q, k, v, is_causal=True)
+        a = a.transpose(0, 1).reshape(n, E)
+        x = x + a @ d(L["proj_w"]) + d(L["proj_b"])
+        h = F.layer_norm(x, (E,), d(L["ln2_w"]), d(L["ln2_b"]), eps=cfg.ln_eps)
+        f = F.gelu(h @ d(L["fc_w"]) + d(L["fc_b"]), approximate="tanh")
+        x = x + f @ d(L["mlp_proj_w"]) + d(L["mlp_proj_b"])
+    x = F.layer_norm(x, (E,), d(w["ln_f_w"]), d(w["ln_f_b"]), eps=cfg.ln_eps)
+    return (x @ d(w["wte"]).T).numpy()
+
+
+# head_dim 32 (tiny) and head_dim 64 (the GPT-2 head, scale 1/8)
+CFG64 = synth.GPT2Config(n_layer=3, n_embd=256, n_head=4, n_positions=48, vocab_size=700)
+
+
+@pytest.mark.parametrize("cfg", [synth.TINY, CFG64], ids=["tiny", "d64"])
+def test_decode_matches_library_float64_forward(cfg):
+    w = synth.make_weights(cfg, seed=0)
+    toks = synth.make_prompt(cfg, 20, seed=1)
+    ref = torch_gpt2_logits(cfg, w, toks)
+    m = orc.OracleModel(cfg, w)
+    for pos, t in enumerate(toks):
+        logits, am = m.forward(int(t), pos)
+        assert np.abs(logits - ref[pos]).max() <= 2e-5
+        top2 = np.sort(ref[pos])[-2:]
+        if top2[1] - top2[0] > 1e-3:
+            assert am == int(np.argmax(ref[pos]))
+    m.close()
+
+
+def test_cached_decode_equals_full_recompute():
+    cfg = synth.TINY
+    w = synth.make_weights(cfg, seed=3)
+    toks = synth.make_prompt(cfg, 24, seed=4)
+    full = orc.forward_full(cfg, w, toks)
+    m = orc.OracleModel(cfg, w)
+    for pos, t in enumerate(toks):
+        logits, _ = m.forward(int(t), pos)
+        assert np.abs(logits - full[pos]).max() <= 1e-5
+    m.close()
+
+
+def test_full_recompute_matches_library():
+    cfg = CFG64
+    w = synth.make_weights(cfg, seed=5)
+    toks = synth.make_prompt(cfg, 16, seed=6)
+    assert np.abs(orc.forward_full(cfg, w, toks) - torch_gpt2_logits(cfg, w, toks)).max() <= 2e-5
+
+
+def test_rewind_and_bad_positions():
+    cfg = synth.TINY
+    w = synth.make_weights(cfg, seed=0)
+    m = orc.OracleModel(cfg, w)
+    a = [m.forward(t, p)[0] for p, t in enumerate([5, 6, 7, 8])]
+    # rewinding to position 2 and feeding the same token reproduces the row
+    again, _ = m.forward(7, 2)
+    assert np.array_equal(again, a[2])
+    with pytest.raises(ValueError):
+        m.forward(9, 4)          # only positions 0..3 are valid after the rewind
+    with pytest.raises(ValueError):
+        m.forward(cfg.vocab_size, 3)
+    with pytest.raises(ValueError):
+        m.forward(-1, 3)
+    m.reset()
+    with pytest.raises(ValueError):
+        m.forward(1, 1)
+    first, _ = m.forward(5, 0)
+    assert np.array_equal(first, a[0])
+    m.close()
+
+
+def test_greedy_teacher_forcing_consistent():
+    cfg = synth.TINY
+    w = synth.make_weights(cfg, seed=0)
+    p = synth.make_prompt(cfg, 4, seed=1)
+    ids, logits = orc.greedy(cfg, w, p, 16)
+    assert len(ids) == 17 and logits.shape == (20, cfg.vocab_size)
+    ids2, logits2 = orc.greedy(cfg, w, p, 16, teacher=ids[:16])
+    assert ids2 == ids and np.array_equal(logits, logits2)
+    assert ids[0] == int(np.argmax(logits[3]))
