@@ -1,0 +1,240 @@
+/*
+ * gpt2.h — C ABI of libgpt2.so: GPT-2 single-token (batch 1) decode on one
+ * GB300 (sm_103a).
+ *
+ * What it computes.  One forward pass per token, as the node list of the
+ * "model.fir" graph file (Resident GPT-2 decode) and the model.s description
+ * of the "gpt2.s" README ("Inner Workings") lay it out:
+ *   x = wte[token] + wpe[position]
+ *   for each of n_layer blocks:
+ *     qkv  = LayerNorm1(x) . W_attn + b_attn          (fused QKV linear)
+ *     attn = causal attention of q over the cached k, v of positions
+ *            0..position, after appending this token's k, v
+ *     x   += attn . W_proj + b_proj
+ *     x   += gelu_new(LayerNorm2(x) . W_fc + b_fc) . W_mlp_proj + b_mlp_proj
+ *   logits = wte . LayerNorm_f(x)                      (tied output head)
+ *   token' = argmax(logits)                            (greedy choice,
+ *            "Let's make GPT-2 in assembly", Step 7; exact ties -> lowest id)
+ *
+ * Conventions shared by every call.
+ *   - Every call returns an int status: GPT2_OK (0) or a negative GPT2_ERR_*
+ *     code; gpt2_strerror() names it.  No call throws, aborts or traps, and no
+ *     kernel traps: a device-side problem is recorded in a device error word
+ *     and returned by the next call that synchronises (gpt2_argmax,
+ *     gpt2_generate, gpt2_copy_logits, gpt2_sync).
+ *   - "stream" arguments are a cudaStream_t passed as void* (NULL = the legacy
+ *     default stream).  All of a model's work is ordered on its stream.
+ *   - Device pointers must come from the CUDA device that is current when the
+ *     call is made; host pointers may be pageable.
+ *   - A model is not thread-safe: serialise calls on one model.
+ */
+#ifndef GPT2_H
+#define GPT2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define GPT2_OK                      0
+#define GPT2_ERR_INVALID_ARG        -1  /* NULL pointer, bad enum, bad shape  */
+#define GPT2_ERR_UNSUPPORTED_DEVICE -2  /* current device is not cc 10.3      */
+#define GPT2_ERR_TOKEN_RANGE        -3  /* token outside [0, vocab_size)      */
+#define GPT2_ERR_POSITION_RANGE     -4  /* position >= n_positions, or past
+                                           the cached length (see decode_step) */
+#define GPT2_ERR_NOT_READY          -5  /* e.g. argmax before any step        */
+#define GPT2_ERR_CUDA               -6  /* a CUDA runtime call failed         */
+#define GPT2_ERR_TIMEOUT            -7  /* a bounded device wait gave up      */
+#define GPT2_ERR_DEVICE_STATE       -8  /* a kernel rejected its inputs       */
+#define GPT2_ERR_OUT_OF_MEMORY      -9  /* device allocation failed           */
+
+/* ---- configuration ------------------------------------------------------- */
+/* Model shape, as the graph file's config checks and symbols define it
+ * ("model.fir": sym hidden = n_embd, nheads = n_head, headdim = hidden/nheads,
+ * mlp = 4*hidden, positions = n_positions, vocab = vocab_size; epsilon
+ * layer_norm_epsilon).  Accepted: n_embd % 32 == 0, n_embd % n_head == 0,
+ * head_dim in {32, 64, 128}; GPT2_INT4 also needs n_embd % 128 == 0. */
+typedef struct gpt2_config {
+    int32_t n_layer;
+    int32_t n_embd;
+    int32_t n_head;
+    int32_t n_positions;
+    int32_t vocab_size;
+    float   ln_eps;            /* GPT-2 uses 1e-5 */
+} gpt2_config;
+
+/* How the 48 (4 * n_layer) block matrices are stored on the device.  The
+ * embeddings, biases, LayerNorm parameters, the tied head and the KV cache
+ * are fp32 in every mode ("gpt2.s" README, Options: -h; "model.fir" header:
+ * wte/lm_head stays tied fp32).
+ *   GPT2_F32 : fp32, transposed to [out][in].
+ *   GPT2_F16 : IEEE fp16 (round to nearest even), [out][in]; widened to fp32
+ *              inside the kernels, products and sums in fp32.
+ *   GPT2_INT4: grouped asymmetric int4 of the [out][in] matrix, groups of 32
+ *              consecutive inputs, fp32 scale s and 4-bit zero point z per
+ *              group, s = (max(0,max w) - min(0,min w)) / 15 (1 if that is 0),
+ *              z = clamp(rint(-min/s), 0, 15), q = clamp(rint(w/s) + z, 0, 15),
+ *              dequantised weight (q - z) * s.  Layout: codes [out][in/2]
+ *              (input 2k in the low nibble of byte k), scales [out][in/32] f32,
+ *              zeros [out][in/64] (group 2j in the low nibble of byte j). */
+typedef enum gpt2_wdtype {
+    GPT2_F32  = 0,
+    GPT2_F16  = 1,
+    GPT2_INT4 = 2
+} gpt2_wdtype;
+
+/* One block's tensors, DEVICE pointers to fp32, in the checkpoint's HF
+ * Conv1D layout (matrices [input][output], row-major): names and shapes as
+ * the graph file's weight lines give them. */
+typedef struct gpt2_layer_weights {
+    const float *ln1_w, *ln1_b;            /* [E]                  */
+    const float *attn_w, *attn_b;          /* [E][3E], [3E]        */
+    const float *proj_w, *proj_b;          /* [E][E],  [E]         */
+    const float *ln2_w, *ln2_b;            /* [E]                  */
+    const float *fc_w, *fc_b;              /* [E][4E], [4E]        */
+    const float *mlp_proj_w, *mlp_proj_b;  /* [4E][E], [E]         */
+} gpt2_layer_weights;
+
+/* All 4 + 12 * n_layer tensors (148 for GPT-2 small).  Tensor pointers are
+ * DEVICE pointers; `layers` itself is a HOST array of n_layer entries. */
+typedef struct gpt2_weights {
+    const float *wte;                      /* [V][E] token embedding = head */
+    const float *wpe;                      /* [P][E]                        */
+    const float *ln_f_w, *ln_f_b;          /* [E]                           */
+    const gpt2_layer_weights *layers;      /* host array, n_layer entries   */
+} gpt2_weights;
+
+typedef struct gpt2_model gpt2_model;
+
+/* ---- model lifecycle ------------------------------------------------------ */
+
+/* Validates cfg (the graph file's `require` checks: hidden = nheads*headdim,
+ * mlp = 4*hidden) and the device (compute capability 10.3), allocates every
+ * device buffer the model needs (weights in the chosen format, the fp32 KV
+ * cache [n_layer][n_head][n_positions][head_dim] — "stored by head", as the
+ * "gpt2.s" README's Inner Workings puts it — activations, logits), repacks
+ * the weights on the device (transpose to [out][in]; fp16 rounding; int4
+ * quantisation), and captures one decode pass into a CUDA graph.
+ * The caller keeps ownership of `w`'s tensors and may free them once this
+ * returns.  On success *out owns everything and must be released with
+ * gpt2_destroy.  Errors: INVALID_ARG, UNSUPPORTED_DEVICE, OUT_OF_MEMORY, CUDA. */
+int gpt2_create(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
+                void *stream, gpt2_model **out);
+
+/* Frees every device buffer and the graph.  NULL is accepted. */
+void gpt2_destroy(gpt2_model *m);
+
+/* Forget the cached tokens (cached length 0). */
+int gpt2_reset(gpt2_model *m);
+
+/* ---- decoding ------------------------------------------------------------ */
+
+/* One forward pass for `token` at `position` ("gpt2.s" README, Inner
+ * Workings: model.s, the forward pass for one token; the KV cache gains one
+ * row per token, "Let's make GPT-2 in assembly" Step 6).  `position` must be
+ * < n_positions and <= the cached length: equal appends; smaller rewinds the
+ * cache to `position` first.  On success the cached length is position + 1
+ * and, if dev_logits is not NULL, *dev_logits points at the model's device
+ * buffer of vocab_size fp32 logits, valid until the next decoding call.
+ * Asynchronous: returns once the work is queued on the model's stream.
+ * Errors: INVALID_ARG, TOKEN_RANGE, POSITION_RANGE, CUDA. */
+int gpt2_decode_step(gpt2_model *m, int32_t token, int32_t position,
+                     const float **dev_logits);
+
+/* Resets the cache, then runs decode steps for ids[0..n-1] at positions
+ * 0..n-1 (the prompt is consumed one token at a time, as in "gpt2.s").
+ * host_ids is a host array.  Afterwards the last step's logits and argmax are
+ * available.  Errors: as gpt2_decode_step; n must be in [1, n_positions]. */
+int gpt2_prefill(gpt2_model *m, const int32_t *host_ids, int32_t n);
+
+/* Greedy choice of the last step's logits: the highest logit, exact ties to
+ * the lowest id ("Let's make GPT-2 in assembly", Step 7).  Synchronises the
+ * model's stream and copies 4 bytes to the host.
+ * Errors: NOT_READY (no step yet), DEVICE_STATE / TIMEOUT (reported by a
+ * kernel), CUDA. */
+int gpt2_argmax(gpt2_model *m, int32_t *token_out);
+
+/* Device-resident greedy decoding: n_steps more decode passes, each fed the
+ * previous pass's argmax without a round trip to the host (token and
+ * position live in device memory).  Needs a previous step; the cached length
+ * grows by n_steps and must stay <= n_positions.  Asynchronous.
+ * Errors: NOT_READY, POSITION_RANGE, INVALID_ARG, CUDA. */
+int gpt2_decode_greedy(gpt2_model *m, int32_t n_steps);
+
+/* Whole greedy generation from host to host: prefill(host_prompt, n_prompt),
+ * then n_steps device-resident decode passes; host_out receives n_steps + 1
+ * ids: the argmax after the last prompt token, then the argmax after each
+ * decode pass (the pass i input is host_out[i]).  Synchronises.
+ * Errors: as prefill and decode_greedy; n_prompt + n_steps <= n_positions. */
+int gpt2_generate(gpt2_model *m, const int32_t *host_prompt, int32_t n_prompt,
+                  int32_t n_steps, int32_t *host_out);
+
+/* Copies the last step's vocab_size logits to dst (host or device memory)
+ * and synchronises.  Errors: NOT_READY, INVALID_ARG, CUDA, DEVICE_STATE. */
+int gpt2_copy_logits(gpt2_model *m, float *dst);
+
+/* Waits for the model's queued work; returns a recorded device error if any. */
+int gpt2_sync(gpt2_model *m);
+
+/* ---- inspection (for parity tests and tools) ---------------------------- */
+
+/* Selects one stored block matrix. */
+#define GPT2_MAT_ATTN      0   /* c_attn   [3E][E] after the transpose */
+#define GPT2_MAT_PROJ      1   /* c_proj   [E][E]                      */
+#define GPT2_MAT_FC        2   /* c_fc     [4E][E]                     */
+#define GPT2_MAT_MLP_PROJ  3   /* mlp proj [E][4E]                     */
+
+/* Byte sizes of a stored matrix's parts: main (fp32/fp16 values or int4
+ * codes), scales and zeros (0 unless GPT2_INT4).  Any out pointer may be NULL. */
+int gpt2_matrix_bytes(const gpt2_model *m, int32_t which, size_t *main_bytes,
+                      size_t *scale_bytes, size_t *zero_bytes);
+
+/* Copies a stored matrix's bytes, in the layout gpt2_wdtype describes, to
+ * host or device memory.  Any destination may be NULL to skip that part. */
+int gpt2_export_matrix(gpt2_model *m, int32_t layer, int32_t which,
+                       void *dst_main, void *dst_scales, void *dst_zeros);
+
+/* Writes the matrix as the kernels see it, widened to fp32 in [out][in]
+ * (fp16 widened, int4 dequantised as (q - z) * s), to DEVICE memory dst. */
+int gpt2_export_dequant(gpt2_model *m, int32_t layer, int32_t which, float *dst);
+
+/* Copies the cached K and V rows 0..n_rows-1 of one layer, laid out
+ * [n_head][n_rows][head_dim] fp32 each, to host or device memory. */
+int gpt2_export_kv(gpt2_model *m, int32_t layer, int32_t n_rows,
+                   float *dst_k, float *dst_v);
+
+/* Number of kernel launches one decode pass makes (for launch accounting). */
+int gpt2_kernels_per_step(const gpt2_model *m, int32_t *count);
+
+/* ---- stand-alone operations on caller buffers --------------------------- */
+
+/* Warp-per-row LayerNorm of `rows` rows of n fp32 values ("model.fir" kernel
+ * g2.layernorm: mean, biased variance, (x-mean)*rsqrt(var+eps)*gamma+beta).
+ * x, gamma, beta, y are DEVICE pointers; y may equal x.  n % 4 == 0. */
+int gpt2_op_layernorm(const float *x, const float *gamma, const float *beta,
+                      int32_t rows, int32_t n, float eps, float *y, void *stream);
+
+/* Final LayerNorm + tied head + greedy argmax on caller buffers (the
+ * graph file's final_norm and head nodes, then "Let's make GPT-2 in
+ * assembly" Step 7): logits[v] = sum_e wte[v][e] * LN(x)[e];
+ * *dev_token = argmax.  All pointers are DEVICE pointers; wte is [V][E] with
+ * E % 4 == 0.  The kernel combines per-block maxima in `workspace`, which must
+ * hold gpt2_op_head_argmax_workspace(V, E) bytes, be 16-byte aligned, and not
+ * be used by another call in flight.  The call zeroes what it needs.
+ * Asynchronous on `stream`.  Errors: INVALID_ARG, CUDA. */
+size_t gpt2_op_head_argmax_workspace(int32_t vocab, int32_t n_embd);
+int gpt2_op_head_argmax(const float *x, const float *ln_w, const float *ln_b,
+                        float eps, const float *wte, int32_t vocab,
+                        int32_t n_embd, float *logits, int32_t *dev_token,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---- errors ------------------------------------------------------------- */
+const char *gpt2_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GPT2_H */

@@ -1,0 +1,278 @@
+"""Thin ctypes binding over libgpt2.so (C ABI: include/gpt2.h).
+
+Argument marshalling only: every step of the decode pass runs in the CUDA
+library.  PyTorch provides device memory and streams.  If the library cannot
+be built or loaded, every call raises: there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+from . import build as _build
+
+GPT2_F32, GPT2_F16, GPT2_INT4 = 0, 1, 2
+WDTYPES = {"f32": GPT2_F32, "f16": GPT2_F16, "int4": GPT2_INT4}
+MAT_ATTN, MAT_PROJ, MAT_FC, MAT_MLP_PROJ = 0, 1, 2, 3
+MATRIX_KEYS = ("attn_w", "proj_w", "fc_w", "mlp_proj_w")   # index = MAT_*
+
+STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED_DEVICE", -3: "TOKEN_RANGE",
+          -4: "POSITION_RANGE", -5: "NOT_READY", -6: "CUDA", -7: "TIMEOUT",
+          -8: "DEVICE_STATE", -9: "OUT_OF_MEMORY"}
+
+EXPORTED = ("gpt2_create", "gpt2_destroy", "gpt2_reset", "gpt2_decode_step", "gpt2_prefill",
+            "gpt2_argmax", "gpt2_decode_greedy", "gpt2_generate", "gpt2_copy_logits", "gpt2_sync",
+            "gpt2_matrix_bytes", "gpt2_export_matrix", "gpt2_export_dequant", "gpt2_export_kv",
+            "gpt2_kernels_per_step", "gpt2_op_layernorm", "gpt2_op_head_argmax_workspace",
+            "gpt2_op_head_argmax", "gpt2_strerror")
+
+
+class GPT2Error(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+        msg = lib().gpt2_strerror(status).decode() if _lib is not None else self.name
+        super().__init__(f"{what}: GPT2_ERR_{self.name} ({msg})" if what else msg)
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("n_layer", ctypes.c_int32), ("n_embd", ctypes.c_int32), ("n_head", ctypes.c_int32),
+                ("n_positions", ctypes.c_int32), ("vocab_size", ctypes.c_int32), ("ln_eps", ctypes.c_float)]
+
+
+_LAYER_KEYS = ("ln1_w", "ln1_b", "attn_w", "attn_b", "proj_w", "proj_b",
+               "ln2_w", "ln2_b", "fc_w", "fc_b", "mlp_proj_w", "mlp_proj_b")
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_void_p) for k in _LAYER_KEYS]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("wte", ctypes.c_void_p), ("wpe", ctypes.c_void_p), ("ln_f_w", ctypes.c_void_p),
+                ("ln_f_b", ctypes.c_void_p), ("layers", ctypes.POINTER(LayerWeights))]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib(build_if_stale: bool = True):
+    """Loads libgpt2.so (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if build_if_stale else _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(f"libgpt2.so not found at {path}")
+            L = ctypes.CDLL(path)
+            vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+            pi32 = ctypes.POINTER(ctypes.c_int32)
+            L.gpt2_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), i32, vp,
+                                      ctypes.POINTER(vp)]
+            L.gpt2_destroy.argtypes = [vp]
+            L.gpt2_destroy.restype = None
+            L.gpt2_reset.argtypes = [vp]
+            L.gpt2_decode_step.argtypes = [vp, i32, i32, ctypes.POINTER(vp)]
+            L.gpt2_prefill.argtypes = [vp, pi32, i32]
+            L.gpt2_argmax.argtypes = [vp, pi32]
+            L.gpt2_decode_greedy.argtypes = [vp, i32]
+            L.gpt2_generate.argtypes = [vp, pi32, i32, i32, pi32]
+            L.gpt2_copy_logits.argtypes = [vp, vp]
+            L.gpt2_sync.argtypes = [vp]
+            L.gpt2_matrix_bytes.argtypes = [vp, i32, ctypes.POINTER(sz), ctypes.POINTER(sz),
+                                            ctypes.POINTER(sz)]
+            L.gpt2_export_matrix.argtypes = [vp, i32, i32, vp, vp, vp]
+            L.gpt2_export_dequant.argtypes = [vp, i32, i32, vp]
+            L.gpt2_export_kv.argtypes = [vp, i32, i32, vp, vp]
+            L.gpt2_kernels_per_step.argtypes = [vp, pi32]
+            L.gpt2_op_layernorm.argtypes = [vp, vp, vp, i32, i32, f32, vp, vp]
+            L.gpt2_op_head_argmax_workspace.argtypes = [i32, i32]
+            L.gpt2_op_head_argmax_workspace.restype = sz
+            L.gpt2_op_head_argmax.argtypes = [vp, vp, vp, f32, vp, i32, i32, vp, vp, vp, sz, vp]
+            L.gpt2_strerror.argtypes = [ctypes.c_int]
+            L.gpt2_strerror.restype = ctypes.c_char_p
+            for n in EXPORTED:
+                if n not in ("gpt2_destroy", "gpt2_op_head_argmax_workspace", "gpt2_strerror"):
+                    getattr(L, n).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def check(status: int, what: str = ""):
+    if status != 0:
+        raise GPT2Error(status, what)
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    """Device (or host) address of a torch tensor / numpy array, or None."""
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data_as(ctypes.c_void_p)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def upload_weights(weights: dict, device="cuda"):
+    """numpy weights (checkpoint layout) -> dict of contiguous fp32 CUDA tensors."""
+    import torch
+
+    def t(a):
+        return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
+
+    out = {k: t(weights[k]) for k in ("wte", "wpe", "ln_f_w", "ln_f_b")}
+    out["layers"] = [{k: t(L[k]) for k in _LAYER_KEYS} for L in weights["layers"]]
+    return out
+
+
+class Model:
+    """One GPT-2 decode model on the current CUDA device."""
+
+    def __init__(self, cfg, dev_weights: dict, wdtype: str = "f32", stream=None):
+        L = lib()
+        self.cfg = cfg
+        self.wdtype = wdtype
+        self._stream_obj = stream
+        c = Config(cfg.n_layer, cfg.n_embd, cfg.n_head, cfg.n_positions, cfg.vocab_size, cfg.ln_eps)
+        layers = (LayerWeights * cfg.n_layer)()
+        for i, Lw in enumerate(dev_weights["layers"]):
+            for k in _LAYER_KEYS:
+                setattr(layers[i], k, Lw[k].data_ptr())
+        w = Weights(dev_weights["wte"].data_ptr(), dev_weights["wpe"].data_ptr(),
+                    dev_weights["ln_f_w"].data_ptr(), dev_weights["ln_f_b"].data_ptr(),
+                    ctypes.cast(layers, ctypes.POINTER(LayerWeights)))
+        h = ctypes.c_void_p()
+        check(L.gpt2_create(ctypes.byref(c), ctypes.byref(w), WDTYPES[wdtype],
+                            _stream_handle(stream), ctypes.byref(h)), "gpt2_create")
+        self._h = h
+
+    # ---- decoding ----
+    def reset(self):
+        check(lib().gpt2_reset(self._h), "gpt2_reset")
+
+    def decode_step(self, token: int, position: int) -> int:
+        """Queues one pass; returns the device address of the logits."""
+        p = ctypes.c_void_p()
+        check(lib().gpt2_decode_step(self._h, int(token), int(position), ctypes.byref(p)),
+              "gpt2_decode_step")
+        return p.value
+
+    def prefill(self, ids):
+        a = np.ascontiguousarray(ids, np.int32)
+        check(lib().gpt2_prefill(self._h, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), a.size),
+              "gpt2_prefill")
+
+    def argmax(self) -> int:
+        t = ctypes.c_int32()
+        check(lib().gpt2_argmax(self._h, ctypes.byref(t)), "gpt2_argmax")
+        return int(t.value)
+
+    def decode_greedy(self, n_steps: int):
+        check(lib().gpt2_decode_greedy(self._h, int(n_steps)), "gpt2_decode_greedy")
+
+    def generate(self, prompt, n_steps: int) -> list:
+        p = np.ascontiguousarray(prompt, np.int32)
+        out = np.zeros(n_steps + 1, np.int32)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        check(lib().gpt2_generate(self._h, p.ctypes.data_as(i32p), p.size, int(n_steps),
+                                  out.ctypes.data_as(i32p)), "gpt2_generate")
+        return out.tolist()
+
+    def logits(self) -> np.ndarray:
+        out = np.empty(self.cfg.vocab_size, np.float32)
+        check(lib().gpt2_copy_logits(self._h, _ptr(out)), "gpt2_copy_logits")
+        return out
+
+    def copy_logits_to(self, dst):
+        check(lib().gpt2_copy_logits(self._h, _ptr(dst)), "gpt2_copy_logits")
+
+    def sync(self):
+        check(lib().gpt2_sync(self._h), "gpt2_sync")
+
+    # ---- inspection ----
+    def matrix_bytes(self, which: int):
+        a, b, c = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+        check(lib().gpt2_matrix_bytes(self._h, which, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
+              "gpt2_matrix_bytes")
+        return a.value, b.value, c.value
+
+    def export_matrix(self, layer: int, which: int):
+        """Raw stored bytes: (main, scales, zeros) as numpy uint8 arrays."""
+        mb, sb, zb = self.matrix_bytes(which)
+        main = np.empty(mb, np.uint8)
+        sc = np.empty(sb, np.uint8) if sb else None
+        z = np.empty(zb, np.uint8) if zb else None
+        check(lib().gpt2_export_matrix(self._h, layer, which, _ptr(main), _ptr(sc), _ptr(z)),
+              "gpt2_export_matrix")
+        return main, sc, z
+
+    def export_dequant(self, layer: int, which: int) -> np.ndarray:
+        import torch
+        E = self.cfg.n_embd
+        shape = {MAT_ATTN: (3 * E, E), MAT_PROJ: (E, E), MAT_FC: (4 * E, E), MAT_MLP_PROJ: (E, 4 * E)}[which]
+        t = torch.empty(shape, dtype=torch.float32, device="cuda")
+        check(lib().gpt2_export_dequant(self._h, layer, which, _ptr(t)), "gpt2_export_dequant")
+        return t.cpu().numpy()
+
+    def export_kv(self, layer: int, n_rows: int):
+        H, D = self.cfg.n_head, self.cfg.n_embd // self.cfg.n_head
+        k = np.empty((H, n_rows, D), np.float32)
+        v = np.empty((H, n_rows, D), np.float32)
+        check(lib().gpt2_export_kv(self._h, layer, n_rows, _ptr(k), _ptr(v)), "gpt2_export_kv")
+        return k, v
+
+    def kernels_per_step(self) -> int:
+        n = ctypes.c_int32()
+        check(lib().gpt2_kernels_per_step(self._h, ctypes.byref(n)), "gpt2_kernels_per_step")
+        return int(n.value)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().gpt2_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ---- stand-alone operations ------------------------------------------------
+
+def op_layernorm(x, gamma, beta, eps: float, y=None, stream=None):
+    """Warp-per-row LayerNorm of a [rows, n] fp32 CUDA tensor."""
+    import torch
+    rows, n = x.shape
+    if y is None:
+        y = torch.empty_like(x)
+    check(lib().gpt2_op_layernorm(_ptr(x), _ptr(gamma), _ptr(beta), rows, n, float(eps), _ptr(y),
+                                  _stream_handle(stream)), "gpt2_op_layernorm")
+    return y
+
+
+def op_head_argmax_workspace(vocab: int, n_embd: int) -> int:
+    return int(lib().gpt2_op_head_argmax_workspace(vocab, n_embd))
+
+
+def op_head_argmax(x, ln_w, ln_b, eps: float, wte, logits, token, workspace, stream=None):
+    """Final LayerNorm + tied head + argmax on CUDA tensors; token is int32[1]."""
+    V, E = wte.shape
+    check(lib().gpt2_op_head_argmax(_ptr(x), _ptr(ln_w), _ptr(ln_b), float(eps), _ptr(wte), V, E,
+                                    _ptr(logits), _ptr(token), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(),
+                                    _stream_handle(stream)), "gpt2_op_head_argmax")

@@ -1,0 +1,710 @@
+// C ABI of libgpt2.so (include/gpt2.h): model lifecycle, the captured decode
+// pass, greedy decoding, inspection and stand-alone operations.
+#include "../../include/gpt2.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace gpt2;
+
+namespace {
+
+struct QMat {
+    void *w = nullptr;
+    float *scales = nullptr;
+    uint8_t *zeros = nullptr;
+    int in = 0, out = 0;
+    size_t main_bytes = 0, scale_bytes = 0, zero_bytes = 0;
+};
+
+struct LayerDev {
+    float *ln1_w, *ln1_b, *attn_b, *proj_b, *ln2_w, *ln2_b, *fc_b, *mlp_proj_b;
+    QMat mat[4];   // GPT2_MAT_ATTN, _PROJ, _FC, _MLP_PROJ
+};
+
+int env_int(const char *name, int dflt)
+{
+    const char *v = std::getenv(name);
+    if (!v || !*v) return dflt;
+    return std::atoi(v);
+}
+
+}  // namespace
+
+struct gpt2_model {
+    gpt2_config cfg{};
+    int wdtype = 0;
+    cudaStream_t stream = nullptr;
+    int device = 0;
+    int num_sms = 0;
+    bool pdl = true;
+    // device memory
+    uint8_t *arena = nullptr;        // weights
+    size_t arena_bytes = 0;
+    uint8_t *work = nullptr;         // cache, activations, state
+    size_t work_bytes = 0;
+    float *wte = nullptr, *wpe = nullptr, *lnf_w = nullptr, *lnf_b = nullptr;
+    std::vector<LayerDev> layers;
+    float *kcache = nullptr, *vcache = nullptr;   // [L][H][P][D]
+    float *x = nullptr, *qkv = nullptr, *attn = nullptr, *h = nullptr, *logits = nullptr;
+    DeviceState *st = nullptr;
+    int32_t *out_ids = nullptr;
+    int32_t out_cap = 0;
+    unsigned long long *partials = nullptr;
+    unsigned int *counter = nullptr;
+    int max_head_ctas = 0;
+    // captured pass
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    int kernels_per_step = 0;
+    // host view of the cache
+    int cached = 0;
+    bool has_step = false;
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t aup(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+size_t main_bytes_of(int wdtype, int in, int out)
+{
+    const size_t n = size_t(in) * out;
+    return wdtype == GPT2_F32 ? n * 4 : wdtype == GPT2_F16 ? n * 2 : n / 2;
+}
+
+int check_config(const gpt2_config *c, int wdtype)
+{
+    if (!c) return GPT2_ERR_INVALID_ARG;
+    if (c->n_layer < 1 || c->n_embd < 32 || c->n_head < 1 || c->n_positions < 1 || c->vocab_size < 1)
+        return GPT2_ERR_INVALID_ARG;
+    if (c->n_embd % 32 || c->n_embd % c->n_head) return GPT2_ERR_INVALID_ARG;
+    const int D = c->n_embd / c->n_head;
+    if (D != 32 && D != 64 && D != 128) return GPT2_ERR_INVALID_ARG;
+    if (!(c->ln_eps > 0.f) || !std::isfinite(c->ln_eps)) return GPT2_ERR_INVALID_ARG;
+    if (wdtype != GPT2_F32 && wdtype != GPT2_F16 && wdtype != GPT2_INT4) return GPT2_ERR_INVALID_ARG;
+    if (wdtype == GPT2_INT4 && c->n_embd % 128) return GPT2_ERR_INVALID_ARG;
+    // index arithmetic inside kernels is 32-bit per matrix row / element count
+    const long long E = c->n_embd;
+    if ((long long)c->vocab_size * E > (1ll << 31) - 1) return GPT2_ERR_INVALID_ARG;
+    if ((long long)c->n_positions * E > (1ll << 31) - 1) return GPT2_ERR_INVALID_ARG;
+    if (4 * E * E > (1ll << 31) - 1) return GPT2_ERR_INVALID_ARG;
+    return GPT2_OK;
+}
+
+bool is_device_ptr(const void *p)
+{
+    if (!p) return false;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+int cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return GPT2_OK;
+    cudaGetLastError();
+    return e == cudaErrorMemoryAllocation ? GPT2_ERR_OUT_OF_MEMORY : GPT2_ERR_CUDA;
+}
+
+#define TRY_CUDA(expr)                                  \
+    do {                                                \
+        cudaError_t _e = (expr);                        \
+        if (_e != cudaSuccess) return cuda_status(_e);  \
+    } while (0)
+
+// Fills GEMV arguments common to every launch of a matrix.
+GemvArgs gemv_for(const gpt2_model *m, const QMat &q, int ctas, int &grid, size_t budget, int max_stages)
+{
+    GemvArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.W = q.w;
+    a.scales = q.scales;
+    a.zeros = q.zeros;
+    a.in = q.in;
+    a.out = q.out;
+    a.eps = m->cfg.ln_eps;
+    a.st = m->st;
+    grid = gemv_plan(a, m->wdtype, ctas, budget, max_stages);
+    return a;
+}
+
+// Records one decode pass on stream s (called under stream capture).
+int record_pass(gpt2_model *m, cudaStream_t s)
+{
+    const gpt2_config &c = m->cfg;
+    const int E = c.n_embd, H = c.n_head, D = E / H, P = c.n_positions;
+    const size_t budget = size_t(env_int("GPT2_STAGE_KB", 96)) * 1024;
+    const int max_stages = env_int("GPT2_MAX_STAGES", 4);
+    const int ctas = m->num_sms;
+    int kernels = 0;
+    bool first = true;
+    auto pdl = [&]() {
+        bool p = m->pdl && !first;
+        first = false;
+        return p;
+    };
+    for (int l = 0; l < c.n_layer; ++l) {
+        const LayerDev &L = m->layers[l];
+        int grid;
+        // qkv = LN1(x) . W_attn + b_attn   (layer 0 builds x from the embeddings)
+        GemvArgs a = gemv_for(m, L.mat[GPT2_MAT_ATTN], ctas, grid, budget, max_stages);
+        a.xin = m->x;
+        a.ln_w = L.ln1_w;
+        a.ln_b = L.ln1_b;
+        a.bias = L.attn_b;
+        a.y = m->qkv;
+        int mode = kModeLnBias;
+        if (l == 0) {
+            mode = kModeEmbLnBias;
+            a.wte = m->wte;
+            a.wpe = m->wpe;
+            a.x_out = m->x;
+            a.vocab = c.vocab_size;
+            a.n_positions = P;
+        }
+        TRY_CUDA(launch_gemv(m->wdtype, mode, a, grid, s, pdl()));
+        ++kernels;
+        // attention over the cache
+        AttnArgs t;
+        t.qkv = m->qkv;
+        t.k_cache = m->kcache + size_t(l) * H * P * D;
+        t.v_cache = m->vcache + size_t(l) * H * P * D;
+        t.out = m->attn;
+        t.n_head = H;
+        t.head_dim = D;
+        t.n_positions = P;
+        t.scale = float(1.0 / std::sqrt(double(D)));
+        t.st = m->st;
+        TRY_CUDA(launch_attention(t, s, pdl()));
+        ++kernels;
+        // x += attn . W_proj + b_proj
+        a = gemv_for(m, L.mat[GPT2_MAT_PROJ], ctas, grid, budget, max_stages);
+        a.xin = m->attn;
+        a.bias = L.proj_b;
+        a.y = m->x;
+        TRY_CUDA(launch_gemv(m->wdtype, kModeBiasRes, a, grid, s, pdl()));
+        ++kernels;
+        // h = gelu_new(LN2(x) . W_fc + b_fc)
+        a = gemv_for(m, L.mat[GPT2_MAT_FC], ctas, grid, budget, max_stages);
+        a.xin = m->x;
+        a.ln_w = L.ln2_w;
+        a.ln_b = L.ln2_b;
+        a.bias = L.fc_b;
+        a.y = m->h;
+        TRY_CUDA(launch_gemv(m->wdtype, kModeLnBiasGelu, a, grid, s, pdl()));
+        ++kernels;
+        // x += h . W_mlp_proj + b_mlp_proj
+        a = gemv_for(m, L.mat[GPT2_MAT_MLP_PROJ], ctas, grid, budget, max_stages);
+        a.xin = m->h;
+        a.bias = L.mlp_proj_b;
+        a.y = m->x;
+        TRY_CUDA(launch_gemv(m->wdtype, kModeBiasRes, a, grid, s, pdl()));
+        ++kernels;
+    }
+    // logits = wte . LN_f(x); argmax; greedy feedback into the state
+    int grid;
+    GemvArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.W = m->wte;
+    a.in = E;
+    a.out = c.vocab_size;
+    a.eps = c.ln_eps;
+    a.st = m->st;
+    grid = gemv_plan(a, kWF32, m->max_head_ctas, budget, max_stages);
+    a.evict_first = 1;
+    a.xin = m->x;
+    a.ln_w = m->lnf_w;
+    a.ln_b = m->lnf_b;
+    a.y = m->logits;
+    a.partials = m->partials;
+    a.counter = m->counter;
+    a.out_ids = m->out_ids;
+    a.out_cap = m->out_cap;
+    TRY_CUDA(launch_gemv(kWF32, kModeHead, a, grid, s, pdl()));
+    ++kernels;
+    m->kernels_per_step = kernels;
+    return GPT2_OK;
+}
+
+int build_graph(gpt2_model *m)
+{
+    cudaStream_t cs;
+    TRY_CUDA(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
+    cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) {
+        cudaStreamDestroy(cs);
+        return cuda_status(e);
+    }
+    int rc = record_pass(m, cs);
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(cs, &g);
+    cudaStreamDestroy(cs);
+    if (rc != GPT2_OK) {
+        if (g) cudaGraphDestroy(g);
+        return rc;
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+    m->graph = g;
+    e = cudaGraphInstantiate(&m->exec, g, 0);
+    if (e != cudaSuccess) return cuda_status(e);
+    return GPT2_OK;
+}
+
+void free_model(gpt2_model *m)
+{
+    if (!m) return;
+    if (m->exec) cudaGraphExecDestroy(m->exec);
+    if (m->graph) cudaGraphDestroy(m->graph);
+    if (m->arena) cudaFree(m->arena);
+    if (m->work) cudaFree(m->work);
+    delete m;
+}
+
+int read_state(gpt2_model *m, DeviceState *hs)
+{
+    TRY_CUDA(cudaStreamSynchronize(m->stream));
+    TRY_CUDA(cudaMemcpy(hs, m->st, sizeof *hs, cudaMemcpyDeviceToHost));
+    if (hs->err != kDevErrNone) {
+        const int err = hs->err;
+        // report once, then clear so the model stays usable
+        TRY_CUDA(cudaMemset(&m->st->err, 0, 2 * sizeof(int32_t)));
+        return err == kDevErrTimeout ? GPT2_ERR_TIMEOUT : GPT2_ERR_DEVICE_STATE;
+    }
+    return GPT2_OK;
+}
+
+int launch_step(gpt2_model *m, int32_t token, int32_t position)
+{
+    TRY_CUDA(launch_set_state(m->st, token, position, kSetTokPos, m->out_ids, m->stream));
+    TRY_CUDA(cudaGraphLaunch(m->exec, m->stream));
+    return GPT2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gpt2_strerror(int status)
+{
+    switch (status) {
+    case GPT2_OK: return "ok";
+    case GPT2_ERR_INVALID_ARG: return "invalid argument";
+    case GPT2_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
+    case GPT2_ERR_TOKEN_RANGE: return "token outside [0, vocab_size)";
+    case GPT2_ERR_POSITION_RANGE: return "position outside the context or past the cached length";
+    case GPT2_ERR_NOT_READY: return "no decode step has run yet";
+    case GPT2_ERR_CUDA: return "CUDA runtime error";
+    case GPT2_ERR_TIMEOUT: return "a bounded device wait timed out";
+    case GPT2_ERR_DEVICE_STATE: return "a kernel rejected its device-side inputs";
+    case GPT2_ERR_OUT_OF_MEMORY: return "device out of memory";
+    default: return "unknown status";
+    }
+}
+
+int gpt2_create(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype, void *stream, gpt2_model **out)
+{
+    if (!out) return GPT2_ERR_INVALID_ARG;
+    *out = nullptr;
+    int rc = check_config(cfg, wdtype);
+    if (rc != GPT2_OK) return rc;
+    if (!w || !w->layers) return GPT2_ERR_INVALID_ARG;
+    int dev;
+    TRY_CUDA(cudaGetDevice(&dev));
+    cudaDeviceProp prop;
+    TRY_CUDA(cudaGetDeviceProperties(&prop, dev));
+    if (!(prop.major == 10 && prop.minor == 3)) return GPT2_ERR_UNSUPPORTED_DEVICE;
+    TRY_CUDA(gemv_init());
+    // every tensor pointer must be device memory
+    const float *top[4] = {w->wte, w->wpe, w->ln_f_w, w->ln_f_b};
+    for (const float *p : top)
+        if (!is_device_ptr(p)) return GPT2_ERR_INVALID_ARG;
+    for (int l = 0; l < cfg->n_layer; ++l) {
+        const gpt2_layer_weights &L = w->layers[l];
+        const float *ps[12] = {L.ln1_w, L.ln1_b, L.attn_w, L.attn_b, L.proj_w, L.proj_b,
+                               L.ln2_w, L.ln2_b, L.fc_w,   L.fc_b,   L.mlp_proj_w, L.mlp_proj_b};
+        for (const float *p : ps)
+            if (!is_device_ptr(p)) return GPT2_ERR_INVALID_ARG;
+    }
+
+    gpt2_model *m = new (std::nothrow) gpt2_model();
+    if (!m) return GPT2_ERR_OUT_OF_MEMORY;
+    m->cfg = *cfg;
+    m->wdtype = wdtype;
+    m->stream = static_cast<cudaStream_t>(stream);
+    m->device = dev;
+    m->num_sms = prop.multiProcessorCount;
+    m->pdl = env_int("GPT2_NO_PDL", 0) == 0;
+    m->max_head_ctas = m->num_sms * std::max(1, env_int("GPT2_HEAD_CTAS_PER_SM", 1));
+    if (m->max_head_ctas > 1024) m->max_head_ctas = 1024;
+
+    const int L = cfg->n_layer, E = cfg->n_embd, H = cfg->n_head, P = cfg->n_positions, V = cfg->vocab_size;
+    const int F = 4 * E;
+    const int D = E / H;
+    // ---- weight arena layout ----
+    const int mat_in[4] = {E, E, E, F};
+    const int mat_out[4] = {3 * E, E, F, E};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off += aup(bytes);
+        return o;
+    };
+    const size_t o_wte = take(size_t(V) * E * 4), o_wpe = take(size_t(P) * E * 4);
+    const size_t o_lnf_w = take(E * 4), o_lnf_b = take(E * 4);
+    struct LOff {
+        size_t ln1_w, ln1_b, attn_b, proj_b, ln2_w, ln2_b, fc_b, mlp_proj_b;
+        size_t w[4], s[4], z[4];
+    };
+    std::vector<LOff> lo(L);
+    for (int l = 0; l < L; ++l) {
+        lo[l].ln1_w = take(E * 4);
+        lo[l].ln1_b = take(E * 4);
+        lo[l].attn_b = take(3 * E * 4);
+        lo[l].proj_b = take(E * 4);
+        lo[l].ln2_w = take(E * 4);
+        lo[l].ln2_b = take(E * 4);
+        lo[l].fc_b = take(F * 4);
+        lo[l].mlp_proj_b = take(E * 4);
+        for (int k = 0; k < 4; ++k) {
+            lo[l].w[k] = take(main_bytes_of(wdtype, mat_in[k], mat_out[k]));
+            if (wdtype == GPT2_INT4) {
+                lo[l].s[k] = take(size_t(mat_out[k]) * (mat_in[k] / 32) * 4);
+                lo[l].z[k] = take(size_t(mat_out[k]) * (mat_in[k] / 64));
+            }
+        }
+    }
+    m->arena_bytes = off;
+    // ---- work area layout ----
+    off = 0;
+    const size_t kv = size_t(L) * H * P * D * 4;
+    const size_t o_k = take(kv), o_v = take(kv);
+    const size_t o_x = take(E * 4), o_qkv = take(3 * E * 4), o_attn = take(E * 4), o_h = take(F * 4);
+    const size_t o_logits = take(size_t(V) * 4);
+    const size_t o_st = take(sizeof(DeviceState));
+    m->out_cap = P + 1;
+    const size_t o_ids = take(size_t(m->out_cap) * 4);
+    const size_t o_part = take(size_t(m->max_head_ctas) * 8);
+    const size_t o_cnt = take(16);
+    m->work_bytes = off;
+
+    cudaError_t e = cudaMalloc(&m->arena, m->arena_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&m->work, m->work_bytes);
+    if (e != cudaSuccess) {
+        free_model(m);
+        return cuda_status(e);
+    }
+    uint8_t *A = m->arena, *W = m->work;
+    m->wte = reinterpret_cast<float *>(A + o_wte);
+    m->wpe = reinterpret_cast<float *>(A + o_wpe);
+    m->lnf_w = reinterpret_cast<float *>(A + o_lnf_w);
+    m->lnf_b = reinterpret_cast<float *>(A + o_lnf_b);
+    m->layers.resize(L);
+    for (int l = 0; l < L; ++l) {
+        LayerDev &d = m->layers[l];
+        d.ln1_w = reinterpret_cast<float *>(A + lo[l].ln1_w);
+        d.ln1_b = reinterpret_cast<float *>(A + lo[l].ln1_b);
+        d.attn_b = reinterpret_cast<float *>(A + lo[l].attn_b);
+        d.proj_b = reinterpret_cast<float *>(A + lo[l].proj_b);
+        d.ln2_w = reinterpret_cast<float *>(A + lo[l].ln2_w);
+        d.ln2_b = reinterpret_cast<float *>(A + lo[l].ln2_b);
+        d.fc_b = reinterpret_cast<float *>(A + lo[l].fc_b);
+        d.mlp_proj_b = reinterpret_cast<float *>(A + lo[l].mlp_proj_b);
+        for (int k = 0; k < 4; ++k) {
+            QMat &q = d.mat[k];
+            q.in = mat_in[k];
+            q.out = mat_out[k];
+            q.w = A + lo[l].w[k];
+            q.main_bytes = main_bytes_of(wdtype, q.in, q.out);
+            if (wdtype == GPT2_INT4) {
+                q.scales = reinterpret_cast<float *>(A + lo[l].s[k]);
+                q.zeros = A + lo[l].z[k];
+                q.scale_bytes = size_t(q.out) * (q.in / 32) * 4;
+                q.zero_bytes = size_t(q.out) * (q.in / 64);
+            }
+        }
+    }
+    m->kcache = reinterpret_cast<float *>(W + o_k);
+    m->vcache = reinterpret_cast<float *>(W + o_v);
+    m->x = reinterpret_cast<float *>(W + o_x);
+    m->qkv = reinterpret_cast<float *>(W + o_qkv);
+    m->attn = reinterpret_cast<float *>(W + o_attn);
+    m->h = reinterpret_cast<float *>(W + o_h);
+    m->logits = reinterpret_cast<float *>(W + o_logits);
+    m->st = reinterpret_cast<DeviceState *>(W + o_st);
+    m->out_ids = reinterpret_cast<int32_t *>(W + o_ids);
+    m->partials = reinterpret_cast<unsigned long long *>(W + o_part);
+    m->counter = reinterpret_cast<unsigned int *>(W + o_cnt);
+
+    // ---- copy and repack ----
+    cudaStream_t s = m->stream;
+    float *tmp = nullptr;
+    auto fail = [&](cudaError_t err) {
+        if (tmp) cudaFree(tmp);
+        cudaStreamSynchronize(s);
+        free_model(m);
+        return cuda_status(err);
+    };
+#define CK(expr)                                  \
+    do {                                          \
+        cudaError_t _e2 = (expr);                 \
+        if (_e2 != cudaSuccess) return fail(_e2); \
+    } while (0)
+    CK(cudaMemsetAsync(m->work, 0, m->work_bytes, s));
+    CK(cudaMemcpyAsync(m->wte, w->wte, size_t(V) * E * 4, cudaMemcpyDeviceToDevice, s));
+    CK(cudaMemcpyAsync(m->wpe, w->wpe, size_t(P) * E * 4, cudaMemcpyDeviceToDevice, s));
+    CK(cudaMemcpyAsync(m->lnf_w, w->ln_f_w, E * 4, cudaMemcpyDeviceToDevice, s));
+    CK(cudaMemcpyAsync(m->lnf_b, w->ln_f_b, E * 4, cudaMemcpyDeviceToDevice, s));
+    if (wdtype == GPT2_INT4) CK(cudaMalloc(&tmp, size_t(F) * E * 4));
+    for (int l = 0; l < L; ++l) {
+        const gpt2_layer_weights &src = w->layers[l];
+        LayerDev &d = m->layers[l];
+        CK(cudaMemcpyAsync(d.ln1_w, src.ln1_w, E * 4, cudaMemcpyDeviceToDevice, s));
+        CK(cudaMemcpyAsync(d.ln1_b, src.ln1_b, E * 4, cudaMemcpyDeviceToDevice, s));
+        CK(cudaMemcpyAsync(d.attn_b, src.attn_b, 3 * E * 4, cudaMemcpyDeviceToDevice, s));
+        CK(cudaMemcpyAsync(d.proj_b, src.proj_b, E * 4, cudaMemcpyDeviceToDevice, s));
+        CK(cudaMemcpyAsync(d.ln2_w, src.ln2_w, E * 4, cudaMemcpyDeviceToDevice, s));
+        CK(cudaMemcpyAsync(d.ln2_b, src.ln2_b, E * 4, cudaMemcpyDeviceToDevice, s));
+        CK(cudaMemcpyAsync(d.fc_b, src.fc_b, F * 4, cudaMemcpyDeviceToDevice, s));
+        CK(cudaMemcpyAsync(d.mlp_proj_b, src.mlp_proj_b, E * 4, cudaMemcpyDeviceToDevice, s));
+        const float *srcm[4] = {src.attn_w, src.proj_w, src.fc_w, src.mlp_proj_w};
+        for (int k = 0; k < 4; ++k) {
+            QMat &q = d.mat[k];
+            if (wdtype == GPT2_F32) CK(repack_f32(srcm[k], q.in, q.out, static_cast<float *>(q.w), s));
+            else if (wdtype == GPT2_F16) CK(repack_f16(srcm[k], q.in, q.out, q.w, s));
+            else CK(repack_int4(srcm[k], q.in, q.out, tmp, static_cast<uint8_t *>(q.w), q.scales, q.zeros, s));
+        }
+    }
+    CK(cudaStreamSynchronize(s));
+    if (tmp) {
+        cudaFree(tmp);
+        tmp = nullptr;
+    }
+#undef CK
+    rc = build_graph(m);
+    if (rc != GPT2_OK) {
+        free_model(m);
+        return rc;
+    }
+    *out = m;
+    return GPT2_OK;
+}
+
+void gpt2_destroy(gpt2_model *m)
+{
+    if (!m) return;
+    cudaStreamSynchronize(m->stream);
+    free_model(m);
+}
+
+int gpt2_reset(gpt2_model *m)
+{
+    if (!m) return GPT2_ERR_INVALID_ARG;
+    m->cached = 0;
+    m->has_step = false;
+    return GPT2_OK;
+}
+
+int gpt2_decode_step(gpt2_model *m, int32_t token, int32_t position, const float **dev_logits)
+{
+    if (!m) return GPT2_ERR_INVALID_ARG;
+    if (token < 0 || token >= m->cfg.vocab_size) return GPT2_ERR_TOKEN_RANGE;
+    if (position < 0 || position >= m->cfg.n_positions || position > m->cached) return GPT2_ERR_POSITION_RANGE;
+    int rc = launch_step(m, token, position);
+    if (rc != GPT2_OK) return rc;
+    m->cached = position + 1;
+    m->has_step = true;
+    if (dev_logits) *dev_logits = m->logits;
+    return GPT2_OK;
+}
+
+int gpt2_prefill(gpt2_model *m, const int32_t *host_ids, int32_t n)
+{
+    if (!m || !host_ids) return GPT2_ERR_INVALID_ARG;
+    if (n < 1 || n > m->cfg.n_positions) return GPT2_ERR_POSITION_RANGE;
+    for (int i = 0; i < n; ++i)
+        if (host_ids[i] < 0 || host_ids[i] >= m->cfg.vocab_size) return GPT2_ERR_TOKEN_RANGE;
+    gpt2_reset(m);
+    for (int i = 0; i < n; ++i) {
+        int rc = gpt2_decode_step(m, host_ids[i], i, nullptr);
+        if (rc != GPT2_OK) return rc;
+    }
+    return GPT2_OK;
+}
+
+int gpt2_argmax(gpt2_model *m, int32_t *token_out)
+{
+    if (!m || !token_out) return GPT2_ERR_INVALID_ARG;
+    if (!m->has_step) return GPT2_ERR_NOT_READY;
+    DeviceState hs;
+    int rc = read_state(m, &hs);
+    if (rc != GPT2_OK) return rc;
+    *token_out = hs.next_tok;
+    return GPT2_OK;
+}
+
+int gpt2_decode_greedy(gpt2_model *m, int32_t n_steps)
+{
+    if (!m || n_steps < 0) return GPT2_ERR_INVALID_ARG;
+    if (!m->has_step) return GPT2_ERR_NOT_READY;
+    if ((long long)m->cached + n_steps > m->cfg.n_positions) return GPT2_ERR_POSITION_RANGE;
+    for (int i = 0; i < n_steps; ++i) TRY_CUDA(cudaGraphLaunch(m->exec, m->stream));
+    m->cached += n_steps;
+    return GPT2_OK;
+}
+
+int gpt2_generate(gpt2_model *m, const int32_t *host_prompt, int32_t n_prompt, int32_t n_steps,
+                  int32_t *host_out)
+{
+    if (!m || !host_prompt || !host_out || n_steps < 0) return GPT2_ERR_INVALID_ARG;
+    if (n_prompt < 1 || (long long)n_prompt + n_steps > m->cfg.n_positions) return GPT2_ERR_POSITION_RANGE;
+    int rc = gpt2_prefill(m, host_prompt, n_prompt);
+    if (rc != GPT2_OK) return rc;
+    TRY_CUDA(launch_set_state(m->st, 0, 0, kSeedOutWithNext, m->out_ids, m->stream));
+    rc = gpt2_decode_greedy(m, n_steps);
+    if (rc != GPT2_OK) return rc;
+    TRY_CUDA(cudaMemcpyAsync(host_out, m->out_ids, size_t(n_steps + 1) * 4, cudaMemcpyDeviceToHost, m->stream));
+    DeviceState hs;
+    return read_state(m, &hs);
+}
+
+int gpt2_copy_logits(gpt2_model *m, float *dst)
+{
+    if (!m || !dst) return GPT2_ERR_INVALID_ARG;
+    if (!m->has_step) return GPT2_ERR_NOT_READY;
+    TRY_CUDA(cudaMemcpyAsync(dst, m->logits, size_t(m->cfg.vocab_size) * 4, cudaMemcpyDefault, m->stream));
+    DeviceState hs;
+    return read_state(m, &hs);
+}
+
+int gpt2_sync(gpt2_model *m)
+{
+    if (!m) return GPT2_ERR_INVALID_ARG;
+    DeviceState hs;
+    return read_state(m, &hs);
+}
+
+int gpt2_matrix_bytes(const gpt2_model *m, int32_t which, size_t *main_bytes, size_t *scale_bytes,
+                      size_t *zero_bytes)
+{
+    if (!m || which < 0 || which > 3) return GPT2_ERR_INVALID_ARG;
+    const QMat &q = m->layers[0].mat[which];
+    if (main_bytes) *main_bytes = q.main_bytes;
+    if (scale_bytes) *scale_bytes = q.scale_bytes;
+    if (zero_bytes) *zero_bytes = q.zero_bytes;
+    return GPT2_OK;
+}
+
+int gpt2_export_matrix(gpt2_model *m, int32_t layer, int32_t which, void *dst_main, void *dst_scales,
+                       void *dst_zeros)
+{
+    if (!m || layer < 0 || layer >= m->cfg.n_layer || which < 0 || which > 3) return GPT2_ERR_INVALID_ARG;
+    const QMat &q = m->layers[layer].mat[which];
+    if (dst_main) TRY_CUDA(cudaMemcpyAsync(dst_main, q.w, q.main_bytes, cudaMemcpyDefault, m->stream));
+    if (dst_scales && q.scales)
+        TRY_CUDA(cudaMemcpyAsync(dst_scales, q.scales, q.scale_bytes, cudaMemcpyDefault, m->stream));
+    if (dst_zeros && q.zeros)
+        TRY_CUDA(cudaMemcpyAsync(dst_zeros, q.zeros, q.zero_bytes, cudaMemcpyDefault, m->stream));
+    TRY_CUDA(cudaStreamSynchronize(m->stream));
+    return GPT2_OK;
+}
+
+int gpt2_export_dequant(gpt2_model *m, int32_t layer, int32_t which, float *dst)
+{
+    if (!m || !dst || layer < 0 || layer >= m->cfg.n_layer || which < 0 || which > 3) return GPT2_ERR_INVALID_ARG;
+    if (!is_device_ptr(dst)) return GPT2_ERR_INVALID_ARG;
+    const QMat &q = m->layers[layer].mat[which];
+    TRY_CUDA(dequant_to_f32(m->wdtype, q.w, q.scales, q.zeros, q.in, q.out, dst, m->stream));
+    TRY_CUDA(cudaStreamSynchronize(m->stream));
+    return GPT2_OK;
+}
+
+int gpt2_export_kv(gpt2_model *m, int32_t layer, int32_t n_rows, float *dst_k, float *dst_v)
+{
+    if (!m || layer < 0 || layer >= m->cfg.n_layer) return GPT2_ERR_INVALID_ARG;
+    const int H = m->cfg.n_head, D = m->cfg.n_embd / H, P = m->cfg.n_positions;
+    if (n_rows < 0 || n_rows > P) return GPT2_ERR_INVALID_ARG;
+    for (int h = 0; h < H; ++h) {
+        const size_t src = (size_t(layer) * H + h) * P * D;
+        const size_t dst = size_t(h) * n_rows * D;
+        const size_t bytes = size_t(n_rows) * D * 4;
+        if (dst_k) TRY_CUDA(cudaMemcpyAsync(dst_k + dst, m->kcache + src, bytes, cudaMemcpyDefault, m->stream));
+        if (dst_v) TRY_CUDA(cudaMemcpyAsync(dst_v + dst, m->vcache + src, bytes, cudaMemcpyDefault, m->stream));
+    }
+    TRY_CUDA(cudaStreamSynchronize(m->stream));
+    return GPT2_OK;
+}
+
+int gpt2_kernels_per_step(const gpt2_model *m, int32_t *count)
+{
+    if (!m || !count) return GPT2_ERR_INVALID_ARG;
+    *count = m->kernels_per_step;
+    return GPT2_OK;
+}
+
+int gpt2_op_layernorm(const float *x, const float *gamma, const float *beta, int32_t rows, int32_t n, float eps,
+                      float *y, void *stream)
+{
+    if (!x || !gamma || !beta || !y || rows < 0 || n < 1 || n % 4 || !(eps > 0.f)) return GPT2_ERR_INVALID_ARG;
+    if (rows == 0) return GPT2_OK;
+    TRY_CUDA(launch_layernorm_rows(x, gamma, beta, rows, n, eps, y, static_cast<cudaStream_t>(stream)));
+    return GPT2_OK;
+}
+
+// Workspace of the stand-alone head: a 16-byte arrival counter, then one
+// 8-byte (value, index) key per CTA; the grid never exceeds 1024 CTAs.
+static constexpr int kOpHeadMaxCtas = 1024;
+
+size_t gpt2_op_head_argmax_workspace(int32_t vocab, int32_t n_embd)
+{
+    (void)vocab;
+    (void)n_embd;
+    return 16 + size_t(kOpHeadMaxCtas) * 8;
+}
+
+int gpt2_op_head_argmax(const float *x, const float *ln_w, const float *ln_b, float eps, const float *wte,
+                        int32_t vocab, int32_t n_embd, float *logits, int32_t *dev_token, void *workspace,
+                        size_t workspace_bytes, void *stream)
+{
+    if (!x || !ln_w || !ln_b || !wte || !logits || !dev_token || !workspace) return GPT2_ERR_INVALID_ARG;
+    if (vocab < 1 || n_embd < 4 || n_embd % 4 || !(eps > 0.f)) return GPT2_ERR_INVALID_ARG;
+    if ((long long)vocab * n_embd > (1ll << 31) - 1) return GPT2_ERR_INVALID_ARG;
+    if (workspace_bytes < gpt2_op_head_argmax_workspace(vocab, n_embd)) return GPT2_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 || reinterpret_cast<uintptr_t>(wte) % 16)
+        return GPT2_ERR_INVALID_ARG;
+    int dev, sms;
+    TRY_CUDA(gemv_init());
+    TRY_CUDA(cudaGetDevice(&dev));
+    TRY_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    GemvArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.W = wte;
+    a.in = n_embd;
+    a.out = vocab;
+    a.eps = eps;
+    const int grid = gemv_plan(a, kWF32, std::min(sms, kOpHeadMaxCtas), 96 * 1024, 4);
+    a.evict_first = 1;
+    a.xin = x;
+    a.ln_w = ln_w;
+    a.ln_b = ln_b;
+    a.y = logits;
+    a.counter = static_cast<unsigned int *>(workspace);
+    a.partials = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(workspace) + 16);
+    a.dev_token = dev_token;
+    TRY_CUDA(cudaMemsetAsync(a.counter, 0, sizeof(unsigned int), s));
+    TRY_CUDA(launch_gemv(kWF32, kModeHead, a, grid, s, false));
+    return GPT2_OK;
+}
+
+}  // extern "C"
