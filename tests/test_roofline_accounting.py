@@ -1,0 +1,49 @@
+"""The byte / multiply-add accounting behind the roofline, pinned to the
+sizes the pages print for GPT-2 small."""
+import json
+import os
+
+import pytest
+
+from transformer_decode_token_gb300 import roofline, synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_sizes.json")
+
+
+def computed(name, cfg=synth.SMALL):
+    E, L, P, V = cfg.n_embd, cfg.n_layer, cfg.n_positions, cfg.vocab_size
+    if name == "kv_cache_bytes":
+        return L * P * E * 2 * 4
+    if name == "block_matrix_bytes_f32":
+        return roofline.block_matrix_bytes(cfg, "f32")
+    if name == "head_padded_bytes":
+        return ((V + 63) // 64 * 64) * E * 4
+    if name == "weight_bytes_f32":
+        return roofline.parameter_count(cfg) * 4
+    if name == "macs_per_token":
+        return roofline.macs_per_token(cfg)
+    raise KeyError(name)
+
+
+@pytest.mark.parametrize("fig", json.load(open(GOLDEN))["figures"], ids=lambda f: f["name"])
+def test_page_figure(fig):
+    v = computed(fig["name"])
+    if "value_mb" in fig:
+        assert abs(v / 1e6 - fig["value_mb"]) <= fig["rel_tol"] * fig["value_mb"]
+    else:
+        assert abs(v / 1e6 - fig["value_m"]) <= fig["rel_tol"] * fig["value_m"]
+
+
+def test_bytes_per_token_components():
+    cfg = synth.SMALL
+    b = roofline.bytes_per_token(cfg, "f32", 0)
+    assert b["block_matrices"] == 339_738_624
+    assert b["head"] == 154_389_504
+    assert b["kv"] == 73_728 * 2
+    i4 = roofline.bytes_per_token(cfg, "int4", 0)
+    assert i4["block_matrices"] == 42_467_328 + 10_616_832 + 1_327_104
+    f16 = roofline.bytes_per_token(cfg, "f16", 0)
+    assert f16["block_matrices"] == 339_738_624 // 2
+    assert roofline.bytes_per_token(cfg, "f32", 1023)["kv"] == 12 * 1025 * 2 * 768 * 4
+    with pytest.raises(ValueError):
+        roofline.block_matrix_bytes(cfg, "int8")

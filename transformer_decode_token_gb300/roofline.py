@@ -1,0 +1,57 @@
+"""Algorithmic bytes and multiply-adds of one decode pass.
+
+"Algorithmic" means what the pass must move at least once: every stored
+weight it multiplies, one row each of wte and wpe for the embedding, the
+biases and LayerNorm parameters, the KV cache rows it reads and the row it
+writes, and the logits it writes.  Activations (a few KB, cache-resident)
+are not counted.  Pinned to the sizes the pages print by
+tests/test_roofline_accounting.py.
+"""
+from __future__ import annotations
+
+
+def block_params(cfg) -> int:
+    """Weights of the 4 block matrices of all layers: 12 E^2 per layer."""
+    E = cfg.n_embd
+    return cfg.n_layer * (3 * E * E + E * E + 4 * E * E + 4 * E * E)
+
+
+def block_matrix_bytes(cfg, wdtype: str) -> int:
+    n = block_params(cfg)
+    if wdtype == "f32":
+        return 4 * n
+    if wdtype in ("f16", "bf16"):
+        return 2 * n
+    if wdtype == "int4":
+        return n // 2 + (n // 32) * 4 + n // 64     # codes + fp32 scales + 4-bit zero points
+    raise ValueError(wdtype)
+
+
+def bytes_per_token(cfg, wdtype: str, pos: int) -> dict:
+    """Bytes one decode pass at position `pos` must move."""
+    E, V, L = cfg.n_embd, cfg.vocab_size, cfg.n_layer
+    parts = {
+        "block_matrices": block_matrix_bytes(cfg, wdtype),
+        "head": V * E * 4,                               # tied wte, fp32 in every mode
+        "biases_ln": L * 13 * E * 4 + 2 * E * 4,         # 9E bias + 4E LN per layer, ln_f
+        "embedding_rows": 2 * E * 4,                     # wte[token], wpe[pos]
+        "logits": V * 4,
+        "kv": L * 2 * E * 4 * (pos + 2),                 # read rows 0..pos, write row pos
+    }
+    parts["total"] = sum(parts.values())
+    return parts
+
+
+def mean_bytes_per_token(cfg, wdtype: str, positions) -> float:
+    positions = list(positions)
+    return sum(bytes_per_token(cfg, wdtype, p)["total"] for p in positions) / len(positions)
+
+
+def macs_per_token(cfg) -> int:
+    """Multiply-adds of the matrix products (block linears + tied head)."""
+    return block_params(cfg) + cfg.vocab_size * cfg.n_embd
+
+
+def parameter_count(cfg) -> int:
+    E, V, P, L = cfg.n_embd, cfg.vocab_size, cfg.n_positions, cfg.n_layer
+    return V * E + P * E + block_params(cfg) + L * 13 * E + 2 * E
