@@ -231,6 +231,30 @@ int gpt2_op_head_argmax(const float *x, const float *ln_w, const float *ln_b,
                         int32_t n_embd, float *logits, int32_t *dev_token,
                         void *workspace, size_t workspace_bytes, void *stream);
 
+/* The same final LayerNorm + tied head + argmax for callers that cannot
+ * allocate device memory (no counterpart on the pages: it exists for hosts
+ * that own all device memory through their own pools, or whose steady-state
+ * loop must never call the CUDA allocator).  It takes no workspace: the
+ * per-CTA maxima and the arrival counter live in a fixed 4112-byte array in
+ * the library's device memory, one copy per GPU that loads the library, kept
+ * until the process exits.  It allocates nothing and calls no allocating
+ * routine.
+ *   - vocab must be <= GPT2_NOALLOC_MAX_VOCAB (131072); larger vocabularies
+ *     return GPT2_ERR_INVALID_ARG (the array holds one key per 256 rows).
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture begins.
+ *   - All calls on a device share the array: calls whose kernels can overlap
+ *     on the GPU (different streams, different threads) race and must be
+ *     serialised by the caller.  Each call clears the counter it needs.
+ * Arguments, layouts and results are those of gpt2_op_head_argmax; outputs
+ * match it.  Asynchronous on `stream`.  Errors: INVALID_ARG, CUDA. */
+#define GPT2_NOALLOC_MAX_VOCAB 131072
+int gpt2_op_head_argmax_noalloc(const float *x, const float *ln_w, const float *ln_b,
+                                float eps, const float *wte, int32_t vocab,
+                                int32_t n_embd, float *logits, int32_t *dev_token,
+                                void *stream);
+
 /* ---- errors ------------------------------------------------------------- */
 const char *gpt2_strerror(int status);
 

@@ -27,7 +27,7 @@ EXPORTED = ("gpt2_create", "gpt2_destroy", "gpt2_reset", "gpt2_decode_step", "gp
             "gpt2_argmax", "gpt2_decode_greedy", "gpt2_generate", "gpt2_copy_logits", "gpt2_sync",
             "gpt2_matrix_bytes", "gpt2_export_matrix", "gpt2_export_dequant", "gpt2_export_kv",
             "gpt2_kernels_per_step", "gpt2_op_layernorm", "gpt2_op_head_argmax_workspace",
-            "gpt2_op_head_argmax", "gpt2_strerror")
+            "gpt2_op_head_argmax", "gpt2_op_head_argmax_noalloc", "gpt2_strerror")
 
 
 class GPT2Error(RuntimeError):
@@ -97,6 +97,7 @@ def lib(build_if_stale: bool = True):
             L.gpt2_op_head_argmax_workspace.argtypes = [i32, i32]
             L.gpt2_op_head_argmax_workspace.restype = sz
             L.gpt2_op_head_argmax.argtypes = [vp, vp, vp, f32, vp, i32, i32, vp, vp, vp, sz, vp]
+            L.gpt2_op_head_argmax_noalloc.argtypes = [vp, vp, vp, f32, vp, i32, i32, vp, vp, vp]
             L.gpt2_strerror.argtypes = [ctypes.c_int]
             L.gpt2_strerror.restype = ctypes.c_char_p
             for n in EXPORTED:
@@ -276,3 +277,12 @@ def op_head_argmax(x, ln_w, ln_b, eps: float, wte, logits, token, workspace, str
                                     _ptr(logits), _ptr(token), _ptr(workspace),
                                     workspace.numel() * workspace.element_size(),
                                     _stream_handle(stream)), "gpt2_op_head_argmax")
+
+
+def op_head_argmax_noalloc(x, ln_w, ln_b, eps: float, wte, logits, token, stream=None):
+    """gpt2_op_head_argmax without a workspace, for callers that cannot
+    allocate device memory; scratch lives inside the library (see gpt2.h)."""
+    V, E = wte.shape
+    check(lib().gpt2_op_head_argmax_noalloc(_ptr(x), _ptr(ln_w), _ptr(ln_b), float(eps), _ptr(wte), V, E,
+                                            _ptr(logits), _ptr(token), _stream_handle(stream)),
+          "gpt2_op_head_argmax_noalloc")
