@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="CPU time budget of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--path", choices=["auto", "per_kernel"], default="auto",
+                   help="auto: the persistent decode kernel where the device allows it")
     a = p.parse_args()
     if a.warmup < 3:
         p.error("--warmup must be >= 3")
@@ -270,10 +272,11 @@ def main():
     w = synth.make_weights(cfg, 0)
     prompt = synth.make_prompt(cfg, PROMPT_LEN, 1)
     dw = binding.upload_weights(w)
-    model = binding.Model(cfg, dw, args.wdtype)
+    model = binding.Model(cfg, dw, args.wdtype, path=args.path)
     del dw
     torch.cuda.empty_cache()
     kps = model.kernels_per_step()
+    path = model.path()
 
     # ---- device-timed value ----
     model.prefill(prompt)
@@ -289,9 +292,11 @@ def main():
     barrier()
     torch.cuda.synchronize()
     t_begin = time.time()
+    n0 = model.launch_count()
     e0.record(stream)
     runner.run(args.steps)
     e1.record(stream)
+    launches = model.launch_count() - n0
     torch.cuda.synchronize()
     t_end = time.time()
     barrier()
@@ -299,7 +304,6 @@ def main():
     model.sync()
     ms = max_over_ranks(e0.elapsed_time(e1))
     value = args.steps * world / (ms / 1e3)
-    launches = runner.host_steps + args.steps * kps
 
     # ---- end to end through gpt2_generate: host prompt in, host ids out ----
     model.generate(prompt, CYCLE)
@@ -324,7 +328,10 @@ def main():
     peaks, peak_kind = measured_peaks()
     achieved = alg / (ms / 1e3 / args.steps) / 1e9
     traffic = load_traffic().get(args.wdtype)
-    roof = {"bound": "hbm", "kernel": f"decode pass: one CUDA graph of {kps} kernels (PDL-chained)",
+    kernel = ("k_decode_persistent: one cooperative launch per call (one per 60-step cycle here, "
+              "a host-fed pass + 59 device-fed passes), one CTA per SM" if path == "persistent" else
+              f"decode pass: one CUDA graph of {kps} kernels (PDL-chained)")
+    roof = {"bound": "hbm", "kernel": kernel,
             "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"], "peak_kind": f"{peak_kind} copy bandwidth",
             "traffic": traffic, "algorithmic_bytes_per_launch": alg}
@@ -333,7 +340,8 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32" if args.wdtype == "f32" else
             f"{args.wdtype} weights, f32 math", "data": "synthetic",
-            "config": workload_config(args.wdtype, world), "e2e": e2e, "gpu_launches": launches,
+            "config": dict(workload_config(args.wdtype, world), path=path), "e2e": e2e,
+            "gpu_launches": launches,
             "roofline": roof, "clocks": clocks}
 
     # ---- CPU baseline: the oracle on this host (rank 0, N = 1) ---------------

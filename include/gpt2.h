@@ -124,6 +124,24 @@ typedef struct gpt2_model gpt2_model;
 int gpt2_create(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
                 void *stream, gpt2_model **out);
 
+/* gpt2_create with options.  flags = 0 is gpt2_create.  By default a model
+ * runs its passes in the persistent decode kernel: one cooperative launch per
+ * call, one CTA per SM, which streams every pass's weights through shared
+ * memory and passes activations between CTAs as value+epoch words (greedy
+ * steps never return to the host).  GPT2_FLAG_PER_KERNEL selects the
+ * per-kernel path instead: the captured CUDA graph of 5 * n_layer + 1 kernels
+ * per pass.  The persistent path is also left out (per-kernel used) when the
+ * device cannot co-schedule one such CTA per SM or n_embd > 4096; the
+ * environment variable GPT2_PATH=graph forces the per-kernel path.  Both paths
+ * compute the same pass; gpt2_path reports which one a model uses. */
+#define GPT2_FLAG_PER_KERNEL 1
+int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
+                   int32_t flags, void *stream, gpt2_model **out);
+
+#define GPT2_PATH_PER_KERNEL 0
+#define GPT2_PATH_PERSISTENT 1
+int gpt2_path(const gpt2_model *m, int32_t *path);
+
 /* Frees every device buffer and the graph.  NULL is accepted. */
 void gpt2_destroy(gpt2_model *m);
 
@@ -206,8 +224,13 @@ int gpt2_export_dequant(gpt2_model *m, int32_t layer, int32_t which, float *dst)
 int gpt2_export_kv(gpt2_model *m, int32_t layer, int32_t n_rows,
                    float *dst_k, float *dst_v);
 
-/* Number of kernel launches one decode pass makes (for launch accounting). */
+/* Kernel launches per decode pass: 5 * n_layer + 1 on the per-kernel path,
+ * 1 on the persistent path (where one launch runs every pass of a call). */
 int gpt2_kernels_per_step(const gpt2_model *m, int32_t *count);
+
+/* Total kernel launches this model has issued so far (graph kernels and the
+ * small state-setting kernel included), for launch accounting. */
+int gpt2_launch_count(const gpt2_model *m, uint64_t *count);
 
 /* ---- stand-alone operations on caller buffers --------------------------- */
 

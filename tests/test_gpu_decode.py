@@ -19,7 +19,15 @@ from gpu_util import check_rows, max_abs, teacher_forced, top2_margin
 pytestmark = pytest.mark.gpu
 
 TOL = {"f32": (1e-3, 1e-4), "f16": (2e-3, None), "int4": (2e-3, None)}
+PATHS = ["persistent", "per_kernel"]
 _cache = {}
+_oracle_cache = {}
+
+
+def model(cfg, dw, wdtype, path):
+    m = binding.Model(cfg, dw, wdtype, path="auto" if path == "persistent" else "per_kernel")
+    assert m.path() == path
+    return m
 
 
 def weights(cfg, seed=0):
@@ -31,13 +39,16 @@ def weights(cfg, seed=0):
     return _cache[key]
 
 
-def run_parity(cfg, wdtype, n_prompt, n_steps, seed=0, prompt_seed=1):
+def run_parity(cfg, wdtype, n_prompt, n_steps, path, seed=0, prompt_seed=1):
     w, dw = weights(cfg, seed)
     prompt = synth.make_prompt(cfg, n_prompt, prompt_seed)
-    sw = orc.stored_weights(w, wdtype)
-    ref_ids, ref_rows = orc.greedy(cfg, sw, prompt, n_steps)
+    key = (cfg, wdtype, n_prompt, n_steps, seed, prompt_seed)
+    if key not in _oracle_cache:
+        sw = orc.stored_weights(w, wdtype)
+        _oracle_cache[key] = orc.greedy(cfg, sw, prompt, n_steps)
+    ref_ids, ref_rows = _oracle_cache[key]
     tokens = list(prompt) + ref_ids[:n_steps]
-    m = binding.Model(cfg, dw, wdtype)
+    m = model(cfg, dw, wdtype, path)
     try:
         rows, ids = teacher_forced(m, tokens)
     finally:
@@ -47,25 +58,46 @@ def run_parity(cfg, wdtype, n_prompt, n_steps, seed=0, prompt_seed=1):
     return ref_ids, ref_rows, ids
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("wdtype", ["f32", "f16", "int4"])
-def test_tiny_teacher_forced(wdtype):
-    run_parity(synth.TINY, wdtype, 4, 16)
+def test_tiny_teacher_forced(wdtype, path):
+    run_parity(synth.TINY, wdtype, 4, 16, path)
 
 
-def test_small_fp32_config():
+@pytest.mark.parametrize("path", PATHS)
+def test_small_fp32_config(path):
     """GPT-2 small fp32: 10-token prompt, 60 greedy steps, every step checked."""
-    run_parity(synth.SMALL, "f32", 10, 60)
+    run_parity(synth.SMALL, "f32", 10, 60, path)
 
 
-def test_small_int4_config():
+@pytest.mark.parametrize("path", PATHS)
+def test_small_int4_config(path):
     """GPT-2 small with int4 block linears: 10-token prompt, 128 steps."""
-    run_parity(synth.SMALL, "int4", 10, 128)
+    run_parity(synth.SMALL, "int4", 10, 128, path)
 
 
-def test_small_fp16_full_context():
+@pytest.mark.parametrize("path", PATHS)
+def test_small_fp16_full_context(path):
     """GPT-2 small with fp16 block linears: 16-token prompt, decode until the
     1024-position cache is full (positions 0..1023)."""
-    run_parity(synth.SMALL, "f16", 16, 1008)
+    run_parity(synth.SMALL, "f16", 16, 1008, path)
+
+
+@pytest.mark.parametrize("wdtype", ["f32", "int4"])
+def test_paths_agree(wdtype):
+    """The persistent kernel and the per-kernel graph compute the same pass
+    (same row dot products; attention merges its warps in a different order)."""
+    cfg = synth.SMALL
+    _, dw = weights(cfg)
+    prompt = synth.make_prompt(cfg, 10, 1)
+    out = {}
+    for path in PATHS:
+        m = model(cfg, dw, wdtype, path)
+        ids = m.generate(prompt, 30)
+        out[path] = (ids, m.logits())
+        m.close()
+    assert max_abs(out["persistent"][1], out["per_kernel"][1]) <= 1e-4
+    assert out["persistent"][0] == out["per_kernel"][0]
 
 
 # ---- stored weights -----------------------------------------------------------
@@ -103,12 +135,13 @@ def test_stored_weights_bit_exact(cfg, wdtype):
 
 # ---- decoding semantics ----------------------------------------------------
 
-def test_generate_matches_oracle_and_host_loop():
+@pytest.mark.parametrize("path", PATHS)
+def test_generate_matches_oracle_and_host_loop(path):
     cfg = synth.TINY
     w, dw = weights(cfg)
     prompt = synth.make_prompt(cfg, 4, 1)
     ref_ids, ref_rows = orc.greedy(cfg, w, prompt, 16)
-    m = binding.Model(cfg, dw, "f32")
+    m = model(cfg, dw, "f32", path)
     try:
         ids = m.generate(prompt, 16)
         for i, (a, b) in enumerate(zip(ids, ref_ids)):
@@ -126,13 +159,14 @@ def test_generate_matches_oracle_and_host_loop():
         m.close()
 
 
-def test_runs_are_bitwise_reproducible():
+@pytest.mark.parametrize("path", PATHS)
+def test_runs_are_bitwise_reproducible(path):
     cfg = synth.TINY
     _, dw = weights(cfg)
     prompt = synth.make_prompt(cfg, 5, 3)
     outs = []
     for _ in range(2):
-        m = binding.Model(cfg, dw, "int4")
+        m = model(cfg, dw, "int4", path)
         ids = m.generate(prompt, 20)
         outs.append((ids, m.logits()))
         m.close()
@@ -140,10 +174,11 @@ def test_runs_are_bitwise_reproducible():
     assert np.array_equal(outs[0][1], outs[1][1])
 
 
-def test_rewind_and_errors():
+@pytest.mark.parametrize("path", PATHS)
+def test_rewind_and_errors(path):
     cfg = synth.TINY
     _, dw = weights(cfg)
-    m = binding.Model(cfg, dw, "f32")
+    m = model(cfg, dw, "f32", path)
     try:
         with pytest.raises(binding.GPT2Error) as e:
             m.argmax()
@@ -172,13 +207,14 @@ def test_rewind_and_errors():
         m.close()
 
 
-def test_full_context_edge():
+@pytest.mark.parametrize("path", PATHS)
+def test_full_context_edge(path):
     """Prefill the whole context, and generate up to the last position."""
     cfg = synth.TINY
     w, dw = weights(cfg)
     prompt = synth.make_prompt(cfg, cfg.n_positions, 4)
     full = orc.forward_full(cfg, w, prompt)
-    m = binding.Model(cfg, dw, "f32")
+    m = model(cfg, dw, "f32", path)
     try:
         m.prefill(prompt)
         assert max_abs(m.logits(), full[-1]) <= 1e-3
@@ -194,12 +230,13 @@ def test_full_context_edge():
         m.close()
 
 
-def test_kv_cache_contents():
+@pytest.mark.parametrize("path", PATHS)
+def test_kv_cache_contents(path):
     """The cache holds each position's k and v (stored by head)."""
     cfg = synth.TINY
     w, dw = weights(cfg)
     toks = synth.make_prompt(cfg, 6, 5)
-    m = binding.Model(cfg, dw, "f32")
+    m = model(cfg, dw, "f32", path)
     try:
         m.prefill(toks)
         m.sync()
@@ -212,6 +249,6 @@ def test_kv_cache_contents():
             qkv = orc.linear(orc.layernorm(x, L0["ln1_w"], L0["ln1_b"]), L0["attn_w"], L0["attn_b"])
             assert max_abs(k[:, p, :].reshape(-1), qkv[E:2 * E]) <= 1e-4
             assert max_abs(v[:, p, :].reshape(-1), qkv[2 * E:]) <= 1e-4
-        assert m.kernels_per_step() == 5 * cfg.n_layer + 1
+        assert m.kernels_per_step() == (5 * cfg.n_layer + 1 if path == "per_kernel" else 1)
     finally:
         m.close()

@@ -23,7 +23,7 @@ STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED_DEVICE", -3: "TOKEN_RANGE
           -4: "POSITION_RANGE", -5: "NOT_READY", -6: "CUDA", -7: "TIMEOUT",
           -8: "DEVICE_STATE", -9: "OUT_OF_MEMORY"}
 
-EXPORTED = ("gpt2_create", "gpt2_destroy", "gpt2_reset", "gpt2_decode_step", "gpt2_prefill",
+EXPORTED = ("gpt2_create", "gpt2_create_ex", "gpt2_path", "gpt2_launch_count", "gpt2_destroy", "gpt2_reset", "gpt2_decode_step", "gpt2_prefill",
             "gpt2_argmax", "gpt2_decode_greedy", "gpt2_generate", "gpt2_copy_logits", "gpt2_sync",
             "gpt2_matrix_bytes", "gpt2_export_matrix", "gpt2_export_dequant", "gpt2_export_kv",
             "gpt2_kernels_per_step", "gpt2_op_layernorm", "gpt2_op_head_argmax_workspace",
@@ -77,6 +77,10 @@ def lib(build_if_stale: bool = True):
             pi32 = ctypes.POINTER(ctypes.c_int32)
             L.gpt2_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), i32, vp,
                                       ctypes.POINTER(vp)]
+            L.gpt2_create_ex.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), i32, i32, vp,
+                                         ctypes.POINTER(vp)]
+            L.gpt2_path.argtypes = [vp, pi32]
+            L.gpt2_launch_count.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64)]
             L.gpt2_destroy.argtypes = [vp]
             L.gpt2_destroy.restype = None
             L.gpt2_reset.argtypes = [vp]
@@ -143,7 +147,8 @@ def upload_weights(weights: dict, device="cuda"):
 class Model:
     """One GPT-2 decode model on the current CUDA device."""
 
-    def __init__(self, cfg, dev_weights: dict, wdtype: str = "f32", stream=None):
+    def __init__(self, cfg, dev_weights: dict, wdtype: str = "f32", stream=None, path: str = "auto"):
+        """path: "auto" (persistent kernel where possible) or "per_kernel"."""
         L = lib()
         self.cfg = cfg
         self.wdtype = wdtype
@@ -157,8 +162,9 @@ class Model:
                     dev_weights["ln_f_w"].data_ptr(), dev_weights["ln_f_b"].data_ptr(),
                     ctypes.cast(layers, ctypes.POINTER(LayerWeights)))
         h = ctypes.c_void_p()
-        check(L.gpt2_create(ctypes.byref(c), ctypes.byref(w), WDTYPES[wdtype],
-                            _stream_handle(stream), ctypes.byref(h)), "gpt2_create")
+        flags = {"auto": 0, "per_kernel": 1}[path]
+        check(L.gpt2_create_ex(ctypes.byref(c), ctypes.byref(w), WDTYPES[wdtype], flags,
+                               _stream_handle(stream), ctypes.byref(h)), "gpt2_create_ex")
         self._h = h
 
     # ---- decoding ----
@@ -235,6 +241,16 @@ class Model:
         v = np.empty((H, n_rows, D), np.float32)
         check(lib().gpt2_export_kv(self._h, layer, n_rows, _ptr(k), _ptr(v)), "gpt2_export_kv")
         return k, v
+
+    def path(self) -> str:
+        p = ctypes.c_int32()
+        check(lib().gpt2_path(self._h, ctypes.byref(p)), "gpt2_path")
+        return "persistent" if p.value == 1 else "per_kernel"
+
+    def launch_count(self) -> int:
+        n = ctypes.c_uint64()
+        check(lib().gpt2_launch_count(self._h, ctypes.byref(n)), "gpt2_launch_count")
+        return int(n.value)
 
     def kernels_per_step(self) -> int:
         n = ctypes.c_int32()

@@ -4,6 +4,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -11,6 +12,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "persistent.h"
 
 using namespace gpt2;
 
@@ -64,9 +66,19 @@ struct gpt2_model {
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
     int kernels_per_step = 0;
+    // persistent path
+    bool persistent = false;
+    PPhase *d_phases = nullptr;
+    int32_t *prompt_buf = nullptr;
+    uint64_t *ll_base = nullptr;
+    size_t ll_bytes = 0;
+    PersistArgs pargs{};
+    int p_grid = 0;
+    size_t p_smem = 0;
     // host view of the cache
     int cached = 0;
     bool has_step = false;
+    unsigned long long launches = 0;
 };
 
 namespace {
@@ -277,17 +289,231 @@ int read_state(gpt2_model *m, DeviceState *hs)
     TRY_CUDA(cudaMemcpy(hs, m->st, sizeof *hs, cudaMemcpyDeviceToHost));
     if (hs->err != kDevErrNone) {
         const int err = hs->err;
-        // report once, then clear so the model stays usable
-        TRY_CUDA(cudaMemset(&m->st->err, 0, 2 * sizeof(int32_t)));
+        // report once, then clear so the model stays usable: the error word,
+        // the abort word, and every tagged activation (stale epochs)
+        TRY_CUDA(cudaMemset(&m->st->err, 0, 3 * sizeof(int32_t)));
+        if (m->ll_base) TRY_CUDA(cudaMemset(m->ll_base, 0, m->ll_bytes));
         return err == kDevErrTimeout ? GPT2_ERR_TIMEOUT : GPT2_ERR_DEVICE_STATE;
     }
     return GPT2_OK;
 }
 
+int launch_persist(gpt2_model *m, int n_steps, const int32_t *prompt, int n_prompt, int tok_first, int pos0)
+{
+    PersistArgs a = m->pargs;
+    a.n_steps = n_steps;
+    a.prompt = prompt;
+    a.n_prompt = n_prompt;
+    a.tok_first = tok_first;
+    a.pos0 = pos0;
+    TRY_CUDA(launch_persistent(m->wdtype, a, m->p_grid, m->p_smem, m->stream));
+    m->launches += 1;
+    return GPT2_OK;
+}
+
 int launch_step(gpt2_model *m, int32_t token, int32_t position)
 {
+    if (m->persistent) return launch_persist(m, 1, nullptr, 1, token, position);
     TRY_CUDA(launch_set_state(m->st, token, position, kSetTokPos, m->out_ids, m->stream));
     TRY_CUDA(cudaGraphLaunch(m->exec, m->stream));
+    m->launches += 1 + m->kernels_per_step;
+    return GPT2_OK;
+}
+
+// Rows of each CTA and rows per ring stage of one persistent GEMV phase.
+void plan_phase(PPhase &ph, int wtype, int grid, uint32_t stage)
+{
+    const int gran = wtype == kWI4 ? 8 : 1;
+    int rpc = (ph.out + grid - 1) / grid;
+    rpc = (rpc + gran - 1) / gran * gran;
+    ph.rpc = rpc;
+    const uint32_t rb = wtype == kWF32 ? uint32_t(ph.in) * 4 : wtype == kWF16 ? uint32_t(ph.in) * 2 : uint32_t(ph.in) / 2;
+    const uint32_t G = uint32_t(ph.in) / 32, zb = uint32_t(ph.in) / 64;
+    auto a16 = [](uint32_t v) { return (v + 15u) / 16u * 16u; };
+    int chunk = std::max(gran, std::min(std::min(rpc, 8), int(stage / std::max(1u, rb)) / gran * gran));
+    for (;; chunk -= gran) {
+        uint32_t total;
+        if (wtype == kWI4) {
+            ph.stage_scale_off = a16(uint32_t(chunk) * rb);
+            ph.stage_zero_off = ph.stage_scale_off + a16(uint32_t(chunk) * G * 4);
+            total = ph.stage_zero_off + uint32_t(chunk) * zb;
+        } else {
+            ph.stage_scale_off = ph.stage_zero_off = 0;
+            total = uint32_t(chunk) * rb;
+        }
+        if (total <= stage || chunk <= gran) break;
+    }
+    ph.chunk_rows = chunk;
+}
+
+// Builds the phase table and launch arguments of the persistent kernel;
+// returns GPT2_OK, or a nonzero status if the path cannot run here (the
+// caller then uses the per-kernel path).
+int setup_persistent(gpt2_model *m, uint64_t *ll, int32_t *prompt_buf, PPhase *d_phases, float *fold)
+{
+    const gpt2_config &c = m->cfg;
+    const int L = c.n_layer, E = c.n_embd, H = c.n_head, D = E / H, V = c.vocab_size;
+    if (E > 4096) return GPT2_ERR_INVALID_ARG;        // LayerNorm pairs held in registers
+    const int F = 4 * E;
+    const uint32_t max_row = m->wdtype == GPT2_F32 ? uint32_t(F) * 4 : m->wdtype == GPT2_F16 ? uint32_t(F) * 2
+                                                                         : 8u * (uint32_t(F) / 2 + uint32_t(F) / 8 + uint32_t(F) / 64 + 32);
+    uint32_t stage = uint32_t(std::max(8, env_int("GPT2_P_STAGE_KB", 24))) * 1024u;
+    stage = std::max(stage, std::max(max_row, uint32_t(E) * 4));
+    stage = (stage + 127u) / 128u * 128u;
+    const int grid = m->num_sms;
+    std::vector<PPhase> ph;
+    ph.reserve(5 * L + 1);
+    int max_rows = 1;
+    for (int l = 0; l < L; ++l) {
+        const LayerDev &Ld = m->layers[l];
+        auto gemv = [&](int mode, const QMat &q, int in_buf, int in_src, int out_buf, const float *lw,
+                        const float *lb, const float *bias, float *c1) {
+            PPhase p{};
+            p.type = kPhGemv;
+            p.mode = mode;
+            p.layer = l;
+            p.in = q.in;
+            p.out = q.out;
+            p.in_buf = in_buf;
+            p.in_src = in_src;
+            p.out_buf = out_buf;
+            p.W = q.w;
+            p.scales = q.scales;
+            p.zeros = q.zeros;
+            p.ln_w = lw;
+            p.ln_b = lb;
+            p.bias = bias;
+            p.c1 = c1;
+            p.c2 = c1 ? c1 + q.out : nullptr;
+            plan_phase(p, m->wdtype, grid, stage);
+            max_rows = std::max(max_rows, p.rpc);
+            ph.push_back(p);
+        };
+        const int base = 5 * l;
+        float *fq = fold + size_t(l) * (3 * E + 4 * E) * 2, *ff = fq + 2 * 3 * E;
+        gemv(l == 0 ? kModeEmbLnBias : kModeLnBias, Ld.mat[GPT2_MAT_ATTN], kBufXA, l == 0 ? -1 : base - 1, kBufQKV,
+             Ld.ln1_w, Ld.ln1_b, Ld.attn_b, fq);
+        PPhase at{};
+        at.type = kPhAttn;
+        at.layer = l;
+        at.in_buf = kBufQKV;
+        at.in_src = base;
+        at.out_buf = kBufATT;
+        ph.push_back(at);
+        gemv(kModeBiasRes, Ld.mat[GPT2_MAT_PROJ], kBufATT, base + 1, kBufXB, nullptr, nullptr, Ld.proj_b, nullptr);
+        gemv(kModeLnBiasGelu, Ld.mat[GPT2_MAT_FC], kBufXB, base + 2, kBufH, Ld.ln2_w, Ld.ln2_b, Ld.fc_b, ff);
+        gemv(kModeBiasRes, Ld.mat[GPT2_MAT_MLP_PROJ], kBufH, base + 3, kBufXA, nullptr, nullptr, Ld.mlp_proj_b,
+             nullptr);
+    }
+    PPhase hd{};
+    hd.type = kPhHead;
+    hd.mode = kModeHead;
+    hd.layer = L;
+    hd.in = E;
+    hd.out = V;
+    hd.in_buf = kBufXA;
+    hd.in_src = 5 * L - 1;
+    hd.out_buf = -1;
+    hd.W = m->wte;
+    hd.ln_w = m->lnf_w;
+    hd.ln_b = m->lnf_b;
+    plan_phase(hd, kWF32, grid, stage);
+    ph.push_back(hd);
+    if (ph.size() > 63) return GPT2_ERR_INVALID_ARG;   // epochs keep the phase in 6 bits
+    // every shared-memory segment before the attention scratch stays 16-byte
+    // aligned (the query is read as float4): round the bias slots to 4
+    max_rows = (max_rows + 3) / 4 * 4;
+    if (max_rows > 512) return GPT2_ERR_INVALID_ARG;   // two bias slots per consumer thread
+    // a stage holds at least one chunk of every phase
+    for (const PPhase &p : ph) {
+        if (p.type == kPhAttn) continue;
+        const int wt = p.type == kPhHead ? int(kWF32) : m->wdtype;
+        const uint32_t rb = wt == kWF32 ? uint32_t(p.in) * 4 : wt == kWF16 ? uint32_t(p.in) * 2 : uint32_t(p.in) / 2;
+        uint32_t need = uint32_t(p.chunk_rows) * rb;
+        if (wt == kWI4) need = p.stage_zero_off + uint32_t(p.chunk_rows) * uint32_t(p.in / 64);
+        if (need > stage) return GPT2_ERR_INVALID_ARG;
+    }
+
+    PersistArgs &a = m->pargs;
+    a = PersistArgs{};
+    a.phases = d_phases;
+    a.n_phases = int(ph.size());
+    for (int b = 0; b < kNumLL; ++b) a.ll[b] = nullptr;
+    a.ll[kBufXA] = ll;
+    a.ll[kBufXB] = ll + E;
+    a.ll[kBufQKV] = ll + 2 * E;
+    a.ll[kBufATT] = ll + 5 * E;
+    a.ll[kBufH] = ll + 6 * E;
+    a.ll_tok = ll + 10 * E;
+    a.kcache = m->kcache;
+    a.vcache = m->vcache;
+    a.logits = m->logits;
+    a.partials = m->partials;
+    a.counter = m->counter;
+    a.out_ids = m->out_ids;
+    a.out_cap = m->out_cap;
+    a.st = m->st;
+    a.wte = m->wte;
+    a.wpe = m->wpe;
+    a.E = E;
+    a.H = H;
+    a.D = D;
+    a.P = c.n_positions;
+    a.V = V;
+    a.scale = float(1.0 / std::sqrt(double(D)));
+    a.eps = c.ln_eps;
+    a.max_rows = max_rows;
+    a.stage_bytes = stage;
+    {
+        const char *fr = std::getenv("GPT2_HEAD_L2_FRAC");
+        float f = fr ? float(std::atof(fr)) : 0.0f;   // measured: no gain on GB300, off by default
+        a.head_l2_frac = f < 0.f ? 0.f : (f > 1.f ? 1.f : f);
+    }
+    a.block_mode = env_int("GPT2_BLOCK_MODE", 0) ? 1 : 0;
+    const size_t fixed = persistent_fixed_smem(E, D, max_rows);
+    a.ring_offset = uint32_t((fixed + 127) / 128 * 128);
+    int optin = 0;
+    TRY_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, m->device));
+    const size_t limit = size_t(optin) - 4096;       // leave room for static shared memory
+    if (a.ring_offset + 2 * size_t(stage) > limit) return GPT2_ERR_INVALID_ARG;
+    int ns = int((limit - a.ring_offset) / stage);
+    ns = std::min(ns, std::min(kMaxRing, std::max(2, env_int("GPT2_P_STAGES", kMaxRing))));
+    if (ns < 5) return GPT2_ERR_INVALID_ARG;   // a warp holds up to 4 stages at once; one more keeps the stream going
+    a.n_stages = ns;
+    m->p_smem = a.ring_offset + size_t(ns) * stage;
+    int blocks = 0;
+    TRY_CUDA(persistent_blocks_per_sm(m->wdtype, D, m->p_smem, limit, &blocks));
+    if (blocks < 1) return GPT2_ERR_INVALID_ARG;
+    int coop = 0;
+    TRY_CUDA(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, m->device));
+    if (!coop) return GPT2_ERR_UNSUPPORTED_DEVICE;
+    // block phases hold their whole row slice: at most kMaxBlockRows rows, in stages that fit the ring
+    for (const PPhase &p : ph) {
+        if (p.type != kPhGemv) continue;
+        if (p.rpc > kMaxBlockRows) return GPT2_ERR_INVALID_ARG;
+        if ((p.rpc + p.chunk_rows - 1) / p.chunk_rows > ns - 1) return GPT2_ERR_INVALID_ARG;
+    }
+    // LayerNorm folded into the QKV and fc matrices, from the weights as stored
+    {
+        float *tmp = nullptr;
+        TRY_CUDA(cudaMalloc(&tmp, size_t(4 * E) * E * 4));
+        cudaError_t e = cudaSuccess;
+        for (const PPhase &p : ph) {
+            if (p.type != kPhGemv || !p.c1 || e != cudaSuccess) continue;
+            e = dequant_to_f32(m->wdtype, p.W, p.scales, p.zeros, p.in, p.out, tmp, m->stream);
+            if (e == cudaSuccess) e = ln_fold(tmp, p.ln_w, p.ln_b, p.in, p.out, const_cast<float *>(p.c1),
+                                              const_cast<float *>(p.c2), m->stream);
+        }
+        if (e == cudaSuccess) e = cudaStreamSynchronize(m->stream);
+        cudaFree(tmp);
+        TRY_CUDA(e);
+    }
+    m->p_grid = grid;
+    TRY_CUDA(cudaMemcpy(d_phases, ph.data(), ph.size() * sizeof(PPhase), cudaMemcpyHostToDevice));
+    m->d_phases = d_phases;
+    m->prompt_buf = prompt_buf;
+    m->ll_base = ll;
+    m->persistent = true;
     return GPT2_OK;
 }
 
@@ -314,11 +540,18 @@ const char *gpt2_strerror(int status)
 
 int gpt2_create(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype, void *stream, gpt2_model **out)
 {
+    return gpt2_create_ex(cfg, w, wdtype, 0, stream, out);
+}
+
+int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype, int32_t flags, void *stream,
+                   gpt2_model **out)
+{
     if (!out) return GPT2_ERR_INVALID_ARG;
     *out = nullptr;
     int rc = check_config(cfg, wdtype);
     if (rc != GPT2_OK) return rc;
     if (!w || !w->layers) return GPT2_ERR_INVALID_ARG;
+    if (flags & ~int32_t(GPT2_FLAG_PER_KERNEL)) return GPT2_ERR_INVALID_ARG;
     int dev;
     TRY_CUDA(cudaGetDevice(&dev));
     cudaDeviceProp prop;
@@ -396,6 +629,11 @@ int gpt2_create(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype, v
     const size_t o_ids = take(size_t(m->out_cap) * 4);
     const size_t o_part = take(size_t(m->max_head_ctas) * 8);
     const size_t o_cnt = take(16);
+    const size_t ll_bytes = (size_t(10) * E + 1) * 8;
+    const size_t o_ll = take(ll_bytes);
+    const size_t o_prompt = take(size_t(P) * 4);
+    const size_t o_phases = take(size_t(5 * L + 1) * sizeof(PPhase));
+    const size_t o_fold = take(size_t(L) * (3 * E + 4 * E) * 2 * 4);
     m->work_bytes = off;
 
     cudaError_t e = cudaMalloc(&m->arena, m->arena_bytes);
@@ -496,6 +734,29 @@ int gpt2_create(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype, v
         free_model(m);
         return rc;
     }
+    const char *path = std::getenv("GPT2_PATH");
+    const bool want_persistent = !(flags & GPT2_FLAG_PER_KERNEL) && !(path && std::strcmp(path, "graph") == 0);
+    if (want_persistent) {
+        m->ll_bytes = ll_bytes;
+        rc = setup_persistent(m, reinterpret_cast<uint64_t *>(W + o_ll), reinterpret_cast<int32_t *>(W + o_prompt),
+                              reinterpret_cast<PPhase *>(W + o_phases), reinterpret_cast<float *>(W + o_fold));
+        if (rc != GPT2_OK) {            // fall back to the per-kernel graph (another GPU path)
+            if (env_int("GPT2_DEBUG", 0))
+                std::fprintf(stderr, "gpt2: persistent path unavailable (%s: %s)\n", gpt2_strerror(rc),
+                             cudaGetErrorString(cudaGetLastError()));
+            cudaGetLastError();
+            m->persistent = false;
+            m->ll_base = nullptr;
+        }
+    }
+    // state: the epoch sequence starts at 1 (tagged words are zero)
+    DeviceState init{};
+    init.seq = 1;
+    rc = cuda_status(cudaMemcpy(m->st, &init, sizeof init, cudaMemcpyHostToDevice));
+    if (rc != GPT2_OK) {
+        free_model(m);
+        return rc;
+    }
     *out = m;
     return GPT2_OK;
 }
@@ -535,6 +796,14 @@ int gpt2_prefill(gpt2_model *m, const int32_t *host_ids, int32_t n)
     for (int i = 0; i < n; ++i)
         if (host_ids[i] < 0 || host_ids[i] >= m->cfg.vocab_size) return GPT2_ERR_TOKEN_RANGE;
     gpt2_reset(m);
+    if (m->persistent) {
+        TRY_CUDA(cudaMemcpyAsync(m->prompt_buf, host_ids, size_t(n) * 4, cudaMemcpyHostToDevice, m->stream));
+        int rc = launch_persist(m, n, m->prompt_buf, n, 0, 0);
+        if (rc != GPT2_OK) return rc;
+        m->cached = n;
+        m->has_step = true;
+        return GPT2_OK;
+    }
     for (int i = 0; i < n; ++i) {
         int rc = gpt2_decode_step(m, host_ids[i], i, nullptr);
         if (rc != GPT2_OK) return rc;
@@ -558,7 +827,14 @@ int gpt2_decode_greedy(gpt2_model *m, int32_t n_steps)
     if (!m || n_steps < 0) return GPT2_ERR_INVALID_ARG;
     if (!m->has_step) return GPT2_ERR_NOT_READY;
     if ((long long)m->cached + n_steps > m->cfg.n_positions) return GPT2_ERR_POSITION_RANGE;
-    for (int i = 0; i < n_steps; ++i) TRY_CUDA(cudaGraphLaunch(m->exec, m->stream));
+    if (n_steps == 0) return GPT2_OK;
+    if (m->persistent) {
+        int rc = launch_persist(m, n_steps, nullptr, 0, 0, m->cached);
+        if (rc != GPT2_OK) return rc;
+    } else {
+        for (int i = 0; i < n_steps; ++i) TRY_CUDA(cudaGraphLaunch(m->exec, m->stream));
+        m->launches += (unsigned long long)n_steps * m->kernels_per_step;
+    }
     m->cached += n_steps;
     return GPT2_OK;
 }
@@ -568,11 +844,27 @@ int gpt2_generate(gpt2_model *m, const int32_t *host_prompt, int32_t n_prompt, i
 {
     if (!m || !host_prompt || !host_out || n_steps < 0) return GPT2_ERR_INVALID_ARG;
     if (n_prompt < 1 || (long long)n_prompt + n_steps > m->cfg.n_positions) return GPT2_ERR_POSITION_RANGE;
-    int rc = gpt2_prefill(m, host_prompt, n_prompt);
-    if (rc != GPT2_OK) return rc;
-    TRY_CUDA(launch_set_state(m->st, 0, 0, kSeedOutWithNext, m->out_ids, m->stream));
-    rc = gpt2_decode_greedy(m, n_steps);
-    if (rc != GPT2_OK) return rc;
+    for (int i = 0; i < n_prompt; ++i)
+        if (host_prompt[i] < 0 || host_prompt[i] >= m->cfg.vocab_size) return GPT2_ERR_TOKEN_RANGE;
+    int rc;
+    if (m->persistent) {
+        gpt2_reset(m);
+        TRY_CUDA(launch_set_state(m->st, 0, 0, kResetOut, m->out_ids, m->stream));
+        TRY_CUDA(cudaMemcpyAsync(m->prompt_buf, host_prompt, size_t(n_prompt) * 4, cudaMemcpyHostToDevice,
+                                 m->stream));
+        rc = launch_persist(m, n_prompt + n_steps, m->prompt_buf, n_prompt, 0, 0);
+        if (rc != GPT2_OK) return rc;
+        m->launches += 1;
+        m->cached = n_prompt + n_steps;
+        m->has_step = true;
+    } else {
+        rc = gpt2_prefill(m, host_prompt, n_prompt);
+        if (rc != GPT2_OK) return rc;
+        TRY_CUDA(launch_set_state(m->st, 0, 0, kSeedOutWithNext, m->out_ids, m->stream));
+        m->launches += 1;
+        rc = gpt2_decode_greedy(m, n_steps);
+        if (rc != GPT2_OK) return rc;
+    }
     TRY_CUDA(cudaMemcpyAsync(host_out, m->out_ids, size_t(n_steps + 1) * 4, cudaMemcpyDeviceToHost, m->stream));
     DeviceState hs;
     return read_state(m, &hs);
@@ -648,7 +940,21 @@ int gpt2_export_kv(gpt2_model *m, int32_t layer, int32_t n_rows, float *dst_k, f
 int gpt2_kernels_per_step(const gpt2_model *m, int32_t *count)
 {
     if (!m || !count) return GPT2_ERR_INVALID_ARG;
-    *count = m->kernels_per_step;
+    *count = m->persistent ? 1 : m->kernels_per_step;
+    return GPT2_OK;
+}
+
+int gpt2_launch_count(const gpt2_model *m, uint64_t *count)
+{
+    if (!m || !count) return GPT2_ERR_INVALID_ARG;
+    *count = m->launches;
+    return GPT2_OK;
+}
+
+int gpt2_path(const gpt2_model *m, int32_t *path)
+{
+    if (!m || !path) return GPT2_ERR_INVALID_ARG;
+    *path = m->persistent ? GPT2_PATH_PERSISTENT : GPT2_PATH_PER_KERNEL;
     return GPT2_OK;
 }
 

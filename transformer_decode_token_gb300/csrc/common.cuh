@@ -38,7 +38,8 @@ struct DeviceState {
     int32_t n_out;      // number of ids appended to out_ids
     int32_t err;        // first recorded kDevErr* code (0 = none)
     int32_t err_info;   // where it happened (kernel-specific)
-    int32_t pad[2];
+    int32_t abort;      // persistent kernel: a CTA gave up, every CTA returns
+    int32_t seq;        // persistent kernel: passes run so far + 1 (epoch base)
 };
 
 __device__ __forceinline__ void record_error(DeviceState *st, int32_t code, int32_t info)
@@ -87,6 +88,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Non-blocking test of phase `parity`: true if it has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_addr(bar)), "r"(parity)

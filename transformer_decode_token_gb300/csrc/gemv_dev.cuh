@@ -22,18 +22,26 @@ inline __host__ __device__ uint32_t vec_region_bytes(int in)
     return align_up(uint32_t(in + in / 32) * 4u, 128u);   // x (in floats) + per-group sums
 }
 
-// Dot product of one stored row (in shared memory) with the input vector,
-// partial per lane: the caller sums over the warp.
+// Units a row is split into for the lanes: 16-byte vectors for fp32 / fp16,
+// 32-bit words (8 codes) for int4.
 template <int WT>
-__device__ __forceinline__ float row_dot(const uint8_t *stg, int rl, int in, const float *xs, const float *xsum,
-                                         uint32_t soff, uint32_t zoff, int lane)
+__host__ __device__ __forceinline__ int row_units(int in)
+{
+    return WT == kWF32 ? in >> 2 : in >> 3;
+}
+
+// Partial dot product over units [vb, ve) of one stored row; see row_dot.
+template <int WT>
+__device__ __forceinline__ float row_dot_range(const uint8_t *stg, int rl, int in, const float *xs,
+                                               const float *xsum, uint32_t soff, uint32_t zoff, int lane, int vb,
+                                               int ve)
 {
     float acc = 0.f;
     const float4 *x4 = reinterpret_cast<const float4 *>(xs);
     if (WT == kWF32) {
         const float4 *w = reinterpret_cast<const float4 *>(stg + size_t(rl) * in * 4);
-        const int nv = in >> 2;
-        for (int v = lane; v < nv; v += 32) {
+        const int nv = ve;
+        for (int v = vb + lane; v < nv; v += 32) {
             const float4 a = w[v], b = x4[v];
             acc = fmaf(a.x, b.x, acc);
             acc = fmaf(a.y, b.y, acc);
@@ -42,8 +50,8 @@ __device__ __forceinline__ float row_dot(const uint8_t *stg, int rl, int in, con
         }
     } else if (WT == kWF16) {
         const uint4 *w = reinterpret_cast<const uint4 *>(stg + size_t(rl) * in * 2);
-        const int nv = in >> 3;
-        for (int v = lane; v < nv; v += 32) {
+        const int nv = ve;
+        for (int v = vb + lane; v < nv; v += 32) {
             const uint4 r = w[v];
             const float4 b0 = x4[2 * v], b1 = x4[2 * v + 1];
             const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&r.x));
@@ -66,8 +74,8 @@ __device__ __forceinline__ float row_dot(const uint8_t *stg, int rl, int in, con
         const uint32_t *w = reinterpret_cast<const uint32_t *>(stg + size_t(rl) * (in >> 1));
         const float *sc = reinterpret_cast<const float *>(stg + soff) + size_t(rl) * G;
         const uint8_t *zp = stg + zoff + size_t(rl) * (in >> 6);
-        const int nw = in >> 3;
-        for (int v = lane; v < nw; v += 32) {
+        const int nw = ve;
+        for (int v = vb + lane; v < nw; v += 32) {
             const uint32_t q = w[v];
             const int g = v >> 2;
             const float4 b0 = x4[2 * v], b1 = x4[2 * v + 1];
@@ -90,6 +98,13 @@ __device__ __forceinline__ float row_dot(const uint8_t *stg, int rl, int in, con
         }
     }
     return acc;
+}
+
+template <int WT>
+__device__ __forceinline__ float row_dot(const uint8_t *stg, int rl, int in, const float *xs, const float *xsum,
+                                         uint32_t soff, uint32_t zoff, int lane)
+{
+    return row_dot_range<WT>(stg, rl, in, xs, xsum, soff, zoff, lane, 0, row_units<WT>(in));
 }
 
 

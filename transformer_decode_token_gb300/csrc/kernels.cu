@@ -449,6 +449,7 @@ __global__ void k_set_state(DeviceState *st, int32_t tok, int32_t pos, int32_t f
     if (flags & kClearErr) {
         st->err = 0;
         st->err_info = 0;
+        st->abort = 0;
     }
     if (flags & kSetTokPos) {
         st->tok = tok;
