@@ -51,8 +51,8 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="CPU time budget of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--path", choices=["auto", "per_kernel"], default="auto",
-                   help="auto: the persistent decode kernel where the device allows it")
+    p.add_argument("--path", choices=["auto", "persistent", "per_kernel"], default="auto",
+                   help="auto: the cluster decode kernel where the device allows it")
     a = p.parse_args()
     if a.warmup < 3:
         p.error("--warmup must be >= 3")
@@ -157,7 +157,8 @@ def measured_peaks():
 
 
 def load_traffic():
-    """DRAM bytes per decode pass from the committed ncu summary, if any."""
+    """DRAM bytes per decode pass from the committed ncu summaries, by path and
+    weight type ({path: {wdtype: bytes}}), if any."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
@@ -327,10 +328,13 @@ def main():
     alg = roofline.mean_bytes_per_token(cfg, args.wdtype, positions)
     peaks, peak_kind = measured_peaks()
     achieved = alg / (ms / 1e3 / args.steps) / 1e9
-    traffic = load_traffic().get(args.wdtype)
-    kernel = ("k_decode_persistent: one cooperative launch per call (one per 60-step cycle here, "
-              "a host-fed pass + 59 device-fed passes), one CTA per SM" if path == "persistent" else
-              f"decode pass: one CUDA graph of {kps} kernels (PDL-chained)")
+    traffic = load_traffic().get(path, {}).get(args.wdtype)
+    kernel = {
+        "cluster": "k_decode_cluster: one cooperative launch per call (one per 60-step cycle here, "
+                   "a host-fed pass + 59 device-fed passes), clusters of 4 CTAs, one CTA per SM",
+        "persistent": "k_decode_persistent: one cooperative launch per call (one per 60-step cycle here, "
+                      "a host-fed pass + 59 device-fed passes), one CTA per SM",
+    }.get(path, f"decode pass: one CUDA graph of {kps} kernels (PDL-chained)")
     roof = {"bound": "hbm", "kernel": kernel,
             "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"], "peak_kind": f"{peak_kind} copy bandwidth",

@@ -124,22 +124,34 @@ typedef struct gpt2_model gpt2_model;
 int gpt2_create(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
                 void *stream, gpt2_model **out);
 
-/* gpt2_create with options.  flags = 0 is gpt2_create.  By default a model
- * runs its passes in the persistent decode kernel: one cooperative launch per
- * call, one CTA per SM, which streams every pass's weights through shared
- * memory and passes activations between CTAs as value+epoch words (greedy
- * steps never return to the host).  GPT2_FLAG_PER_KERNEL selects the
- * per-kernel path instead: the captured CUDA graph of 5 * n_layer + 1 kernels
- * per pass.  The persistent path is also left out (per-kernel used) when the
- * device cannot co-schedule one such CTA per SM or n_embd > 4096; the
- * environment variable GPT2_PATH=graph forces the per-kernel path.  Both paths
- * compute the same pass; gpt2_path reports which one a model uses. */
+/* gpt2_create with options.  flags = 0 is gpt2_create.  Three paths compute
+ * the same pass (the decode forward pass of "The Illustrated GPT-2", "Model
+ * Output" and "Self-Attention" sections; greedy choice as in "model.fir"):
+ *  - cluster (default): one cooperative launch per call of a kernel whose
+ *    CTAs form clusters of 4.  One cluster per attention head computes that
+ *    head's q, k, v, attention and its share of the output projection,
+ *    trading values inside the cluster through distributed shared memory; the
+ *    other CTAs own slices of the MLP.  Residual sums between the two groups
+ *    are fixed-point integer atomics, so runs are bitwise reproducible; two
+ *    GPU-wide exchanges per block.  Greedy steps never return to the host.
+ *  - persistent (GPT2_FLAG_NO_CLUSTER, or GPT2_PATH=persistent): one
+ *    cooperative launch per call, one CTA per SM, weights streamed through
+ *    shared memory, activations passed between CTAs as value+epoch words
+ *    (five GPU-wide exchanges per block).
+ *  - per-kernel (GPT2_FLAG_PER_KERNEL, or GPT2_PATH=graph): the captured CUDA
+ *    graph of 5 * n_layer + 1 kernels per pass.
+ * A path that cannot run on the device or configuration (too few
+ * co-resident clusters, n_embd not a multiple of 64 for the cluster kernel,
+ * n_embd > 4096 for the persistent kernel) is left out and the next one is
+ * used; gpt2_path reports which one a model uses. */
 #define GPT2_FLAG_PER_KERNEL 1
+#define GPT2_FLAG_NO_CLUSTER 2
 int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
                    int32_t flags, void *stream, gpt2_model **out);
 
 #define GPT2_PATH_PER_KERNEL 0
 #define GPT2_PATH_PERSISTENT 1
+#define GPT2_PATH_CLUSTER 2
 int gpt2_path(const gpt2_model *m, int32_t *path);
 
 /* Frees every device buffer and the graph.  NULL is accepted. */

@@ -19,13 +19,14 @@ from gpu_util import check_rows, max_abs, teacher_forced, top2_margin
 pytestmark = pytest.mark.gpu
 
 TOL = {"f32": (1e-3, 1e-4), "f16": (2e-3, None), "int4": (2e-3, None)}
-PATHS = ["persistent", "per_kernel"]
+PATHS = ["cluster", "persistent", "per_kernel"]
+_BINDING_PATH = {"cluster": "auto", "persistent": "persistent", "per_kernel": "per_kernel"}
 _cache = {}
 _oracle_cache = {}
 
 
 def model(cfg, dw, wdtype, path):
-    m = binding.Model(cfg, dw, wdtype, path="auto" if path == "persistent" else "per_kernel")
+    m = binding.Model(cfg, dw, wdtype, path=_BINDING_PATH[path])
     assert m.path() == path
     return m
 
@@ -85,8 +86,9 @@ def test_small_fp16_full_context(path):
 
 @pytest.mark.parametrize("wdtype", ["f32", "int4"])
 def test_paths_agree(wdtype):
-    """The persistent kernel and the per-kernel graph compute the same pass
-    (same row dot products; attention merges its warps in a different order)."""
+    """The three paths compute the same pass: the same row dot products up to
+    summation order (the cluster kernel adds the residual stream as
+    fixed-point integers, the others in fp32)."""
     cfg = synth.SMALL
     _, dw = weights(cfg)
     prompt = synth.make_prompt(cfg, 10, 1)
@@ -96,8 +98,9 @@ def test_paths_agree(wdtype):
         ids = m.generate(prompt, 30)
         out[path] = (ids, m.logits())
         m.close()
-    assert max_abs(out["persistent"][1], out["per_kernel"][1]) <= 1e-4
-    assert out["persistent"][0] == out["per_kernel"][0]
+    for path in PATHS[:-1]:
+        assert max_abs(out[path][1], out["per_kernel"][1]) <= 1e-4, path
+        assert out[path][0] == out["per_kernel"][0], path
 
 
 # ---- stored weights -----------------------------------------------------------

@@ -148,7 +148,9 @@ class Model:
     """One GPT-2 decode model on the current CUDA device."""
 
     def __init__(self, cfg, dev_weights: dict, wdtype: str = "f32", stream=None, path: str = "auto"):
-        """path: "auto" (persistent kernel where possible) or "per_kernel"."""
+        """path: "auto" (cluster kernel where possible, else the persistent
+        kernel, else the per-kernel graph), "persistent" (skip the cluster
+        kernel) or "per_kernel"."""
         L = lib()
         self.cfg = cfg
         self.wdtype = wdtype
@@ -162,7 +164,7 @@ class Model:
                     dev_weights["ln_f_w"].data_ptr(), dev_weights["ln_f_b"].data_ptr(),
                     ctypes.cast(layers, ctypes.POINTER(LayerWeights)))
         h = ctypes.c_void_p()
-        flags = {"auto": 0, "per_kernel": 1}[path]
+        flags = {"auto": 0, "persistent": 2, "per_kernel": 1}[path]
         check(L.gpt2_create_ex(ctypes.byref(c), ctypes.byref(w), WDTYPES[wdtype], flags,
                                _stream_handle(stream), ctypes.byref(h)), "gpt2_create_ex")
         self._h = h
@@ -245,7 +247,7 @@ class Model:
     def path(self) -> str:
         p = ctypes.c_int32()
         check(lib().gpt2_path(self._h, ctypes.byref(p)), "gpt2_path")
-        return "persistent" if p.value == 1 else "per_kernel"
+        return {0: "per_kernel", 1: "persistent", 2: "cluster"}[p.value]
 
     def launch_count(self) -> int:
         n = ctypes.c_uint64()

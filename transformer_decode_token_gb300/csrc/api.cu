@@ -10,6 +10,7 @@
 #include <new>
 #include <vector>
 
+#include "cluster.h"
 #include "common.cuh"
 #include "kernels.h"
 #include "persistent.h"
@@ -75,6 +76,14 @@ struct gpt2_model {
     PersistArgs pargs{};
     int p_grid = 0;
     size_t p_smem = 0;
+    // cluster path (uses the prompt buffer of the persistent path)
+    bool cluster = false;
+    uint8_t *cbuf = nullptr;         // tiled matrices, sums, counters, token word, layer table
+    uint8_t *c_state = nullptr;      // sums + counters + token word (zeroed together)
+    size_t c_state_bytes = 0;
+    ClusterArgs cargs{};
+    int c_clusters = 0;
+    size_t c_smem = 0;
     // host view of the cache
     int cached = 0;
     bool has_step = false;
@@ -280,6 +289,7 @@ void free_model(gpt2_model *m)
     if (m->graph) cudaGraphDestroy(m->graph);
     if (m->arena) cudaFree(m->arena);
     if (m->work) cudaFree(m->work);
+    if (m->cbuf) cudaFree(m->cbuf);
     delete m;
 }
 
@@ -293,6 +303,11 @@ int read_state(gpt2_model *m, DeviceState *hs)
         // the abort word, and every tagged activation (stale epochs)
         TRY_CUDA(cudaMemset(&m->st->err, 0, 3 * sizeof(int32_t)));
         if (m->ll_base) TRY_CUDA(cudaMemset(m->ll_base, 0, m->ll_bytes));
+        if (m->cluster) {   // sums and counters restart with the sequence
+            const int32_t one = 1;
+            TRY_CUDA(cudaMemset(m->c_state, 0, m->c_state_bytes));
+            TRY_CUDA(cudaMemcpy(&m->st->seq, &one, sizeof one, cudaMemcpyHostToDevice));
+        }
         return err == kDevErrTimeout ? GPT2_ERR_TIMEOUT : GPT2_ERR_DEVICE_STATE;
     }
     return GPT2_OK;
@@ -306,7 +321,17 @@ int launch_persist(gpt2_model *m, int n_steps, const int32_t *prompt, int n_prom
     a.n_prompt = n_prompt;
     a.tok_first = tok_first;
     a.pos0 = pos0;
-    TRY_CUDA(launch_persistent(m->wdtype, a, m->p_grid, m->p_smem, m->stream));
+    if (m->cluster) {
+        ClusterArgs c = m->cargs;
+        c.n_steps = n_steps;
+        c.prompt = prompt;
+        c.n_prompt = n_prompt;
+        c.tok_first = tok_first;
+        c.pos0 = pos0;
+        TRY_CUDA(launch_cluster(m->wdtype, c, m->c_clusters, m->c_smem, m->stream));
+    } else {
+        TRY_CUDA(launch_persistent(m->wdtype, a, m->p_grid, m->p_smem, m->stream));
+    }
     m->launches += 1;
     return GPT2_OK;
 }
@@ -517,6 +542,182 @@ int setup_persistent(gpt2_model *m, uint64_t *ll, int32_t *prompt_buf, PPhase *d
     return GPT2_OK;
 }
 
+// Sets up the cluster decode kernel (cluster.cu): tiled copies of the two
+// projection matrices, the fixed-point sums and their counters, and the
+// launch shape.  Returns GPT2_OK, or a nonzero status if the path cannot run
+// here (the caller then keeps the persistent kernel).
+int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
+{
+    const gpt2_config &c = m->cfg;
+    const int L = c.n_layer, E = c.n_embd, H = c.n_head, D = E / H, V = c.vocab_size, F = 4 * E;
+    const int wt = m->wdtype;
+    if (E % 64) return GPT2_ERR_INVALID_ARG;   // E/4 tile rows in chunks of 16
+    if (E > 2048) return GPT2_ERR_INVALID_ARG;  // sums read 8 words per thread
+    int optin = 0, coop = 0;
+    TRY_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, m->device));
+    TRY_CUDA(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, m->device));
+    if (!coop) return GPT2_ERR_UNSUPPORTED_DEVICE;
+    const size_t limit = size_t(optin) - 4096;   // room for static shared memory
+    const int ns = kClusterRing;
+    // co-resident clusters at (nearly) the full shared-memory size
+    int max_clusters = 0;
+    TRY_CUDA(cluster_max_active(wt, D, limit, limit, &max_clusters));
+    // fc CTAs: a multiple of the cluster size, each owning fr = F / nfc fc rows
+    // (a multiple of one int4 group)
+    int nfc = 0;
+    for (int n = (max_clusters - H) * kClusterSize; n >= kClusterSize; n -= kClusterSize)
+        if (F % n == 0 && (F / n) % 32 == 0) {
+            nfc = n;
+            break;
+        }
+    if (nfc == 0) return GPT2_ERR_INVALID_ARG;
+    const int fr = F / nfc;
+    const int n_clusters = H + nfc / kClusterSize, grid = n_clusters * kClusterSize;
+    if (grid > m->max_head_ctas) return GPT2_ERR_INVALID_ARG;   // per-CTA argmax slots
+    const size_t fixed = cluster_fixed_smem(E, D, fr, L);
+    const uint32_t ring_offset = uint32_t((fixed + 127) / 128 * 128);
+    if (ring_offset >= limit) return GPT2_ERR_INVALID_ARG;
+    const uint32_t stage = uint32_t((limit - ring_offset) / ns) / 16u * 16u;
+    // every segment's smallest chunk fits a stage
+    auto rbw = [&](int w, int n) {
+        return w == kWF32 ? uint32_t(n) * 4 : w == kWF16 ? uint32_t(n) * 2 : uint32_t(n) / 2;
+    };
+    const bool i4 = wt == kWI4;
+    uint32_t need = cluster_stage_need(1, uint32_t(E) * 4, 0, 0);   // LM head rows
+    need = std::max(need, cluster_stage_need(i4 ? 8 : 1, rbw(wt, E), i4 ? uint32_t(E / 32) * 4 : 0,
+                                             i4 ? uint32_t(E / 64) : 0));
+    for (int cols : {D, fr})
+        need = std::max(need, cluster_stage_need(i4 ? 16 : 1, rbw(wt, cols), i4 ? uint32_t(cols / 32) * 4 : 0,
+                                                 i4 ? uint32_t(cols / 32) : 0));
+    if (need > stage) return GPT2_ERR_INVALID_ARG;
+    m->c_smem = ring_offset + size_t(ns) * stage;
+    int fit = 0;
+    TRY_CUDA(cluster_max_active(wt, D, m->c_smem, limit, &fit));
+    if (fit < n_clusters) return GPT2_ERR_INVALID_ARG;
+
+    // ---- device buffer: tiles, then the zeroed state, then the layer table ----
+    const size_t mat_o = main_bytes_of(wt, E, E), mat_p = main_bytes_of(wt, F, E);
+    const size_t sc_o = i4 ? size_t(E) * (E / 32) * 4 : 0, zp_o = i4 ? size_t(E) * (E / 32) : 0;
+    const size_t sc_p = i4 ? size_t(E) * (F / 32) * 4 : 0, zp_p = i4 ? size_t(E) * (F / 32) : 0;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off += aup(bytes);
+        return o;
+    };
+    const size_t mat_q = main_bytes_of(wt, E, 3 * E);
+    const size_t sc_q = i4 ? size_t(3 * E) * (E / 32) * 4 : 0, zp_q = i4 ? size_t(3 * E) * (E / 64) : 0;
+    std::vector<size_t> o_wq(L), o_sq(L), o_zq(L), o_wo(L), o_so(L), o_zo(L), o_wp(L), o_sp(L), o_zp(L);
+    for (int l = 0; l < L; ++l) {
+        o_wq[l] = take(mat_q);
+        if (i4) {
+            o_sq[l] = take(sc_q);
+            o_zq[l] = take(zp_q);
+        }
+        o_wo[l] = take(mat_o);
+        o_wp[l] = take(mat_p);
+        if (i4) {
+            o_so[l] = take(sc_o);
+            o_zo[l] = take(zp_o);
+            o_sp[l] = take(sc_p);
+            o_zp[l] = take(zp_p);
+        }
+    }
+    const size_t o_state = off;
+    const size_t o_accn = take(size_t(2) * L * E * 8), o_accx = take(size_t(2) * L * E * 8);
+    const size_t o_cnt = take(size_t(2) * L * 4), o_tok = take(8);
+    const size_t state_bytes = off - o_state;
+    const size_t o_layers = take(sizeof(CLayer) * L);
+    uint8_t *B = nullptr;
+    TRY_CUDA(cudaMalloc(&B, off));
+    m->cbuf = B;
+    m->c_state = B + o_state;
+    m->c_state_bytes = state_bytes;
+    cudaStream_t s = m->stream;
+    std::vector<CLayer> cl(L);
+    for (int l = 0; l < L; ++l) {
+        const LayerDev &Ld = m->layers[l];
+        const QMat &qa = Ld.mat[GPT2_MAT_ATTN], &qo = Ld.mat[GPT2_MAT_PROJ], &qf = Ld.mat[GPT2_MAT_FC],
+                   &qp = Ld.mat[GPT2_MAT_MLP_PROJ];
+        CLayer &x = cl[l];
+        x = CLayer{};
+        x.Wqkv = B + o_wq[l];
+        x.qkv_s = i4 ? reinterpret_cast<const float *>(B + o_sq[l]) : nullptr;
+        x.qkv_z = i4 ? B + o_zq[l] : nullptr;
+        x.ln1_w = Ld.ln1_w;
+        x.ln1_b = Ld.ln1_b;
+        x.attn_b = Ld.attn_b;
+        x.Wo_t = B + o_wo[l];
+        x.o_s = i4 ? reinterpret_cast<const float *>(B + o_so[l]) : nullptr;
+        x.o_z = i4 ? B + o_zo[l] : nullptr;
+        x.proj_b = Ld.proj_b;
+        x.Wfc = qf.w;
+        x.fc_s = qf.scales;
+        x.fc_z = qf.zeros;
+        x.ln2_w = Ld.ln2_w;
+        x.ln2_b = Ld.ln2_b;
+        x.fc_b = Ld.fc_b;
+        x.Wp_t = B + o_wp[l];
+        x.p_s = i4 ? reinterpret_cast<const float *>(B + o_sp[l]) : nullptr;
+        x.p_z = i4 ? B + o_zp[l] : nullptr;
+        x.mlp_proj_b = Ld.mlp_proj_b;
+        TRY_CUDA(cluster_gather_qkv(wt, qa.w, qa.scales, qa.zeros, E, D, B + o_wq[l],
+                                    i4 ? reinterpret_cast<float *>(B + o_sq[l]) : nullptr, i4 ? B + o_zq[l] : nullptr,
+                                    s));
+        TRY_CUDA(cluster_tile(wt, qo.w, qo.scales, qo.zeros, E, H * kClusterSize, kClusterSize, E / kClusterSize, D,
+                              B + o_wo[l], i4 ? reinterpret_cast<float *>(B + o_so[l]) : nullptr,
+                              i4 ? B + o_zo[l] : nullptr, s));
+        TRY_CUDA(cluster_tile(wt, qp.w, qp.scales, qp.zeros, F, nfc, 1, E, fr, B + o_wp[l],
+                              i4 ? reinterpret_cast<float *>(B + o_sp[l]) : nullptr, i4 ? B + o_zp[l] : nullptr, s));
+    }
+    TRY_CUDA(cudaMemsetAsync(m->c_state, 0, state_bytes, s));
+    TRY_CUDA(cudaMemcpyAsync(B + o_layers, cl.data(), sizeof(CLayer) * L, cudaMemcpyHostToDevice, s));
+    TRY_CUDA(cudaStreamSynchronize(s));
+
+    ClusterArgs &a = m->cargs;
+    a = ClusterArgs{};
+    a.layers = reinterpret_cast<const CLayer *>(B + o_layers);
+    a.L = L;
+    a.E = E;
+    a.H = H;
+    a.D = D;
+    a.F = F;
+    a.P = c.n_positions;
+    a.V = V;
+    a.eps = c.ln_eps;
+    a.scale = float(1.0 / std::sqrt(double(D)));
+    a.nfc = nfc;
+    a.fr = fr;
+    a.head_rpc = (V + grid - 1) / grid;
+    a.pr_b0 = (std::max(3 * D, fr) + 3) / 4 * 4;
+    a.acc_new = reinterpret_cast<long long *>(B + o_accn);
+    a.acc_next = reinterpret_cast<long long *>(B + o_accx);
+    a.cnt_new = reinterpret_cast<unsigned int *>(B + o_cnt);
+    a.cnt_next = a.cnt_new + L;
+    a.ll_tok = reinterpret_cast<uint64_t *>(B + o_tok);
+    a.kcache = m->kcache;
+    a.vcache = m->vcache;
+    a.logits = m->logits;
+    a.partials = m->partials;
+    a.counter = m->counter;
+    a.out_ids = m->out_ids;
+    a.out_cap = m->out_cap;
+    a.st = m->st;
+    a.wte = m->wte;
+    a.wpe = m->wpe;
+    a.lnf_w = m->lnf_w;
+    a.lnf_b = m->lnf_b;
+    a.wtype = wt;
+    a.n_stages = ns;
+    a.stage_bytes = stage;
+    a.ring_offset = ring_offset;
+    m->c_clusters = n_clusters;
+    m->prompt_buf = prompt_buf;
+    m->cluster = true;
+    m->persistent = true;   // one launch per call, like the persistent kernel
+    return GPT2_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -551,7 +752,7 @@ int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype
     int rc = check_config(cfg, wdtype);
     if (rc != GPT2_OK) return rc;
     if (!w || !w->layers) return GPT2_ERR_INVALID_ARG;
-    if (flags & ~int32_t(GPT2_FLAG_PER_KERNEL)) return GPT2_ERR_INVALID_ARG;
+    if (flags & ~int32_t(GPT2_FLAG_PER_KERNEL | GPT2_FLAG_NO_CLUSTER)) return GPT2_ERR_INVALID_ARG;
     int dev;
     TRY_CUDA(cudaGetDevice(&dev));
     cudaDeviceProp prop;
@@ -736,7 +937,22 @@ int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype
     }
     const char *path = std::getenv("GPT2_PATH");
     const bool want_persistent = !(flags & GPT2_FLAG_PER_KERNEL) && !(path && std::strcmp(path, "graph") == 0);
-    if (want_persistent) {
+    const bool want_cluster = want_persistent && !(flags & GPT2_FLAG_NO_CLUSTER) &&
+                              !(path && std::strcmp(path, "persistent") == 0);
+    if (want_cluster) {
+        rc = setup_cluster(m, reinterpret_cast<int32_t *>(W + o_prompt));
+        if (rc != GPT2_OK) {            // keep the persistent kernel
+            if (env_int("GPT2_DEBUG", 0))
+                std::fprintf(stderr, "gpt2: cluster path unavailable (%s: %s)\n", gpt2_strerror(rc),
+                             cudaGetErrorString(cudaGetLastError()));
+            cudaGetLastError();
+            if (m->cbuf) cudaFree(m->cbuf);
+            m->cbuf = nullptr;
+            m->cluster = false;
+            m->persistent = false;
+        }
+    }
+    if (want_persistent && !m->cluster) {
         m->ll_bytes = ll_bytes;
         rc = setup_persistent(m, reinterpret_cast<uint64_t *>(W + o_ll), reinterpret_cast<int32_t *>(W + o_prompt),
                               reinterpret_cast<PPhase *>(W + o_phases), reinterpret_cast<float *>(W + o_fold));
@@ -954,7 +1170,7 @@ int gpt2_launch_count(const gpt2_model *m, uint64_t *count)
 int gpt2_path(const gpt2_model *m, int32_t *path)
 {
     if (!m || !path) return GPT2_ERR_INVALID_ARG;
-    *path = m->persistent ? GPT2_PATH_PERSISTENT : GPT2_PATH_PER_KERNEL;
+    *path = m->cluster ? GPT2_PATH_CLUSTER : m->persistent ? GPT2_PATH_PERSISTENT : GPT2_PATH_PER_KERNEL;
     return GPT2_OK;
 }
 

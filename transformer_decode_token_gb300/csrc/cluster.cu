@@ -1,0 +1,1379 @@
+// Cluster decode kernel: the decode pass with two GPU-wide exchanges per
+// transformer block.
+//
+// A pass needs the whole output vector of one step on every SM before the
+// next step can start (LayerNorm needs all of x, a linear needs all of its
+// input).  Measured on GB300, one such GPU-wide exchange costs ~2-3 us, so a
+// pass of 61 of them cannot be fast.  Here one block needs two:
+//
+//   head clusters (one per attention head, 4 CTAs):
+//     wait for x (GPU-wide) -> LN1 -> this head's q, k, v rows of the QKV
+//     matrix (a quarter per CTA) -> exchanged inside the cluster through
+//     distributed shared memory -> attention, positions split over the 4 CTAs,
+//     partial softmax states exchanged the same way -> the head's slice of
+//     the output projection (split-K by head: columns hD..hD+D, a quarter of
+//     the rows per CTA) -> added into x_new
+//   fc clusters (the other CTAs):
+//     wait for x_new (GPU-wide) -> LN2 -> fr rows of the fc matrix, gelu_new ->
+//     the matching fr columns of the MLP projection (split-K) -> added into
+//     the next x
+//   every CTA: wait for the last x -> LN_f -> its rows of the tied head ->
+//     argmax -> the next token (a tagged word read by the next pass).
+//
+// GPU-wide sums are fixed-point (int64, 2^-32 units) atomic additions: integer
+// addition does not depend on the order of the atomics, so every run gives
+// the same bits.  A contributor adds its values, fences, and bumps a per-layer
+// counter with release semantics; a consumer waits (acquire) until the
+// counter reaches pass * contributors.  Sums are double-buffered by pass
+// parity; each CTA zeroes its share of the other parity at the start of a pass
+// (the previous pass finished reading it before its token existed).
+//
+// Weights stream through a ring of shared-memory stages as in the persistent
+// kernel (one producer thread, cp.async.bulk, mbarriers).  Every wait is
+// bounded by 2 s of %globaltimer; on timeout the kernel records
+// GPT2_ERR_TIMEOUT, raises the abort word and runs its remaining steps without
+// waiting; all CTAs of a cluster meet at a final cluster barrier, so no CTA
+// exits while a peer may still write its shared memory.
+#include "cluster.h"
+#include "gemv_dev.cuh"
+
+#include <algorithm>
+
+namespace gpt2 {
+
+#ifdef GPT2_CTRACE
+// Debug builds only: %globaltimer, SM clock and thread 0's accumulated
+// ring-stage wait (clock cycles) of every CTA at the phase boundaries of two
+// passes.
+constexpr int kTrCtas = 160, kTrPasses = 2, kTrSlots = 208, kTrPass0 = 20;
+__device__ unsigned long long g_ctrace[kTrCtas][kTrPasses][kTrSlots][6];
+__device__ __forceinline__ void ctrace(int s, int slot, unsigned long long waited, const unsigned long long *sub)
+{
+    if (threadIdx.x == 0 && blockIdx.x < kTrCtas && s >= kTrPass0 && s < kTrPass0 + kTrPasses && slot < kTrSlots) {
+        unsigned long long t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        g_ctrace[blockIdx.x][s - kTrPass0][slot][0] = t;
+        g_ctrace[blockIdx.x][s - kTrPass0][slot][1] = clock64();
+        g_ctrace[blockIdx.x][s - kTrPass0][slot][2] = waited;
+        for (int i = 0; i < 3; ++i) g_ctrace[blockIdx.x][s - kTrPass0][slot][3 + i] = sub[i];
+    }
+}
+#define CTRACE(s, slot) ctrace(s, slot, *c.twait, c.tsub)
+#define TSUB(i, t) do { if (threadIdx.x == 0) c.tsub[i] += clock64() - (t); } while (0)
+#define TSTAMP(t) const long long t = clock64()
+#else
+#define CTRACE(s, slot) ((void)0)
+#define TSUB(i, t) ((void)0)
+#define TSTAMP(t) ((void)0)
+#endif
+
+namespace {
+
+constexpr int kCWarps = 8;
+constexpr int kCThreads = kCWarps * 32;
+constexpr int kCAll = kCThreads + 32;      // + producer warp
+constexpr int kCRing = kClusterRing;
+constexpr int kRowGroup = 4;
+constexpr float kFix = 4294967296.0f;      // 2^32
+constexpr uint32_t kKvWin = 16384;         // K/V rows of this CTA's positions held in shared memory
+constexpr uint32_t kBarBytes = 512;        // mbarriers at the start of shared memory
+
+// Shared-memory layout before the ring (byte offsets): barriers, x, LN(x),
+// this head's q | k | v, the cluster's attention partials, the attention
+// output, the MLP hidden slice, a scratch vector, the layer parameters, the
+// K/V window and the layer table.
+struct CLayout {
+    uint32_t x, xn, qkv, part, attn, hloc, outv, pr, kvw, layers, end;
+};
+__host__ __device__ __forceinline__ CLayout cluster_layout(int E, int D, int fr, int L)
+{
+    auto r16 = [](uint32_t v) { return (v + 15u) & ~15u; };
+    const uint32_t b0 = uint32_t(max(3 * D, fr) + 3) / 4u * 4u;
+    CLayout o;
+    o.x = kBarBytes;
+    o.xn = o.x + r16(uint32_t(E) * 4u);
+    o.qkv = o.xn + r16(uint32_t(E) * 4u);
+    o.part = o.qkv + r16(3u * D * 4u);
+    o.attn = o.part + r16(uint32_t(kClusterSize) * (D + 4) * 4u);
+    o.hloc = o.attn + r16(uint32_t(D) * 4u);
+    o.outv = o.hloc + r16(uint32_t(fr) * 4u);
+    o.pr = o.outv + r16((uint32_t(E) + 2u * kCWarps + uint32_t(kCWarps) * D) * 4u);
+    o.kvw = o.pr + r16((2u * E + b0 + uint32_t(E)) * 4u);
+    o.layers = o.kvw + kKvWin;
+    o.end = o.layers + r16(uint32_t(sizeof(CLayer)) * uint32_t(L));
+    return o;
+}
+
+// ---- primitives -------------------------------------------------------------
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(kCThreads) : "memory"); }
+
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// Store to a CTA of the cluster that completes `bytes` on that CTA's mbarrier
+// (address and barrier both mapped into the destination CTA).
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
+                 "r"(__float_as_uint(v)), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ bool try_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void cluster_barrier_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ int ld_relaxed_i32(const int *p)
+{
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_i64(long long *p, long long v)
+{
+    asm volatile("st.relaxed.gpu.global.s64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void red_add_i64(long long *p, long long v)
+{
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void red_release_add_u32(unsigned *p, unsigned v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void ll_store64(uint64_t *p, uint32_t bits, uint32_t epoch)
+{
+    const uint64_t w = (uint64_t(epoch) << 32) | bits;
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ uint64_t ll_load64(const uint64_t *p)
+{
+    uint64_t w;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
+}
+__device__ __forceinline__ long long to_fix(float v) { return __float2ll_rn(v * kFix); }
+__device__ __forceinline__ float from_fix(long long v) { return float(__ll2double_rn(v) * (1.0 / 4294967296.0)); }
+
+struct Sh {
+    int last;
+    unsigned long long keys[kCWarps];
+    float red[2][kCWarps];
+};
+
+// Shared-memory views of a consumer thread.
+struct CS {
+    uint64_t *full, *empty, *qkv_bar, *att_bar, *kv_bar, *prm_bar;
+    float *x, *xn, *qkv, *part, *attn, *hloc, *outv, *kvw;
+    float *pr;                 // this layer's LayerNorm parameters and bias slices
+    const CLayer *layers;      // the layer table, copied to shared memory
+    uint8_t *ring;
+    uint32_t uses_qkv, uses_att, uses_kv, uses_prm;   // barrier phases consumed so far
+#ifdef GPT2_CTRACE
+    unsigned long long *twait, *tsub;
+#endif
+};
+
+struct Waiter {
+    unsigned long long t0 = 0;
+    uint32_t it = 0;
+};
+
+__device__ __forceinline__ bool aborted(const ClusterArgs &a) { return ld_relaxed_i32(&a.st->abort) != 0; }
+
+__device__ __forceinline__ void raise_abort(const ClusterArgs &a, int info)
+{
+    record_error(a.st, kDevErrTimeout, info);
+    atomicExch(&a.st->abort, 1);
+}
+
+// One step of a bounded spin: false once the spin must end (abort or timeout).
+__device__ __forceinline__ bool keep_waiting(const ClusterArgs &a, Waiter &w, int info)
+{
+    if ((++w.it & 127u) != 0) return true;
+    if (aborted(a)) return false;
+    const unsigned long long t = global_ns();
+    if (w.t0 == 0) w.t0 = t;
+    else if (t - w.t0 > kWaitLimitNs) {
+        raise_abort(a, info);
+        return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ bool wait_stage(const ClusterArgs &a, const CS &c, uint32_t kk)
+{
+    const uint32_t st = kk & (kCRing - 1), par = (kk / kCRing) & 1u;
+    if (mbar_test_wait(&c.full[st], par)) return true;
+#ifdef GPT2_CTRACE
+    const long long t0 = clock64();
+#endif
+    Waiter w;
+    bool good = true;
+    while (!mbar_try_wait(&c.full[st], par))
+        if (!keep_waiting(a, w, 3000 + int(blockIdx.x))) {
+            good = false;
+            break;
+        }
+#ifdef GPT2_CTRACE
+    if ((threadIdx.x & 31) == 0) atomicAdd(c.twait, (unsigned long long)(clock64() - t0));
+#endif
+    return good;
+}
+
+// Bounded wait on a barrier of this CTA that completes by transaction bytes
+// (bulk copies, or stores from CTAs of the cluster).
+__device__ __forceinline__ bool wait_tx_bar(const ClusterArgs &a, uint64_t *bar, uint32_t &uses, int info)
+{
+    const uint32_t par = uses & 1u;
+    ++uses;
+    if (mbar_test_wait(bar, par)) return true;
+    Waiter w;
+    while (!try_wait_cluster(bar, par))
+        if (!keep_waiting(a, w, info)) return false;
+    return true;
+}
+
+// ---- roles and row segments ---------------------------------------------------
+struct Role {
+    bool head;      // a head-cluster CTA (else an fc CTA)
+    int h, r;       // head and rank (head CTAs)
+    int f;          // fc CTA index (fc CTAs)
+    int g;          // CTA index in the grid (LM head)
+};
+
+// Geometry of one kind of segment (the same in every layer): `rows` rows of
+// rb bytes (+ srb scale bytes, + zrb zero-point bytes for int4), streamed in
+// chunks of `chunk` rows per ring stage; a stage holds the chunk's rows, then
+// its scales at soff, then its zero points at zoff.
+struct Geo {
+    uint32_t rb, srb, zrb;
+    int32_t rows, chunk, nch;
+    uint32_t soff, zoff;
+    float inv_chunk;            // row i lies in chunk floor((i + 0.5) * inv_chunk)
+};
+// A segment: a geometry and where its rows start in this layer.
+struct Seg {
+    const uint8_t *main, *sc, *zp;
+};
+
+__host__ __device__ __forceinline__ uint32_t a16(uint32_t v) { return (v + 15u) & ~15u; }
+
+__host__ __device__ __forceinline__ uint32_t seg_stage_bytes(uint32_t c, uint32_t rb, uint32_t srb, uint32_t zrb)
+{
+    return a16(c * rb) + a16(c * srb) + c * zrb;
+}
+
+// Chunk of a row index without an integer division: for i < 2^20 and
+// chunks below 2^11, (i + 0.5) / chunk is at least 2^-12 away from an
+// integer, far more than the float rounding of the product.
+__device__ __forceinline__ int chunk_of(const Geo &g, int i)
+{
+    return __float2int_rz((float(i) + 0.5f) * g.inv_chunk);
+}
+
+// Largest chunk (a multiple of gran, or all rows) whose sections fit a stage.
+__device__ __forceinline__ Geo make_geo(uint32_t rb, uint32_t srb, uint32_t zrb, int rows, int gran, uint32_t stage)
+{
+    Geo g;
+    g.rb = rb;
+    g.srb = srb;
+    g.zrb = zrb;
+    g.rows = rows;
+    int c = int(stage / (rb + srb + zrb)) / gran * gran;
+    while (c > gran && seg_stage_bytes(uint32_t(c), rb, srb, zrb) > stage) c -= gran;
+    if (c < gran) c = gran;
+    if (c > rows) c = rows > 0 ? rows : 1;
+    g.chunk = c;
+    g.nch = rows > 0 ? (rows + c - 1) / c : 0;
+    g.soff = a16(uint32_t(c) * rb);
+    g.zoff = g.soff + a16(uint32_t(c) * srb);
+    g.inv_chunk = 1.0f / float(c);
+    return g;
+}
+
+__device__ __forceinline__ uint32_t wt_row_bytes(int wt, int n)
+{
+    return wt == kWF32 ? uint32_t(n) * 4 : wt == kWF16 ? uint32_t(n) * 2 : uint32_t(n) / 2;
+}
+
+// Canonical rows of an [out][in] matrix (int4: codes [out][in/2], scales
+// [out][in/32], zero points [out][in/64] two per byte).
+__device__ __forceinline__ Geo long_geo(int wt, int in, int rows, uint32_t stage)
+{
+    const bool i4 = wt == kWI4;
+    return make_geo(wt_row_bytes(wt, in), i4 ? uint32_t(in / 32) * 4 : 0, i4 ? uint32_t(in / 64) : 0, rows,
+                    i4 ? 8 : 1, stage);
+}
+__device__ __forceinline__ Seg long_seg(const Geo &g, const void *W, const float *sc, const uint8_t *zp, int row0)
+{
+    Seg s;
+    s.main = static_cast<const uint8_t *>(W) + size_t(row0) * g.rb;
+    s.sc = sc ? reinterpret_cast<const uint8_t *>(sc) + size_t(row0) * g.srb : nullptr;
+    s.zp = zp ? zp + size_t(row0) * g.zrb : nullptr;
+    return s;
+}
+
+// Tile rows of `cols` columns (int4: codes [rows][cols/2], scales
+// [rows][cols/32], one zero-point byte per group).
+__device__ __forceinline__ Geo tile_geo(int wt, int rows, int cols, uint32_t stage)
+{
+    const bool i4 = wt == kWI4;
+    return make_geo(wt_row_bytes(wt, cols), i4 ? uint32_t(cols / 32) * 4 : 0, i4 ? uint32_t(cols / 32) : 0, rows,
+                    i4 ? 16 : 1, stage);
+}
+__device__ __forceinline__ Seg tile_seg(const Geo &g, const void *W, const float *sc, const uint8_t *zp, int t)
+{
+    return long_seg(g, W, sc, zp, t * g.rows);
+}
+
+// The geometries of a CTA's segments: head CTAs stream their gathered q, k, v
+// rows (3 D/4 rows), then their tile of the output projection; fc CTAs their
+// fc rows, then their tile of the MLP projection; every CTA its LM-head rows.
+struct Geos {
+    Geo a, b, head;
+    int head_row0;
+};
+
+__device__ __forceinline__ Geos make_geos(const ClusterArgs &a, const Role &ro)
+{
+    Geos G;
+    if (ro.head) {
+        G.a = long_geo(a.wtype, a.E, 3 * (a.D / 4), a.stage_bytes);
+        G.b = tile_geo(a.wtype, a.E / kClusterSize, a.D, a.stage_bytes);
+    } else {
+        G.a = long_geo(a.wtype, a.E, a.fr, a.stage_bytes);
+        G.b = tile_geo(a.wtype, a.E, a.fr, a.stage_bytes);
+    }
+    const int r0 = min(a.V, ro.g * a.head_rpc), r1 = min(a.V, r0 + a.head_rpc);
+    G.head = long_geo(kWF32, a.E, r1 - r0, a.stage_bytes);
+    G.head_row0 = r0;
+    return G;
+}
+
+__device__ __forceinline__ Seg seg_a(const Role &ro, const Geos &G, const CLayer &L)
+{
+    return ro.head ? tile_seg(G.a, L.Wqkv, L.qkv_s, L.qkv_z, ro.h * kClusterSize + ro.r)
+                   : tile_seg(G.a, L.Wfc, L.fc_s, L.fc_z, ro.f);
+}
+__device__ __forceinline__ Seg seg_b(const Role &ro, const Geos &G, const CLayer &L)
+{
+    return ro.head ? tile_seg(G.b, L.Wo_t, L.o_s, L.o_z, ro.h * kClusterSize + ro.r)
+                   : tile_seg(G.b, L.Wp_t, L.p_s, L.p_z, ro.f);
+}
+__device__ __forceinline__ Seg seg_head(const ClusterArgs &a, const Geos &G)
+{
+    return long_seg(G.head, a.wte, nullptr, nullptr, G.head_row0);
+}
+
+// ---- producer --------------------------------------------------------------------
+__device__ __forceinline__ void stream_seg(const ClusterArgs &a, const Geo &g, const Seg &sg, uint8_t *ring,
+                                           uint64_t *full, uint64_t *empty, uint32_t &k, bool &ok, uint64_t pol)
+{
+    const int C = g.chunk;
+    for (int rs = 0; rs < g.rows && ok; rs += C) {
+        const int n = min(C, g.rows - rs);
+        const uint32_t st = k & (kCRing - 1);
+        if (k >= uint32_t(kCRing)) {
+            const uint32_t par = ((k / kCRing) - 1u) & 1u;
+            Waiter w;
+            while (!mbar_try_wait(&empty[st], par)) {
+                if (!keep_waiting(a, w, 2000 + int(blockIdx.x))) { ok = false; break; }
+                __nanosleep(32);   // the ring is full: leave the issue slots to the consumer warps
+            }
+            if (!ok) break;
+        }
+        uint8_t *dst = ring + size_t(st) * a.stage_bytes;
+        const uint32_t b0 = uint32_t(n) * g.rb, b1 = uint32_t(n) * g.srb, b2 = uint32_t(n) * g.zrb;
+        mbar_arrive_expect_tx(&full[st], b0 + b1 + b2);
+        bulk_g2s_hint(dst, sg.main + size_t(rs) * g.rb, b0, &full[st], pol);
+        if (b1) bulk_g2s_hint(dst + g.soff, sg.sc + size_t(rs) * g.srb, b1, &full[st], pol);
+        if (b2) bulk_g2s_hint(dst + g.zoff, sg.zp + size_t(rs) * g.zrb, b2, &full[st], pol);
+        ++k;
+    }
+}
+
+__device__ void producer(const ClusterArgs &a, const CLayer *layers, const Role &ro, const Geos &G, uint8_t *ring,
+                         uint64_t *full, uint64_t *empty)
+{
+    uint32_t k = 0;
+    bool ok = true;
+    const uint64_t pol = l2_evict_first_policy();
+    for (int s = 0; s < a.n_steps && ok; ++s) {
+        for (int l = 0; l < a.L && ok; ++l) {
+            stream_seg(a, G.a, seg_a(ro, G, layers[l]), ring, full, empty, k, ok, pol);
+            if (ok) stream_seg(a, G.b, seg_b(ro, G, layers[l]), ring, full, empty, k, ok, pol);
+        }
+        if (ok) stream_seg(a, G.head, seg_head(a, G), ring, full, empty, k, ok, pol);
+    }
+    // the copies still in flight land before the CTA leaves
+    const uint32_t first = k > uint32_t(kCRing) ? k - uint32_t(kCRing) : 0u;
+    for (uint32_t j = first; j < k; ++j) {
+        Waiter w;
+        while (!mbar_try_wait(&full[j & (kCRing - 1)], (j / kCRing) & 1u))
+            if ((++w.it & 127u) == 0) {
+                const unsigned long long t = global_ns();
+                if (w.t0 == 0) w.t0 = t;
+                else if (t - w.t0 > kWaitLimitNs) break;
+            }
+    }
+}
+
+// ---- consumer math -------------------------------------------------------------
+// int4 code t of a 32-bit word minus the zero point, exactly: 2^23 + q has q
+// in its low mantissa bits, and zf = 2^23 + z.
+__device__ __forceinline__ float nib_minus(uint32_t q, int t, float zf)
+{
+    return __uint_as_float(0x4B000000u | ((q >> (4 * t)) & 15u)) - zf;
+}
+
+// Column unit c of canonical row rr of a stage times the matching inputs:
+// fp32 4 inputs (16 bytes), fp16 8 inputs (16 bytes), int4 8 inputs (one
+// 32-bit word).
+template <int WT>
+__device__ __forceinline__ float canon_unit(const uint8_t *stg, const Geo &g, int rr, int c, const float4 *x4, float acc)
+{
+    const uint8_t *row = stg + size_t(rr) * g.rb;
+    if (WT == kWF32) {
+        const float4 v = reinterpret_cast<const float4 *>(row)[c];
+        const float4 x = x4[c];
+        return fmaf(v.w, x.w, fmaf(v.z, x.z, fmaf(v.y, x.y, fmaf(v.x, x.x, acc))));
+    } else if (WT == kWF16) {
+        const uint4 u = reinterpret_cast<const uint4 *>(row)[c];
+        const float4 x0 = x4[2 * c], x1 = x4[2 * c + 1];
+        const float2 p0 = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
+        const float2 p1 = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
+        const float2 p2 = __half22float2(*reinterpret_cast<const __half2 *>(&u.z));
+        const float2 p3 = __half22float2(*reinterpret_cast<const __half2 *>(&u.w));
+        acc = fmaf(p0.x, x0.x, acc);
+        acc = fmaf(p0.y, x0.y, acc);
+        acc = fmaf(p1.x, x0.z, acc);
+        acc = fmaf(p1.y, x0.w, acc);
+        acc = fmaf(p2.x, x1.x, acc);
+        acc = fmaf(p2.y, x1.y, acc);
+        acc = fmaf(p3.x, x1.z, acc);
+        return fmaf(p3.y, x1.w, acc);
+    } else {
+        const int grp = c >> 2;
+        const uint32_t q = reinterpret_cast<const uint32_t *>(row)[c];
+        const int z = ((stg + g.zoff + size_t(rr) * g.zrb)[grp >> 1] >> ((grp & 1) * 4)) & 15;
+        const float s = reinterpret_cast<const float *>(stg + g.soff + size_t(rr) * g.srb)[grp];
+        const float zf = 8388608.0f + float(z);
+        const float4 x0 = x4[2 * c], x1 = x4[2 * c + 1];
+        float d = nib_minus(q, 0, zf) * x0.x;
+        d = fmaf(nib_minus(q, 1, zf), x0.y, d);
+        d = fmaf(nib_minus(q, 2, zf), x0.z, d);
+        d = fmaf(nib_minus(q, 3, zf), x0.w, d);
+        d = fmaf(nib_minus(q, 4, zf), x1.x, d);
+        d = fmaf(nib_minus(q, 5, zf), x1.y, d);
+        d = fmaf(nib_minus(q, 6, zf), x1.z, d);
+        d = fmaf(nib_minus(q, 7, zf), x1.w, d);
+        return fmaf(s, d, acc);
+    }
+}
+
+// Sums 4 per-lane values over the warp in 6 shuffles; lanes 0, 8, 16, 24 end
+// with the totals of values 0, 1, 2, 3 (fixed order, so every run gives the
+// same bits).
+__device__ __forceinline__ float warp_sum4(float (&v)[kRowGroup], int lane)
+{
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const bool hi = lane & 16;
+        const float send = hi ? v[i] : v[i + 2], keep = hi ? v[i + 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+    {
+        const bool hi = lane & 8;
+        const float send = hi ? v[0] : v[1], keep = hi ? v[1] : v[0];
+        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 4);
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+    return v[0];
+}
+
+// Stages are consumed in windows of at most half the ring.  At a window's
+// start warp w waits for its stage w (all in parallel), then one CTA barrier
+// makes every stage of the window visible to every warp; at its end one CTA
+// barrier, then one lane per stage releases it (empty barriers count one
+// arrival).  The producer fills the next window while this one is read.
+constexpr int kWindow = kCRing / 2;
+static_assert(kWindow <= kCWarps, "one warp waits for each stage of a window");
+
+__device__ __forceinline__ void window_acquire(const ClusterArgs &a, const CS &c, uint32_t k, int q0, int q1, bool &ok)
+{
+    const int warp = threadIdx.x >> 5;
+    if (warp < q1 - q0 && ok && !wait_stage(a, c, k + uint32_t(q0 + warp))) ok = false;
+    csync();
+}
+
+__device__ __forceinline__ void window_release(const CS &c, uint32_t k, int q0, int q1)
+{
+    csync();
+    const int tid = threadIdx.x;
+    if (tid < q1 - q0)
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&c.empty[(k + uint32_t(q0 + tid)) & (kCRing - 1)]))
+                     : "memory");
+}
+
+__device__ __forceinline__ const uint8_t *stage_ptr(const ClusterArgs &a, const CS &c, uint32_t kk)
+{
+    return c.ring + (kk & (kCRing - 1)) * a.stage_bytes;
+}
+
+// Dot products of the canonical rows of a segment (length in) with xin: each
+// warp takes 4 rows of a window at a time (rows i, i+8, i+16, i+24),
+// lanes over the column units.  Results go to out[i], or, for the LM head
+// (logit_row0 >= 0), to the logits and this thread's argmax key.
+template <int WT>
+__device__ void canon_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &k, int in, const float *xin,
+                           float *out, int logit_row0, unsigned long long &best, bool &ok)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int C = g.chunk, nch = g.nch;
+    const int units = WT == kWF32 ? in >> 2 : in >> 3;
+    const float4 *x4 = reinterpret_cast<const float4 *>(xin);
+    for (int q0 = 0; q0 < nch; q0 += kWindow) {
+        const int q1 = min(nch, q0 + kWindow);
+        const int r0 = q0 * C, r1 = min(g.rows, q1 * C);
+        window_acquire(a, c, k, q0, q1, ok);
+        for (int i0 = r0 + warp; i0 < r1; i0 += kCWarps * kRowGroup) {
+            TSTAMP(t_a);
+            const int ng = min(kRowGroup, (r1 - i0 + kCWarps - 1) >> 3);
+            const uint8_t *stg[kRowGroup];
+            int rr[kRowGroup];
+#pragma unroll
+            for (int j = 0; j < kRowGroup; ++j) {
+                const int i = i0 + j * kCWarps;
+                const int q = j < ng ? chunk_of(g, i) : q0;
+                rr[j] = j < ng ? i - q * C : 0;
+                stg[j] = stage_ptr(a, c, k + uint32_t(q));
+            }
+            TSUB(0, t_a);
+            TSTAMP(t_b);
+            float acc[kRowGroup] = {0.f, 0.f, 0.f, 0.f};
+            if (ok) {
+                if (ng == kRowGroup) {
+                    for (int u = lane; u < units; u += 32) {
+#pragma unroll
+                        for (int j = 0; j < kRowGroup; ++j) acc[j] = canon_unit<WT>(stg[j], g, rr[j], u, x4, acc[j]);
+                    }
+                } else {
+                    for (int u = lane; u < units; u += 32) {
+#pragma unroll
+                        for (int j = 0; j < kRowGroup; ++j)
+                            if (j < ng) acc[j] = canon_unit<WT>(stg[j], g, rr[j], u, x4, acc[j]);
+                    }
+                }
+            }
+            const float t = warp_sum4(acc, lane);
+            const int j = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+            if ((lane & 7) == 0 && j < ng && ok) {
+                const int i = i0 + j * kCWarps;
+                if (logit_row0 >= 0) {
+                    a.logits[logit_row0 + i] = t;
+                    const unsigned long long key = argmax_key(t, uint32_t(logit_row0 + i));
+                    best = key > best ? key : best;
+                } else {
+                    out[i] = t;
+                }
+            }
+            TSUB(1, t_b);
+        }
+        TSTAMP(t_c);
+        window_release(c, k, q0, q1);
+        TSUB(2, t_c);
+    }
+    k += uint32_t(nch);
+}
+
+// One tile row: units [0, U) of 16 bytes, unit u stored at u ^ sw, dotted
+// with vin in two interleaved chains.
+template <int WT>
+__device__ __forceinline__ float tile_row_dot(const uint8_t *stg, const Geo &g, int rr, int sw, int U,
+                                              const float4 *v4)
+{
+    const uint8_t *rp = stg + size_t(rr) * g.rb;
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 2
+    for (int u = 0; u < U; ++u) {
+        const int us = u ^ sw;
+        float part;
+        if (WT == kWF32) {
+            const float4 w = reinterpret_cast<const float4 *>(rp)[us];
+            const float4 v = v4[u];
+            part = fmaf(w.w, v.w, fmaf(w.z, v.z, w.y * v.y)) + w.x * v.x;
+        } else if (WT == kWF16) {
+            const uint4 w = reinterpret_cast<const uint4 *>(rp)[us];
+            const float4 v0 = v4[2 * u], v1 = v4[2 * u + 1];
+            const float2 p0 = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
+            const float2 p1 = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
+            const float2 p2 = __half22float2(*reinterpret_cast<const __half2 *>(&w.z));
+            const float2 p3 = __half22float2(*reinterpret_cast<const __half2 *>(&w.w));
+            const float e0 = fmaf(p0.y, v0.y, p0.x * v0.x), e1 = fmaf(p1.y, v0.w, p1.x * v0.z);
+            const float e2 = fmaf(p2.y, v1.y, p2.x * v1.x), e3 = fmaf(p3.y, v1.w, p3.x * v1.z);
+            part = (e0 + e1) + (e2 + e3);
+        } else {
+            const uint4 w = reinterpret_cast<const uint4 *>(rp)[us];
+            const float s = reinterpret_cast<const float *>(stg + g.soff + size_t(rr) * g.srb)[u];
+            const float zf = 8388608.0f + float((stg + g.zoff + size_t(rr) * g.zrb)[u]);
+            const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+            float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+            for (int wi = 0; wi < 4; ++wi) {
+                const float4 v0 = v4[8 * u + 2 * wi], v1 = v4[8 * u + 2 * wi + 1];
+                const uint32_t qw = words[wi];
+                d0 = fmaf(nib_minus(qw, 0, zf), v0.x, d0);
+                d1 = fmaf(nib_minus(qw, 1, zf), v0.y, d1);
+                d0 = fmaf(nib_minus(qw, 2, zf), v0.z, d0);
+                d1 = fmaf(nib_minus(qw, 3, zf), v0.w, d1);
+                d0 = fmaf(nib_minus(qw, 4, zf), v1.x, d0);
+                d1 = fmaf(nib_minus(qw, 5, zf), v1.y, d1);
+                d0 = fmaf(nib_minus(qw, 6, zf), v1.z, d0);
+                d1 = fmaf(nib_minus(qw, 7, zf), v1.w, d1);
+            }
+            part = s * (d0 + d1);
+        }
+        if (u & 1) acc1 += part;
+        else acc0 += part;
+    }
+    return acc0 + acc1;
+}
+
+// Dot products of the tile rows of a segment (cols columns) with vin: one
+// thread per row; 16-byte units of row r are stored at u ^ (r & m), so the
+// threads of a quarter-warp read different banks.  out[row] for every row.
+template <int WT>
+__device__ void tile_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &k, int cols, const float *vin,
+                          float *out, bool &ok)
+{
+    const int tid = threadIdx.x;
+    const int per_unit = WT == kWF32 ? 4 : WT == kWF16 ? 8 : 32;
+    const int U = cols / per_unit;
+    const int m = (U & (U - 1)) == 0 ? min(U, 8) - 1 : 0;
+    const int C = g.chunk, nch = g.nch;
+    const float4 *v4 = reinterpret_cast<const float4 *>(vin);
+    for (int q0 = 0; q0 < nch; q0 += kWindow) {
+        const int q1 = min(nch, q0 + kWindow);
+        const int r1 = min(g.rows, q1 * C);
+        window_acquire(a, c, k, q0, q1, ok);
+        if (ok)
+            for (int row = q0 * C + tid; row < r1; row += kCThreads) {
+                const int q = chunk_of(g, row), rr = row - q * C;
+                out[row] = tile_row_dot<WT>(stage_ptr(a, c, k + uint32_t(q)), g, rr, row & m, U, v4);
+            }
+        window_release(c, k, q0, q1);   // its barrier also completes out[]
+    }
+    k += uint32_t(nch);
+}
+
+// LayerNorm of c.x into c.xn with gamma, beta in shared memory (all
+// consumer threads; mean, then the biased variance around it).
+__device__ __forceinline__ void layer_norm(const ClusterArgs &a, CS &c, Sh &sh, const float *gamma, const float *beta)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, E = a.E;
+    float s = 0.f;
+    for (int i = tid; i < E; i += kCThreads) s += c.x[i];
+    s = warp_sum(s);
+    if (lane == 0) sh.red[0][warp] = s;
+    csync();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCWarps; ++w) tot += sh.red[0][w];
+    const float mean = tot / float(E);
+    float q = 0.f;
+    for (int i = tid; i < E; i += kCThreads) {
+        const float d = c.x[i] - mean;
+        q = fmaf(d, d, q);
+    }
+    q = warp_sum(q);
+    if (lane == 0) sh.red[1][warp] = q;
+    csync();
+    float ss = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCWarps; ++w) ss += sh.red[1][w];
+    const float rstd = 1.0f / sqrtf(ss / float(E) + a.eps);
+    for (int i = tid; i < E; i += kCThreads) c.xn[i] = (c.x[i] - mean) * rstd * gamma[i] + beta[i];
+    csync();
+}
+
+constexpr int kMaxPerThread = 8;   // n_embd <= 8 * kCThreads
+
+// Wait until `cnt` reaches `target`, then read the fixed-point sum into dst
+// (all loads issued before the first is used).
+__device__ __forceinline__ void read_sum(const ClusterArgs &a, const unsigned *cnt, unsigned target,
+                                         const long long *src, float *dst, bool &ok)
+{
+    const int tid = threadIdx.x;
+    __shared__ int s_ok;
+    if (tid == 0) {
+        Waiter w;
+        bool good = ok;
+        while (good && int(ld_acquire_u32(cnt) - target) < 0)   // counters wrap; differences stay small
+            if (!keep_waiting(a, w, 5000 + int(blockIdx.x))) good = false;
+        s_ok = good ? 1 : 0;
+    }
+    csync();
+    if (!s_ok) ok = false;
+    long long v[kMaxPerThread];
+#pragma unroll
+    for (int j = 0; j < kMaxPerThread; ++j) {
+        const int i = tid + j * kCThreads;
+        v[j] = i < a.E ? __ldcg(src + i) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxPerThread; ++j) {
+        const int i = tid + j * kCThreads;
+        if (i < a.E) dst[i] = from_fix(v[j]);
+    }
+    csync();
+}
+
+// Adds values[i] (+ extra[base + i] + extra2[i] if extra is given) into
+// sum[base + i], i < n, as fixed point; then one arrival on `cnt`.  The
+// release by thread 0 after the barrier publishes every thread's additions.
+__device__ __forceinline__ void add_sum(long long *sum, int base, const float *values, const float *extra,
+                                        const float *extra2, int n, unsigned *cnt)
+{
+    const int tid = threadIdx.x;
+    for (int i = tid; i < n; i += kCThreads) {
+        float v = values[i];
+        if (extra) v += extra[base + i] + extra2[i];
+        red_add_i64(sum + base + i, to_fix(v));
+    }
+    csync();
+    if (tid == 0) red_release_add_u32(cnt, 1u);
+}
+
+// ---- attention of one head, positions split over the cluster ----------------------
+template <int D>
+__device__ void attention(const ClusterArgs &a, CS &c, int l, int h, int r, int pos, bool &ok)
+{
+    constexpr int DPL = D / 32;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float *kh = a.kcache + (size_t(l) * a.H + h) * a.P * D;
+    float *vh = a.vcache + (size_t(l) * a.H + h) * a.P * D;
+    const int n = pos + 1;
+    const int j0 = (r * n) / kClusterSize, j1 = ((r + 1) * n) / kClusterSize;
+    const int jc = min(j1, pos);                       // cached rows of this CTA: [j0, jc)
+    const int win = int(kKvWin / (2u * D * 4u));
+    const int n_pre = max(0, min(jc - j0, win));
+    float *kw = c.kvw, *vw = c.kvw + size_t(win) * D;
+    if (r == 0 && tid < D) {                           // append this token's k, v to the cache
+        kh[size_t(pos) * D + tid] = c.qkv[D + tid];
+        vh[size_t(pos) * D + tid] = c.qkv[2 * D + tid];
+    }
+    if (n_pre > 0) {
+        const uint32_t par = c.uses_kv & 1u;
+        ++c.uses_kv;
+        Waiter w;
+        while (ok && !mbar_try_wait(c.kv_bar, par))
+            if (!keep_waiting(a, w, 4000 + int(blockIdx.x))) ok = false;
+    }
+    // this CTA's positions, split over warps; online softmax in 32-position tiles
+    const int cnt = max(0, j1 - j0);
+    const int per = (cnt + kCWarps - 1) / kCWarps;
+    const int w0 = j0 + warp * per, w1 = min(j1, w0 + per);
+    float m = -INFINITY, lsum = 0.f, o[DPL];
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) o[i] = 0.f;
+    const float4 *q4 = reinterpret_cast<const float4 *>(c.qkv);
+    auto krow = [&](int j) -> const float * {
+        return j == pos ? c.qkv + D : (j - j0 < n_pre ? kw + size_t(j - j0) * D : kh + size_t(j) * D);
+    };
+    auto vrow = [&](int j) -> const float * {
+        return j == pos ? c.qkv + 2 * D : (j - j0 < n_pre ? vw + size_t(j - j0) * D : vh + size_t(j) * D);
+    };
+    for (int base = w0; base < w1 && ok; base += 32) {
+        const int j = base + lane;
+        const bool valid = j < w1;
+        float sc = -INFINITY;
+        if (valid) {
+            const float4 *kr = reinterpret_cast<const float4 *>(krow(j));
+            float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < D / 4; i += 2) {
+                const float4 k0 = kr[i], k1 = kr[i + 1], qa = q4[i], qb = q4[i + 1];
+                d0 = fmaf(qa.x, k0.x, fmaf(qa.y, k0.y, fmaf(qa.z, k0.z, fmaf(qa.w, k0.w, d0))));
+                d1 = fmaf(qb.x, k1.x, fmaf(qb.y, k1.y, fmaf(qb.z, k1.z, fmaf(qb.w, k1.w, d1))));
+            }
+            sc = (d0 + d1) * a.scale;
+        }
+        const float mn = fmaxf(m, warp_max(sc));
+        const float corr = expf(m - mn);
+        const float p = valid ? expf(sc - mn) : 0.f;
+        lsum = fmaf(lsum, corr, warp_sum(p));
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) o[i] *= corr;
+        const int cntt = min(32, w1 - base);
+        for (int i = 0; i < cntt; ++i) {
+            const float pi = __shfl_sync(0xffffffffu, p, i);
+            const float *vr = vrow(base + i);
+#pragma unroll
+            for (int dd = 0; dd < DPL; ++dd) o[dd] = fmaf(pi, vr[lane + 32 * dd], o[dd]);
+        }
+        m = mn;
+    }
+    // merge the warps (shared scratch = the part slot of this rank, staged in outv)
+    float *wm = c.outv, *wl = c.outv + kCWarps, *wo = c.outv + 2 * kCWarps;
+    if (lane == 0) {
+        wm[warp] = m;
+        wl[warp] = lsum;
+    }
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) wo[warp * D + lane + 32 * i] = o[i];
+    csync();
+    // this CTA's (max, sum, unnormalised output) to every CTA of the cluster;
+    // the stores complete on each receiver's att_bar
+    const uint32_t slot = smem_addr(c.part + size_t(r) * (D + 4));
+    const uint32_t abar = smem_addr(c.att_bar);
+    for (int t = tid; t < D + 2; t += kCThreads) {
+        float M = -INFINITY;
+        for (int w = 0; w < kCWarps; ++w)
+            if (wl[w] > 0.f) M = fmaxf(M, wm[w]);
+        float L = 0.f, O = 0.f;
+        for (int w = 0; w < kCWarps; ++w) {
+            if (wl[w] > 0.f) {
+                const float e = expf(wm[w] - M);
+                L = fmaf(wl[w], e, L);
+                if (t >= 2) O = fmaf(wo[w * D + t - 2], e, O);
+            }
+        }
+        const float v = t == 0 ? M : (t == 1 ? L : O);
+        const uint32_t off = t < 2 ? uint32_t(t) * 4u : uint32_t(t + 2) * 4u;
+#pragma unroll
+        for (int dst = 0; dst < kClusterSize; ++dst)
+            st_async_f32(mapa(slot + off, uint32_t(dst)), v, mapa(abar, uint32_t(dst)));
+    }
+    if (!wait_tx_bar(a, c.att_bar, c.uses_att, 6000 + int(blockIdx.x))) ok = false;
+    // combine the 4 ranks in rank order (every CTA gets the same bits)
+    for (int t = tid; t < D; t += kCThreads) {
+        float M = -INFINITY;
+        for (int q = 0; q < kClusterSize; ++q) {
+            const float *pq = c.part + size_t(q) * (D + 4);
+            if (pq[1] > 0.f) M = fmaxf(M, pq[0]);
+        }
+        float L = 0.f, O = 0.f;
+        for (int q = 0; q < kClusterSize; ++q) {
+            const float *pq = c.part + size_t(q) * (D + 4);
+            if (pq[1] > 0.f) {
+                const float e = expf(pq[0] - M);
+                L = fmaf(pq[1], e, L);
+                O = fmaf(pq[4 + t], e, O);
+            }
+        }
+        c.attn[t] = O / L;
+    }
+    csync();
+}
+
+// Issue the bulk copies of this CTA's cached K/V rows of a head (before q, k,
+// v of the pass exist).
+template <int D>
+__device__ __forceinline__ void prefetch_kv(const ClusterArgs &a, CS &c, int l, int h, int r, int pos)
+{
+    if (threadIdx.x != 0) return;
+    const int n = pos + 1;
+    const int j0 = (r * n) / kClusterSize, j1 = ((r + 1) * n) / kClusterSize;
+    const int jc = min(j1, pos);
+    const int win = int(kKvWin / (2u * D * 4u));
+    const int n_pre = max(0, min(jc - j0, win));
+    if (n_pre <= 0) return;
+    const float *kh = a.kcache + ((size_t(l) * a.H + h) * a.P + j0) * D;
+    const float *vh = a.vcache + ((size_t(l) * a.H + h) * a.P + j0) * D;
+    const uint32_t bytes = uint32_t(n_pre) * D * 4u;
+    asm volatile("fence.proxy.async;" ::: "memory");   // cache rows written by generic stores; window last read by them
+    mbar_arrive_expect_tx(c.kv_bar, 2u * bytes);
+    bulk_g2s(c.kvw, kh, bytes, c.kv_bar);
+    bulk_g2s(c.kvw + size_t(win) * D, vh, bytes, c.kv_bar);
+}
+
+// Zeroes this CTA's share of the other parity's sums.  Called after the
+// pass's first GPU-wide wait: by then every CTA has finished the previous
+// pass, the last reader of those sums.
+__device__ __forceinline__ void zero_other_parity(const ClusterArgs &a, int par)
+{
+    const size_t words = size_t(a.L) * a.E;
+    const size_t per = (words + gridDim.x - 1) / gridDim.x;
+    const size_t w0 = size_t(blockIdx.x) * per, w1 = min(words, w0 + per);
+    long long *zn = a.acc_new + size_t(1 - par) * words, *zx = a.acc_next + size_t(1 - par) * words;
+    for (size_t i = w0 + threadIdx.x; i < w1; i += kCThreads) {
+        st_relaxed_i64(zn + i, 0);
+        st_relaxed_i64(zx + i, 0);
+    }
+}
+
+// The last CTA to finish the LM head reduces the per-CTA argmax keys,
+// publishes the token and updates the state.
+__device__ __forceinline__ void finish_head(const ClusterArgs &a, Sh &sh, int s, uint32_t seq, unsigned long long best)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    best = warp_max_u64(best);
+    if (lane == 0) sh.keys[warp] = best;
+    csync();
+    if (tid == 0) {
+        unsigned long long b = 0ull;
+        for (int w = 0; w < kCWarps; ++w) b = sh.keys[w] > b ? sh.keys[w] : b;
+        a.partials[blockIdx.x] = b;
+        __threadfence();
+        const unsigned t = atomicAdd(a.counter, 1u);
+        sh.last = (t == gridDim.x - 1) ? 1 : 0;
+    }
+    csync();
+    if (sh.last && warp == 0) {
+        __threadfence();
+        unsigned long long b = 0ull;
+        for (int i = lane; i < int(gridDim.x); i += 32) {
+            const unsigned long long v = __ldcg(a.partials + i);
+            b = v > b ? v : b;
+        }
+        b = warp_max_u64(b);
+        if (lane == 0) {
+            const int32_t tok = argmax_key_index(b);
+            *a.counter = 0u;
+            DeviceState *st = a.st;
+            st->next_tok = tok;
+            if (s >= a.n_prompt - 1) {
+                const int32_t n = st->n_out;
+                if (a.out_ids && n >= 0 && n < a.out_cap) a.out_ids[n] = tok;
+                st->n_out = n + 1;
+            }
+            if (s == a.n_steps - 1) {
+                st->tok = tok;
+                st->pos = a.pos0 + a.n_steps;
+                st->seq = int32_t(seq + 1);
+            }
+            __threadfence();
+            ll_store64(a.ll_tok, uint32_t(tok), seq);
+        }
+    }
+    csync();
+}
+
+// Bulk copies of the LayerNorm parameters and bias slices a CTA needs in one
+// layer (L != nullptr) or in the LM head (L == nullptr) into c.pr, completing
+// on prm_bar.  Thread 0, before the wait for the layer's input, so the copies
+// overlap that wait.  The area's previous contents were last read before the
+// barrier that precedes this call.
+__device__ __forceinline__ void issue_params(const ClusterArgs &a, CS &c, const Role &ro, const CLayer *L)
+{
+    if (threadIdx.x != 0) return;
+    const int E = a.E, D = a.D;
+    float *pw = c.pr, *pb = c.pr + E, *b0 = c.pr + 2 * E, *b1 = c.pr + 2 * E + a.pr_b0;
+    const uint32_t ev = uint32_t(E) * 4u;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (!L) {
+        mbar_arrive_expect_tx(c.prm_bar, 2u * ev);
+        bulk_g2s(pw, a.lnf_w, ev, c.prm_bar);
+        bulk_g2s(pb, a.lnf_b, ev, c.prm_bar);
+    } else if (ro.head) {
+        const uint32_t dv = uint32_t(D) * 4u, qv = ev / kClusterSize;
+        mbar_arrive_expect_tx(c.prm_bar, 2u * ev + 3u * dv + (ro.h == 0 ? qv : 0u));
+        bulk_g2s(pw, L->ln1_w, ev, c.prm_bar);
+        bulk_g2s(pb, L->ln1_b, ev, c.prm_bar);
+        for (int part = 0; part < 3; ++part)
+            bulk_g2s(b0 + part * D, L->attn_b + size_t(part) * E + size_t(ro.h) * D, dv, c.prm_bar);
+        if (ro.h == 0) bulk_g2s(b1, L->proj_b + size_t(ro.r) * (E / kClusterSize), qv, c.prm_bar);
+    } else {
+        const uint32_t fv = uint32_t(a.fr) * 4u;
+        mbar_arrive_expect_tx(c.prm_bar, 2u * ev + fv + (ro.f == 0 ? ev : 0u));
+        bulk_g2s(pw, L->ln2_w, ev, c.prm_bar);
+        bulk_g2s(pb, L->ln2_b, ev, c.prm_bar);
+        bulk_g2s(b0, L->fc_b + size_t(ro.f) * a.fr, fv, c.prm_bar);
+        if (ro.f == 0) bulk_g2s(b1, L->mlp_proj_b, ev, c.prm_bar);
+    }
+}
+
+template <int WT, int D>
+__device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, const Geos &G)
+{
+    const int tid = threadIdx.x;
+    const uint32_t seq0 = uint32_t(ld_relaxed_i32(&a.st->seq));
+    const unsigned n_head_ctas = unsigned(a.H * kClusterSize);
+    const int E = a.E, q4 = D / 4, rq = E / kClusterSize;
+    const float *b0 = c.pr + 2 * E, *b1 = c.pr + 2 * E + a.pr_b0;
+    uint32_t k = 0;
+    bool ok = true;
+    for (int s = 0; s < a.n_steps; ++s) {
+        const uint32_t seq = seq0 + uint32_t(s);
+        const int par = int(seq & 1u);
+        const int pos = min(max(a.pos0 + s, 0), a.P - 1);
+        unsigned long long best = 0ull;
+        for (int l = 0; l < a.L; ++l) {
+            const CLayer &L = c.layers[l];
+            long long *an = a.acc_new + (size_t(par) * a.L + l) * E;
+            CTRACE(s, l * 16 + 0);
+            issue_params(a, c, ro, &L);
+            if (ro.head) {
+                if (tid == 0) {   // this layer's phases of the two cluster exchanges
+                    mbar_arrive_expect_tx(c.qkv_bar, 3u * D * 4u);
+                    mbar_arrive_expect_tx(c.att_bar, uint32_t(kClusterSize) * (D + 2) * 4u);
+                }
+                prefetch_kv<D>(a, c, l, ro.h, ro.r, pos);
+                // x entering the block
+                if (l == 0) {
+                    // every pass after the first waits for the previous one (its
+                    // token, tagged with its sequence number), prompt passes too:
+                    // the GPU-wide order of passes is what makes reusing the
+                    // sums, the exchange slots and the cache rows safe
+                    int tok = 0;
+                    if (s > 0) {
+                        uint64_t w = ll_load64(a.ll_tok);
+                        Waiter wt;
+                        while (ok && uint32_t(w >> 32) != seq - 1) {
+                            if (!keep_waiting(a, wt, 7000 + int(blockIdx.x))) ok = false;
+                            w = ll_load64(a.ll_tok);
+                        }
+                        tok = int(uint32_t(w));
+                        __threadfence();   // acquire: the previous pass is complete
+                    }
+                    if (s < a.n_prompt) tok = a.prompt ? __ldg(a.prompt + s) : a.tok_first;
+                    else if (s == 0) tok = ld_relaxed_i32(&a.st->tok);
+                    if (tok < 0 || tok >= a.V || a.pos0 + s >= a.P) {
+                        if (tid == 0) record_error(a.st, tok < 0 || tok >= a.V ? kDevErrBadToken : kDevErrBadPosition, tok);
+                        tok = min(max(tok, 0), a.V - 1);
+                    }
+                    for (int i = tid; i < E; i += kCThreads)
+                        c.x[i] = __ldg(a.wte + size_t(tok) * E + i) + __ldg(a.wpe + size_t(pos) * E + i);
+                    zero_other_parity(a, par);
+                    csync();
+                } else {
+                    read_sum(a, a.cnt_next + (l - 1), seq * unsigned(a.nfc),
+                             a.acc_next + (size_t(par) * a.L + (l - 1)) * E, c.x, ok);
+                }
+                CTRACE(s, l * 16 + 1);
+                if (!wait_tx_bar(a, c.prm_bar, c.uses_prm, 9000 + int(blockIdx.x))) ok = false;
+                layer_norm(a, c, sh, c.pr, c.pr + E);
+                CTRACE(s, l * 16 + 2);
+                // q, k, v quarters of this head (+ bias) -> every CTA of the cluster
+                canon_rows<WT>(a, c, G.a, k, E, c.xn, c.outv, -1, best, ok);
+                csync();
+                CTRACE(s, l * 16 + 3);
+                {
+                    const uint32_t qbar = smem_addr(c.qkv_bar);
+                    for (int t = tid; t < 3 * q4; t += kCThreads) {
+                        const int part = t / q4, d = ro.r * q4 + t % q4;
+                        const float v = c.outv[t] + b0[part * D + d];
+                        const uint32_t dsm = smem_addr(c.qkv + part * D + d);
+#pragma unroll
+                        for (int dst = 0; dst < kClusterSize; ++dst)
+                            st_async_f32(mapa(dsm, uint32_t(dst)), v, mapa(qbar, uint32_t(dst)));
+                    }
+                }
+                if (!wait_tx_bar(a, c.qkv_bar, c.uses_qkv, 8000 + int(blockIdx.x))) ok = false;
+                CTRACE(s, l * 16 + 4);
+                attention<D>(a, c, l, ro.h, ro.r, pos, ok);
+                CTRACE(s, l * 16 + 5);
+                // the head's slice of the output projection, rows rank*E/4.. (+ x + bias once, by head 0)
+                tile_rows<WT>(a, c, G.b, k, D, c.attn, c.outv, ok);
+                CTRACE(s, l * 16 + 6);
+                add_sum(an, ro.r * rq, c.outv, ro.h == 0 ? c.x : nullptr, b1, rq, a.cnt_new + l);
+                CTRACE(s, l * 16 + 7);
+            } else {
+                read_sum(a, a.cnt_new + l, seq * n_head_ctas, an, c.x, ok);
+                if (l == 0) zero_other_parity(a, par);
+                CTRACE(s, l * 16 + 1);
+                if (!wait_tx_bar(a, c.prm_bar, c.uses_prm, 9000 + int(blockIdx.x))) ok = false;
+                layer_norm(a, c, sh, c.pr, c.pr + E);
+                CTRACE(s, l * 16 + 2);
+                canon_rows<WT>(a, c, G.a, k, E, c.xn, c.outv, -1, best, ok);
+                csync();
+                CTRACE(s, l * 16 + 3);
+                for (int t = tid; t < a.fr; t += kCThreads) c.hloc[t] = gelu_new(c.outv[t] + b0[t]);
+                csync();
+                CTRACE(s, l * 16 + 4);
+                tile_rows<WT>(a, c, G.b, k, a.fr, c.hloc, c.outv, ok);
+                CTRACE(s, l * 16 + 5);
+                add_sum(a.acc_next + (size_t(par) * a.L + l) * E, 0, c.outv, ro.f == 0 ? c.x : nullptr, b1, E,
+                        a.cnt_next + l);
+                CTRACE(s, l * 16 + 6);
+            }
+        }
+        // LM head (every CTA)
+        CTRACE(s, 200);
+        issue_params(a, c, ro, nullptr);
+        read_sum(a, a.cnt_next + (a.L - 1), seq * unsigned(a.nfc), a.acc_next + (size_t(par) * a.L + (a.L - 1)) * E,
+                 c.x, ok);
+        CTRACE(s, 201);
+        if (!wait_tx_bar(a, c.prm_bar, c.uses_prm, 9000 + int(blockIdx.x))) ok = false;
+        layer_norm(a, c, sh, c.pr, c.pr + E);
+        canon_rows<kWF32>(a, c, G.head, k, E, c.xn, nullptr, G.head_row0, best, ok);
+        CTRACE(s, 202);
+        finish_head(a, sh, s, seq, best);
+        CTRACE(s, 203);
+    }
+}
+
+template <int WT, int D>
+__global__ void __launch_bounds__(kCAll, 1) k_decode_cluster(const ClusterArgs a)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ Sh sh;
+#ifdef GPT2_CTRACE
+    __shared__ unsigned long long twait, tsub[3];
+#endif
+    const CLayout lo = cluster_layout(a.E, D, a.fr, a.L);
+    CS c;
+    c.full = reinterpret_cast<uint64_t *>(smem);
+    c.empty = c.full + kCRing;
+    c.qkv_bar = c.empty + kCRing;
+    c.att_bar = c.qkv_bar + 1;
+    c.kv_bar = c.qkv_bar + 2;
+    c.prm_bar = c.qkv_bar + 3;
+    c.x = reinterpret_cast<float *>(smem + lo.x);
+    c.xn = reinterpret_cast<float *>(smem + lo.xn);
+    c.qkv = reinterpret_cast<float *>(smem + lo.qkv);
+    c.part = reinterpret_cast<float *>(smem + lo.part);
+    c.attn = reinterpret_cast<float *>(smem + lo.attn);
+    c.hloc = reinterpret_cast<float *>(smem + lo.hloc);
+    c.outv = reinterpret_cast<float *>(smem + lo.outv);
+    c.pr = reinterpret_cast<float *>(smem + lo.pr);
+    c.kvw = reinterpret_cast<float *>(smem + lo.kvw);
+    CLayer *tab = reinterpret_cast<CLayer *>(smem + lo.layers);
+    c.layers = tab;
+    c.ring = smem + a.ring_offset;
+    c.uses_qkv = c.uses_att = c.uses_kv = c.uses_prm = 0;
+#ifdef GPT2_CTRACE
+    c.twait = &twait;
+    c.tsub = tsub;
+#endif
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // the layer table, word by word
+    {
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(a.layers);
+        uint32_t *dst = reinterpret_cast<uint32_t *>(tab);
+        const int words = int(sizeof(CLayer) / 4) * a.L;
+        for (int i = tid; i < words; i += kCAll) dst[i] = __ldg(src + i);
+    }
+    if (tid == 0) {
+        for (int i = 0; i < kCRing; ++i) {
+            mbar_init(&c.full[i], 1);
+            mbar_init(&c.empty[i], 1);
+        }
+        mbar_init(c.qkv_bar, 1);   // + the bytes of the 4 ranks' stores
+        mbar_init(c.att_bar, 1);
+        mbar_init(c.kv_bar, 1);
+        mbar_init(c.prm_bar, 1);
+        mbar_init_fence();
+        sh.last = 0;
+#ifdef GPT2_CTRACE
+        twait = 0;
+        tsub[0] = tsub[1] = tsub[2] = 0;
+#endif
+    }
+    __syncthreads();
+    cluster_barrier_all();   // every CTA's barriers exist before a peer stores to them
+    Role ro;
+    const int cl = int(blockIdx.x) / kClusterSize;
+    ro.r = int(blockIdx.x) % kClusterSize;
+    ro.head = cl < a.H;
+    ro.h = ro.head ? cl : -1;
+    ro.f = ro.head ? -1 : (cl - a.H) * kClusterSize + ro.r;
+    ro.g = int(blockIdx.x);
+    const Geos G = make_geos(a, ro);
+    if (warp == kCWarps) {
+        if (lane == 0) producer(a, c.layers, ro, G, c.ring, c.full, c.empty);
+        __syncwarp();
+    } else {
+        consumer<WT, D>(a, c, sh, ro, G);
+    }
+    __syncthreads();
+    cluster_barrier_all();   // no CTA leaves while a peer may still write its shared memory
+}
+
+template <int WT, int D>
+cudaError_t launch_t(const ClusterArgs &a, int n_clusters, size_t smem, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_clusters * kClusterSize);
+    cfg.blockDim = dim3(kCAll);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = kClusterSize;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeCooperative;
+    at[1].val.cooperative = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, k_decode_cluster<WT, D>, a);
+}
+
+template <int WT, int D>
+cudaError_t occ_t(size_t smem, size_t limit, int *clusters)
+{
+    cudaError_t e = cudaFuncSetAttribute(k_decode_cluster<WT, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(limit));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kClusterSize * 8);
+    cfg.blockDim = dim3(kCAll);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = kClusterSize;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(clusters, k_decode_cluster<WT, D>, &cfg);
+}
+
+// Re-tiling of a stored [out][in] matrix (see CLayer): tile t, row i holds
+// canonical row (t % rdiv) * rows + i, columns (t / rdiv) * cols + [0, cols),
+// as 16-byte units stored at u ^ (i & m).  The values are the stored ones,
+// moved, never recomputed (int4: the same codes, scales and zero points).
+__global__ void __launch_bounds__(256) k_tile(int wt, const uint8_t *W, const float *sc, const uint8_t *zp, int in,
+                                              int T, int rdiv, int rows, int cols, uint8_t *dW, float *dsc,
+                                              uint8_t *dzp)
+{
+    const int per_unit = wt == kWF32 ? 4 : wt == kWF16 ? 8 : 32;
+    const int U = cols / per_unit;
+    const int m = (U & (U - 1)) == 0 ? min(U, 8) - 1 : 0;
+    const long long total = (long long)T * rows * U;
+    const uint32_t rb_in = wt == kWF32 ? uint32_t(in) * 4 : wt == kWF16 ? uint32_t(in) * 2 : uint32_t(in) / 2;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int u = int(idx % U);
+        const long long ti = idx / U;
+        const int i = int(ti % rows), t = int(ti / rows);
+        const long long R = (long long)(t % rdiv) * rows + i;
+        const int col0 = (t / rdiv) * cols;
+        const uint4 v = *reinterpret_cast<const uint4 *>(W + R * rb_in + size_t(col0 / per_unit + u) * 16);
+        *reinterpret_cast<uint4 *>(dW + (size_t(ti) * U + (u ^ (i & m))) * 16) = v;
+        if (wt == kWI4) {
+            const int g = col0 / 32 + u;
+            dsc[size_t(ti) * U + u] = sc[R * (in / 32) + g];
+            dzp[size_t(ti) * U + u] = uint8_t((zp[R * (in / 64) + g / 2] >> ((g & 1) * 4)) & 15);
+        }
+    }
+}
+
+// Gathers the q, k, v rows of each (head, rank) into one contiguous block of
+// 3 D/4 rows: destination row j = ((h * 4 + r) * 3 + part) * D/4 + d holds
+// canonical row part * E + h * D + r * D/4 + d.  Rows keep the canonical
+// format (int4: codes, scales and packed zero points, moved unchanged).
+__global__ void __launch_bounds__(128) k_gather_qkv(int wt, const uint8_t *W, const float *sc, const uint8_t *zp,
+                                                    int E, int D, uint8_t *dW, float *dsc, uint8_t *dzp)
+{
+    const int j = blockIdx.x, q4 = D / 4;
+    const int i = j % (3 * q4), t = j / (3 * q4);
+    const int h = t / kClusterSize, r = t % kClusterSize, part = i / q4, d = i % q4;
+    const size_t src = size_t(part) * E + size_t(h) * D + size_t(r) * q4 + d;
+    const uint32_t rb = wt == kWF32 ? uint32_t(E) * 4 : wt == kWF16 ? uint32_t(E) * 2 : uint32_t(E) / 2;
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(W + src * rb);
+    uint4 *d4 = reinterpret_cast<uint4 *>(dW + size_t(j) * rb);
+    for (uint32_t u = threadIdx.x; u < rb / 16; u += blockDim.x) d4[u] = s4[u];
+    if (wt == kWI4) {
+        for (int g = threadIdx.x; g < E / 32; g += blockDim.x) dsc[size_t(j) * (E / 32) + g] = sc[src * (E / 32) + g];
+        for (int b = threadIdx.x; b < E / 64; b += blockDim.x) dzp[size_t(j) * (E / 64) + b] = zp[src * (E / 64) + b];
+    }
+}
+
+}  // namespace
+
+size_t cluster_fixed_smem(int E, int D, int fr, int L)
+{
+    return (size_t(cluster_layout(E, D, fr, L).end) + 127) / 128 * 128;
+}
+
+cudaError_t launch_cluster(int wtype, const ClusterArgs &a, int n_clusters, size_t smem, cudaStream_t s)
+{
+#define GPT2_C_CASE(WT)                                              \
+    switch (a.D) {                                                   \
+    case 32: return launch_t<WT, 32>(a, n_clusters, smem, s);        \
+    case 64: return launch_t<WT, 64>(a, n_clusters, smem, s);        \
+    case 128: return launch_t<WT, 128>(a, n_clusters, smem, s);      \
+    default: return cudaErrorInvalidValue;                           \
+    }
+    switch (wtype) {
+    case kWF32: GPT2_C_CASE(kWF32)
+    case kWF16: GPT2_C_CASE(kWF16)
+    case kWI4: GPT2_C_CASE(kWI4)
+    default: return cudaErrorInvalidValue;
+    }
+#undef GPT2_C_CASE
+}
+
+cudaError_t cluster_max_active(int wtype, int D, size_t smem, size_t limit, int *clusters)
+{
+#define GPT2_CO_CASE(WT)                                             \
+    switch (D) {                                                     \
+    case 32: return occ_t<WT, 32>(smem, limit, clusters);            \
+    case 64: return occ_t<WT, 64>(smem, limit, clusters);            \
+    case 128: return occ_t<WT, 128>(smem, limit, clusters);          \
+    default: return cudaErrorInvalidValue;                           \
+    }
+    switch (wtype) {
+    case kWF32: GPT2_CO_CASE(kWF32)
+    case kWF16: GPT2_CO_CASE(kWF16)
+    case kWI4: GPT2_CO_CASE(kWI4)
+    default: return cudaErrorInvalidValue;
+    }
+#undef GPT2_CO_CASE
+}
+
+cudaError_t cluster_tile(int wtype, const void *W, const float *scales, const uint8_t *zeros, int in, int T,
+                         int rdiv, int rows, int cols, void *dW, float *dscales, uint8_t *dzeros, cudaStream_t s)
+{
+    const int per_unit = wtype == kWF32 ? 4 : wtype == kWF16 ? 8 : 32;
+    if (cols % per_unit || in % per_unit || T < 1 || rows < 1) return cudaErrorInvalidValue;
+    const long long total = (long long)T * rows * (cols / per_unit);
+    const int grid = int(std::min<long long>((total + 255) / 256, 4096));
+    k_tile<<<grid, 256, 0, s>>>(wtype, static_cast<const uint8_t *>(W), scales, zeros, in, T, rdiv, rows, cols,
+                                static_cast<uint8_t *>(dW), dscales, dzeros);
+    return cudaGetLastError();
+}
+
+// Largest chunk of rows of `rb`/`srb`/`zrb` bytes each (gran rows at least)
+// that a stage holds; 0 if not even gran rows fit.
+uint32_t cluster_stage_need(int gran, uint32_t rb, uint32_t srb, uint32_t zrb)
+{
+    return seg_stage_bytes(uint32_t(gran), rb, srb, zrb);
+}
+
+#ifdef GPT2_CTRACE
+// Debug builds only: copies the stamps to host memory (`bytes` must be the
+// trace's exact size).
+extern "C" int gpt2_debug_ctrace(void *stamps, size_t bytes)
+{
+    if (!stamps || bytes != sizeof g_ctrace) return 2;
+    if (cudaMemcpyFromSymbol(stamps, g_ctrace, sizeof g_ctrace) != cudaSuccess) return 1;
+    return 0;
+}
+#endif
+
+cudaError_t cluster_gather_qkv(int wtype, const void *W, const float *scales, const uint8_t *zeros, int E, int D,
+                               void *dW, float *dscales, uint8_t *dzeros, cudaStream_t s)
+{
+    if (E % 64 || D % 4 || E % D) return cudaErrorInvalidValue;
+    k_gather_qkv<<<3 * E, 128, 0, s>>>(wtype, static_cast<const uint8_t *>(W), scales, zeros, E, D,
+                                       static_cast<uint8_t *>(dW), dscales, dzeros);
+    return cudaGetLastError();
+}
+
+}  // namespace gpt2

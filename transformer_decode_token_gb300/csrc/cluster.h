@@ -1,0 +1,95 @@
+// Host-visible interface of the cluster decode kernel (cluster.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kernels.h"
+
+namespace gpt2 {
+
+constexpr int kClusterSize = 4;
+constexpr int kClusterRing = 16;   // ring stages of the weight stream (a power of two)
+
+// Weights of one layer as the cluster kernel reads them.  The fc matrix is
+// the canonical [out][in] copy; the QKV matrix is a copy with its rows
+// grouped by (head, rank) (cluster_gather_qkv); the two matrices consumed by
+// column slices are re-tiled so that one CTA's slice is contiguous:
+//   Wo_t: [H][4 ranks][E/4 rows][D cols] (head h's columns, rank's rows)
+//   Wp_t: [nfc][E rows][fr cols]         (fc CTA f's columns fr = F / nfc)
+// Tiles store 16-byte units of a row swizzled by (row & (units - 1)) (units a
+// power of two, at most 8) so that threads reading consecutive rows hit
+// different shared-memory banks.  int4 tiles: codes [rows][cols/2], scales
+// [rows][cols/32] f32, zero points [rows][cols/32] one byte each.
+struct CLayer {
+    const void *Wqkv;
+    const float *qkv_s;
+    const uint8_t *qkv_z;
+    const float *ln1_w, *ln1_b, *attn_b;
+    const void *Wo_t;
+    const float *o_s;
+    const uint8_t *o_z;
+    const float *proj_b;
+    const void *Wfc;
+    const float *fc_s;
+    const uint8_t *fc_z;
+    const float *ln2_w, *ln2_b, *fc_b;
+    const void *Wp_t;
+    const float *p_s;
+    const uint8_t *p_z;
+    const float *mlp_proj_b;
+};
+
+struct ClusterArgs {
+    const CLayer *layers;
+    int32_t L;
+    int32_t n_steps;
+    const int32_t *prompt;
+    int32_t n_prompt, tok_first, pos0;
+    int32_t E, H, D, F, P, V;
+    float eps, scale;
+    int32_t nfc, fr;             // fc CTAs, fc rows (= mlp-proj columns) per fc CTA
+    int32_t head_rpc;            // LM-head rows per CTA
+    int32_t pr_b0;               // floats of the first bias slot of the parameter area
+    // fixed-point sums (int64, 2^32 units) of the residual stream and their
+    // arrival counters (monotonic: pass s of the model waits for s * contributors)
+    long long *acc_new;          // [2 parity][L][E]  x after the attention block
+    long long *acc_next;         // [2 parity][L][E]  x after the MLP block
+    unsigned int *cnt_new;       // [L]
+    unsigned int *cnt_next;      // [L]
+    uint64_t *ll_tok;            // the next token, tagged with its pass
+    float *kcache, *vcache;      // [L][H][P][D]
+    float *logits;
+    unsigned long long *partials;
+    unsigned int *counter;
+    int32_t *out_ids;
+    int32_t out_cap;
+    DeviceState *st;
+    const float *wte, *wpe, *lnf_w, *lnf_b;
+    int32_t wtype;
+    int32_t n_stages;
+    uint32_t stage_bytes, ring_offset;
+};
+
+// Dynamic shared memory before the ring.
+size_t cluster_fixed_smem(int E, int D, int fr, int L);
+cudaError_t launch_cluster(int wtype, const ClusterArgs &a, int n_clusters, size_t smem, cudaStream_t s);
+// Co-resident clusters of kClusterSize CTAs with `smem` bytes each (sets the
+// kernel's shared-memory limit to `limit` first).
+cudaError_t cluster_max_active(int wtype, int D, size_t smem, size_t limit, int *clusters);
+// Writes the tiled copy of a stored [out][in] matrix: T tiles of rows x cols;
+// tile t, row i = canonical row (t % rdiv) * rows + i, columns
+// (t / rdiv) * cols + [0, cols).  int4 also writes per-row scales and one
+// zero-point byte per 32-column group.
+cudaError_t cluster_tile(int wtype, const void *W, const float *scales, const uint8_t *zeros, int in, int T,
+                         int rdiv, int rows, int cols, void *dW, float *dscales, uint8_t *dzeros, cudaStream_t s);
+// Writes the copy of a stored QKV matrix [3E][E] whose rows are grouped by
+// (head, rank): block h * 4 + r holds that CTA's D/4 q rows, then its D/4 k
+// rows, then its D/4 v rows, in the canonical row format.
+cudaError_t cluster_gather_qkv(int wtype, const void *W, const float *scales, const uint8_t *zeros, int E, int D,
+                               void *dW, float *dscales, uint8_t *dzeros, cudaStream_t s);
+// Stage bytes that `gran` rows of a segment need (sections 16-byte aligned).
+uint32_t cluster_stage_need(int gran, uint32_t rb, uint32_t srb, uint32_t zrb);
+
+}  // namespace gpt2
