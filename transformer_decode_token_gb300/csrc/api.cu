@@ -557,7 +557,7 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
     TRY_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, m->device));
     TRY_CUDA(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, m->device));
     if (!coop) return GPT2_ERR_UNSUPPORTED_DEVICE;
-    const size_t limit = size_t(optin) - 4096;   // room for static shared memory
+    const size_t limit = size_t(optin) - 1024;   // room for static shared memory
     const int ns = kClusterRing;
     // co-resident clusters at (nearly) the full shared-memory size
     int max_clusters = 0;
@@ -574,7 +574,9 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
     const int fr = F / nfc;
     const int n_clusters = H + nfc / kClusterSize, grid = n_clusters * kClusterSize;
     if (grid > m->max_head_ctas) return GPT2_ERR_INVALID_ARG;   // per-CTA argmax slots
-    const size_t fixed = cluster_fixed_smem(E, D, fr, L);
+    const int head_rpc = ((V + grid - 1) / grid + 3) / 4 * 4;
+    const int pr_rows = (std::max(std::max(3 * (D / 4), fr), head_rpc) + 3) / 4 * 4;
+    const size_t fixed = cluster_fixed_smem(E, D, fr, L, pr_rows);
     const uint32_t ring_offset = uint32_t((fixed + 127) / 128 * 128);
     if (ring_offset >= limit) return GPT2_ERR_INVALID_ARG;
     const uint32_t stage = uint32_t((limit - ring_offset) / ns) / 16u * 16u;
@@ -623,9 +625,19 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
             o_zp[l] = take(zp_p);
         }
     }
+    std::vector<size_t> o_qc1(L), o_qcb(L), o_fc1(L), o_fcb(L);
+    for (int l = 0; l < L; ++l) {
+        o_qc1[l] = take(size_t(3 * E) * 4);
+        o_qcb[l] = take(size_t(3 * E) * 4);
+        o_fc1[l] = take(size_t(F) * 4);
+        o_fcb[l] = take(size_t(F) * 4);
+    }
+    const size_t head_pad = size_t(head_rpc) * grid;
+    const size_t o_hc1 = take(head_pad * 4), o_hcb = take(head_pad * 4);
     const size_t o_state = off;
-    const size_t o_accn = take(size_t(2) * L * E * 8), o_accx = take(size_t(2) * L * E * 8);
-    const size_t o_cnt = take(size_t(2) * L * 4), o_tok = take(8);
+    const size_t acc_bytes = size_t(2) * L * E * 8 * kClusterAccStride;
+    const size_t o_accn = take(acc_bytes), o_accx = take(acc_bytes);
+    const size_t o_tok = take(8);
     const size_t state_bytes = off - o_state;
     const size_t o_layers = take(sizeof(CLayer) * L);
     uint8_t *B = nullptr;
@@ -670,6 +682,61 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
         TRY_CUDA(cluster_tile(wt, qp.w, qp.scales, qp.zeros, F, nfc, 1, E, fr, B + o_wp[l],
                               i4 ? reinterpret_cast<float *>(B + o_sp[l]) : nullptr, i4 ? B + o_zp[l] : nullptr, s));
     }
+    // LayerNorm folded into the QKV, fc and LM-head rows, from the weights as
+    // stored: c1 = W.gamma, cb = W.beta + bias (QKV in the gathered order)
+    {
+        float *tmp = nullptr, *d1 = nullptr, *d2 = nullptr;
+        const size_t nmax = std::max(size_t(V), size_t(F));
+        cudaError_t e = cudaMalloc(&tmp, size_t(F) * E * 4);
+        if (e == cudaSuccess) e = cudaMalloc(&d1, nmax * 4);
+        if (e == cudaSuccess) e = cudaMalloc(&d2, nmax * 4);
+        std::vector<float> h1(nmax), h2(nmax), hb(nmax), g1(nmax, 0.f), g2(nmax, 0.f);
+        auto fold = [&](const QMat &q, const float *gamma, const float *beta) -> cudaError_t {
+            cudaError_t r = dequant_to_f32(wt, q.w, q.scales, q.zeros, q.in, q.out, tmp, s);
+            if (r == cudaSuccess) r = ln_fold(tmp, gamma, beta, q.in, q.out, d1, d2, s);
+            if (r == cudaSuccess) r = cudaMemcpyAsync(h1.data(), d1, size_t(q.out) * 4, cudaMemcpyDeviceToHost, s);
+            if (r == cudaSuccess) r = cudaMemcpyAsync(h2.data(), d2, size_t(q.out) * 4, cudaMemcpyDeviceToHost, s);
+            return r;
+        };
+        const int q4 = D / 4, Rq = 3 * q4;
+        for (int l = 0; l < L && e == cudaSuccess; ++l) {
+            const LayerDev &Ld = m->layers[l];
+            e = fold(Ld.mat[GPT2_MAT_ATTN], Ld.ln1_w, Ld.ln1_b);
+            if (e == cudaSuccess) e = cudaMemcpyAsync(hb.data(), Ld.attn_b, size_t(3 * E) * 4, cudaMemcpyDeviceToHost, s);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+            if (e != cudaSuccess) break;
+            for (int j = 0; j < 3 * E; ++j) {
+                const int t = j / Rq, i = j % Rq, h = t / kClusterSize, r = t % kClusterSize;
+                const int src = (i / q4) * E + h * D + r * q4 + i % q4;
+                g1[j] = h1[src];
+                g2[j] = h2[src] + hb[src];
+            }
+            e = cudaMemcpy(B + o_qc1[l], g1.data(), size_t(3 * E) * 4, cudaMemcpyHostToDevice);
+            if (e == cudaSuccess) e = cudaMemcpy(B + o_qcb[l], g2.data(), size_t(3 * E) * 4, cudaMemcpyHostToDevice);
+            if (e == cudaSuccess) e = fold(Ld.mat[GPT2_MAT_FC], Ld.ln2_w, Ld.ln2_b);
+            if (e == cudaSuccess) e = cudaMemcpyAsync(hb.data(), Ld.fc_b, size_t(F) * 4, cudaMemcpyDeviceToHost, s);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+            if (e != cudaSuccess) break;
+            for (int j = 0; j < F; ++j) h2[j] += hb[j];
+            e = cudaMemcpy(B + o_fc1[l], h1.data(), size_t(F) * 4, cudaMemcpyHostToDevice);
+            if (e == cudaSuccess) e = cudaMemcpy(B + o_fcb[l], h2.data(), size_t(F) * 4, cudaMemcpyHostToDevice);
+        }
+        if (e == cudaSuccess) e = cudaMemsetAsync(B + o_hc1, 0, head_pad * 4, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(B + o_hcb, 0, head_pad * 4, s);
+        if (e == cudaSuccess) e = ln_fold(m->wte, m->lnf_w, m->lnf_b, E, V, reinterpret_cast<float *>(B + o_hc1),
+                                          reinterpret_cast<float *>(B + o_hcb), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (tmp) cudaFree(tmp);
+        if (d1) cudaFree(d1);
+        if (d2) cudaFree(d2);
+        TRY_CUDA(e);
+    }
+    for (int l = 0; l < L; ++l) {
+        cl[l].q_c1 = reinterpret_cast<const float *>(B + o_qc1[l]);
+        cl[l].q_cb = reinterpret_cast<const float *>(B + o_qcb[l]);
+        cl[l].f_c1 = reinterpret_cast<const float *>(B + o_fc1[l]);
+        cl[l].f_cb = reinterpret_cast<const float *>(B + o_fcb[l]);
+    }
     TRY_CUDA(cudaMemsetAsync(m->c_state, 0, state_bytes, s));
     TRY_CUDA(cudaMemcpyAsync(B + o_layers, cl.data(), sizeof(CLayer) * L, cudaMemcpyHostToDevice, s));
     TRY_CUDA(cudaStreamSynchronize(s));
@@ -688,12 +755,17 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
     a.scale = float(1.0 / std::sqrt(double(D)));
     a.nfc = nfc;
     a.fr = fr;
-    a.head_rpc = (V + grid - 1) / grid;
-    a.pr_b0 = (std::max(3 * D, fr) + 3) / 4 * 4;
+    a.head_rpc = head_rpc;
+    a.pr_rows = pr_rows;
+    a.h_c1 = reinterpret_cast<const float *>(B + o_hc1);
+    a.h_cb = reinterpret_cast<const float *>(B + o_hcb);
+    {
+        const char *fr_env = std::getenv("GPT2_HEAD_L2_FRAC");
+        float f = fr_env ? float(std::atof(fr_env)) : 0.0f;   // measured: no gain on GB300
+        a.head_l2_frac = f < 0.f ? 0.f : (f > 1.f ? 1.f : f);
+    }
     a.acc_new = reinterpret_cast<long long *>(B + o_accn);
     a.acc_next = reinterpret_cast<long long *>(B + o_accx);
-    a.cnt_new = reinterpret_cast<unsigned int *>(B + o_cnt);
-    a.cnt_next = a.cnt_new + L;
     a.ll_tok = reinterpret_cast<uint64_t *>(B + o_tok);
     a.kcache = m->kcache;
     a.vcache = m->vcache;

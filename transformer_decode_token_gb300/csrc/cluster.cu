@@ -74,8 +74,19 @@ constexpr int kCThreads = kCWarps * 32;
 constexpr int kCAll = kCThreads + 32;      // + producer warp
 constexpr int kCRing = kClusterRing;
 constexpr int kRowGroup = 4;
-constexpr float kFix = 4294967296.0f;      // 2^32
-constexpr uint32_t kKvWin = 16384;         // K/V rows of this CTA's positions held in shared memory
+// Residual sums: each contribution is one 64-bit atomic addition of
+//   (round(v * 2^24) + 2^40) + 2^56
+// so a word holds the biased fixed-point sum in its low 56 bits and the
+// number of contributions above.  A reader polls its words until the count
+// is complete: the data is its own arrival flag (one L2 round trip, no
+// counter, no release fence), and integer addition makes the sum independent
+// of the order of the atomics.  |v| < 2^16 keeps each term inside its field
+// (values are clamped there); 2^15 contributions fit.
+constexpr float kFixScale = 16777216.0f;              // 2^24
+constexpr float kFixLimit = 65000.0f;
+constexpr unsigned long long kFixBias = 1ull << 40;
+constexpr int kCountShift = 56;
+constexpr uint32_t kKvWin = 8192;          // K/V rows of this CTA's positions held in shared memory
 constexpr uint32_t kBarBytes = 512;        // mbarriers at the start of shared memory
 
 // Shared-memory layout before the ring (byte offsets): barriers, x, LN(x),
@@ -83,22 +94,21 @@ constexpr uint32_t kBarBytes = 512;        // mbarriers at the start of shared m
 // output, the MLP hidden slice, a scratch vector, the layer parameters, the
 // K/V window and the layer table.
 struct CLayout {
-    uint32_t x, xn, qkv, part, attn, hloc, outv, pr, kvw, layers, end;
+    uint32_t x, qkv, part, attn, hloc, outv, red, pr, kvw, layers, end;
 };
-__host__ __device__ __forceinline__ CLayout cluster_layout(int E, int D, int fr, int L)
+__host__ __device__ __forceinline__ CLayout cluster_layout(int E, int D, int fr, int L, int R)
 {
     auto r16 = [](uint32_t v) { return (v + 15u) & ~15u; };
-    const uint32_t b0 = uint32_t(max(3 * D, fr) + 3) / 4u * 4u;
     CLayout o;
     o.x = kBarBytes;
-    o.xn = o.x + r16(uint32_t(E) * 4u);
-    o.qkv = o.xn + r16(uint32_t(E) * 4u);
+    o.qkv = o.x + r16(uint32_t(E) * 4u);
     o.part = o.qkv + r16(3u * D * 4u);
     o.attn = o.part + r16(uint32_t(kClusterSize) * (D + 4) * 4u);
     o.hloc = o.attn + r16(uint32_t(D) * 4u);
     o.outv = o.hloc + r16(uint32_t(fr) * 4u);
-    o.pr = o.outv + r16((uint32_t(E) + 2u * kCWarps + uint32_t(kCWarps) * D) * 4u);
-    o.kvw = o.pr + r16((2u * E + b0 + uint32_t(E)) * 4u);
+    o.red = o.outv + r16((uint32_t(E) + 2u * kCWarps + uint32_t(kCWarps) * D) * 4u);
+    o.pr = o.red + r16(uint32_t(E) * 4u);
+    o.kvw = o.pr + r16((2u * E + 2u * uint32_t(R)) * 4u);
     o.layers = o.kvw + kKvWin;
     o.end = o.layers + r16(uint32_t(sizeof(CLayer)) * uint32_t(L));
     return o;
@@ -113,6 +123,14 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank)
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
     return r;
 }
+__device__ __forceinline__ void st_async_f32x4(uint32_t addr, const float4 &v, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+                 "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)),
+                 "r"(__float_as_uint(v.w)), "r"(bar)
+                 : "memory");
+}
+
 // Store to a CTA of the cluster that completes `bytes` on that CTA's mbarrier
 // (address and barrier both mapped into the destination CTA).
 __device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar)
@@ -143,12 +161,6 @@ __device__ __forceinline__ int ld_relaxed_i32(const int *p)
     asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p)
-{
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
 __device__ __forceinline__ void st_relaxed_i64(long long *p, long long v)
 {
     asm volatile("st.relaxed.gpu.global.s64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
@@ -156,10 +168,6 @@ __device__ __forceinline__ void st_relaxed_i64(long long *p, long long v)
 __device__ __forceinline__ void red_add_i64(long long *p, long long v)
 {
     asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-__device__ __forceinline__ void red_release_add_u32(unsigned *p, unsigned v)
-{
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ void ll_store64(uint64_t *p, uint32_t bits, uint32_t epoch)
 {
@@ -172,23 +180,32 @@ __device__ __forceinline__ uint64_t ll_load64(const uint64_t *p)
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
     return w;
 }
-__device__ __forceinline__ long long to_fix(float v) { return __float2ll_rn(v * kFix); }
-__device__ __forceinline__ float from_fix(long long v) { return float(__ll2double_rn(v) * (1.0 / 4294967296.0)); }
+__device__ __forceinline__ unsigned long long to_word(float v)
+{
+    v = fminf(fmaxf(v, -kFixLimit), kFixLimit);
+    return (unsigned long long)(__float2ll_rn(v * kFixScale) + (long long)kFixBias) + (1ull << kCountShift);
+}
+__device__ __forceinline__ int word_count(unsigned long long w) { return int(w >> kCountShift); }
+__device__ __forceinline__ float word_value(unsigned long long w)
+{
+    const long long n = (long long)(w >> kCountShift);
+    const long long f = (long long)(w & ((1ull << kCountShift) - 1)) - n * (long long)kFixBias;
+    return float(__ll2double_rn(f) * (1.0 / 16777216.0));
+}
 
 struct Sh {
     int last;
     unsigned long long keys[kCWarps];
-    float red[2][kCWarps];
 };
 
 // Shared-memory views of a consumer thread.
 struct CS {
-    uint64_t *full, *empty, *qkv_bar, *att_bar, *kv_bar, *prm_bar;
-    float *x, *xn, *qkv, *part, *attn, *hloc, *outv, *kvw;
+    uint64_t *full, *empty, *qkv_bar, *att_bar, *kv_bar, *prm_bar, *red_bar, *x_bar;
+    float *x, *qkv, *part, *attn, *hloc, *outv, *red, *kvw;
     float *pr;                 // this layer's LayerNorm parameters and bias slices
     const CLayer *layers;      // the layer table, copied to shared memory
     uint8_t *ring;
-    uint32_t uses_qkv, uses_att, uses_kv, uses_prm;   // barrier phases consumed so far
+    uint32_t uses_qkv, uses_att, uses_kv, uses_prm, uses_red, uses_x;   // barrier phases consumed so far
 #ifdef GPT2_CTRACE
     unsigned long long *twait, *tsub;
 #endif
@@ -419,7 +436,20 @@ __device__ void producer(const ClusterArgs &a, const CLayer *layers, const Role 
     uint32_t k = 0;
     bool ok = true;
     const uint64_t pol = l2_evict_first_policy();
+    uint64_t keep;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
+    // the share of this CTA's LM-head rows that is pulled into L2 at the start
+    // of a pass, while the block phases leave HBM mostly idle
+    const uint32_t head_bytes = uint32_t(G.head.rows) * G.head.rb;
+    const uint32_t pf_bytes = uint32_t(float(head_bytes) * a.head_l2_frac) & ~15u;
+    const uint8_t *head_src = reinterpret_cast<const uint8_t *>(a.wte) + size_t(G.head_row0) * G.head.rb;
     for (int s = 0; s < a.n_steps && ok; ++s) {
+        for (uint32_t off = 0; off < pf_bytes; off += 32768u) {
+            const uint32_t n = min(32768u, pf_bytes - off);
+            asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(head_src + off), "r"(n),
+                         "l"(keep)
+                         : "memory");
+        }
         for (int l = 0; l < a.L && ok; ++l) {
             stream_seg(a, G.a, seg_a(ro, G, layers[l]), ring, full, empty, k, ok, pol);
             if (ok) stream_seg(a, G.b, seg_b(ro, G, layers[l]), ring, full, empty, k, ok, pol);
@@ -447,20 +477,19 @@ __device__ __forceinline__ float nib_minus(uint32_t q, int t, float zf)
     return __uint_as_float(0x4B000000u | ((q >> (4 * t)) & 15u)) - zf;
 }
 
-// Column unit c of canonical row rr of a stage times the matching inputs:
-// fp32 4 inputs (16 bytes), fp16 8 inputs (16 bytes), int4 8 inputs (one
-// 32-bit word).
+// Column unit c of canonical row rr of a stage times its inputs: fp32 4
+// inputs (16 bytes, x0), fp16 8 inputs (16 bytes, x0 then x1), int4 8 inputs
+// (one 32-bit word, x0 then x1).
 template <int WT>
-__device__ __forceinline__ float canon_unit(const uint8_t *stg, const Geo &g, int rr, int c, const float4 *x4, float acc)
+__device__ __forceinline__ float canon_unit(const uint8_t *stg, const Geo &g, int rr, int c, const float4 &x0,
+                                            const float4 &x1, float acc)
 {
     const uint8_t *row = stg + size_t(rr) * g.rb;
     if (WT == kWF32) {
         const float4 v = reinterpret_cast<const float4 *>(row)[c];
-        const float4 x = x4[c];
-        return fmaf(v.w, x.w, fmaf(v.z, x.z, fmaf(v.y, x.y, fmaf(v.x, x.x, acc))));
+        return fmaf(v.w, x0.w, fmaf(v.z, x0.z, fmaf(v.y, x0.y, fmaf(v.x, x0.x, acc))));
     } else if (WT == kWF16) {
         const uint4 u = reinterpret_cast<const uint4 *>(row)[c];
-        const float4 x0 = x4[2 * c], x1 = x4[2 * c + 1];
         const float2 p0 = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
         const float2 p1 = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
         const float2 p2 = __half22float2(*reinterpret_cast<const __half2 *>(&u.z));
@@ -479,7 +508,6 @@ __device__ __forceinline__ float canon_unit(const uint8_t *stg, const Geo &g, in
         const int z = ((stg + g.zoff + size_t(rr) * g.zrb)[grp >> 1] >> ((grp & 1) * 4)) & 15;
         const float s = reinterpret_cast<const float *>(stg + g.soff + size_t(rr) * g.srb)[grp];
         const float zf = 8388608.0f + float(z);
-        const float4 x0 = x4[2 * c], x1 = x4[2 * c + 1];
         float d = nib_minus(q, 0, zf) * x0.x;
         d = fmaf(nib_minus(q, 1, zf), x0.y, d);
         d = fmaf(nib_minus(q, 2, zf), x0.z, d);
@@ -490,6 +518,19 @@ __device__ __forceinline__ float canon_unit(const uint8_t *stg, const Geo &g, in
         d = fmaf(nib_minus(q, 7, zf), x1.w, d);
         return fmaf(s, d, acc);
     }
+}
+
+__device__ __forceinline__ float4 mul4(const float4 &a, const float4 &b)
+{
+    return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w);
+}
+
+// Shifted sum and sum of squares of 4 values (LayerNorm statistics).
+__device__ __forceinline__ void stat4(const float4 &v, float k, float &s, float &q)
+{
+    const float a = v.x - k, b = v.y - k, c = v.z - k, d = v.w - k;
+    s += (a + b) + (c + d);
+    q = fmaf(a, a, fmaf(b, b, fmaf(c, c, fmaf(d, d, q))));
 }
 
 // Sums 4 per-lane values over the warp in 6 shuffles; lanes 0, 8, 16, 24 end
@@ -514,18 +555,21 @@ __device__ __forceinline__ float warp_sum4(float (&v)[kRowGroup], int lane)
     return v[0];
 }
 
-// Stages are consumed in windows of at most half the ring.  At a window's
-// start warp w waits for its stage w (all in parallel), then one CTA barrier
-// makes every stage of the window visible to every warp; at its end one CTA
-// barrier, then one lane per stage releases it (empty barriers count one
-// arrival).  The producer fills the next window while this one is read.
-constexpr int kWindow = kCRing / 2;
-static_assert(kWindow <= kCWarps, "one warp waits for each stage of a window");
+// Stages are consumed in windows of at most the ring's size.  At a window's
+// start the warps wait for its stages (warp w for stages w, w + 8, in
+// parallel), then one CTA barrier makes every stage of the window visible to
+// every warp; at its end one CTA barrier, then one lane per stage releases it
+// (empty barriers count one arrival).  Every stage before a window is
+// released before the window is waited for, so the producer can always fill
+// it.  Layer segments, whose stages are resident ahead of time, take one
+// window of up to the whole ring; the LM head, which streams, takes windows of
+// half the ring so the producer fills one while the other is read.
+constexpr int kStreamWindow = kCRing / 2;
 
 __device__ __forceinline__ void window_acquire(const ClusterArgs &a, const CS &c, uint32_t k, int q0, int q1, bool &ok)
 {
-    const int warp = threadIdx.x >> 5;
-    if (warp < q1 - q0 && ok && !wait_stage(a, c, k + uint32_t(q0 + warp))) ok = false;
+    for (int q = q0 + int(threadIdx.x >> 5); q < q1; q += kCWarps)
+        if (ok && !wait_stage(a, c, k + uint32_t(q))) ok = false;
     csync();
 }
 
@@ -543,20 +587,33 @@ __device__ __forceinline__ const uint8_t *stage_ptr(const ClusterArgs &a, const 
     return c.ring + (kk & (kCRing - 1)) * a.stage_bytes;
 }
 
-// Dot products of the canonical rows of a segment (length in) with xin: each
-// warp takes 4 rows of a window at a time (rows i, i+8, i+16, i+24),
-// lanes over the column units.  Results go to out[i], or, for the LM head
+// Dot products of the canonical rows of a segment (length in) with x: each
+// warp takes 4 rows of a window at a time (rows i, i+8, i+16, i+24), lanes
+// over the column units.  Results go to out[i], or, for the LM head
 // (logit_row0 >= 0), to the logits and this thread's argmax key.
-template <int WT>
-__device__ void canon_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &k, int in, const float *xin,
-                           float *out, int logit_row0, unsigned long long &best, bool &ok)
+//
+// LN: the LayerNorm before the rows is folded into them (see CLayer).  The
+// lanes multiply x by gamma as they read it, and the warp's first row group
+// also accumulates the statistics of x, shifted by x[0] (every lane of the warp
+// together reads x once), so no barrier separates the LayerNorm from the dot
+// products; each result is rstd * (dot - mean * c1[i]) + cb[i].  Every warp
+// reduces the statistics in the same order and gets the same bits.
+template <int WT, bool LN>
+__device__ void canon_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &k, int win, int in,
+                           const float *xin, const float *gamma, const float *c1, const float *cb, float *out,
+                           int logit_row0, unsigned long long &best, bool &ok)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int C = g.chunk, nch = g.nch;
-    const int units = WT == kWF32 ? in >> 2 : in >> 3;
+    constexpr int kIn = WT == kWF32 ? 4 : 8;   // inputs per column unit
+    const int units = in / kIn;
     const float4 *x4 = reinterpret_cast<const float4 *>(xin);
-    for (int q0 = 0; q0 < nch; q0 += kWindow) {
-        const int q1 = min(nch, q0 + kWindow);
+    const float4 *g4 = reinterpret_cast<const float4 *>(gamma);
+    bool have_stats = false;
+    float mean = 0.f, rstd = 0.f;
+    const float shift = LN ? xin[0] : 0.f;
+    for (int q0 = 0; q0 < nch; q0 += win) {
+        const int q1 = min(nch, q0 + win);
         const int r0 = q0 * C, r1 = min(g.rows, q1 * C);
         window_acquire(a, c, k, q0, q1, ok);
         for (int i0 = r0 + warp; i0 < r1; i0 += kCWarps * kRowGroup) {
@@ -573,25 +630,47 @@ __device__ void canon_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &
             }
             TSUB(0, t_a);
             TSTAMP(t_b);
+            const bool stats = LN && !have_stats;
             float acc[kRowGroup] = {0.f, 0.f, 0.f, 0.f};
+            float ssum = 0.f, ssq = 0.f;
             if (ok) {
-                if (ng == kRowGroup) {
-                    for (int u = lane; u < units; u += 32) {
-#pragma unroll
-                        for (int j = 0; j < kRowGroup; ++j) acc[j] = canon_unit<WT>(stg[j], g, rr[j], u, x4, acc[j]);
+                for (int u = lane; u < units; u += 32) {
+                    float4 xa = x4[u * (kIn / 4)], xb = kIn == 8 ? x4[u * 2 + 1] : xa;
+                    if (LN) {
+                        if (stats) {
+                            stat4(xa, shift, ssum, ssq);
+                            if (kIn == 8) stat4(xb, shift, ssum, ssq);
+                        }
+                        xa = mul4(xa, g4[u * (kIn / 4)]);
+                        if (kIn == 8) xb = mul4(xb, g4[u * 2 + 1]);
                     }
-                } else {
-                    for (int u = lane; u < units; u += 32) {
+                    if (ng == kRowGroup) {
+#pragma unroll
+                        for (int j = 0; j < kRowGroup; ++j) acc[j] = canon_unit<WT>(stg[j], g, rr[j], u, xa, xb, acc[j]);
+                    } else {
 #pragma unroll
                         for (int j = 0; j < kRowGroup; ++j)
-                            if (j < ng) acc[j] = canon_unit<WT>(stg[j], g, rr[j], u, x4, acc[j]);
+                            if (j < ng) acc[j] = canon_unit<WT>(stg[j], g, rr[j], u, xa, xb, acc[j]);
                     }
                 }
             }
-            const float t = warp_sum4(acc, lane);
+            if (stats) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+                    ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
+                }
+                const float inv = 1.0f / float(in);
+                const float ms = ssum * inv;
+                mean = shift + ms;
+                rstd = rsqrtf(fmaxf(fmaf(ssq, inv, -ms * ms), 0.f) + a.eps);
+                have_stats = true;
+            }
+            float t = warp_sum4(acc, lane);
             const int j = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
             if ((lane & 7) == 0 && j < ng && ok) {
                 const int i = i0 + j * kCWarps;
+                if (LN) t = rstd * fmaf(-mean, c1[i], t) + cb[i];
                 if (logit_row0 >= 0) {
                     a.logits[logit_row0 + i] = t;
                     const unsigned long long key = argmax_key(t, uint32_t(logit_row0 + i));
@@ -666,8 +745,8 @@ __device__ __forceinline__ float tile_row_dot(const uint8_t *stg, const Geo &g, 
 // thread per row; 16-byte units of row r are stored at u ^ (r & m), so the
 // threads of a quarter-warp read different banks.  out[row] for every row.
 template <int WT>
-__device__ void tile_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &k, int cols, const float *vin,
-                          float *out, bool &ok)
+__device__ void tile_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &k, int win, int cols,
+                          const float *vin, float *out, bool &ok)
 {
     const int tid = threadIdx.x;
     const int per_unit = WT == kWF32 ? 4 : WT == kWF16 ? 8 : 32;
@@ -675,8 +754,8 @@ __device__ void tile_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &k
     const int m = (U & (U - 1)) == 0 ? min(U, 8) - 1 : 0;
     const int C = g.chunk, nch = g.nch;
     const float4 *v4 = reinterpret_cast<const float4 *>(vin);
-    for (int q0 = 0; q0 < nch; q0 += kWindow) {
-        const int q1 = min(nch, q0 + kWindow);
+    for (int q0 = 0; q0 < nch; q0 += win) {
+        const int q1 = min(nch, q0 + win);
         const int r1 = min(g.rows, q1 * C);
         window_acquire(a, c, k, q0, q1, ok);
         if (ok)
@@ -689,82 +768,78 @@ __device__ void tile_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &k
     k += uint32_t(nch);
 }
 
-// LayerNorm of c.x into c.xn with gamma, beta in shared memory (all
-// consumer threads; mean, then the biased variance around it).
-__device__ __forceinline__ void layer_norm(const ClusterArgs &a, CS &c, Sh &sh, const float *gamma, const float *beta)
-{
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, E = a.E;
-    float s = 0.f;
-    for (int i = tid; i < E; i += kCThreads) s += c.x[i];
-    s = warp_sum(s);
-    if (lane == 0) sh.red[0][warp] = s;
-    csync();
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < kCWarps; ++w) tot += sh.red[0][w];
-    const float mean = tot / float(E);
-    float q = 0.f;
-    for (int i = tid; i < E; i += kCThreads) {
-        const float d = c.x[i] - mean;
-        q = fmaf(d, d, q);
-    }
-    q = warp_sum(q);
-    if (lane == 0) sh.red[1][warp] = q;
-    csync();
-    float ss = 0.f;
-#pragma unroll
-    for (int w = 0; w < kCWarps; ++w) ss += sh.red[1][w];
-    const float rstd = 1.0f / sqrtf(ss / float(E) + a.eps);
-    for (int i = tid; i < E; i += kCThreads) c.xn[i] = (c.x[i] - mean) * rstd * gamma[i] + beta[i];
-    csync();
-}
-
 constexpr int kMaxPerThread = 8;   // n_embd <= 8 * kCThreads
 
-// Wait until `cnt` reaches `target`, then read the fixed-point sum into dst
-// (all loads issued before the first is used).
-__device__ __forceinline__ void read_sum(const ClusterArgs &a, const unsigned *cnt, unsigned target,
-                                         const long long *src, float *dst, bool &ok)
+__device__ __forceinline__ unsigned long long ld_word(const long long *p)
 {
-    const int tid = threadIdx.x;
-    __shared__ int s_ok;
-    if (tid == 0) {
-        Waiter w;
-        bool good = ok;
-        while (good && int(ld_acquire_u32(cnt) - target) < 0)   // counters wrap; differences stay small
-            if (!keep_waiting(a, w, 5000 + int(blockIdx.x))) good = false;
-        s_ok = good ? 1 : 0;
-    }
-    csync();
-    if (!s_ok) ok = false;
-    long long v[kMaxPerThread];
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Reads a residual sum into c.x once every word holds `count` contributions.
+// The CTAs of a cluster share the work: rank r polls words [r E/4, (r+1) E/4)
+// (each thread its own words), then stores their values into c.x of all four
+// CTAs; every thread then waits for the whole vector on x_bar.  A fence after
+// the poll orders what follows after the contributions.
+__device__ __forceinline__ void read_sum(const ClusterArgs &a, CS &c, int count, const long long *src, bool &ok)
+{
+    const int tid = threadIdx.x, rq = a.E / kClusterSize;
+    const int r = int(blockIdx.x) % kClusterSize;
+    if (tid == 0) mbar_arrive_expect_tx(c.x_bar, uint32_t(a.E) * 4u);
+    constexpr int kW = kMaxPerThread / kClusterSize;   // words per thread
+    unsigned long long v[kW];
 #pragma unroll
-    for (int j = 0; j < kMaxPerThread; ++j) {
-        const int i = tid + j * kCThreads;
-        v[j] = i < a.E ? __ldcg(src + i) : 0;
+    for (int j = 0; j < kW; ++j) {
+        const int t = tid + j * kCThreads;
+        v[j] = t < rq ? ld_word(src + size_t(r * rq + t) * kClusterAccStride) : 0ull;
     }
+    Waiter w;
+    for (;;) {
+        bool done = true;
 #pragma unroll
-    for (int j = 0; j < kMaxPerThread; ++j) {
-        const int i = tid + j * kCThreads;
-        if (i < a.E) dst[i] = from_fix(v[j]);
+        for (int j = 0; j < kW; ++j) {
+            const int t = tid + j * kCThreads;
+            if (t < rq && word_count(v[j]) < count) {
+                done = false;
+                v[j] = ld_word(src + size_t(r * rq + t) * kClusterAccStride);
+            }
+        }
+        if (done || !ok) break;
+        if (!keep_waiting(a, w, 5000 + int(blockIdx.x))) {
+            ok = false;
+            break;
+        }
     }
-    csync();
+    __threadfence();
+    const uint32_t xbar = smem_addr(c.x_bar);
+#pragma unroll
+    for (int j = 0; j < kW; ++j) {
+        const int t = tid + j * kCThreads;
+        if (t < rq) {
+            const float val = word_value(v[j]);
+            const uint32_t dsm = smem_addr(c.x + r * rq + t);
+#pragma unroll
+            for (int dst = 0; dst < kClusterSize; ++dst)
+                st_async_f32(mapa(dsm, uint32_t(dst)), val, mapa(xbar, uint32_t(dst)));
+        }
+    }
+    if (!wait_tx_bar(a, c.x_bar, c.uses_x, 5500 + int(blockIdx.x))) ok = false;
 }
 
 // Adds values[i] (+ extra[base + i] + extra2[i] if extra is given) into
-// sum[base + i], i < n, as fixed point; then one arrival on `cnt`.  The
-// release by thread 0 after the barrier publishes every thread's additions.
+// sum[base + i], i < n, one contribution per word.  The closing barrier keeps
+// the parameter area (extra2) unchanged until every thread has read it.
 __device__ __forceinline__ void add_sum(long long *sum, int base, const float *values, const float *extra,
-                                        const float *extra2, int n, unsigned *cnt)
+                                        const float *extra2, int n)
 {
     const int tid = threadIdx.x;
     for (int i = tid; i < n; i += kCThreads) {
         float v = values[i];
         if (extra) v += extra[base + i] + extra2[i];
-        red_add_i64(sum + base + i, to_fix(v));
+        red_add_i64(sum + size_t(base + i) * kClusterAccStride, (long long)to_word(v));
     }
     csync();
-    if (tid == 0) red_release_add_u32(cnt, 1u);
 }
 
 // ---- attention of one head, positions split over the cluster ----------------------
@@ -792,9 +867,12 @@ __device__ void attention(const ClusterArgs &a, CS &c, int l, int h, int r, int 
         while (ok && !mbar_try_wait(c.kv_bar, par))
             if (!keep_waiting(a, w, 4000 + int(blockIdx.x))) ok = false;
     }
-    // this CTA's positions, split over warps; online softmax in 32-position tiles
+    // this CTA's positions, split over warps; online softmax in 32-position
+    // tiles.  Up to 32 positions take one warp, which sends its partial state
+    // directly (no merge across warps).
     const int cnt = max(0, j1 - j0);
-    const int per = (cnt + kCWarps - 1) / kCWarps;
+    const bool single = cnt <= 32;
+    const int per = single ? 32 : (cnt + kCWarps - 1) / kCWarps;
     const int w0 = j0 + warp * per, w1 = min(j1, w0 + per);
     float m = -INFINITY, lsum = 0.f, o[DPL];
 #pragma unroll
@@ -836,36 +914,54 @@ __device__ void attention(const ClusterArgs &a, CS &c, int l, int h, int r, int 
         }
         m = mn;
     }
-    // merge the warps (shared scratch = the part slot of this rank, staged in outv)
-    float *wm = c.outv, *wl = c.outv + kCWarps, *wo = c.outv + 2 * kCWarps;
-    if (lane == 0) {
-        wm[warp] = m;
-        wl[warp] = lsum;
-    }
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) wo[warp * D + lane + 32 * i] = o[i];
-    csync();
     // this CTA's (max, sum, unnormalised output) to every CTA of the cluster;
     // the stores complete on each receiver's att_bar
     const uint32_t slot = smem_addr(c.part + size_t(r) * (D + 4));
     const uint32_t abar = smem_addr(c.att_bar);
-    for (int t = tid; t < D + 2; t += kCThreads) {
-        float M = -INFINITY;
-        for (int w = 0; w < kCWarps; ++w)
-            if (wl[w] > 0.f) M = fmaxf(M, wm[w]);
-        float L = 0.f, O = 0.f;
-        for (int w = 0; w < kCWarps; ++w) {
-            if (wl[w] > 0.f) {
-                const float e = expf(wm[w] - M);
-                L = fmaf(wl[w], e, L);
-                if (t >= 2) O = fmaf(wo[w * D + t - 2], e, O);
+    if (single) {
+        if (warp == 0) {
+#pragma unroll
+            for (int dd = 0; dd < DPL; ++dd) {
+                const uint32_t off = uint32_t(lane + 32 * dd + 4) * 4u;
+#pragma unroll
+                for (int dst = 0; dst < kClusterSize; ++dst)
+                    st_async_f32(mapa(slot + off, uint32_t(dst)), o[dd], mapa(abar, uint32_t(dst)));
+            }
+            if (lane < 2) {
+                const float v = lane == 0 ? (lsum > 0.f ? m : -INFINITY) : lsum;
+#pragma unroll
+                for (int dst = 0; dst < kClusterSize; ++dst)
+                    st_async_f32(mapa(slot + uint32_t(lane) * 4u, uint32_t(dst)), v, mapa(abar, uint32_t(dst)));
             }
         }
-        const float v = t == 0 ? M : (t == 1 ? L : O);
-        const uint32_t off = t < 2 ? uint32_t(t) * 4u : uint32_t(t + 2) * 4u;
+    } else {
+        // merge the warps through shared scratch (outv), then send
+        float *wm = c.outv, *wl = c.outv + kCWarps, *wo = c.outv + 2 * kCWarps;
+        if (lane == 0) {
+            wm[warp] = m;
+            wl[warp] = lsum;
+        }
 #pragma unroll
-        for (int dst = 0; dst < kClusterSize; ++dst)
-            st_async_f32(mapa(slot + off, uint32_t(dst)), v, mapa(abar, uint32_t(dst)));
+        for (int i = 0; i < DPL; ++i) wo[warp * D + lane + 32 * i] = o[i];
+        csync();
+        for (int t = tid; t < D + 2; t += kCThreads) {
+            float M = -INFINITY;
+            for (int w = 0; w < kCWarps; ++w)
+                if (wl[w] > 0.f) M = fmaxf(M, wm[w]);
+            float L = 0.f, O = 0.f;
+            for (int w = 0; w < kCWarps; ++w) {
+                if (wl[w] > 0.f) {
+                    const float e = expf(wm[w] - M);
+                    L = fmaf(wl[w], e, L);
+                    if (t >= 2) O = fmaf(wo[w * D + t - 2], e, O);
+                }
+            }
+            const float v = t == 0 ? M : (t == 1 ? L : O);
+            const uint32_t off = t < 2 ? uint32_t(t) * 4u : uint32_t(t + 2) * 4u;
+#pragma unroll
+            for (int dst = 0; dst < kClusterSize; ++dst)
+                st_async_f32(mapa(slot + off, uint32_t(dst)), v, mapa(abar, uint32_t(dst)));
+        }
     }
     if (!wait_tx_bar(a, c.att_bar, c.uses_att, 6000 + int(blockIdx.x))) ok = false;
     // combine the 4 ranks in rank order (every CTA gets the same bits)
@@ -886,7 +982,7 @@ __device__ void attention(const ClusterArgs &a, CS &c, int l, int h, int r, int 
         }
         c.attn[t] = O / L;
     }
-    csync();
+    // (the next phase opens with a CTA barrier, which publishes c.attn)
 }
 
 // Issue the bulk copies of this CTA's cached K/V rows of a head (before q, k,
@@ -918,10 +1014,11 @@ __device__ __forceinline__ void zero_other_parity(const ClusterArgs &a, int par)
     const size_t words = size_t(a.L) * a.E;
     const size_t per = (words + gridDim.x - 1) / gridDim.x;
     const size_t w0 = size_t(blockIdx.x) * per, w1 = min(words, w0 + per);
-    long long *zn = a.acc_new + size_t(1 - par) * words, *zx = a.acc_next + size_t(1 - par) * words;
+    long long *zn = a.acc_new + size_t(1 - par) * words * kClusterAccStride;
+    long long *zx = a.acc_next + size_t(1 - par) * words * kClusterAccStride;
     for (size_t i = w0 + threadIdx.x; i < w1; i += kCThreads) {
-        st_relaxed_i64(zn + i, 0);
-        st_relaxed_i64(zx + i, 0);
+        st_relaxed_i64(zn + i * kClusterAccStride, 0);
+        st_relaxed_i64(zx + i * kClusterAccStride, 0);
     }
 }
 
@@ -972,37 +1069,44 @@ __device__ __forceinline__ void finish_head(const ClusterArgs &a, Sh &sh, int s,
     csync();
 }
 
-// Bulk copies of the LayerNorm parameters and bias slices a CTA needs in one
-// layer (L != nullptr) or in the LM head (L == nullptr) into c.pr, completing
-// on prm_bar.  Thread 0, before the wait for the layer's input, so the copies
-// overlap that wait.  The area's previous contents were last read before the
-// barrier that precedes this call.
-__device__ __forceinline__ void issue_params(const ClusterArgs &a, CS &c, const Role &ro, const CLayer *L)
+// Bulk copies of what a CTA needs besides weights in one layer
+// (L != nullptr) or in the LM head (L == nullptr) into the parameter area
+// c.pr: gamma [E], the fold vectors c1 and cb of its rows [pr_rows each], and
+// the bias slice of its residual sum [E].  Issued by thread 0 before the wait
+// for the layer's input, so the copies overlap that wait; the area's previous
+// contents were last read before the barrier that precedes this call.
+__device__ __forceinline__ void issue_params(const ClusterArgs &a, CS &c, const Role &ro, const Geos &G,
+                                             const CLayer *L)
 {
     if (threadIdx.x != 0) return;
-    const int E = a.E, D = a.D;
-    float *pw = c.pr, *pb = c.pr + E, *b0 = c.pr + 2 * E, *b1 = c.pr + 2 * E + a.pr_b0;
+    const int E = a.E, R = a.pr_rows;
+    float *pg = c.pr, *p1 = c.pr + E, *pc = c.pr + E + R, *pb = c.pr + E + 2 * R;
     const uint32_t ev = uint32_t(E) * 4u;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (!L) {
-        mbar_arrive_expect_tx(c.prm_bar, 2u * ev);
-        bulk_g2s(pw, a.lnf_w, ev, c.prm_bar);
-        bulk_g2s(pb, a.lnf_b, ev, c.prm_bar);
+        const uint32_t rv = uint32_t(a.head_rpc) * 4u;   // padded vectors: whole slots exist
+        const size_t r0 = size_t(ro.g) * a.head_rpc;
+        mbar_arrive_expect_tx(c.prm_bar, ev + 2u * rv);
+        bulk_g2s(pg, a.lnf_w, ev, c.prm_bar);
+        bulk_g2s(p1, a.h_c1 + r0, rv, c.prm_bar);
+        bulk_g2s(pc, a.h_cb + r0, rv, c.prm_bar);
     } else if (ro.head) {
-        const uint32_t dv = uint32_t(D) * 4u, qv = ev / kClusterSize;
-        mbar_arrive_expect_tx(c.prm_bar, 2u * ev + 3u * dv + (ro.h == 0 ? qv : 0u));
-        bulk_g2s(pw, L->ln1_w, ev, c.prm_bar);
-        bulk_g2s(pb, L->ln1_b, ev, c.prm_bar);
-        for (int part = 0; part < 3; ++part)
-            bulk_g2s(b0 + part * D, L->attn_b + size_t(part) * E + size_t(ro.h) * D, dv, c.prm_bar);
-        if (ro.h == 0) bulk_g2s(b1, L->proj_b + size_t(ro.r) * (E / kClusterSize), qv, c.prm_bar);
+        const uint32_t rv = uint32_t(G.a.rows) * 4u, qv = ev / kClusterSize;
+        const size_t r0 = size_t(ro.h * kClusterSize + ro.r) * G.a.rows;
+        mbar_arrive_expect_tx(c.prm_bar, ev + 2u * rv + (ro.h == 0 ? qv : 0u));
+        bulk_g2s(pg, L->ln1_w, ev, c.prm_bar);
+        bulk_g2s(p1, L->q_c1 + r0, rv, c.prm_bar);
+        bulk_g2s(pc, L->q_cb + r0, rv, c.prm_bar);
+        if (ro.h == 0) bulk_g2s(pb, L->proj_b + size_t(ro.r) * (E / kClusterSize), qv, c.prm_bar);
     } else {
-        const uint32_t fv = uint32_t(a.fr) * 4u;
-        mbar_arrive_expect_tx(c.prm_bar, 2u * ev + fv + (ro.f == 0 ? ev : 0u));
-        bulk_g2s(pw, L->ln2_w, ev, c.prm_bar);
-        bulk_g2s(pb, L->ln2_b, ev, c.prm_bar);
-        bulk_g2s(b0, L->fc_b + size_t(ro.f) * a.fr, fv, c.prm_bar);
-        if (ro.f == 0) bulk_g2s(b1, L->mlp_proj_b, ev, c.prm_bar);
+        const uint32_t rv = uint32_t(a.fr) * 4u, qv = ev / kClusterSize;
+        const size_t r0 = size_t(ro.f) * a.fr;
+        const bool first = ro.f < kClusterSize;   // fc cluster 0 adds x and the bias, a slice per rank
+        mbar_arrive_expect_tx(c.prm_bar, ev + 2u * rv + (first ? qv : 0u));
+        bulk_g2s(pg, L->ln2_w, ev, c.prm_bar);
+        bulk_g2s(p1, L->f_c1 + r0, rv, c.prm_bar);
+        bulk_g2s(pc, L->f_cb + r0, rv, c.prm_bar);
+        if (first) bulk_g2s(pb, L->mlp_proj_b + size_t(ro.r) * (E / kClusterSize), qv, c.prm_bar);
     }
 }
 
@@ -1011,9 +1115,8 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
 {
     const int tid = threadIdx.x;
     const uint32_t seq0 = uint32_t(ld_relaxed_i32(&a.st->seq));
-    const unsigned n_head_ctas = unsigned(a.H * kClusterSize);
-    const int E = a.E, q4 = D / 4, rq = E / kClusterSize;
-    const float *b0 = c.pr + 2 * E, *b1 = c.pr + 2 * E + a.pr_b0;
+    const int E = a.E, q4 = D / 4, rq = E / kClusterSize, R = a.pr_rows;
+    const float *p1 = c.pr + E, *pc = c.pr + E + R, *pb = c.pr + E + 2 * R;
     uint32_t k = 0;
     bool ok = true;
     for (int s = 0; s < a.n_steps; ++s) {
@@ -1023,9 +1126,9 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
         unsigned long long best = 0ull;
         for (int l = 0; l < a.L; ++l) {
             const CLayer &L = c.layers[l];
-            long long *an = a.acc_new + (size_t(par) * a.L + l) * E;
+            long long *an = a.acc_new + (size_t(par) * a.L + l) * E * kClusterAccStride;
             CTRACE(s, l * 16 + 0);
-            issue_params(a, c, ro, &L);
+            issue_params(a, c, ro, G, &L);
             if (ro.head) {
                 if (tid == 0) {   // this layer's phases of the two cluster exchanges
                     mbar_arrive_expect_tx(c.qkv_bar, 3u * D * 4u);
@@ -1060,22 +1163,21 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                     zero_other_parity(a, par);
                     csync();
                 } else {
-                    read_sum(a, a.cnt_next + (l - 1), seq * unsigned(a.nfc),
-                             a.acc_next + (size_t(par) * a.L + (l - 1)) * E, c.x, ok);
+                    read_sum(a, c, a.nfc / kClusterSize,
+                             a.acc_next + (size_t(par) * a.L + (l - 1)) * E * kClusterAccStride, ok);
                 }
                 CTRACE(s, l * 16 + 1);
                 if (!wait_tx_bar(a, c.prm_bar, c.uses_prm, 9000 + int(blockIdx.x))) ok = false;
-                layer_norm(a, c, sh, c.pr, c.pr + E);
                 CTRACE(s, l * 16 + 2);
-                // q, k, v quarters of this head (+ bias) -> every CTA of the cluster
-                canon_rows<WT>(a, c, G.a, k, E, c.xn, c.outv, -1, best, ok);
-                csync();
-                CTRACE(s, l * 16 + 3);
+                // this CTA's q, k, v rows (LayerNorm folded, bias included) ->
+                // every CTA of the cluster
+                canon_rows<WT, true>(a, c, G.a, k, kCRing, E, c.x, c.pr, p1, pc, c.outv, -1, best, ok);
+                CTRACE(s, l * 16 + 3);   // (the window's closing barrier published c.outv)
                 {
                     const uint32_t qbar = smem_addr(c.qkv_bar);
                     for (int t = tid; t < 3 * q4; t += kCThreads) {
                         const int part = t / q4, d = ro.r * q4 + t % q4;
-                        const float v = c.outv[t] + b0[part * D + d];
+                        const float v = c.outv[t];
                         const uint32_t dsm = smem_addr(c.qkv + part * D + d);
 #pragma unroll
                         for (int dst = 0; dst < kClusterSize; ++dst)
@@ -1087,39 +1189,54 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                 attention<D>(a, c, l, ro.h, ro.r, pos, ok);
                 CTRACE(s, l * 16 + 5);
                 // the head's slice of the output projection, rows rank*E/4.. (+ x + bias once, by head 0)
-                tile_rows<WT>(a, c, G.b, k, D, c.attn, c.outv, ok);
+                tile_rows<WT>(a, c, G.b, k, kCRing, D, c.attn, c.outv, ok);
                 CTRACE(s, l * 16 + 6);
-                add_sum(an, ro.r * rq, c.outv, ro.h == 0 ? c.x : nullptr, b1, rq, a.cnt_new + l);
+                add_sum(an, ro.r * rq, c.outv, ro.h == 0 ? c.x : nullptr, pb, rq);
                 CTRACE(s, l * 16 + 7);
             } else {
-                read_sum(a, a.cnt_new + l, seq * n_head_ctas, an, c.x, ok);
+                if (tid == 0) mbar_arrive_expect_tx(c.red_bar, uint32_t(E) * 4u);   // this layer's partial slices
+                read_sum(a, c, a.H, an, ok);
                 if (l == 0) zero_other_parity(a, par);
                 CTRACE(s, l * 16 + 1);
                 if (!wait_tx_bar(a, c.prm_bar, c.uses_prm, 9000 + int(blockIdx.x))) ok = false;
-                layer_norm(a, c, sh, c.pr, c.pr + E);
                 CTRACE(s, l * 16 + 2);
-                canon_rows<WT>(a, c, G.a, k, E, c.xn, c.outv, -1, best, ok);
-                csync();
+                canon_rows<WT, true>(a, c, G.a, k, kCRing, E, c.x, c.pr, p1, pc, c.outv, -1, best, ok);
                 CTRACE(s, l * 16 + 3);
-                for (int t = tid; t < a.fr; t += kCThreads) c.hloc[t] = gelu_new(c.outv[t] + b0[t]);
+                for (int t = tid; t < a.fr; t += kCThreads) c.hloc[t] = gelu_new(c.outv[t]);
                 csync();
                 CTRACE(s, l * 16 + 4);
-                tile_rows<WT>(a, c, G.b, k, a.fr, c.hloc, c.outv, ok);
+                tile_rows<WT>(a, c, G.b, k, kCRing, a.fr, c.hloc, c.outv, ok);
                 CTRACE(s, l * 16 + 5);
-                add_sum(a.acc_next + (size_t(par) * a.L + l) * E, 0, c.outv, ro.f == 0 ? c.x : nullptr, b1, E,
-                        a.cnt_next + l);
+                // the cluster's four partial vectors meet first: rank r sums
+                // slice r of all four (in rank order) and adds that once
+                {
+                    const int q = rq / 4;   // float4 per slice
+                    const uint32_t rbar = smem_addr(c.red_bar);
+                    const float4 *o4 = reinterpret_cast<const float4 *>(c.outv);
+                    for (int t = tid; t < kClusterSize * q; t += kCThreads) {
+                        const int dst = t / q, u = t % q;
+                        const uint32_t slot = smem_addr(c.red + ro.r * rq + u * 4);
+                        st_async_f32x4(mapa(slot, uint32_t(dst)), o4[dst * q + u], mapa(rbar, uint32_t(dst)));
+                    }
+                    if (!wait_tx_bar(a, c.red_bar, c.uses_red, 9500 + int(blockIdx.x))) ok = false;
+                    for (int i = tid; i < rq; i += kCThreads)
+                        c.outv[i] = ((c.red[i] + c.red[rq + i]) + c.red[2 * rq + i]) + c.red[3 * rq + i];
+                    csync();
+                }
+                add_sum(a.acc_next + (size_t(par) * a.L + l) * E * kClusterAccStride, ro.r * rq, c.outv,
+                        ro.f < kClusterSize ? c.x : nullptr, pb, rq);
                 CTRACE(s, l * 16 + 6);
             }
         }
         // LM head (every CTA)
         CTRACE(s, 200);
-        issue_params(a, c, ro, nullptr);
-        read_sum(a, a.cnt_next + (a.L - 1), seq * unsigned(a.nfc), a.acc_next + (size_t(par) * a.L + (a.L - 1)) * E,
-                 c.x, ok);
+        issue_params(a, c, ro, G, nullptr);
+        read_sum(a, c, a.nfc / kClusterSize, a.acc_next + (size_t(par) * a.L + (a.L - 1)) * E * kClusterAccStride,
+                 ok);
         CTRACE(s, 201);
         if (!wait_tx_bar(a, c.prm_bar, c.uses_prm, 9000 + int(blockIdx.x))) ok = false;
-        layer_norm(a, c, sh, c.pr, c.pr + E);
-        canon_rows<kWF32>(a, c, G.head, k, E, c.xn, nullptr, G.head_row0, best, ok);
+        canon_rows<kWF32, true>(a, c, G.head, k, kStreamWindow, E, c.x, c.pr, p1, pc, nullptr, G.head_row0, best,
+                                ok);
         CTRACE(s, 202);
         finish_head(a, sh, s, seq, best);
         CTRACE(s, 203);
@@ -1134,7 +1251,7 @@ __global__ void __launch_bounds__(kCAll, 1) k_decode_cluster(const ClusterArgs a
 #ifdef GPT2_CTRACE
     __shared__ unsigned long long twait, tsub[3];
 #endif
-    const CLayout lo = cluster_layout(a.E, D, a.fr, a.L);
+    const CLayout lo = cluster_layout(a.E, D, a.fr, a.L, a.pr_rows);
     CS c;
     c.full = reinterpret_cast<uint64_t *>(smem);
     c.empty = c.full + kCRing;
@@ -1142,8 +1259,10 @@ __global__ void __launch_bounds__(kCAll, 1) k_decode_cluster(const ClusterArgs a
     c.att_bar = c.qkv_bar + 1;
     c.kv_bar = c.qkv_bar + 2;
     c.prm_bar = c.qkv_bar + 3;
+    c.red_bar = c.qkv_bar + 4;
+    c.x_bar = c.qkv_bar + 5;
+    c.red = reinterpret_cast<float *>(smem + lo.red);
     c.x = reinterpret_cast<float *>(smem + lo.x);
-    c.xn = reinterpret_cast<float *>(smem + lo.xn);
     c.qkv = reinterpret_cast<float *>(smem + lo.qkv);
     c.part = reinterpret_cast<float *>(smem + lo.part);
     c.attn = reinterpret_cast<float *>(smem + lo.attn);
@@ -1154,7 +1273,7 @@ __global__ void __launch_bounds__(kCAll, 1) k_decode_cluster(const ClusterArgs a
     CLayer *tab = reinterpret_cast<CLayer *>(smem + lo.layers);
     c.layers = tab;
     c.ring = smem + a.ring_offset;
-    c.uses_qkv = c.uses_att = c.uses_kv = c.uses_prm = 0;
+    c.uses_qkv = c.uses_att = c.uses_kv = c.uses_prm = c.uses_red = c.uses_x = 0;
 #ifdef GPT2_CTRACE
     c.twait = &twait;
     c.tsub = tsub;
@@ -1176,6 +1295,8 @@ __global__ void __launch_bounds__(kCAll, 1) k_decode_cluster(const ClusterArgs a
         mbar_init(c.att_bar, 1);
         mbar_init(c.kv_bar, 1);
         mbar_init(c.prm_bar, 1);
+        mbar_init(c.red_bar, 1);   // + the bytes of the cluster's four partial slices
+        mbar_init(c.x_bar, 1);     // + the bytes of x, a quarter from each CTA of the cluster
         mbar_init_fence();
         sh.last = 0;
 #ifdef GPT2_CTRACE
@@ -1296,9 +1417,9 @@ __global__ void __launch_bounds__(128) k_gather_qkv(int wt, const uint8_t *W, co
 
 }  // namespace
 
-size_t cluster_fixed_smem(int E, int D, int fr, int L)
+size_t cluster_fixed_smem(int E, int D, int fr, int L, int pr_rows)
 {
-    return (size_t(cluster_layout(E, D, fr, L).end) + 127) / 128 * 128;
+    return (size_t(cluster_layout(E, D, fr, L, pr_rows).end) + 127) / 128 * 128;
 }
 
 cudaError_t launch_cluster(int wtype, const ClusterArgs &a, int n_clusters, size_t smem, cudaStream_t s)

@@ -11,6 +11,12 @@ namespace gpt2 {
 
 constexpr int kClusterSize = 4;
 constexpr int kClusterRing = 16;   // ring stages of the weight stream (a power of two)
+// Words between consecutive elements of a residual sum (1: contiguous; 4: one
+// element per 32-byte sector, spreading the atomics over more L2 lines).
+#ifndef GPT2_ACC_STRIDE
+#define GPT2_ACC_STRIDE 1
+#endif
+constexpr int kClusterAccStride = GPT2_ACC_STRIDE;
 
 // Weights of one layer as the cluster kernel reads them.  The fc matrix is
 // the canonical [out][in] copy; the QKV matrix is a copy with its rows
@@ -39,6 +45,11 @@ struct CLayer {
     const float *p_s;
     const uint8_t *p_z;
     const float *mlp_proj_b;
+    // LayerNorm folded into the rows that follow it:
+    //   W.LN(x) + b = rstd * (W.(gamma*x) - mean * c1) + cb,
+    //   c1 = W.gamma, cb = W.beta + b (from the weights as stored)
+    const float *q_c1, *q_cb;    // [3E], in the gathered QKV row order
+    const float *f_c1, *f_cb;    // [F]
 };
 
 struct ClusterArgs {
@@ -50,14 +61,15 @@ struct ClusterArgs {
     int32_t E, H, D, F, P, V;
     float eps, scale;
     int32_t nfc, fr;             // fc CTAs, fc rows (= mlp-proj columns) per fc CTA
-    int32_t head_rpc;            // LM-head rows per CTA
-    int32_t pr_b0;               // floats of the first bias slot of the parameter area
-    // fixed-point sums (int64, 2^32 units) of the residual stream and their
-    // arrival counters (monotonic: pass s of the model waits for s * contributors)
-    long long *acc_new;          // [2 parity][L][E]  x after the attention block
-    long long *acc_next;         // [2 parity][L][E]  x after the MLP block
-    unsigned int *cnt_new;       // [L]
-    unsigned int *cnt_next;      // [L]
+    int32_t head_rpc;            // LM-head rows per CTA (a multiple of 4)
+    int32_t pr_rows;             // row slots of the parameter area (a multiple of 4)
+    const float *h_c1, *h_cb;    // LM head: wte.gamma_f, wte.beta_f, padded to head_rpc * grid
+    float head_l2_frac;          // share of each CTA's LM-head rows prefetched into L2 at pass start
+    // residual-stream sums, one 64-bit word per element holding the biased
+    // fixed-point sum and the number of contributions (double-buffered by
+    // pass parity; the other parity is zeroed during a pass)
+    long long *acc_new;          // [2 parity][L][E][kClusterAccStride]  x after the attention block
+    long long *acc_next;         // [2 parity][L][E][kClusterAccStride]  x after the MLP block
     uint64_t *ll_tok;            // the next token, tagged with its pass
     float *kcache, *vcache;      // [L][H][P][D]
     float *logits;
@@ -73,7 +85,7 @@ struct ClusterArgs {
 };
 
 // Dynamic shared memory before the ring.
-size_t cluster_fixed_smem(int E, int D, int fr, int L);
+size_t cluster_fixed_smem(int E, int D, int fr, int L, int pr_rows);
 cudaError_t launch_cluster(int wtype, const ClusterArgs &a, int n_clusters, size_t smem, cudaStream_t s);
 // Co-resident clusters of kClusterSize CTAs with `smem` bytes each (sets the
 // kernel's shared-memory limit to `limit` first).
