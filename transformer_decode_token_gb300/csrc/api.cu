@@ -552,7 +552,7 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
     const int L = c.n_layer, E = c.n_embd, H = c.n_head, D = E / H, V = c.vocab_size, F = 4 * E;
     const int wt = m->wdtype;
     if (E % 64) return GPT2_ERR_INVALID_ARG;   // E/4 tile rows in chunks of 16
-    if (E > 2048) return GPT2_ERR_INVALID_ARG;  // sums read 8 words per thread
+    if (E > 1024) return GPT2_ERR_INVALID_ARG;  // input vectors held in registers (1024 values)
     int optin = 0, coop = 0;
     TRY_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, m->device));
     TRY_CUDA(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, m->device));
@@ -572,6 +572,7 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
         }
     if (nfc == 0) return GPT2_ERR_INVALID_ARG;
     const int fr = F / nfc;
+    if (fr > 16 + 8 * D || 3 * (D / 4) > 16 + 8 * D) return GPT2_ERR_INVALID_ARG;   // canon_rows outputs below its x*gamma scratch
     const int n_clusters = H + nfc / kClusterSize, grid = n_clusters * kClusterSize;
     if (grid > m->max_head_ctas) return GPT2_ERR_INVALID_ARG;   // per-CTA argmax slots
     const int head_rpc = ((V + grid - 1) / grid + 3) / 4 * 4;
@@ -759,11 +760,6 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
     a.pr_rows = pr_rows;
     a.h_c1 = reinterpret_cast<const float *>(B + o_hc1);
     a.h_cb = reinterpret_cast<const float *>(B + o_hcb);
-    {
-        const char *fr_env = std::getenv("GPT2_HEAD_L2_FRAC");
-        float f = fr_env ? float(std::atof(fr_env)) : 0.0f;   // measured: no gain on GB300
-        a.head_l2_frac = f < 0.f ? 0.f : (f > 1.f ? 1.f : f);
-    }
     a.acc_new = reinterpret_cast<long long *>(B + o_accn);
     a.acc_next = reinterpret_cast<long long *>(B + o_accx);
     a.ll_tok = reinterpret_cast<uint64_t *>(B + o_tok);

@@ -73,7 +73,7 @@ constexpr int kCWarps = 8;
 constexpr int kCThreads = kCWarps * 32;
 constexpr int kCAll = kCThreads + 32;      // + producer warp
 constexpr int kCRing = kClusterRing;
-constexpr int kRowGroup = 4;
+constexpr int kRowGroup = 8;   // rows a warp dots at once
 // Residual sums: each contribution is one 64-bit atomic addition of
 //   (round(v * 2^24) + 2^40) + 2^56
 // so a word holds the biased fixed-point sum in its low 56 bits and the
@@ -202,6 +202,7 @@ struct Sh {
 struct CS {
     uint64_t *full, *empty, *qkv_bar, *att_bar, *kv_bar, *prm_bar, *red_bar, *x_bar;
     float *x, *qkv, *part, *attn, *hloc, *outv, *red, *kvw;
+    float *xg;                 // x * gamma for canon_rows: the tail of outv (E values after the 2 * 8 + 8 D scratch)
     float *pr;                 // this layer's LayerNorm parameters and bias slices
     const CLayer *layers;      // the layer table, copied to shared memory
     uint8_t *ring;
@@ -436,20 +437,7 @@ __device__ void producer(const ClusterArgs &a, const CLayer *layers, const Role 
     uint32_t k = 0;
     bool ok = true;
     const uint64_t pol = l2_evict_first_policy();
-    uint64_t keep;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
-    // the share of this CTA's LM-head rows that is pulled into L2 at the start
-    // of a pass, while the block phases leave HBM mostly idle
-    const uint32_t head_bytes = uint32_t(G.head.rows) * G.head.rb;
-    const uint32_t pf_bytes = uint32_t(float(head_bytes) * a.head_l2_frac) & ~15u;
-    const uint8_t *head_src = reinterpret_cast<const uint8_t *>(a.wte) + size_t(G.head_row0) * G.head.rb;
     for (int s = 0; s < a.n_steps && ok; ++s) {
-        for (uint32_t off = 0; off < pf_bytes; off += 32768u) {
-            const uint32_t n = min(32768u, pf_bytes - off);
-            asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(head_src + off), "r"(n),
-                         "l"(keep)
-                         : "memory");
-        }
         for (int l = 0; l < a.L && ok; ++l) {
             stream_seg(a, G.a, seg_a(ro, G, layers[l]), ring, full, empty, k, ok, pol);
             if (ok) stream_seg(a, G.b, seg_b(ro, G, layers[l]), ring, full, empty, k, ok, pol);
@@ -470,26 +458,81 @@ __device__ void producer(const ClusterArgs &a, const CLayer *layers, const Role 
 }
 
 // ---- consumer math -------------------------------------------------------------
-// int4 code t of a 32-bit word minus the zero point, exactly: 2^23 + q has q
-// in its low mantissa bits, and zf = 2^23 + z.
-__device__ __forceinline__ float nib_minus(uint32_t q, int t, float zf)
+// Inputs per column unit of a canonical row: 4 fp32 (16 bytes), 8 fp16 (16
+// bytes) or 8 int4 codes (one 32-bit word; four words share a group's scale
+// and zero point).
+template <int WT>
+struct UnitOf {
+    static constexpr int kIn = WT == kWF32 ? 4 : 8;
+    static constexpr int kF4 = kIn / 4;                    // float4 of inputs per unit
+};
+
+// 2^23 + (byte b of w), as a float: byte b of w must be below 16.
+__device__ __forceinline__ float byte_f23(uint32_t w, int b)
 {
-    return __uint_as_float(0x4B000000u | ((q >> (4 * t)) & 15u)) - zf;
+    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u + uint32_t(b)));
 }
 
-// Column unit c of canonical row rr of a stage times its inputs: fp32 4
-// inputs (16 bytes, x0), fp16 8 inputs (16 bytes, x0 then x1), int4 8 inputs
-// (one 32-bit word, x0 then x1).
-template <int WT>
-__device__ __forceinline__ float canon_unit(const uint8_t *stg, const Geo &g, int rr, int c, const float4 &x0,
-                                            const float4 &x1, float acc)
+// Shared-memory loads by 32-bit shared address (the ring and the vectors are
+// addressed in the shared window explicitly, never through generic pointers).
+__device__ __forceinline__ float4 lds_f4(uint32_t a)
 {
-    const uint8_t *row = stg + size_t(rr) * g.rb;
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint4 lds_u4(uint32_t a)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float lds_f(uint32_t a)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u8(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+// Rows of a stage by shared address: row rr's values at m + rr * rb, its
+// scales at s + rr * srb, its zero points at z + rr * zrb.
+struct RowAddr {
+    uint32_t m, s, z;
+};
+__device__ __forceinline__ RowAddr row_addr(uint32_t stage, const Geo &g, int rr)
+{
+    RowAddr r;
+    r.m = stage + uint32_t(rr) * g.rb;
+    r.s = stage + g.soff + uint32_t(rr) * g.srb;
+    r.z = stage + g.zoff + uint32_t(rr) * g.zrb;
+    return r;
+}
+
+// Unit c of a canonical row dotted with its inputs xu[0..kF4).  int4: the 8
+// codes q of word c, (q - z) taken exactly as (2^23 + q) - (2^23 + z), summed
+// in two chains, times the group's scale.
+template <int WT>
+__device__ __forceinline__ float canon_unit(const RowAddr &ra, int c, const float4 *xu, float acc)
+{
     if (WT == kWF32) {
-        const float4 v = reinterpret_cast<const float4 *>(row)[c];
+        const float4 v = lds_f4(ra.m + 16u * uint32_t(c));
+        const float4 x0 = xu[0];
         return fmaf(v.w, x0.w, fmaf(v.z, x0.z, fmaf(v.y, x0.y, fmaf(v.x, x0.x, acc))));
     } else if (WT == kWF16) {
-        const uint4 u = reinterpret_cast<const uint4 *>(row)[c];
+        const uint4 u = lds_u4(ra.m + 16u * uint32_t(c));
+        const float4 x0 = xu[0], x1 = xu[1];
         const float2 p0 = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
         const float2 p1 = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
         const float2 p2 = __half22float2(*reinterpret_cast<const __half2 *>(&u.z));
@@ -503,20 +546,24 @@ __device__ __forceinline__ float canon_unit(const uint8_t *stg, const Geo &g, in
         acc = fmaf(p3.x, x1.z, acc);
         return fmaf(p3.y, x1.w, acc);
     } else {
+        // word c: inputs 8c..8c+7 of group c / 4; byte b of the word holds
+        // inputs 2b (low nibble) and 2b + 1
+        const uint32_t q = lds_u32(ra.m + 4u * uint32_t(c));
         const int grp = c >> 2;
-        const uint32_t q = reinterpret_cast<const uint32_t *>(row)[c];
-        const int z = ((stg + g.zoff + size_t(rr) * g.zrb)[grp >> 1] >> ((grp & 1) * 4)) & 15;
-        const float s = reinterpret_cast<const float *>(stg + g.soff + size_t(rr) * g.srb)[grp];
+        const float s = lds_f(ra.s + 4u * uint32_t(grp));
+        const int z = int(lds_u8(ra.z + uint32_t(grp >> 1)) >> ((grp & 1) * 4)) & 15;
         const float zf = 8388608.0f + float(z);
-        float d = nib_minus(q, 0, zf) * x0.x;
-        d = fmaf(nib_minus(q, 1, zf), x0.y, d);
-        d = fmaf(nib_minus(q, 2, zf), x0.z, d);
-        d = fmaf(nib_minus(q, 3, zf), x0.w, d);
-        d = fmaf(nib_minus(q, 4, zf), x1.x, d);
-        d = fmaf(nib_minus(q, 5, zf), x1.y, d);
-        d = fmaf(nib_minus(q, 6, zf), x1.z, d);
-        d = fmaf(nib_minus(q, 7, zf), x1.w, d);
-        return fmaf(s, d, acc);
+        const uint32_t lo = q & 0x0F0F0F0Fu, hi = (q >> 4) & 0x0F0F0F0Fu;
+        const float4 xa = xu[0], xb = xu[1];
+        float d0 = (byte_f23(lo, 0) - zf) * xa.x;
+        float d1 = (byte_f23(hi, 0) - zf) * xa.y;
+        d0 = fmaf(byte_f23(lo, 1) - zf, xa.z, d0);
+        d1 = fmaf(byte_f23(hi, 1) - zf, xa.w, d1);
+        d0 = fmaf(byte_f23(lo, 2) - zf, xb.x, d0);
+        d1 = fmaf(byte_f23(hi, 2) - zf, xb.y, d1);
+        d0 = fmaf(byte_f23(lo, 3) - zf, xb.z, d0);
+        d1 = fmaf(byte_f23(hi, 3) - zf, xb.w, d1);
+        return fmaf(s, d0 + d1, acc);
     }
 }
 
@@ -533,26 +580,40 @@ __device__ __forceinline__ void stat4(const float4 &v, float k, float &s, float 
     q = fmaf(a, a, fmaf(b, b, fmaf(c, c, fmaf(d, d, q))));
 }
 
-// Sums 4 per-lane values over the warp in 6 shuffles; lanes 0, 8, 16, 24 end
-// with the totals of values 0, 1, 2, 3 (fixed order, so every run gives the
-// same bits).
-__device__ __forceinline__ float warp_sum4(float (&v)[kRowGroup], int lane)
+// Sums 8 per-lane values over the warp in 9 shuffles (each step halves the
+// values a lane keeps); lane l ends with the total of value
+// 4 * bit4(l) + 2 * bit3(l) + bit2(l).  The order is fixed, so every run gives
+// the same bits.
+__device__ __forceinline__ float warp_sum8(float (&v)[kRowGroup], int lane)
 {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    {
         const bool hi = lane & 16;
-        const float send = hi ? v[i] : v[i + 2], keep = hi ? v[i + 2] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float send = hi ? v[i] : v[i + 4], keep = hi ? v[i + 4] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
     }
     {
         const bool hi = lane & 8;
-        const float send = hi ? v[0] : v[1], keep = hi ? v[1] : v[0];
-        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float send = hi ? v[i] : v[i + 2], keep = hi ? v[i + 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
     }
-    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 4);
+    {
+        const bool hi = lane & 4;
+        const float send = hi ? v[0] : v[1], keep = hi ? v[1] : v[0];
+        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
     v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
     v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
     return v[0];
+}
+__device__ __forceinline__ int warp_sum8_row(int lane)
+{
+    return ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
 }
 
 // Stages are consumed in windows of at most the ring's size.  At a window's
@@ -582,94 +643,90 @@ __device__ __forceinline__ void window_release(const CS &c, uint32_t k, int q0, 
                      : "memory");
 }
 
-__device__ __forceinline__ const uint8_t *stage_ptr(const ClusterArgs &a, const CS &c, uint32_t kk)
+__device__ __forceinline__ uint32_t stage_addr(const ClusterArgs &a, const CS &c, uint32_t kk)
 {
-    return c.ring + (kk & (kCRing - 1)) * a.stage_bytes;
+    return smem_addr(c.ring) + (kk & (kCRing - 1)) * a.stage_bytes;
 }
 
-// Dot products of the canonical rows of a segment (length in) with x: each
-// warp takes 4 rows of a window at a time (rows i, i+8, i+16, i+24), lanes
-// over the column units.  Results go to out[i], or, for the LM head
+// Dot products of the canonical rows of a segment (length in) with x.  In
+// each window, warp w takes a contiguous block of the window's rows, 8 rows
+// at a time, lanes over the 16-byte column units; the inputs of a unit are
+// read once for the 8 rows.  Results go to out[i], or, for the LM head
 // (logit_row0 >= 0), to the logits and this thread's argmax key.
 //
 // LN: the LayerNorm before the rows is folded into them (see CLayer).  The
-// lanes multiply x by gamma as they read it, and the warp's first row group
-// also accumulates the statistics of x, shifted by x[0] (every lane of the warp
-// together reads x once), so no barrier separates the LayerNorm from the dot
-// products; each result is rstd * (dot - mean * c1[i]) + cb[i].  Every warp
-// reduces the statistics in the same order and gets the same bits.
+// threads first write x * gamma to the scratch vector xg (published by the
+// window's opening barrier); every warp takes the statistics of x (shifted by
+// x[0]) with the same fixed-order sums, so all warps get the same bits; each
+// result is rstd * (dot - mean * c1[i]) + cb[i].  Without LN, xg is x.
+//
+// Each phase runs this once per layer, so the unit loop is kept compact (not
+// unrolled over the units).
 template <int WT, bool LN>
-__device__ void canon_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &k, int win, int in,
-                           const float *xin, const float *gamma, const float *c1, const float *cb, float *out,
-                           int logit_row0, unsigned long long &best, bool &ok)
+__device__ __forceinline__ void canon_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &k_io, int win, int in,
+                                        const float *xin, const float *gamma, float *xg, const float *c1,
+                                        const float *cb, float *out, int logit_row0, unsigned long long &best_io,
+                                        bool &ok_io)
 {
+    using U = UnitOf<WT>;
+    constexpr int kF4 = U::kF4;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int C = g.chunk, nch = g.nch;
-    constexpr int kIn = WT == kWF32 ? 4 : 8;   // inputs per column unit
-    const int units = in / kIn;
+    const int units = in / U::kIn;
+    uint32_t k = k_io;
+    bool ok = ok_io;
+    unsigned long long best = best_io;
     const float4 *x4 = reinterpret_cast<const float4 *>(xin);
     const float4 *g4 = reinterpret_cast<const float4 *>(gamma);
-    bool have_stats = false;
+    float4 *xg4 = reinterpret_cast<float4 *>(xg);
+    for (int i = tid; i < in / 4; i += kCThreads) xg4[i] = LN ? mul4(x4[i], g4[i]) : x4[i];
     float mean = 0.f, rstd = 0.f;
-    const float shift = LN ? xin[0] : 0.f;
+    if (LN) {
+        const float shift = xin[0];
+        float ssum = 0.f, ssq = 0.f;
+        for (int i = lane; i < in / 4; i += 32) stat4(x4[i], shift, ssum, ssq);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+            ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
+        }
+        const float inv = 1.0f / float(in);
+        const float ms = ssum * inv;
+        mean = shift + ms;
+        rstd = rsqrtf(fmaxf(fmaf(ssq, inv, -ms * ms), 0.f) + a.eps);
+    }
+    const uint32_t xga = smem_addr(xg);
+    const int jrow = warp_sum8_row(lane);
     for (int q0 = 0; q0 < nch; q0 += win) {
         const int q1 = min(nch, q0 + win);
         const int r0 = q0 * C, r1 = min(g.rows, q1 * C);
-        window_acquire(a, c, k, q0, q1, ok);
-        for (int i0 = r0 + warp; i0 < r1; i0 += kCWarps * kRowGroup) {
-            TSTAMP(t_a);
-            const int ng = min(kRowGroup, (r1 - i0 + kCWarps - 1) >> 3);
-            const uint8_t *stg[kRowGroup];
-            int rr[kRowGroup];
+        window_acquire(a, c, k, q0, q1, ok);   // its barrier also publishes xg
+        const int per = (r1 - r0 + kCWarps - 1) / kCWarps;
+        const int w0 = r0 + warp * per, w1 = min(r1, w0 + per);
+        for (int g0 = w0; g0 < w1; g0 += kRowGroup) {
+            const int ng = min(kRowGroup, w1 - g0);
+            RowAddr ra[kRowGroup];
 #pragma unroll
             for (int j = 0; j < kRowGroup; ++j) {
-                const int i = i0 + j * kCWarps;
-                const int q = j < ng ? chunk_of(g, i) : q0;
-                rr[j] = j < ng ? i - q * C : 0;
-                stg[j] = stage_ptr(a, c, k + uint32_t(q));
+                const int i = j < ng ? g0 + j : g0;
+                const int q = chunk_of(g, i);
+                ra[j] = row_addr(stage_addr(a, c, k + uint32_t(q)), g, i - q * C);
             }
-            TSUB(0, t_a);
-            TSTAMP(t_b);
-            const bool stats = LN && !have_stats;
-            float acc[kRowGroup] = {0.f, 0.f, 0.f, 0.f};
-            float ssum = 0.f, ssq = 0.f;
+            float acc[kRowGroup] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             if (ok) {
+#pragma unroll 1
                 for (int u = lane; u < units; u += 32) {
-                    float4 xa = x4[u * (kIn / 4)], xb = kIn == 8 ? x4[u * 2 + 1] : xa;
-                    if (LN) {
-                        if (stats) {
-                            stat4(xa, shift, ssum, ssq);
-                            if (kIn == 8) stat4(xb, shift, ssum, ssq);
-                        }
-                        xa = mul4(xa, g4[u * (kIn / 4)]);
-                        if (kIn == 8) xb = mul4(xb, g4[u * 2 + 1]);
-                    }
-                    if (ng == kRowGroup) {
+                    float4 xu[kF4];
 #pragma unroll
-                        for (int j = 0; j < kRowGroup; ++j) acc[j] = canon_unit<WT>(stg[j], g, rr[j], u, xa, xb, acc[j]);
-                    } else {
+                    for (int f = 0; f < kF4; ++f) xu[f] = lds_f4(xga + 16u * uint32_t(u * kF4 + f));
 #pragma unroll
-                        for (int j = 0; j < kRowGroup; ++j)
-                            if (j < ng) acc[j] = canon_unit<WT>(stg[j], g, rr[j], u, xa, xb, acc[j]);
-                    }
+                    for (int j = 0; j < kRowGroup; ++j)
+                        if (j < ng) acc[j] = canon_unit<WT>(ra[j], u, xu, acc[j]);
                 }
             }
-            if (stats) {
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
-                    ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
-                }
-                const float inv = 1.0f / float(in);
-                const float ms = ssum * inv;
-                mean = shift + ms;
-                rstd = rsqrtf(fmaxf(fmaf(ssq, inv, -ms * ms), 0.f) + a.eps);
-                have_stats = true;
-            }
-            float t = warp_sum4(acc, lane);
-            const int j = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
-            if ((lane & 7) == 0 && j < ng && ok) {
-                const int i = i0 + j * kCWarps;
+            float t = warp_sum8(acc, lane);
+            if ((lane & 3) == 0 && jrow < ng && ok) {
+                const int i = g0 + jrow;
                 if (LN) t = rstd * fmaf(-mean, c1[i], t) + cb[i];
                 if (logit_row0 >= 0) {
                     a.logits[logit_row0 + i] = t;
@@ -679,89 +736,87 @@ __device__ void canon_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &
                     out[i] = t;
                 }
             }
-            TSUB(1, t_b);
         }
-        TSTAMP(t_c);
         window_release(c, k, q0, q1);
-        TSUB(2, t_c);
     }
-    k += uint32_t(nch);
+    k_io = k + uint32_t(nch);
+    ok_io = ok;
+    best_io = best;
 }
 
-// One tile row: units [0, U) of 16 bytes, unit u stored at u ^ sw, dotted
-// with vin in two interleaved chains.
+// Unit u of a tile row (stored at unit us) dotted with its inputs, read
+// from the input vector at shared address v.
 template <int WT>
-__device__ __forceinline__ float tile_row_dot(const uint8_t *stg, const Geo &g, int rr, int sw, int U,
-                                              const float4 *v4)
+__device__ __forceinline__ float tile_unit(const RowAddr &ra, uint32_t us, int u, uint32_t v)
 {
-    const uint8_t *rp = stg + size_t(rr) * g.rb;
-    float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 2
-    for (int u = 0; u < U; ++u) {
-        const int us = u ^ sw;
-        float part;
-        if (WT == kWF32) {
-            const float4 w = reinterpret_cast<const float4 *>(rp)[us];
-            const float4 v = v4[u];
-            part = fmaf(w.w, v.w, fmaf(w.z, v.z, w.y * v.y)) + w.x * v.x;
-        } else if (WT == kWF16) {
-            const uint4 w = reinterpret_cast<const uint4 *>(rp)[us];
-            const float4 v0 = v4[2 * u], v1 = v4[2 * u + 1];
-            const float2 p0 = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
-            const float2 p1 = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
-            const float2 p2 = __half22float2(*reinterpret_cast<const __half2 *>(&w.z));
-            const float2 p3 = __half22float2(*reinterpret_cast<const __half2 *>(&w.w));
-            const float e0 = fmaf(p0.y, v0.y, p0.x * v0.x), e1 = fmaf(p1.y, v0.w, p1.x * v0.z);
-            const float e2 = fmaf(p2.y, v1.y, p2.x * v1.x), e3 = fmaf(p3.y, v1.w, p3.x * v1.z);
-            part = (e0 + e1) + (e2 + e3);
-        } else {
-            const uint4 w = reinterpret_cast<const uint4 *>(rp)[us];
-            const float s = reinterpret_cast<const float *>(stg + g.soff + size_t(rr) * g.srb)[u];
-            const float zf = 8388608.0f + float((stg + g.zoff + size_t(rr) * g.zrb)[u]);
-            const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-            float d0 = 0.f, d1 = 0.f;
+    if (WT == kWF32) {
+        const float4 w = lds_f4(ra.m + 16u * us);
+        const float4 x = lds_f4(v + 16u * uint32_t(u));
+        return fmaf(w.w, x.w, fmaf(w.z, x.z, w.y * x.y)) + w.x * x.x;
+    } else if (WT == kWF16) {
+        const uint4 w = lds_u4(ra.m + 16u * us);
+        const float4 v0 = lds_f4(v + 32u * uint32_t(u)), v1 = lds_f4(v + 32u * uint32_t(u) + 16u);
+        const float2 p0 = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
+        const float2 p1 = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
+        const float2 p2 = __half22float2(*reinterpret_cast<const __half2 *>(&w.z));
+        const float2 p3 = __half22float2(*reinterpret_cast<const __half2 *>(&w.w));
+        const float e0 = fmaf(p0.y, v0.y, p0.x * v0.x), e1 = fmaf(p1.y, v0.w, p1.x * v0.z);
+        const float e2 = fmaf(p2.y, v1.y, p2.x * v1.x), e3 = fmaf(p3.y, v1.w, p3.x * v1.z);
+        return (e0 + e1) + (e2 + e3);
+    } else {
+        const uint4 w = lds_u4(ra.m + 16u * us);
+        const float s = lds_f(ra.s + 4u * uint32_t(u));
+        const float zf = 8388608.0f + float(lds_u8(ra.z + uint32_t(u)));
+        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+        float d0 = 0.f, d1 = 0.f;
 #pragma unroll
-            for (int wi = 0; wi < 4; ++wi) {
-                const float4 v0 = v4[8 * u + 2 * wi], v1 = v4[8 * u + 2 * wi + 1];
-                const uint32_t qw = words[wi];
-                d0 = fmaf(nib_minus(qw, 0, zf), v0.x, d0);
-                d1 = fmaf(nib_minus(qw, 1, zf), v0.y, d1);
-                d0 = fmaf(nib_minus(qw, 2, zf), v0.z, d0);
-                d1 = fmaf(nib_minus(qw, 3, zf), v0.w, d1);
-                d0 = fmaf(nib_minus(qw, 4, zf), v1.x, d0);
-                d1 = fmaf(nib_minus(qw, 5, zf), v1.y, d1);
-                d0 = fmaf(nib_minus(qw, 6, zf), v1.z, d0);
-                d1 = fmaf(nib_minus(qw, 7, zf), v1.w, d1);
-            }
-            part = s * (d0 + d1);
+        for (int wi = 0; wi < 4; ++wi) {
+            const uint32_t lo = words[wi] & 0x0F0F0F0Fu, hi = (words[wi] >> 4) & 0x0F0F0F0Fu;
+            const float4 v0 = lds_f4(v + 128u * uint32_t(u) + 32u * uint32_t(wi));
+            const float4 v1 = lds_f4(v + 128u * uint32_t(u) + 32u * uint32_t(wi) + 16u);
+            d0 = fmaf(byte_f23(lo, 0) - zf, v0.x, d0);
+            d1 = fmaf(byte_f23(hi, 0) - zf, v0.y, d1);
+            d0 = fmaf(byte_f23(lo, 1) - zf, v0.z, d0);
+            d1 = fmaf(byte_f23(hi, 1) - zf, v0.w, d1);
+            d0 = fmaf(byte_f23(lo, 2) - zf, v1.x, d0);
+            d1 = fmaf(byte_f23(hi, 2) - zf, v1.y, d1);
+            d0 = fmaf(byte_f23(lo, 3) - zf, v1.z, d0);
+            d1 = fmaf(byte_f23(hi, 3) - zf, v1.w, d1);
         }
-        if (u & 1) acc1 += part;
-        else acc0 += part;
+        return s * (d0 + d1);
     }
-    return acc0 + acc1;
 }
 
 // Dot products of the tile rows of a segment (cols columns) with vin: one
 // thread per row; 16-byte units of row r are stored at u ^ (r & m), so the
 // threads of a quarter-warp read different banks.  out[row] for every row.
 template <int WT>
-__device__ void tile_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &k, int win, int cols,
-                          const float *vin, float *out, bool &ok)
+__device__ __forceinline__ void tile_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &k, int win, int cols,
+                                          const float *vin, float *out, bool &ok)
 {
     const int tid = threadIdx.x;
     const int per_unit = WT == kWF32 ? 4 : WT == kWF16 ? 8 : 32;
     const int U = cols / per_unit;
     const int m = (U & (U - 1)) == 0 ? min(U, 8) - 1 : 0;
     const int C = g.chunk, nch = g.nch;
-    const float4 *v4 = reinterpret_cast<const float4 *>(vin);
+    const uint32_t v4 = smem_addr(vin);
     for (int q0 = 0; q0 < nch; q0 += win) {
         const int q1 = min(nch, q0 + win);
         const int r1 = min(g.rows, q1 * C);
         window_acquire(a, c, k, q0, q1, ok);
         if (ok)
             for (int row = q0 * C + tid; row < r1; row += kCThreads) {
-                const int q = chunk_of(g, row), rr = row - q * C;
-                out[row] = tile_row_dot<WT>(stage_ptr(a, c, k + uint32_t(q)), g, rr, row & m, U, v4);
+                const int q = chunk_of(g, row);
+                const RowAddr ra = row_addr(stage_addr(a, c, k + uint32_t(q)), g, row - q * C);
+                const int sw = row & m;
+                float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 2
+                for (int u = 0; u < U; ++u) {
+                    const float part = tile_unit<WT>(ra, uint32_t(u ^ sw), u, v4);
+                    if (u & 1) acc1 += part;
+                    else acc0 += part;
+                }
+                out[row] = acc0 + acc1;
             }
         window_release(c, k, q0, q1);   // its barrier also completes out[]
     }
@@ -889,11 +944,14 @@ __device__ void attention(const ClusterArgs &a, CS &c, int l, int h, int r, int 
         const bool valid = j < w1;
         float sc = -INFINITY;
         if (valid) {
+            // lane j starts at unit j: the rows of a quarter-warp, 4 D bytes
+            // apart, then fall in different shared-memory banks
             const float4 *kr = reinterpret_cast<const float4 *>(krow(j));
             float d0 = 0.f, d1 = 0.f;
 #pragma unroll
             for (int i = 0; i < D / 4; i += 2) {
-                const float4 k0 = kr[i], k1 = kr[i + 1], qa = q4[i], qb = q4[i + 1];
+                const int u0 = (i + lane) & (D / 4 - 1), u1 = (i + 1 + lane) & (D / 4 - 1);
+                const float4 k0 = kr[u0], k1 = kr[u1], qa = q4[u0], qb = q4[u1];
                 d0 = fmaf(qa.x, k0.x, fmaf(qa.y, k0.y, fmaf(qa.z, k0.z, fmaf(qa.w, k0.w, d0))));
                 d1 = fmaf(qb.x, k1.x, fmaf(qb.y, k1.y, fmaf(qb.z, k1.z, fmaf(qb.w, k1.w, d1))));
             }
@@ -1171,7 +1229,7 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                 CTRACE(s, l * 16 + 2);
                 // this CTA's q, k, v rows (LayerNorm folded, bias included) ->
                 // every CTA of the cluster
-                canon_rows<WT, true>(a, c, G.a, k, kCRing, E, c.x, c.pr, p1, pc, c.outv, -1, best, ok);
+                canon_rows<WT, true>(a, c, G.a, k, kCRing, E, c.x, c.pr, c.xg, p1, pc, c.outv, -1, best, ok);
                 CTRACE(s, l * 16 + 3);   // (the window's closing barrier published c.outv)
                 {
                     const uint32_t qbar = smem_addr(c.qkv_bar);
@@ -1200,7 +1258,7 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                 CTRACE(s, l * 16 + 1);
                 if (!wait_tx_bar(a, c.prm_bar, c.uses_prm, 9000 + int(blockIdx.x))) ok = false;
                 CTRACE(s, l * 16 + 2);
-                canon_rows<WT, true>(a, c, G.a, k, kCRing, E, c.x, c.pr, p1, pc, c.outv, -1, best, ok);
+                canon_rows<WT, true>(a, c, G.a, k, kCRing, E, c.x, c.pr, c.xg, p1, pc, c.outv, -1, best, ok);
                 CTRACE(s, l * 16 + 3);
                 for (int t = tid; t < a.fr; t += kCThreads) c.hloc[t] = gelu_new(c.outv[t]);
                 csync();
@@ -1235,7 +1293,7 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                  ok);
         CTRACE(s, 201);
         if (!wait_tx_bar(a, c.prm_bar, c.uses_prm, 9000 + int(blockIdx.x))) ok = false;
-        canon_rows<kWF32, true>(a, c, G.head, k, kStreamWindow, E, c.x, c.pr, p1, pc, nullptr, G.head_row0, best,
+        canon_rows<kWF32, true>(a, c, G.head, k, kStreamWindow, E, c.x, c.pr, c.xg, p1, pc, nullptr, G.head_row0, best,
                                 ok);
         CTRACE(s, 202);
         finish_head(a, sh, s, seq, best);
@@ -1251,6 +1309,21 @@ __global__ void __launch_bounds__(kCAll, 1) k_decode_cluster(const ClusterArgs a
 #ifdef GPT2_CTRACE
     __shared__ unsigned long long twait, tsub[3];
 #endif
+    // The kernel addresses its cluster peers' shared memory by rank: run only
+    // in the launch shape it was written for (the same answer in every CTA,
+    // so either all CTAs return here or none does).
+    {
+        uint32_t nct, crank;
+        asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(nct));
+        asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
+        if (nct != uint32_t(kClusterSize) || blockDim.x != uint32_t(kCAll) ||
+            gridDim.x != uint32_t(kClusterSize * a.H + a.nfc) || gridDim.y != 1u || gridDim.z != 1u) {
+            if (threadIdx.x == 0) record_error(a.st, kDevErrLaunchShape, int(nct));
+            return;
+        }
+        if (crank != blockIdx.x % uint32_t(kClusterSize) && threadIdx.x == 0)
+            record_error(a.st, kDevErrLaunchShape, int(blockIdx.x));
+    }
     const CLayout lo = cluster_layout(a.E, D, a.fr, a.L, a.pr_rows);
     CS c;
     c.full = reinterpret_cast<uint64_t *>(smem);
@@ -1268,6 +1341,7 @@ __global__ void __launch_bounds__(kCAll, 1) k_decode_cluster(const ClusterArgs a
     c.attn = reinterpret_cast<float *>(smem + lo.attn);
     c.hloc = reinterpret_cast<float *>(smem + lo.hloc);
     c.outv = reinterpret_cast<float *>(smem + lo.outv);
+    c.xg = c.outv + 2 * kCWarps + kCWarps * D;
     c.pr = reinterpret_cast<float *>(smem + lo.pr);
     c.kvw = reinterpret_cast<float *>(smem + lo.kvw);
     CLayer *tab = reinterpret_cast<CLayer *>(smem + lo.layers);

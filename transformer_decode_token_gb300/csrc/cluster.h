@@ -64,7 +64,6 @@ struct ClusterArgs {
     int32_t head_rpc;            // LM-head rows per CTA (a multiple of 4)
     int32_t pr_rows;             // row slots of the parameter area (a multiple of 4)
     const float *h_c1, *h_cb;    // LM head: wte.gamma_f, wte.beta_f, padded to head_rpc * grid
-    float head_l2_frac;          // share of each CTA's LM-head rows prefetched into L2 at pass start
     // residual-stream sums, one 64-bit word per element holding the biased
     // fixed-point sum and the number of contributions (double-buffered by
     // pass parity; the other parity is zeroed during a pass)

@@ -26,6 +26,7 @@ enum : int32_t {
     kDevErrTimeout = 1,        // a bounded wait gave up
     kDevErrBadToken = 2,       // token outside [0, vocab)
     kDevErrBadPosition = 3,    // position outside [0, n_positions)
+    kDevErrLaunchShape = 4,    // a kernel found a grid / cluster shape it was not built for
 };
 
 // Per-model scalars that live in device memory so that a captured graph can
