@@ -572,7 +572,6 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
         }
     if (nfc == 0) return GPT2_ERR_INVALID_ARG;
     const int fr = F / nfc;
-    if (fr > 16 + 8 * D || 3 * (D / 4) > 16 + 8 * D) return GPT2_ERR_INVALID_ARG;   // canon_rows outputs below its x*gamma scratch
     const int n_clusters = H + nfc / kClusterSize, grid = n_clusters * kClusterSize;
     if (grid > m->max_head_ctas) return GPT2_ERR_INVALID_ARG;   // per-CTA argmax slots
     const int head_rpc = ((V + grid - 1) / grid + 3) / 4 * 4;

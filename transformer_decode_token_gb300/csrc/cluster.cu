@@ -59,12 +59,13 @@ __device__ __forceinline__ void ctrace(int s, int slot, unsigned long long waite
     }
 }
 #define CTRACE(s, slot) ctrace(s, slot, *c.twait, c.tsub)
-#define TSUB(i, t) do { if (threadIdx.x == 0) c.tsub[i] += clock64() - (t); } while (0)
-#define TSTAMP(t) const long long t = clock64()
+// stamps inside a dot-product phase, at slots c.tslot + i of pass c.tpass
+#define CSUB(i) ctrace(c.tpass, c.tslot + (i), *c.twait, c.tsub)
+#define TSET(s, slot) (c.tpass = (s), c.tslot = (slot))
 #else
 #define CTRACE(s, slot) ((void)0)
-#define TSUB(i, t) ((void)0)
-#define TSTAMP(t) ((void)0)
+#define CSUB(i) ((void)0)
+#define TSET(s, slot) ((void)0)
 #endif
 
 namespace {
@@ -202,13 +203,13 @@ struct Sh {
 struct CS {
     uint64_t *full, *empty, *qkv_bar, *att_bar, *kv_bar, *prm_bar, *red_bar, *x_bar;
     float *x, *qkv, *part, *attn, *hloc, *outv, *red, *kvw;
-    float *xg;                 // x * gamma for canon_rows: the tail of outv (E values after the 2 * 8 + 8 D scratch)
     float *pr;                 // this layer's LayerNorm parameters and bias slices
     const CLayer *layers;      // the layer table, copied to shared memory
     uint8_t *ring;
     uint32_t uses_qkv, uses_att, uses_kv, uses_prm, uses_red, uses_x;   // barrier phases consumed so far
 #ifdef GPT2_CTRACE
     unsigned long long *twait, *tsub;
+    int tpass, tslot;
 #endif
 };
 
@@ -616,23 +617,56 @@ __device__ __forceinline__ int warp_sum8_row(int lane)
     return ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
 }
 
-// Stages are consumed in windows of at most the ring's size.  At a window's
-// start the warps wait for its stages (warp w for stages w, w + 8, in
-// parallel), then one CTA barrier makes every stage of the window visible to
-// every warp; at its end one CTA barrier, then one lane per stage releases it
-// (empty barriers count one arrival).  Every stage before a window is
-// released before the window is waited for, so the producer can always fill
-// it.  Layer segments, whose stages are resident ahead of time, take one
-// window of up to the whole ring; the LM head, which streams, takes windows of
-// half the ring so the producer fills one while the other is read.
-constexpr int kStreamWindow = kCRing / 2;
-
-__device__ __forceinline__ void window_acquire(const ClusterArgs &a, const CS &c, uint32_t k, int q0, int q1, bool &ok)
+// The same for 4 values in 6 shuffles: lane l ends with the total of value
+// 2 * bit4(l) + bit3(l).
+__device__ __forceinline__ float warp_sum4(float (&v)[4], int lane)
 {
-    for (int q = q0 + int(threadIdx.x >> 5); q < q1; q += kCWarps)
-        if (ok && !wait_stage(a, c, k + uint32_t(q))) ok = false;
-    csync();
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const bool hi = lane & 16;
+        const float send = hi ? v[i] : v[i + 2], keep = hi ? v[i + 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+    {
+        const bool hi = lane & 8;
+        const float send = hi ? v[0] : v[1], keep = hi ? v[1] : v[0];
+        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 4);
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+    return v[0];
 }
+
+// Row sums of RG (4 or 8) rows held across a warp: the value of row
+// group_row<RG>(lane), complete in the lanes where group_writer<RG>(lane).
+template <int RG>
+__device__ __forceinline__ float warp_sum_rows(float (&v)[RG], int lane)
+{
+    if constexpr (RG == 8) return warp_sum8(v, lane);
+    else return warp_sum4(v, lane);
+}
+template <int RG>
+__device__ __forceinline__ int group_row(int lane)
+{
+    return RG == 8 ? warp_sum8_row(lane) : ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+}
+template <int RG>
+__device__ __forceinline__ bool group_writer(int lane)
+{
+    return (lane & (RG == 8 ? 3 : 7)) == 0;
+}
+
+// Stages are consumed in windows of at most the ring's size.  Within a window
+// every thread waits (on the stages' full barriers) only for the stages that
+// hold the rows it reads; at the window's end one CTA barrier, then one lane
+// per stage releases it (empty barriers count one arrival).  Every stage
+// before a window is released before the window is waited for, so the
+// producer can always fill it.  Layer segments, whose stages are resident
+// ahead of time, take one window of up to the whole ring; the LM head, which
+// streams, takes windows of half the ring so the producer fills one while the
+// other is read.
+constexpr int kStreamWindow = kCRing / 2;
 
 __device__ __forceinline__ void window_release(const CS &c, uint32_t k, int q0, int q1)
 {
@@ -648,100 +682,119 @@ __device__ __forceinline__ uint32_t stage_addr(const ClusterArgs &a, const CS &c
     return smem_addr(c.ring) + (kk & (kCRing - 1)) * a.stage_bytes;
 }
 
+// Row groups of one warp in one window: rows [w0, w1), RG at a time, lanes
+// over the column units; the inputs of a unit are read once for the RG rows
+// (and multiplied by gamma on the way, LN).  The warp's first group of a
+// segment also takes the LayerNorm statistics of x (shifted by x[0]) from the
+// same reads, reduced in a fixed order, so every warp gets the same bits.
+template <int WT, bool LN, int RG>
+__device__ __forceinline__ void canon_groups(const ClusterArgs &a, const CS &c, const Geo &g, uint32_t k, int w0,
+                                             int w1, int units, uint32_t xa, uint32_t ga, float shift,
+                                             bool &have_stats, float &mean, float &rstd, int in, const float *c1,
+                                             const float *cb, float *out, int logit_row0, unsigned long long &best)
+{
+    constexpr int kF4 = UnitOf<WT>::kF4;
+    const int lane = threadIdx.x & 31, C = g.chunk;
+    for (int g0 = w0; g0 < w1; g0 += RG) {
+        const int ng = min(RG, w1 - g0);
+        RowAddr ra[RG];
+#pragma unroll
+        for (int j = 0; j < RG; ++j) {
+            const int i = j < ng ? g0 + j : g0;
+            const int q = chunk_of(g, i);
+            ra[j] = row_addr(stage_addr(a, c, k + uint32_t(q)), g, i - q * C);
+        }
+        float acc[RG];
+#pragma unroll
+        for (int j = 0; j < RG; ++j) acc[j] = 0.f;
+        const bool stats = LN && !have_stats;
+        float ssum = 0.f, ssq = 0.f;
+#pragma unroll 1
+        for (int u = lane; u < units; u += 32) {
+            float4 xu[kF4];
+#pragma unroll
+            for (int f = 0; f < kF4; ++f) {
+                const uint32_t off = 16u * uint32_t(u * kF4 + f);
+                const float4 v = lds_f4(xa + off);
+                if (stats) stat4(v, shift, ssum, ssq);
+                xu[f] = LN ? mul4(v, lds_f4(ga + off)) : v;
+            }
+#pragma unroll
+            for (int j = 0; j < RG; ++j)
+                if (j < ng) acc[j] = canon_unit<WT>(ra[j], u, xu, acc[j]);
+        }
+        if (stats) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+                ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
+            }
+            const float inv = 1.0f / float(in);
+            const float ms = ssum * inv;
+            mean = shift + ms;
+            rstd = rsqrtf(fmaxf(fmaf(ssq, inv, -ms * ms), 0.f) + a.eps);
+            have_stats = true;
+        }
+        float t = warp_sum_rows<RG>(acc, lane);
+        const int jr = group_row<RG>(lane);
+        if (group_writer<RG>(lane) && jr < ng) {
+            const int i = g0 + jr;
+            if (LN) t = rstd * fmaf(-mean, c1[i], t) + cb[i];
+            if (logit_row0 >= 0) {
+                a.logits[logit_row0 + i] = t;
+                const unsigned long long key = argmax_key(t, uint32_t(logit_row0 + i));
+                best = key > best ? key : best;
+            } else {
+                out[i] = t;
+            }
+        }
+    }
+}
+
 // Dot products of the canonical rows of a segment (length in) with x.  In
-// each window, warp w takes a contiguous block of the window's rows, 8 rows
-// at a time, lanes over the 16-byte column units; the inputs of a unit are
-// read once for the 8 rows.  Results go to out[i], or, for the LM head
+// each window, warp w takes a contiguous block of the window's rows, in
+// groups of 8 (4 when the block has at most 4 rows), and waits only for the
+// stages that hold them.  Results go to out[i], or, for the LM head
 // (logit_row0 >= 0), to the logits and this thread's argmax key.
 //
-// LN: the LayerNorm before the rows is folded into them (see CLayer).  The
-// threads first write x * gamma to the scratch vector xg (published by the
-// window's opening barrier); every warp takes the statistics of x (shifted by
-// x[0]) with the same fixed-order sums, so all warps get the same bits; each
-// result is rstd * (dot - mean * c1[i]) + cb[i].  Without LN, xg is x.
-//
-// Each phase runs this once per layer, so the unit loop is kept compact (not
-// unrolled over the units).
+// LN: the LayerNorm before the rows is folded into them (see CLayer): each
+// result is rstd * (W.(gamma*x) - mean * c1[i]) + cb[i].
 template <int WT, bool LN>
-__device__ __forceinline__ void canon_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &k_io, int win, int in,
-                                        const float *xin, const float *gamma, float *xg, const float *c1,
-                                        const float *cb, float *out, int logit_row0, unsigned long long &best_io,
-                                        bool &ok_io)
+__device__ __forceinline__ void canon_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &k, int win, int in,
+                                          const float *xin, const float *gamma, const float *c1, const float *cb,
+                                          float *out, int logit_row0, unsigned long long &best, bool &ok)
 {
-    using U = UnitOf<WT>;
-    constexpr int kF4 = U::kF4;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int warp = threadIdx.x >> 5;
     const int C = g.chunk, nch = g.nch;
-    const int units = in / U::kIn;
-    uint32_t k = k_io;
-    bool ok = ok_io;
-    unsigned long long best = best_io;
-    const float4 *x4 = reinterpret_cast<const float4 *>(xin);
-    const float4 *g4 = reinterpret_cast<const float4 *>(gamma);
-    float4 *xg4 = reinterpret_cast<float4 *>(xg);
-    for (int i = tid; i < in / 4; i += kCThreads) xg4[i] = LN ? mul4(x4[i], g4[i]) : x4[i];
+    const int units = in / UnitOf<WT>::kIn;
+    const uint32_t xa = smem_addr(xin), ga = smem_addr(gamma);
+    const float shift = LN ? xin[0] : 0.f;
+    bool have_stats = false;
     float mean = 0.f, rstd = 0.f;
-    if (LN) {
-        const float shift = xin[0];
-        float ssum = 0.f, ssq = 0.f;
-        for (int i = lane; i < in / 4; i += 32) stat4(x4[i], shift, ssum, ssq);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
-            ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
-        }
-        const float inv = 1.0f / float(in);
-        const float ms = ssum * inv;
-        mean = shift + ms;
-        rstd = rsqrtf(fmaxf(fmaf(ssq, inv, -ms * ms), 0.f) + a.eps);
-    }
-    const uint32_t xga = smem_addr(xg);
-    const int jrow = warp_sum8_row(lane);
+    CSUB(0);
     for (int q0 = 0; q0 < nch; q0 += win) {
         const int q1 = min(nch, q0 + win);
         const int r0 = q0 * C, r1 = min(g.rows, q1 * C);
-        window_acquire(a, c, k, q0, q1, ok);   // its barrier also publishes xg
         const int per = (r1 - r0 + kCWarps - 1) / kCWarps;
         const int w0 = r0 + warp * per, w1 = min(r1, w0 + per);
-        for (int g0 = w0; g0 < w1; g0 += kRowGroup) {
-            const int ng = min(kRowGroup, w1 - g0);
-            RowAddr ra[kRowGroup];
-#pragma unroll
-            for (int j = 0; j < kRowGroup; ++j) {
-                const int i = j < ng ? g0 + j : g0;
-                const int q = chunk_of(g, i);
-                ra[j] = row_addr(stage_addr(a, c, k + uint32_t(q)), g, i - q * C);
-            }
-            float acc[kRowGroup] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (ok) {
-#pragma unroll 1
-                for (int u = lane; u < units; u += 32) {
-                    float4 xu[kF4];
-#pragma unroll
-                    for (int f = 0; f < kF4; ++f) xu[f] = lds_f4(xga + 16u * uint32_t(u * kF4 + f));
-#pragma unroll
-                    for (int j = 0; j < kRowGroup; ++j)
-                        if (j < ng) acc[j] = canon_unit<WT>(ra[j], u, xu, acc[j]);
-                }
-            }
-            float t = warp_sum8(acc, lane);
-            if ((lane & 3) == 0 && jrow < ng && ok) {
-                const int i = g0 + jrow;
-                if (LN) t = rstd * fmaf(-mean, c1[i], t) + cb[i];
-                if (logit_row0 >= 0) {
-                    a.logits[logit_row0 + i] = t;
-                    const unsigned long long key = argmax_key(t, uint32_t(logit_row0 + i));
-                    best = key > best ? key : best;
-                } else {
-                    out[i] = t;
-                }
-            }
+        if (w0 < w1) {
+            const int qa = chunk_of(g, w0), qb = chunk_of(g, w1 - 1);
+            for (int q = qa; q <= qb; ++q)
+                if (ok && !wait_stage(a, c, k + uint32_t(q))) ok = false;
         }
-        window_release(c, k, q0, q1);
+        CSUB(1);
+        if (ok && w0 < w1) {
+            if (per <= 4)
+                canon_groups<WT, LN, 4>(a, c, g, k, w0, w1, units, xa, ga, shift, have_stats, mean, rstd, in, c1, cb,
+                                        out, logit_row0, best);
+            else
+                canon_groups<WT, LN, 8>(a, c, g, k, w0, w1, units, xa, ga, shift, have_stats, mean, rstd, in, c1, cb,
+                                        out, logit_row0, best);
+        }
+        CSUB(2);
+        window_release(c, k, q0, q1);   // its barrier also publishes out[]
     }
-    k_io = k + uint32_t(nch);
-    ok_io = ok;
-    best_io = best;
+    k += uint32_t(nch);
 }
 
 // Unit u of a tile row (stored at unit us) dotted with its inputs, read
@@ -788,8 +841,9 @@ __device__ __forceinline__ float tile_unit(const RowAddr &ra, uint32_t us, int u
 }
 
 // Dot products of the tile rows of a segment (cols columns) with vin: one
-// thread per row; 16-byte units of row r are stored at u ^ (r & m), so the
-// threads of a quarter-warp read different banks.  out[row] for every row.
+// thread per row, which waits for its row's stage; 16-byte units of row r are
+// stored at u ^ (r & m), so the threads of a quarter-warp read different
+// banks.  out[row] for every row.
 template <int WT>
 __device__ __forceinline__ void tile_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &k, int win, int cols,
                                           const float *vin, float *out, bool &ok)
@@ -803,10 +857,14 @@ __device__ __forceinline__ void tile_rows(const ClusterArgs &a, CS &c, const Geo
     for (int q0 = 0; q0 < nch; q0 += win) {
         const int q1 = min(nch, q0 + win);
         const int r1 = min(g.rows, q1 * C);
-        window_acquire(a, c, k, q0, q1, ok);
+        CSUB(0);
         if (ok)
             for (int row = q0 * C + tid; row < r1; row += kCThreads) {
                 const int q = chunk_of(g, row);
+                if (!wait_stage(a, c, k + uint32_t(q))) {
+                    ok = false;
+                    break;
+                }
                 const RowAddr ra = row_addr(stage_addr(a, c, k + uint32_t(q)), g, row - q * C);
                 const int sw = row & m;
                 float acc0 = 0.f, acc1 = 0.f;
@@ -818,6 +876,7 @@ __device__ __forceinline__ void tile_rows(const ClusterArgs &a, CS &c, const Geo
                 }
                 out[row] = acc0 + acc1;
             }
+        CSUB(2);
         window_release(c, k, q0, q1);   // its barrier also completes out[]
     }
     k += uint32_t(nch);
@@ -1040,7 +1099,6 @@ __device__ void attention(const ClusterArgs &a, CS &c, int l, int h, int r, int 
         }
         c.attn[t] = O / L;
     }
-    // (the next phase opens with a CTA barrier, which publishes c.attn)
 }
 
 // Issue the bulk copies of this CTA's cached K/V rows of a head (before q, k,
@@ -1229,7 +1287,8 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                 CTRACE(s, l * 16 + 2);
                 // this CTA's q, k, v rows (LayerNorm folded, bias included) ->
                 // every CTA of the cluster
-                canon_rows<WT, true>(a, c, G.a, k, kCRing, E, c.x, c.pr, c.xg, p1, pc, c.outv, -1, best, ok);
+                TSET(s, l * 16 + 8);
+                canon_rows<WT, true>(a, c, G.a, k, kCRing, E, c.x, c.pr, p1, pc, c.outv, -1, best, ok);
                 CTRACE(s, l * 16 + 3);   // (the window's closing barrier published c.outv)
                 {
                     const uint32_t qbar = smem_addr(c.qkv_bar);
@@ -1245,8 +1304,10 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                 if (!wait_tx_bar(a, c.qkv_bar, c.uses_qkv, 8000 + int(blockIdx.x))) ok = false;
                 CTRACE(s, l * 16 + 4);
                 attention<D>(a, c, l, ro.h, ro.r, pos, ok);
+                csync();   // publishes c.attn; the attention scratch in c.outv is free again
                 CTRACE(s, l * 16 + 5);
                 // the head's slice of the output projection, rows rank*E/4.. (+ x + bias once, by head 0)
+                TSET(s, l * 16 + 11);
                 tile_rows<WT>(a, c, G.b, k, kCRing, D, c.attn, c.outv, ok);
                 CTRACE(s, l * 16 + 6);
                 add_sum(an, ro.r * rq, c.outv, ro.h == 0 ? c.x : nullptr, pb, rq);
@@ -1258,11 +1319,13 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                 CTRACE(s, l * 16 + 1);
                 if (!wait_tx_bar(a, c.prm_bar, c.uses_prm, 9000 + int(blockIdx.x))) ok = false;
                 CTRACE(s, l * 16 + 2);
-                canon_rows<WT, true>(a, c, G.a, k, kCRing, E, c.x, c.pr, c.xg, p1, pc, c.outv, -1, best, ok);
+                TSET(s, l * 16 + 8);
+                canon_rows<WT, true>(a, c, G.a, k, kCRing, E, c.x, c.pr, p1, pc, c.outv, -1, best, ok);
                 CTRACE(s, l * 16 + 3);
                 for (int t = tid; t < a.fr; t += kCThreads) c.hloc[t] = gelu_new(c.outv[t]);
                 csync();
                 CTRACE(s, l * 16 + 4);
+                TSET(s, l * 16 + 11);
                 tile_rows<WT>(a, c, G.b, k, kCRing, a.fr, c.hloc, c.outv, ok);
                 CTRACE(s, l * 16 + 5);
                 // the cluster's four partial vectors meet first: rank r sums
@@ -1293,7 +1356,8 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                  ok);
         CTRACE(s, 201);
         if (!wait_tx_bar(a, c.prm_bar, c.uses_prm, 9000 + int(blockIdx.x))) ok = false;
-        canon_rows<kWF32, true>(a, c, G.head, k, kStreamWindow, E, c.x, c.pr, c.xg, p1, pc, nullptr, G.head_row0, best,
+        TSET(s, 204);
+        canon_rows<kWF32, true>(a, c, G.head, k, kStreamWindow, E, c.x, c.pr, p1, pc, nullptr, G.head_row0, best,
                                 ok);
         CTRACE(s, 202);
         finish_head(a, sh, s, seq, best);
@@ -1341,7 +1405,6 @@ __global__ void __launch_bounds__(kCAll, 1) k_decode_cluster(const ClusterArgs a
     c.attn = reinterpret_cast<float *>(smem + lo.attn);
     c.hloc = reinterpret_cast<float *>(smem + lo.hloc);
     c.outv = reinterpret_cast<float *>(smem + lo.outv);
-    c.xg = c.outv + 2 * kCWarps + kCWarps * D;
     c.pr = reinterpret_cast<float *>(smem + lo.pr);
     c.kvw = reinterpret_cast<float *>(smem + lo.kvw);
     CLayer *tab = reinterpret_cast<CLayer *>(smem + lo.layers);
