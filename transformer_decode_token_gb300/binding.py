@@ -64,12 +64,23 @@ def lib_path() -> str:
     return _build.LIB
 
 
-def lib(build_if_stale: bool = True):
+def load_library(path: str):
+    """Loads a specific build of the library (for example the phase-trace build
+    that trace_cluster.py makes) in place of libgpt2.so.  Must come before any
+    other call into the library."""
+    global _lib
+    if _lib is not None:
+        raise RuntimeError("the library is already loaded")
+    return lib(path=path)
+
+
+def lib(build_if_stale: bool = True, path: str = None):
     """Loads libgpt2.so (building it first if it is missing or stale)."""
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.build() if build_if_stale else _build.LIB
+            if path is None:
+                path = _build.build() if build_if_stale else _build.LIB
             if not os.path.exists(path):
                 raise RuntimeError(f"libgpt2.so not found at {path}")
             L = ctypes.CDLL(path)

@@ -46,14 +46,18 @@ def stale() -> bool:
     return any(os.path.getmtime(p) > t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    if not force and not stale():
+def build(force: bool = False, verbose: bool = False, extra=(), lib: str = None, objdir: str = None) -> str:
+    """Compiles every .cu file and links the library (default: libgpt2.so next
+    to this file); `extra` nvcc flags, `lib` / `objdir` for a variant build."""
+    lib = lib or LIB
+    objdir = objdir or OBJDIR
+    if not force and lib == LIB and not stale():
         return LIB
-    os.makedirs(OBJDIR, exist_ok=True)
+    os.makedirs(objdir, exist_ok=True)
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(OBJDIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -65,13 +69,13 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -1366,7 +1366,7 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
 }
 
 template <int WT, int D>
-__global__ void __launch_bounds__(kCAll, 1) k_decode_cluster(const ClusterArgs a)
+__global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kCAll, 1) k_decode_cluster(const ClusterArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ Sh sh;
@@ -1469,15 +1469,13 @@ cudaError_t launch_t(const ClusterArgs &a, int n_clusters, size_t smem, cudaStre
     cfg.blockDim = dim3(kCAll);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute at[2];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = kClusterSize;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    at[1].id = cudaLaunchAttributeCooperative;
-    at[1].val.cooperative = 1;
+    // the cluster shape is compiled into the kernel (__cluster_dims__), so no
+    // launch path can run it without its peers
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeCooperative;
+    at[0].val.cooperative = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k_decode_cluster<WT, D>, a);
 }
 
