@@ -894,9 +894,13 @@ __device__ __forceinline__ unsigned long long ld_word(const long long *p)
 // Reads a residual sum into c.x once every word holds `count` contributions.
 // The CTAs of a cluster share the work: rank r polls words [r E/4, (r+1) E/4)
 // (each thread its own words), then stores their values into c.x of all four
-// CTAs; every thread then waits for the whole vector on x_bar.  A fence after
-// the poll orders what follows after the contributions.
-__device__ __forceinline__ void read_sum(const ClusterArgs &a, CS &c, int count, const long long *src, bool &ok)
+// CTAs; every thread then waits for the whole vector on x_bar.  The words carry
+// the data themselves, so nothing after the poll reads memory that the
+// contributors wrote; `fence` (the first wait of a pass, which the zeroing of
+// the other parity's sums follows) orders this CTA's later stores after the
+// contributors' earlier reads.
+__device__ __forceinline__ void read_sum(const ClusterArgs &a, CS &c, int count, const long long *src, bool &ok,
+                                         bool fence = false)
 {
     const int tid = threadIdx.x, rq = a.E / kClusterSize;
     const int r = int(blockIdx.x) % kClusterSize;
@@ -925,7 +929,7 @@ __device__ __forceinline__ void read_sum(const ClusterArgs &a, CS &c, int count,
             break;
         }
     }
-    __threadfence();
+    if (fence) __threadfence();
     const uint32_t xbar = smem_addr(c.x_bar);
 #pragma unroll
     for (int j = 0; j < kW; ++j) {
@@ -1314,7 +1318,7 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                 CTRACE(s, l * 16 + 7);
             } else {
                 if (tid == 0) mbar_arrive_expect_tx(c.red_bar, uint32_t(E) * 4u);   // this layer's partial slices
-                read_sum(a, c, a.H, an, ok);
+                read_sum(a, c, a.H, an, ok, l == 0);
                 if (l == 0) zero_other_parity(a, par);
                 CTRACE(s, l * 16 + 1);
                 if (!wait_tx_bar(a, c.prm_bar, c.uses_prm, 9000 + int(blockIdx.x))) ok = false;
