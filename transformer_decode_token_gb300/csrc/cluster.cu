@@ -682,8 +682,10 @@ __device__ __forceinline__ uint32_t stage_addr(const ClusterArgs &a, const CS &c
     return smem_addr(c.ring) + (kk & (kCRing - 1)) * a.stage_bytes;
 }
 
-// Row groups of one warp in one window: rows [w0, w1), RG at a time, lanes
-// over the column units; the inputs of a unit are read once for the RG rows
+// Row groups of one warp in one window: rows [w0, w1), RG at a time (a short
+// last group repeats its first row in the empty slots, whose sums are not
+// stored: no per-row branches in the loop), lanes over the column units; the
+// inputs of a unit are read once for the RG rows
 // (and multiplied by gamma on the way, LN).  The warp's first group of a
 // segment also takes the LayerNorm statistics of x (shifted by x[0]) from the
 // same reads, reduced in a fixed order, so every warp gets the same bits.
@@ -709,7 +711,7 @@ __device__ __forceinline__ void canon_groups(const ClusterArgs &a, const CS &c, 
         for (int j = 0; j < RG; ++j) acc[j] = 0.f;
         const bool stats = LN && !have_stats;
         float ssum = 0.f, ssq = 0.f;
-#pragma unroll 1
+#pragma unroll 2
         for (int u = lane; u < units; u += 32) {
             float4 xu[kF4];
 #pragma unroll
@@ -720,8 +722,7 @@ __device__ __forceinline__ void canon_groups(const ClusterArgs &a, const CS &c, 
                 xu[f] = LN ? mul4(v, lds_f4(ga + off)) : v;
             }
 #pragma unroll
-            for (int j = 0; j < RG; ++j)
-                if (j < ng) acc[j] = canon_unit<WT>(ra[j], u, xu, acc[j]);
+            for (int j = 0; j < RG; ++j) acc[j] = canon_unit<WT>(ra[j], u, xu, acc[j]);   // rows >= ng repeat row g0
         }
         if (stats) {
 #pragma unroll
