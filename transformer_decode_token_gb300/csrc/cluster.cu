@@ -74,7 +74,6 @@ constexpr int kCWarps = 8;
 constexpr int kCThreads = kCWarps * 32;
 constexpr int kCAll = kCThreads + 32;      // + producer warp
 constexpr int kCRing = kClusterRing;
-constexpr int kRowGroup = 8;   // rows a warp dots at once
 // Residual sums: each contribution is one 64-bit atomic addition of
 //   (round(v * 2^24) + 2^40) + 2^56
 // so a word holds the biased fixed-point sum in its low 56 bits and the
@@ -466,6 +465,7 @@ template <int WT>
 struct UnitOf {
     static constexpr int kIn = WT == kWF32 ? 4 : 8;
     static constexpr int kF4 = kIn / 4;                    // float4 of inputs per unit
+    static constexpr int kPL = 1024 / kIn / 32;            // units per lane for n_embd <= 1024
 };
 
 // 2^23 + (byte b of w), as a float: byte b of w must be below 16.
@@ -585,7 +585,7 @@ __device__ __forceinline__ void stat4(const float4 &v, float k, float &s, float 
 // values a lane keeps); lane l ends with the total of value
 // 4 * bit4(l) + 2 * bit3(l) + bit2(l).  The order is fixed, so every run gives
 // the same bits.
-__device__ __forceinline__ float warp_sum8(float (&v)[kRowGroup], int lane)
+__device__ __forceinline__ float warp_sum8(float (&v)[8], int lane)
 {
     {
         const bool hi = lane & 16;
@@ -638,23 +638,30 @@ __device__ __forceinline__ float warp_sum4(float (&v)[4], int lane)
     return v[0];
 }
 
-// Row sums of RG (4 or 8) rows held across a warp: the value of row
+// Row sums of RG (4, or up to 8) rows held across a warp: the value of row
 // group_row<RG>(lane), complete in the lanes where group_writer<RG>(lane).
 template <int RG>
-__device__ __forceinline__ float warp_sum_rows(float (&v)[RG], int lane)
+__device__ __forceinline__ float warp_sum_rows(const float (&acc)[RG], int lane)
 {
-    if constexpr (RG == 8) return warp_sum8(v, lane);
-    else return warp_sum4(v, lane);
+    if constexpr (RG == 4) {
+        float v[4] = {acc[0], acc[1], acc[2], acc[3]};
+        return warp_sum4(v, lane);
+    } else {
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = j < RG ? acc[j] : 0.f;
+        return warp_sum8(v, lane);
+    }
 }
 template <int RG>
 __device__ __forceinline__ int group_row(int lane)
 {
-    return RG == 8 ? warp_sum8_row(lane) : ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+    return RG == 4 ? ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1) : warp_sum8_row(lane);
 }
 template <int RG>
 __device__ __forceinline__ bool group_writer(int lane)
 {
-    return (lane & (RG == 8 ? 3 : 7)) == 0;
+    return (lane & (RG == 4 ? 7 : 3)) == 0;
 }
 
 // Stages are consumed in windows of at most the ring's size.  Within a window
@@ -684,16 +691,14 @@ __device__ __forceinline__ uint32_t stage_addr(const ClusterArgs &a, const CS &c
 
 // Row groups of one warp in one window: rows [w0, w1), RG at a time (a short
 // last group repeats its first row in the empty slots, whose sums are not
-// stored: no per-row branches in the loop), lanes over the column units; the
-// inputs of a unit are read once for the RG rows
-// (and multiplied by gamma on the way, LN).  The warp's first group of a
-// segment also takes the LayerNorm statistics of x (shifted by x[0]) from the
-// same reads, reduced in a fixed order, so every warp gets the same bits.
+// stored: no per-row branches in the loop), lanes over the column units; each
+// lane's inputs (x * gamma) are in registers, xr[m] for unit lane + 32 m.
 template <int WT, bool LN, int RG>
 __device__ __forceinline__ void canon_groups(const ClusterArgs &a, const CS &c, const Geo &g, uint32_t k, int w0,
-                                             int w1, int units, uint32_t xa, uint32_t ga, float shift,
-                                             bool &have_stats, float &mean, float &rstd, int in, const float *c1,
-                                             const float *cb, float *out, int logit_row0, unsigned long long &best)
+                                             int w1, int units, const float4 (&xr)[UnitOf<WT>::kPL * UnitOf<WT>::kF4],
+                                             bool &have_stats, float ssum, float ssq, float shift, int in,
+                                             float &mean, float &rstd, const float *c1, const float *cb, float *out,
+                                             int logit_row0, unsigned long long &best)
 {
     constexpr int kF4 = UnitOf<WT>::kF4;
     const int lane = threadIdx.x & 31, C = g.chunk;
@@ -709,22 +714,16 @@ __device__ __forceinline__ void canon_groups(const ClusterArgs &a, const CS &c, 
         float acc[RG];
 #pragma unroll
         for (int j = 0; j < RG; ++j) acc[j] = 0.f;
-        const bool stats = LN && !have_stats;
-        float ssum = 0.f, ssq = 0.f;
-#pragma unroll 2
-        for (int u = lane; u < units; u += 32) {
-            float4 xu[kF4];
 #pragma unroll
-            for (int f = 0; f < kF4; ++f) {
-                const uint32_t off = 16u * uint32_t(u * kF4 + f);
-                const float4 v = lds_f4(xa + off);
-                if (stats) stat4(v, shift, ssum, ssq);
-                xu[f] = LN ? mul4(v, lds_f4(ga + off)) : v;
+        for (int m = 0; m < UnitOf<WT>::kPL; ++m) {
+            const int u = lane + 32 * m;
+            if (u < units) {
+#pragma unroll
+                for (int j = 0; j < RG; ++j) acc[j] = canon_unit<WT>(ra[j], u, &xr[m * kF4], acc[j]);
             }
-#pragma unroll
-            for (int j = 0; j < RG; ++j) acc[j] = canon_unit<WT>(ra[j], u, xu, acc[j]);   // rows >= ng repeat row g0
         }
-        if (stats) {
+        if (LN && !have_stats) {
+            // the statistics' butterfly runs here, after the first group's loads
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
                 ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
@@ -752,33 +751,85 @@ __device__ __forceinline__ void canon_groups(const ClusterArgs &a, const CS &c, 
     }
 }
 
-// Dot products of the canonical rows of a segment (length in) with x.  In
-// each window, warp w takes a contiguous block of the window's rows, in
-// groups of 8 (4 when the block has at most 4 rows), and waits only for the
-// stages that hold them.  Results go to out[i], or, for the LM head
+// Dot products of the canonical rows of a segment (length in) with x.  Each
+// lane first loads the inputs of its column units (x * gamma, LN) into
+// registers and, for LN, every warp takes the statistics of x (shifted by
+// x[0]) from them with the same fixed-order butterfly, so all warps get the
+// same bits.  In each window, warp w takes a contiguous block of the window's
+// rows, in groups of 6 (4 when the block has at most 4 rows), and waits only
+// for the stages that hold them.  Results go to out[i], or, for the LM head
 // (logit_row0 >= 0), to the logits and this thread's argmax key.
 //
 // LN: the LayerNorm before the rows is folded into them (see CLayer): each
 // result is rstd * (W.(gamma*x) - mean * c1[i]) + cb[i].
+// The rows of a window that warp `warp` takes: [w0, w1).
+__device__ __forceinline__ void warp_rows(const Geo &g, int q0, int q1, int &w0, int &w1, int &per)
+{
+    const int warp = threadIdx.x >> 5;
+    const int r0 = q0 * g.chunk, r1 = min(g.rows, q1 * g.chunk);
+    per = (r1 - r0 + kCWarps - 1) / kCWarps;
+    w0 = r0 + warp * per;
+    w1 = min(r1, w0 + per);
+}
+
+// Waits for the stages that hold this warp's rows of a segment's first window
+// (called before the segment's input arrives, so the barrier tests overlap
+// that wait; canon_rows is then told not to repeat them).
+__device__ __forceinline__ void prewait_rows(const ClusterArgs &a, const CS &c, const Geo &g, uint32_t k, int win,
+                                             bool &ok)
+{
+    int w0, w1, per;
+    warp_rows(g, 0, min(g.nch, win), w0, w1, per);
+    if (w0 < w1)
+        for (int q = chunk_of(g, w0), qb = chunk_of(g, w1 - 1); q <= qb; ++q)
+            if (ok && !wait_stage(a, c, k + uint32_t(q))) ok = false;
+}
+
 template <int WT, bool LN>
 __device__ __forceinline__ void canon_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &k, int win, int in,
                                           const float *xin, const float *gamma, const float *c1, const float *cb,
-                                          float *out, int logit_row0, unsigned long long &best, bool &ok)
+                                          float *out, int logit_row0, unsigned long long &best, bool &ok,
+                                          bool prewaited = false)
 {
-    const int warp = threadIdx.x >> 5;
+    constexpr int kF4 = UnitOf<WT>::kF4;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C = g.chunk, nch = g.nch;
     const int units = in / UnitOf<WT>::kIn;
     const uint32_t xa = smem_addr(xin), ga = smem_addr(gamma);
-    const float shift = LN ? xin[0] : 0.f;
-    bool have_stats = false;
+    float4 xr[UnitOf<WT>::kPL * kF4];
     float mean = 0.f, rstd = 0.f;
+    const float shift = LN ? xin[0] : 0.f;
+    float ssum = 0.f, ssq = 0.f;   // this lane's share of the LayerNorm statistics
+    {
+        float s1 = 0.f, q1s = 0.f;  // two chains
+#pragma unroll
+        for (int m = 0; m < UnitOf<WT>::kPL; ++m) {
+            const int u = lane + 32 * m;
+#pragma unroll
+            for (int f = 0; f < kF4; ++f) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (u < units) {
+                    const uint32_t off = 16u * uint32_t(u * kF4 + f);
+                    v = lds_f4(xa + off);
+                    if (LN) {
+                        if ((m * kF4 + f) & 1) stat4(v, shift, s1, q1s);
+                        else stat4(v, shift, ssum, ssq);
+                        v = mul4(v, lds_f4(ga + off));
+                    }
+                }
+                xr[m * kF4 + f] = v;
+            }
+        }
+        ssum += s1;
+        ssq += q1s;
+    }
+    bool have_stats = false;
     CSUB(0);
     for (int q0 = 0; q0 < nch; q0 += win) {
         const int q1 = min(nch, q0 + win);
-        const int r0 = q0 * C, r1 = min(g.rows, q1 * C);
-        const int per = (r1 - r0 + kCWarps - 1) / kCWarps;
-        const int w0 = r0 + warp * per, w1 = min(r1, w0 + per);
-        if (w0 < w1) {
+        int w0, w1, per;
+        warp_rows(g, q0, q1, w0, w1, per);
+        if (w0 < w1 && !(prewaited && q0 == 0)) {
             const int qa = chunk_of(g, w0), qb = chunk_of(g, w1 - 1);
             for (int q = qa; q <= qb; ++q)
                 if (ok && !wait_stage(a, c, k + uint32_t(q))) ok = false;
@@ -786,11 +837,11 @@ __device__ __forceinline__ void canon_rows(const ClusterArgs &a, CS &c, const Ge
         CSUB(1);
         if (ok && w0 < w1) {
             if (per <= 4)
-                canon_groups<WT, LN, 4>(a, c, g, k, w0, w1, units, xa, ga, shift, have_stats, mean, rstd, in, c1, cb,
-                                        out, logit_row0, best);
+                canon_groups<WT, LN, 4>(a, c, g, k, w0, w1, units, xr, have_stats, ssum, ssq, shift, in, mean, rstd,
+                                        c1, cb, out, logit_row0, best);
             else
-                canon_groups<WT, LN, 8>(a, c, g, k, w0, w1, units, xa, ga, shift, have_stats, mean, rstd, in, c1, cb,
-                                        out, logit_row0, best);
+                canon_groups<WT, LN, 6>(a, c, g, k, w0, w1, units, xr, have_stats, ssum, ssq, shift, in, mean, rstd,
+                                        c1, cb, out, logit_row0, best);
         }
         CSUB(2);
         window_release(c, k, q0, q1);   // its barrier also publishes out[]
@@ -1256,6 +1307,7 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                     mbar_arrive_expect_tx(c.att_bar, uint32_t(kClusterSize) * (D + 2) * 4u);
                 }
                 prefetch_kv<D>(a, c, l, ro.h, ro.r, pos);
+                prewait_rows(a, c, G.a, k, kCRing, ok);   // this layer's QKV rows, while x is on its way
                 // x entering the block
                 if (l == 0) {
                     // every pass after the first waits for the previous one (its
@@ -1293,7 +1345,7 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                 // this CTA's q, k, v rows (LayerNorm folded, bias included) ->
                 // every CTA of the cluster
                 TSET(s, l * 16 + 8);
-                canon_rows<WT, true>(a, c, G.a, k, kCRing, E, c.x, c.pr, p1, pc, c.outv, -1, best, ok);
+                canon_rows<WT, true>(a, c, G.a, k, kCRing, E, c.x, c.pr, p1, pc, c.outv, -1, best, ok, true);
                 CTRACE(s, l * 16 + 3);   // (the window's closing barrier published c.outv)
                 {
                     const uint32_t qbar = smem_addr(c.qkv_bar);
@@ -1319,13 +1371,14 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                 CTRACE(s, l * 16 + 7);
             } else {
                 if (tid == 0) mbar_arrive_expect_tx(c.red_bar, uint32_t(E) * 4u);   // this layer's partial slices
+                prewait_rows(a, c, G.a, k, kCRing, ok);   // this layer's fc rows, while x_new is on its way
                 read_sum(a, c, a.H, an, ok, l == 0);
                 if (l == 0) zero_other_parity(a, par);
                 CTRACE(s, l * 16 + 1);
                 if (!wait_tx_bar(a, c.prm_bar, c.uses_prm, 9000 + int(blockIdx.x))) ok = false;
                 CTRACE(s, l * 16 + 2);
                 TSET(s, l * 16 + 8);
-                canon_rows<WT, true>(a, c, G.a, k, kCRing, E, c.x, c.pr, p1, pc, c.outv, -1, best, ok);
+                canon_rows<WT, true>(a, c, G.a, k, kCRing, E, c.x, c.pr, p1, pc, c.outv, -1, best, ok, true);
                 CTRACE(s, l * 16 + 3);
                 for (int t = tid; t < a.fr; t += kCThreads) c.hloc[t] = gelu_new(c.outv[t]);
                 csync();
