@@ -255,3 +255,44 @@ def test_kv_cache_contents(path):
         assert m.kernels_per_step() == (5 * cfg.n_layer + 1 if path == "per_kernel" else 1)
     finally:
         m.close()
+
+
+# ---- the launch configuration bench.py times -----------------------------------
+
+@pytest.mark.parametrize("wdtype", ["f32", "int4"])
+def test_bench_launch_configuration(wdtype):
+    """GPT-2 small, default path, in the calls bench.py times: after a 10-token
+    prefill, one host-fed pass (decode_step at position 10) and 59 device-fed
+    greedy passes in one launch (decode_greedy).  The free-running greedy ids
+    of gpt2_generate must equal the oracle's while the oracle's top-2 margin
+    exceeds 1e-3; the bench's sequence of calls must end with bitwise the same
+    logits as gpt2_generate (same kernels, same order), and those must match
+    the oracle's last pass within the tolerance when no near tie intervened."""
+    cfg = synth.SMALL
+    w, dw = weights(cfg)
+    prompt = synth.make_prompt(cfg, 10, 1)
+    ref_ids, ref_rows = orc.greedy(cfg, orc.stored_weights(w, wdtype), prompt, 60)
+    m = binding.Model(cfg, dw, wdtype)
+    try:
+        ids = m.generate(prompt, 60)
+        gen_last = m.logits()
+        clean = True
+        for i, (a, b) in enumerate(zip(ids, ref_ids)):
+            if top2_margin(ref_rows[len(prompt) - 1 + i]) <= 1e-3:
+                clean = False            # a legal near-tie flip: the runs may diverge from here
+                break
+            assert a == b, f"{wdtype}: greedy id {i} differs"
+        # the bench's calls: prefill, argmax, decode_step, decode_greedy(59)
+        m.prefill(prompt)
+        tok0 = m.argmax()
+        assert tok0 == ids[0]
+        m.decode_step(tok0, len(prompt))
+        m.decode_greedy(59)
+        assert m.argmax() == ids[60]
+        bench_last = m.logits()
+        assert np.array_equal(bench_last, gen_last)
+        if clean:
+            atol, rl2 = TOL[wdtype]
+            check_rows(bench_last[None, :], ref_rows[-1][None, :], [ids[60]], atol, rl2)
+    finally:
+        m.close()
