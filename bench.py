@@ -3,12 +3,16 @@
 
 Workload (default): GPT-2 small (12 layers, n_embd 768, 12 heads, vocab 50257,
 1024 positions), fp32 weights drawn from N(0, 0.02) with seed 0, a 10-token
-prompt (seed 1) and 60 greedy decode steps at positions 10..69.  A bench
+prompt (seed 1) and 60 greedy decode steps at positions 10..69.  With
+--wdtype int4 the block matrices are grouped int4 and the workload is a
+10-token prompt + 128 steps; with --wdtype f16 they are fp16 and the workload
+is a 16-token prompt decoded to the full 1024-position cache (1008 steps),
+with tok/s and GB/s also reported per 64 positions ("context_sweep").  A bench
 "step" is one decode pass over one token: embedding, 12 blocks, final
 LayerNorm, tied head and argmax.  The timed region runs exactly --steps
-passes; they cycle through the 60-step generation (every 60th pass re-enters
-position 10 with the generation's first token, the other 59 are device-fed
-greedy passes), so any step count keeps the workload's positions.
+passes; they cycle through the workload's generation (each cycle re-enters
+its first position with the generation's first token, the rest are
+device-fed greedy passes), so any step count keeps the workload's positions.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--wdtype f32|f16|int4]
   python bench.py --impl reference ...     # the CPU oracle, same metric
@@ -33,7 +37,17 @@ if ROOT not in sys.path:
 
 METRIC = "GPT-2 124M decode tok/s @batch1; achieved HBM GB/s vs GB300 peak"
 UNIT = "tok/s"
-PROMPT_LEN, CYCLE = 10, 60
+# The workload of each block-weight type (GPT-2 small; prompt tokens, greedy
+# passes): fp32 10 + 60, int4 10 + 128, fp16 16 + 1008 (to the full
+# 1024-position cache, with tok/s reported per 64 positions).
+WORKLOADS = {"f32": (10, 60), "int4": (10, 128), "f16": (16, 1008)}
+PROMPT_LEN, CYCLE = WORKLOADS["f32"]
+SWEEP_BUCKET = 64
+
+
+def set_workload(wdtype: str):
+    global PROMPT_LEN, CYCLE
+    PROMPT_LEN, CYCLE = WORKLOADS[wdtype]
 L2_BYTES = 129 * 1024 * 1024
 CLOCK_FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
                 "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
@@ -244,6 +258,7 @@ class StepRunner:
 
 def main():
     args = parse()
+    set_workload(args.wdtype)
     if args.impl == "reference":
         return run_reference(args)
     import torch
@@ -307,20 +322,48 @@ def main():
     value = args.steps * world / (ms / 1e3)
 
     # ---- end to end through gpt2_generate: host prompt in, host ids out ----
+    passes_per_call = PROMPT_LEN + CYCLE
+    e2e_calls = max(3, min(args.e2e_calls, 3000 // passes_per_call))
     model.generate(prompt, CYCLE)
     barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(args.e2e_calls):
+    for _ in range(e2e_calls):
         model.generate(prompt, CYCLE)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0)
-    passes_per_call = PROMPT_LEN + CYCLE
-    e2e = {"value": args.e2e_calls * passes_per_call * world / e2e_s, "unit": UNIT,
+    e2e = {"value": e2e_calls * passes_per_call * world / e2e_s, "unit": UNIT,
            "h2d_bytes_per_step": PROMPT_LEN * 4, "d2h_bytes_per_step": (CYCLE + 1) * 4,
            "step": f"one gpt2_generate call: {PROMPT_LEN}-id host prompt, {PROMPT_LEN} prompt passes "
                    f"+ {CYCLE} greedy passes, {CYCLE + 1} ids back to host; value counts passes",
-           "calls": args.e2e_calls}
+           "calls": e2e_calls}
+
+    # ---- tok/s against context length (long workloads): one cycle, an event
+    # every SWEEP_BUCKET positions ----
+    sweep = None
+    if CYCLE >= 2 * SWEEP_BUCKET:
+        peaks_s, _ = measured_peaks()
+        marks = []
+        torch.cuda.synchronize()
+        ev = torch.cuda.Event(enable_timing=True)
+        ev.record(stream)
+        marks.append((PROMPT_LEN, ev))
+        model.decode_step(tok0, PROMPT_LEN)
+        pos = PROMPT_LEN + 1
+        while pos < PROMPT_LEN + CYCLE:
+            n = min(SWEEP_BUCKET - (pos - PROMPT_LEN) % SWEEP_BUCKET, PROMPT_LEN + CYCLE - pos)
+            model.decode_greedy(n)
+            pos += n
+            ev = torch.cuda.Event(enable_timing=True)
+            ev.record(stream)
+            marks.append((pos, ev))
+        torch.cuda.synchronize()
+        sweep = []
+        for (p0, e_a), (p1, e_b) in zip(marks, marks[1:]):
+            t = e_a.elapsed_time(e_b) / 1e3 / (p1 - p0)
+            b = roofline.mean_bytes_per_token(cfg, args.wdtype, range(p0, p1))
+            sweep.append({"positions": f"{p0}..{p1 - 1}", "us_per_token": t * 1e6, "tok_s": 1.0 / t,
+                          "gbs": b / t / 1e9, "frac": b / t / 1e9 / peaks_s["hbm_gbs"]})
     model.close()
 
     # ---- roofline of the decode pass --------------------------------------
@@ -347,6 +390,8 @@ def main():
             "config": dict(workload_config(args.wdtype, world), path=path), "e2e": e2e,
             "gpu_launches": launches,
             "roofline": roof, "clocks": clocks}
+    if sweep is not None:
+        line["context_sweep"] = sweep
 
     # ---- CPU baseline: the oracle on this host (rank 0, N = 1) ---------------
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
