@@ -1078,12 +1078,25 @@ __device__ void attention(const ClusterArgs &a, CS &c, int l, int h, int r, int 
         lsum = fmaf(lsum, corr, warp_sum(p));
 #pragma unroll
         for (int i = 0; i < DPL; ++i) o[i] *= corr;
+        // sum of p_j v_j, 8 positions at a time: their value rows are loaded
+        // before any is used, so the loads (shared or global) overlap
         const int cntt = min(32, w1 - base);
-        for (int i = 0; i < cntt; ++i) {
-            const float pi = __shfl_sync(0xffffffffu, p, i);
-            const float *vr = vrow(base + i);
+        for (int i0 = 0; i0 < cntt; i0 += 8) {
+            float pv[8], vv[8][DPL];
 #pragma unroll
-            for (int dd = 0; dd < DPL; ++dd) o[dd] = fmaf(pi, vr[lane + 32 * dd], o[dd]);
+            for (int u = 0; u < 8; ++u) {
+                const int i = min(i0 + u, cntt - 1);
+                pv[u] = __shfl_sync(0xffffffffu, p, i);
+                const float *vr = vrow(base + i);
+#pragma unroll
+                for (int dd = 0; dd < DPL; ++dd) vv[u][dd] = vr[lane + 32 * dd];
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (i0 + u < cntt) {
+#pragma unroll
+                    for (int dd = 0; dd < DPL; ++dd) o[dd] = fmaf(pv[u], vv[u][dd], o[dd]);
+                }
         }
         m = mn;
     }
