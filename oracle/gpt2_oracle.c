@@ -199,6 +199,58 @@ int32_t orc_argmax(const float *v, int32_t n)
 }
 
 /* ======================================================================== */
+/* Temperature sampling ([P2] "Step 7": divide the scores by a temperature, */
+/* apply softmax and draw at random; [P1] Options: -t, 0 means greedy).    */
+/* ======================================================================== */
+
+/* Output k of a counter-based SplitMix64 generator (Steele, Lea and Flood,
+ * "Fast splittable pseudorandom number generators", OOPSLA 2014): the state
+ * seed + (k + 1) * gamma, gamma = 0x9E3779B97F4A7C15, through the generator's
+ * output mixer. */
+uint64_t orc_splitmix64(uint64_t seed, uint64_t k)
+{
+    uint64_t z = seed + (k + 1u) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+/* A uniform float in (0, 1): the top 24 bits of output k, plus one half,
+ * times 2^-24 (exact in fp32). */
+float orc_uniform(uint64_t seed, uint64_t k)
+{
+    return ((float)(orc_splitmix64(seed, k) >> 40) + 0.5f) * 5.9604644775390625e-8f;
+}
+
+/* The Gumbel-max form of a draw from softmax(s / T): score i is
+ * s_i / T - log(-log u_i), u_i = uniform(seed, pos * n + i), in fp32 (the
+ * logarithms correctly rounded from double); the draw is the highest score.
+ * The pages draw one uniform number per token and walk the softmax
+ * distribution; this is the same distribution, with one number per score. */
+void orc_sample_scores(const float *s, int32_t n, float T, uint64_t seed, int32_t pos, float *out)
+{
+    for (int32_t i = 0; i < n; ++i) {
+        const float u = orc_uniform(seed, (uint64_t)pos * (uint64_t)n + (uint64_t)i);
+        const float e = (float)(-log((double)u));        /* -log u > 0 */
+        const float g = -(float)log((double)e);          /* Gumbel noise */
+        out[i] = s[i] / T + g;
+    }
+}
+
+/* The token the pass at position `pos` chooses: greedy when T == 0, else the
+ * draw above (exact ties to the lowest id, as for greedy). */
+int32_t orc_sample(const float *s, int32_t n, float T, uint64_t seed, int32_t pos)
+{
+    if (!(T > 0.f)) return orc_argmax(s, n);
+    float *v = (float *)malloc(sizeof(float) * (size_t)n);
+    if (!v) return -1;
+    orc_sample_scores(s, n, T, seed, pos, v);
+    const int32_t id = orc_argmax(v, n);
+    free(v);
+    return id;
+}
+
+/* ======================================================================== */
 /* The model: one token's forward pass ([P1] model.s description; [P3]     */
 /* node list: token, positional, embeddings, repeat layers { ln1, qkv,     */
 /* attention, out-projection, residual, ln2, fc, gelu, proj, residual },   */

@@ -121,6 +121,15 @@ void orc_quant_int4(const float *W, int32_t in, int32_t out,
 void orc_dequant_int4(const uint8_t *codes, const float *scales,
                       const uint8_t *zeros, int32_t in, int32_t out,
                       float *W_oi);
+/* Temperature sampling ("Let's make GPT-2 in assembly", Step 7; "gpt2.s"
+ * README, Options -t): counter-based SplitMix64 output k, a uniform float in
+ * (0, 1) from it, the Gumbel-max scores s_i / T - log(-log u_i) with
+ * u_i = uniform(seed, pos * n + i), and the chosen token (greedy if T == 0). */
+uint64_t orc_splitmix64(uint64_t seed, uint64_t k);
+float orc_uniform(uint64_t seed, uint64_t k);
+void orc_sample_scores(const float *s, int32_t n, float T, uint64_t seed, int32_t pos, float *out);
+int32_t orc_sample(const float *s, int32_t n, float T, uint64_t seed, int32_t pos);
+
 /* nibble helpers (for the round-trip pin) */
 void orc_pack_nibbles(const uint8_t *vals, size_t n, uint8_t *packed);
 void orc_unpack_nibbles(const uint8_t *packed, size_t n, uint8_t *vals);

@@ -80,6 +80,11 @@ def lib():
             L.orc_linear_t.argtypes = [vp, vp, c_i32, c_i32, vp]
             L.orc_attn_decode.argtypes = [vp, c_i32, c_i32, c_i32, c_i32, vp, vp, vp]
             L.orc_argmax.restype = c_i32; L.orc_argmax.argtypes = [vp, c_i32]
+            c_u64 = ctypes.c_uint64
+            L.orc_splitmix64.restype = c_u64; L.orc_splitmix64.argtypes = [c_u64, c_u64]
+            L.orc_uniform.restype = c_f; L.orc_uniform.argtypes = [c_u64, c_u64]
+            L.orc_sample_scores.argtypes = [vp, c_i32, c_f, c_u64, c_i32, vp]
+            L.orc_sample.restype = c_i32; L.orc_sample.argtypes = [vp, c_i32, c_f, c_u64, c_i32]
             L.orc_create.restype = vp
             L.orc_create.argtypes = [ctypes.POINTER(_Cfg), ctypes.POINTER(_Weights)]
             L.orc_destroy.argtypes = [vp]
@@ -191,6 +196,29 @@ def argmax(v) -> int:
 
 
 # ---- stored-weight formats -------------------------------------------------
+
+def splitmix64(seed: int, k: int) -> int:
+    return int(lib().orc_splitmix64(seed, k))
+
+
+def uniform(seed: int, k: int) -> float:
+    return float(lib().orc_uniform(seed, k))
+
+
+def sample_scores(logits, temperature: float, seed: int, pos: int) -> np.ndarray:
+    """Gumbel-max scores of a temperature draw (their argmax is the draw)."""
+    s = _f32(logits)
+    out = np.empty_like(s)
+    lib().orc_sample_scores(_p(s), s.size, temperature, seed, pos, _p(out))
+    return out
+
+
+def sample(logits, temperature: float, seed: int, pos: int) -> int:
+    """The token chosen from these logits by the pass at position `pos`:
+    greedy when temperature is 0, else a draw from softmax(logits / T)."""
+    s = _f32(logits)
+    return int(lib().orc_sample(_p(s), s.size, temperature, seed, pos))
+
 
 def f32_to_f16_bits(x) -> np.ndarray:
     x = _f32(x)
@@ -360,11 +388,12 @@ def forward_full(cfg, weights: dict, tokens) -> np.ndarray:
     return out
 
 
-def greedy(cfg, weights: dict, prompt, n_steps: int, teacher=None):
+def greedy(cfg, weights: dict, prompt, n_steps: int, teacher=None, temperature: float = 0.0, seed: int = 0):
     """Prefill the prompt one token at a time (positions 0..n-1), then run
-    ``n_steps`` decode passes.  Returns (ids, logits): ids[i] is the greedy
-    argmax after pass n-1+i (so ids has n_steps + 1 entries), logits has one
-    row per pass (n + n_steps rows).  Decode pass i consumes ids[i], or
+    ``n_steps`` decode passes.  Returns (ids, logits): ids[i] is the token
+    chosen after pass n-1+i (so ids has n_steps + 1 entries): the greedy
+    argmax, or with temperature > 0 the draw of sample(); logits has one row
+    per pass (n + n_steps rows).  Decode pass i consumes ids[i], or
     teacher[i] when ``teacher`` is given (teacher forcing)."""
     m = OracleModel(cfg, weights)
     try:
@@ -374,11 +403,15 @@ def greedy(cfg, weights: dict, prompt, n_steps: int, teacher=None):
         for pos, t in enumerate(prompt):
             logits, last = m.forward(t, pos)
             rows.append(logits)
+        if temperature > 0:
+            last = sample(rows[-1], temperature, seed, len(prompt) - 1)
         ids = [last]
         pos = len(prompt)
         for i in range(n_steps):
             feed = ids[-1] if teacher is None else int(teacher[i])
             logits, last = m.forward(feed, pos)
+            if temperature > 0:
+                last = sample(logits, temperature, seed, pos)
             rows.append(logits)
             ids.append(last)
             pos += 1
