@@ -187,6 +187,21 @@ int gpt2_prefill(gpt2_model *m, const int32_t *host_ids, int32_t n);
  * kernel), CUDA. */
 int gpt2_argmax(gpt2_model *m, int32_t *token_out);
 
+/* How the following passes choose their token ("Let's make GPT-2 in
+ * assembly", Step 7: divide the scores by a temperature, apply softmax, draw
+ * at random; "gpt2.s" README, Options: -t, 0 means greedy).  temperature 0
+ * (the default) is greedy.  temperature > 0 draws each pass's token from
+ * softmax(logits / temperature), in the Gumbel-max form: the token with the
+ * highest logit / temperature - log(-log u), u the uniform number of counter
+ * position * vocab_size + id from a counter-based SplitMix64 generator with
+ * this seed (u = (top 24 bits of the output + 0.5) * 2^-24).  The same seed,
+ * prompt and weights give the same tokens.  The drawn token is what
+ * gpt2_argmax returns and what gpt2_decode_greedy / gpt2_generate feed to the
+ * next pass; the logits stay the plain ones.  Takes effect from the next
+ * call.  Errors: INVALID_ARG (temperature negative or not finite, or
+ * temperature > 0 on a model that does not use the cluster kernel). */
+int gpt2_set_sampling(gpt2_model *m, float temperature, uint64_t seed);
+
 /* Device-resident greedy decoding: n_steps more decode passes, each fed the
  * previous pass's argmax without a round trip to the host (token and
  * position live in device memory).  Needs a previous step; the cached length

@@ -296,3 +296,64 @@ def test_bench_launch_configuration(wdtype):
             check_rows(bench_last[None, :], ref_rows[-1][None, :], [ids[60]], atol, rl2)
     finally:
         m.close()
+
+
+# ---- temperature sampling ---------------------------------------------------------
+
+@pytest.mark.parametrize("cfg_name,n_prompt,n_steps", [("tiny", 4, 16), ("small", 10, 40)])
+def test_sampling_matches_oracle(cfg_name, n_prompt, n_steps):
+    """Temperature sampling (T = 0.8) on the default path, fed the oracle's own
+    draws (teacher forcing): every drawn id equals the oracle's wherever the
+    top-2 margin of the oracle's perturbed scores exceeds 1e-3, and the logits
+    meet the fp32 tolerance."""
+    cfg = synth.TINY if cfg_name == "tiny" else synth.SMALL
+    T, seed = 0.8, 20241
+    w, dw = weights(cfg)
+    prompt = synth.make_prompt(cfg, n_prompt, 1)
+    ref_ids, ref_rows = orc.greedy(cfg, w, prompt, n_steps, temperature=T, seed=seed)
+    tokens = list(prompt) + ref_ids[:n_steps]
+    m = binding.Model(cfg, dw, "f32")
+    try:
+        assert m.path() == "cluster"
+        m.set_sampling(T, seed)
+        rows, ids = teacher_forced(m, tokens)
+    finally:
+        m.close()
+    atol, _ = TOL["f32"]
+    checked = 0
+    for pos in range(len(tokens)):
+        assert max_abs(rows[pos], ref_rows[pos]) <= atol, f"step {pos}"
+        sc = orc.sample_scores(ref_rows[pos], T, seed, pos)
+        if top2_margin(sc) > 1e-3:
+            assert ids[pos] == int(np.argmax(sc)), f"step {pos}: drawn id differs"
+            checked += 1
+    assert checked >= len(tokens) // 2
+    # a draw, not the greedy choice: at T = 0.8 some tokens differ from the argmax
+    assert any(ids[p] != int(np.argmax(ref_rows[p])) for p in range(len(tokens)))
+
+
+def test_sampling_controls():
+    cfg = synth.TINY
+    w, dw = weights(cfg)
+    prompt = synth.make_prompt(cfg, 4, 1)
+    ref_ids, _ = orc.greedy(cfg, w, prompt, 8)
+    m = binding.Model(cfg, dw, "f32")
+    try:
+        for bad in (-0.5, float("nan"), float("inf")):
+            with pytest.raises(binding.GPT2Error):
+                m.set_sampling(bad, 1)
+        m.set_sampling(0.9, 5)
+        a = m.generate(prompt, 8)
+        b = m.generate(prompt, 8)
+        assert a == b                                    # same seed and prompt: same draws
+        m.set_sampling(0.0, 5)
+        assert m.generate(prompt, 8) == ref_ids          # temperature 0 is greedy again
+    finally:
+        m.close()
+    m = binding.Model(cfg, dw, "f32", path="per_kernel")
+    try:
+        with pytest.raises(binding.GPT2Error):
+            m.set_sampling(0.8, 1)                       # drawn only by the cluster kernel
+        m.set_sampling(0.0, 1)
+    finally:
+        m.close()

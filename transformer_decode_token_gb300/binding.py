@@ -27,7 +27,7 @@ EXPORTED = ("gpt2_create", "gpt2_create_ex", "gpt2_path", "gpt2_launch_count", "
             "gpt2_argmax", "gpt2_decode_greedy", "gpt2_generate", "gpt2_copy_logits", "gpt2_sync",
             "gpt2_matrix_bytes", "gpt2_export_matrix", "gpt2_export_dequant", "gpt2_export_kv",
             "gpt2_kernels_per_step", "gpt2_op_layernorm", "gpt2_op_head_argmax_workspace",
-            "gpt2_op_head_argmax", "gpt2_op_head_argmax_noalloc", "gpt2_strerror")
+            "gpt2_op_head_argmax", "gpt2_op_head_argmax_noalloc", "gpt2_set_sampling", "gpt2_strerror")
 
 
 class GPT2Error(RuntimeError):
@@ -113,6 +113,7 @@ def lib(build_if_stale: bool = True, path: str = None):
             L.gpt2_op_head_argmax_workspace.restype = sz
             L.gpt2_op_head_argmax.argtypes = [vp, vp, vp, f32, vp, i32, i32, vp, vp, vp, sz, vp]
             L.gpt2_op_head_argmax_noalloc.argtypes = [vp, vp, vp, f32, vp, i32, i32, vp, vp, vp]
+            L.gpt2_set_sampling.argtypes = [vp, f32, ctypes.c_uint64]
             L.gpt2_strerror.argtypes = [ctypes.c_int]
             L.gpt2_strerror.restype = ctypes.c_char_p
             for n in EXPORTED:
@@ -203,6 +204,9 @@ class Model:
 
     def decode_greedy(self, n_steps: int):
         check(lib().gpt2_decode_greedy(self._h, int(n_steps)), "gpt2_decode_greedy")
+
+    def set_sampling(self, temperature: float, seed: int = 0):
+        check(lib().gpt2_set_sampling(self._h, float(temperature), int(seed) & (2**64 - 1)), "gpt2_set_sampling")
 
     def generate(self, prompt, n_steps: int) -> list:
         p = np.ascontiguousarray(prompt, np.int32)

@@ -1051,6 +1051,15 @@ void gpt2_destroy(gpt2_model *m)
     free_model(m);
 }
 
+int gpt2_set_sampling(gpt2_model *m, float temperature, uint64_t seed)
+{
+    if (!m || !(temperature >= 0.f) || !std::isfinite(temperature)) return GPT2_ERR_INVALID_ARG;
+    if (temperature > 0.f && !m->cluster) return GPT2_ERR_INVALID_ARG;   // drawn in the cluster kernel's head
+    m->cargs.temperature = temperature;
+    m->cargs.seed = (unsigned long long)seed;
+    return GPT2_OK;
+}
+
 int gpt2_reset(gpt2_model *m)
 {
     if (!m) return GPT2_ERR_INVALID_ARG;

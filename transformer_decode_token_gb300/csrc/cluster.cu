@@ -689,6 +689,24 @@ __device__ __forceinline__ uint32_t stage_addr(const ClusterArgs &a, const CS &c
     return smem_addr(c.ring) + (kk & (kCRing - 1)) * a.stage_bytes;
 }
 
+// Temperature sampling ("Let's make GPT-2 in assembly", Step 7: divide the
+// scores by a temperature, softmax, draw at random): the Gumbel-max form, the
+// token with the highest logit / T - log(-log u), u = the uniform number of
+// counter pos * V + id from a counter-based SplitMix64 generator (Steele, Lea
+// and Flood, 2014): seed + (k + 1) * 0x9E3779B97F4A7C15 through its output
+// mixer; u = (top 24 bits + 0.5) * 2^-24.  The argmax key is built from that
+// score; the stored logit stays the plain one.
+__device__ __forceinline__ float sample_score(float logit, float temperature, unsigned long long seed,
+                                              unsigned long long k)
+{
+    unsigned long long z = seed + (k + 1ull) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    z ^= z >> 31;
+    const float u = (float(uint32_t(z >> 40)) + 0.5f) * 5.9604644775390625e-8f;
+    return logit / temperature - logf(-logf(u));
+}
+
 // Row groups of one warp in one window: rows [w0, w1), RG at a time (a short
 // last group repeats its first row in the empty slots, whose sums are not
 // stored: no per-row branches in the loop), lanes over the column units; each
@@ -698,7 +716,7 @@ __device__ __forceinline__ void canon_groups(const ClusterArgs &a, const CS &c, 
                                              int w1, int units, const float4 (&xr)[UnitOf<WT>::kPL * UnitOf<WT>::kF4],
                                              bool &have_stats, float ssum, float ssq, float shift, int in,
                                              float &mean, float &rstd, const float *c1, const float *cb, float *out,
-                                             int logit_row0, unsigned long long &best)
+                                             int logit_row0, unsigned long long &best, long long sample_k0)
 {
     constexpr int kF4 = UnitOf<WT>::kF4;
     const int lane = threadIdx.x & 31, C = g.chunk;
@@ -742,7 +760,10 @@ __device__ __forceinline__ void canon_groups(const ClusterArgs &a, const CS &c, 
             if (LN) t = rstd * fmaf(-mean, c1[i], t) + cb[i];
             if (logit_row0 >= 0) {
                 a.logits[logit_row0 + i] = t;
-                const unsigned long long key = argmax_key(t, uint32_t(logit_row0 + i));
+                const float score = sample_k0 >= 0 ? sample_score(t, a.temperature, a.seed,
+                                                                  (unsigned long long)(sample_k0 + logit_row0 + i))
+                                                   : t;
+                const unsigned long long key = argmax_key(score, uint32_t(logit_row0 + i));
                 best = key > best ? key : best;
             } else {
                 out[i] = t;
@@ -789,7 +810,7 @@ template <int WT, bool LN>
 __device__ __forceinline__ void canon_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &k, int win, int in,
                                           const float *xin, const float *gamma, const float *c1, const float *cb,
                                           float *out, int logit_row0, unsigned long long &best, bool &ok,
-                                          bool prewaited = false)
+                                          bool prewaited = false, long long sample_k0 = -1)
 {
     constexpr int kF4 = UnitOf<WT>::kF4;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -838,10 +859,10 @@ __device__ __forceinline__ void canon_rows(const ClusterArgs &a, CS &c, const Ge
         if (ok && w0 < w1) {
             if (per <= 4)
                 canon_groups<WT, LN, 4>(a, c, g, k, w0, w1, units, xr, have_stats, ssum, ssq, shift, in, mean, rstd,
-                                        c1, cb, out, logit_row0, best);
+                                        c1, cb, out, logit_row0, best, sample_k0);
             else
                 canon_groups<WT, LN, 6>(a, c, g, k, w0, w1, units, xr, have_stats, ssum, ssq, shift, in, mean, rstd,
-                                        c1, cb, out, logit_row0, best);
+                                        c1, cb, out, logit_row0, best, sample_k0);
         }
         CSUB(2);
         window_release(c, k, q0, q1);   // its barrier also publishes out[]
@@ -1429,7 +1450,7 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
         if (!wait_tx_bar(a, c.prm_bar, c.uses_prm, 9000 + int(blockIdx.x))) ok = false;
         TSET(s, 204);
         canon_rows<kWF32, true>(a, c, G.head, k, kStreamWindow, E, c.x, c.pr, p1, pc, nullptr, G.head_row0, best,
-                                ok);
+                                ok, false, a.temperature > 0.f ? (long long)pos * (long long)a.V : -1ll);
         CTRACE(s, 202);
         finish_head(a, sh, s, seq, best);
         CTRACE(s, 203);

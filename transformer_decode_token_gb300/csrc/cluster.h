@@ -62,6 +62,8 @@ struct ClusterArgs {
     float eps, scale;
     int32_t nfc, fr;             // fc CTAs, fc rows (= mlp-proj columns) per fc CTA
     int32_t head_rpc;            // LM-head rows per CTA (a multiple of 4)
+    float temperature;           // token choice: 0 = greedy, > 0 = a draw from softmax(logits / T)
+    unsigned long long seed;     // sampling: seed of the counter-based generator
     int32_t pr_rows;             // row slots of the parameter area (a multiple of 4)
     const float *h_c1, *h_cb;    // LM head: wte.gamma_f, wte.beta_f, padded to head_rpc * grid
     // residual-stream sums, one 64-bit word per element holding the biased
