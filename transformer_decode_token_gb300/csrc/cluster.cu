@@ -3,8 +3,8 @@
 //
 // A pass needs the whole output vector of one step on every SM before the
 // next step can start (LayerNorm needs all of x, a linear needs all of its
-// input).  Measured on GB300, one such GPU-wide exchange costs ~2-3 us, so a
-// pass of 61 of them cannot be fast.  Here one block needs two:
+// input).  Measured on GB300, one such GPU-wide exchange costs ~1.4-3 us, so
+// a pass of 61 of them cannot be fast.  Here one block needs two:
 //
 //   head clusters (one per attention head, 4 CTAs):
 //     wait for x (GPU-wide) -> LN1 -> this head's q, k, v rows of the QKV
@@ -15,25 +15,26 @@
 //     the rows per CTA) -> added into x_new
 //   fc clusters (the other CTAs):
 //     wait for x_new (GPU-wide) -> LN2 -> fr rows of the fc matrix, gelu_new ->
-//     the matching fr columns of the MLP projection (split-K) -> added into
-//     the next x
+//     the matching fr columns of the MLP projection (split-K), reduced over
+//     the cluster -> added into the next x
 //   every CTA: wait for the last x -> LN_f -> its rows of the tied head ->
-//     argmax -> the next token (a tagged word read by the next pass).
+//     argmax (or a temperature draw) -> the next token (a tagged word read by
+//     the next pass).
 //
-// GPU-wide sums are fixed-point (int64, 2^-32 units) atomic additions: integer
-// addition does not depend on the order of the atomics, so every run gives
-// the same bits.  A contributor adds its values, fences, and bumps a per-layer
-// counter with release semantics; a consumer waits (acquire) until the
-// counter reaches pass * contributors.  Sums are double-buffered by pass
-// parity; each CTA zeroes its share of the other parity at the start of a pass
-// (the previous pass finished reading it before its token existed).
+// GPU-wide sums are fixed-point atomic additions that carry their own count
+// (see kFixScale below): integer addition does not depend on the order of the
+// atomics, so every run gives the same bits, and a reader polls the words
+// until their counts are complete.  Sums are double-buffered by pass parity;
+// each CTA zeroes its share of the other parity after the first wait of a
+// pass (by then every CTA has finished the previous pass).
 //
-// Weights stream through a ring of shared-memory stages as in the persistent
-// kernel (one producer thread, cp.async.bulk, mbarriers).  Every wait is
-// bounded by 2 s of %globaltimer; on timeout the kernel records
-// GPT2_ERR_TIMEOUT, raises the abort word and runs its remaining steps without
-// waiting; all CTAs of a cluster meet at a final cluster barrier, so no CTA
-// exits while a peer may still write its shared memory.
+// Weights stream through a ring of shared-memory stages (one producer thread,
+// cp.async.bulk, mbarriers); a CTA's slice of a layer fits the ring, so it is
+// resident before the layer's input arrives.  Every wait is bounded by 2 s of
+// %globaltimer; on timeout the kernel records GPT2_ERR_TIMEOUT, raises the
+// abort word and runs its remaining steps without waiting; all CTAs of a
+// cluster meet at a final cluster barrier, so no CTA exits while a peer may
+// still write its shared memory.
 #include "cluster.h"
 #include "gemv_dev.cuh"
 
