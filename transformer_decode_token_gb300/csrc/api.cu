@@ -79,7 +79,7 @@ struct gpt2_model {
     // cluster path (uses the prompt buffer of the persistent path)
     bool cluster = false;
     uint8_t *cbuf = nullptr;         // tiled matrices, sums, counters, token word, layer table
-    uint8_t *c_state = nullptr;      // sums + counters + token word (zeroed together)
+    uint8_t *c_state = nullptr;      // sums + tagged LM-head keys (zeroed together)
     size_t c_state_bytes = 0;
     ClusterArgs cargs{};
     int c_clusters = 0;
@@ -573,7 +573,8 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
     if (nfc == 0) return GPT2_ERR_INVALID_ARG;
     const int fr = F / nfc;
     const int n_clusters = H + nfc / kClusterSize, grid = n_clusters * kClusterSize;
-    if (grid > m->max_head_ctas) return GPT2_ERR_INVALID_ARG;   // per-CTA argmax slots
+    if (grid > 256) return GPT2_ERR_INVALID_ARG;   // each consumer thread polls one CTA's LM-head key
+    if (V > (1 << 17)) return GPT2_ERR_INVALID_ARG;   // tagged keys keep 17 bits of the id
     const int head_rpc = ((V + grid - 1) / grid + 3) / 4 * 4;
     const int pr_rows = (std::max(std::max(3 * (D / 4), fr), head_rpc) + 3) / 4 * 4;
     const size_t fixed = cluster_fixed_smem(E, D, fr, L, pr_rows);
@@ -637,7 +638,7 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
     const size_t o_state = off;
     const size_t acc_bytes = size_t(2) * L * E * 8 * kClusterAccStride;
     const size_t o_accn = take(acc_bytes), o_accx = take(acc_bytes);
-    const size_t o_tok = take(8);
+    const size_t o_keys = take(size_t(grid) * 8);   // per-CTA LM-head keys, tagged with their pass
     const size_t state_bytes = off - o_state;
     const size_t o_layers = take(sizeof(CLayer) * L);
     uint8_t *B = nullptr;
@@ -761,12 +762,10 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
     a.h_cb = reinterpret_cast<const float *>(B + o_hcb);
     a.acc_new = reinterpret_cast<long long *>(B + o_accn);
     a.acc_next = reinterpret_cast<long long *>(B + o_accx);
-    a.ll_tok = reinterpret_cast<uint64_t *>(B + o_tok);
     a.kcache = m->kcache;
     a.vcache = m->vcache;
     a.logits = m->logits;
-    a.partials = m->partials;
-    a.counter = m->counter;
+    a.partials = reinterpret_cast<unsigned long long *>(B + o_keys);
     a.out_ids = m->out_ids;
     a.out_cap = m->out_cap;
     a.st = m->st;

@@ -170,17 +170,6 @@ __device__ __forceinline__ void red_add_i64(long long *p, long long v)
 {
     asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
-__device__ __forceinline__ void ll_store64(uint64_t *p, uint32_t bits, uint32_t epoch)
-{
-    const uint64_t w = (uint64_t(epoch) << 32) | bits;
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
-}
-__device__ __forceinline__ uint64_t ll_load64(const uint64_t *p)
-{
-    uint64_t w;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
-    return w;
-}
 __device__ __forceinline__ unsigned long long to_word(float v)
 {
     v = fminf(fmaxf(v, -kFixLimit), kFixLimit);
@@ -195,7 +184,6 @@ __device__ __forceinline__ float word_value(unsigned long long w)
 }
 
 struct Sh {
-    int last;
     unsigned long long keys[kCWarps];
 };
 
@@ -1229,9 +1217,24 @@ __device__ __forceinline__ void zero_other_parity(const ClusterArgs &a, int par)
     }
 }
 
-// The last CTA to finish the LM head reduces the per-CTA argmax keys,
-// publishes the token and updates the state.
-__device__ __forceinline__ void finish_head(const ClusterArgs &a, Sh &sh, int s, uint32_t seq, unsigned long long best)
+// The LM head's hand-off: each CTA publishes its best (value, ~id) key with
+// the pass's epoch (its sequence number mod 2^15) in bits 17..31, in place
+// of the top bits of ~id (ids < 2^17), so the word is its own arrival flag;
+// the head CTAs of the next pass (and CTA 0 after the last pass) poll all the
+// keys, each thread one CTA's word, until every word carries the epoch, and
+// take the maximum.  Keys of one epoch compare as untagged keys do.
+constexpr unsigned long long kKeyEpochMask = 0x7FFFull << 17;
+
+__device__ __forceinline__ unsigned long long tag_key(unsigned long long key, uint32_t seq)
+{
+    return (key & ~kKeyEpochMask) | ((unsigned long long)(seq & 0x7FFFu) << 17);
+}
+__device__ __forceinline__ int32_t tagged_key_index(unsigned long long key)
+{
+    return int32_t(0x1FFFFu - uint32_t(key & 0x1FFFFull));
+}
+
+__device__ __forceinline__ void publish_key(const ClusterArgs &a, Sh &sh, uint32_t seq, unsigned long long best)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     best = warp_max_u64(best);
@@ -1240,40 +1243,53 @@ __device__ __forceinline__ void finish_head(const ClusterArgs &a, Sh &sh, int s,
     if (tid == 0) {
         unsigned long long b = 0ull;
         for (int w = 0; w < kCWarps; ++w) b = sh.keys[w] > b ? sh.keys[w] : b;
-        a.partials[blockIdx.x] = b;
-        __threadfence();
-        const unsigned t = atomicAdd(a.counter, 1u);
-        sh.last = (t == gridDim.x - 1) ? 1 : 0;
+        asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a.partials + blockIdx.x), "l"(tag_key(b, seq))
+                     : "memory");
     }
-    csync();
-    if (sh.last && warp == 0) {
-        __threadfence();
-        unsigned long long b = 0ull;
-        for (int i = lane; i < int(gridDim.x); i += 32) {
-            const unsigned long long v = __ldcg(a.partials + i);
-            b = v > b ? v : b;
-        }
-        b = warp_max_u64(b);
-        if (lane == 0) {
-            const int32_t tok = argmax_key_index(b);
-            *a.counter = 0u;
-            DeviceState *st = a.st;
-            st->next_tok = tok;
-            if (s >= a.n_prompt - 1) {
-                const int32_t n = st->n_out;
-                if (a.out_ids && n >= 0 && n < a.out_cap) a.out_ids[n] = tok;
-                st->n_out = n + 1;
-            }
-            if (s == a.n_steps - 1) {
-                st->tok = tok;
-                st->pos = a.pos0 + a.n_steps;
-                st->seq = int32_t(seq + 1);
-            }
-            __threadfence();
-            ll_store64(a.ll_tok, uint32_t(tok), seq);
+    // sh.keys is written again only after every CTA has published this pass's key
+}
+
+// The token chosen by pass `seq`: polls every CTA's key (all threads of the
+// CTA call it), returns the id of the largest.  Ends with a fence: what the
+// CTAs did before publishing is ordered before what follows.
+__device__ __forceinline__ int32_t collect_token(const ClusterArgs &a, Sh &sh, uint32_t seq, bool &ok)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const unsigned long long want = (unsigned long long)(seq & 0x7FFFu) << 17;
+    unsigned long long v = 0ull;
+    if (tid < int(gridDim.x)) {
+        v = ld_word(reinterpret_cast<const long long *>(a.partials + tid));
+        Waiter w;
+        while (ok && (v & kKeyEpochMask) != want) {
+            if (!keep_waiting(a, w, 7000 + int(blockIdx.x))) ok = false;
+            v = ld_word(reinterpret_cast<const long long *>(a.partials + tid));
         }
     }
+    v = warp_max_u64(v);
+    if (lane == 0) sh.keys[warp] = v;
     csync();
+    unsigned long long b = 0ull;
+    for (int w = 0; w < kCWarps; ++w) b = sh.keys[w] > b ? sh.keys[w] : b;
+    __threadfence();
+    csync();   // every thread has read sh.keys
+    return tagged_key_index(b);
+}
+
+// CTA 0, thread 0: the state after pass s chose `tok`.
+__device__ __forceinline__ void record_token(const ClusterArgs &a, int s, uint32_t seq, int32_t tok)
+{
+    DeviceState *st = a.st;
+    st->next_tok = tok;
+    if (s >= a.n_prompt - 1) {
+        const int32_t n = st->n_out;
+        if (a.out_ids && n >= 0 && n < a.out_cap) a.out_ids[n] = tok;
+        st->n_out = n + 1;
+    }
+    if (s == a.n_steps - 1) {
+        st->tok = tok;
+        st->pos = a.pos0 + a.n_steps;
+        st->seq = int32_t(seq + 1);
+    }
 }
 
 // Bulk copies of what a CTA needs besides weights in one layer
@@ -1351,14 +1367,8 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                     // sums, the exchange slots and the cache rows safe
                     int tok = 0;
                     if (s > 0) {
-                        uint64_t w = ll_load64(a.ll_tok);
-                        Waiter wt;
-                        while (ok && uint32_t(w >> 32) != seq - 1) {
-                            if (!keep_waiting(a, wt, 7000 + int(blockIdx.x))) ok = false;
-                            w = ll_load64(a.ll_tok);
-                        }
-                        tok = int(uint32_t(w));
-                        __threadfence();   // acquire: the previous pass is complete
+                        tok = collect_token(a, sh, seq - 1, ok);
+                        if (blockIdx.x == 0 && tid == 0) record_token(a, s - 1, seq - 1, tok);
                     }
                     if (s < a.n_prompt) tok = a.prompt ? __ldg(a.prompt + s) : a.tok_first;
                     else if (s == 0) tok = ld_relaxed_i32(&a.st->tok);
@@ -1453,7 +1463,11 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
         canon_rows<kWF32, true>(a, c, G.head, k, kStreamWindow, E, c.x, c.pr, p1, pc, nullptr, G.head_row0, best,
                                 ok, false, a.temperature > 0.f ? (long long)pos * (long long)a.V : -1ll);
         CTRACE(s, 202);
-        finish_head(a, sh, s, seq, best);
+        publish_key(a, sh, seq, best);
+        if (s == a.n_steps - 1 && blockIdx.x == 0) {   // the last pass's token: CTA 0 records it
+            const int32_t tok = collect_token(a, sh, seq, ok);
+            if (tid == 0) record_token(a, s, seq, tok);
+        }
         CTRACE(s, 203);
     }
 }
@@ -1528,7 +1542,6 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kCAll, 1)
         mbar_init(c.red_bar, 1);   // + the bytes of the cluster's four partial slices
         mbar_init(c.x_bar, 1);     // + the bytes of x, a quarter from each CTA of the cluster
         mbar_init_fence();
-        sh.last = 0;
 #ifdef GPT2_CTRACE
         twait = 0;
         tsub[0] = tsub[1] = tsub[2] = 0;

@@ -71,11 +71,9 @@ struct ClusterArgs {
     // pass parity; the other parity is zeroed during a pass)
     long long *acc_new;          // [2 parity][L][E][kClusterAccStride]  x after the attention block
     long long *acc_next;         // [2 parity][L][E][kClusterAccStride]  x after the MLP block
-    uint64_t *ll_tok;            // the next token, tagged with its pass
     float *kcache, *vcache;      // [L][H][P][D]
     float *logits;
-    unsigned long long *partials;
-    unsigned int *counter;
+    unsigned long long *partials;  // [grid] each CTA's best LM-head key, tagged with its pass
     int32_t *out_ids;
     int32_t out_cap;
     DeviceState *st;
