@@ -343,7 +343,7 @@ int32_t orc_forward(orc_model *m, int32_t token, int32_t pos, float *logits)
         for (int32_t e = 0; e < E; ++e) m->x[e] = m->x[e] + m->mix[e];
     }
     orc_layernorm(m->x, m->w.lnf_w, m->w.lnf_b, E, eps, m->norm);
-    orc_linear_t(m->norm, m->w.wte, E, c->vocab_size, logits);
+    orc_linear_t(m->norm, m->w.head ? m->w.head : m->w.wte, E, c->vocab_size, logits);
     return orc_argmax(logits, c->vocab_size);
 }
 
@@ -413,7 +413,7 @@ int32_t orc_forward_full(const orc_config *c, const orc_weights *w,
     }
     for (int32_t t = 0; t < n; ++t) {
         orc_layernorm(X + (size_t)t * E, w->lnf_w, w->lnf_b, E, eps, N + (size_t)t * E);
-        orc_linear_t(N + (size_t)t * E, w->wte, E, c->vocab_size,
+        orc_linear_t(N + (size_t)t * E, w->head ? w->head : w->wte, E, c->vocab_size,
                      logits_all + (size_t)t * c->vocab_size);
     }
     free(X); free(N); free(QKV); free(O); free(M); free(Fh); free(S);

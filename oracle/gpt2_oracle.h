@@ -58,6 +58,9 @@ typedef struct {
     const float *wpe;      /* [P][E]  position embedding                  */
     const float *lnf_w, *lnf_b;          /* [E]                            */
     const orc_layer *layers;             /* n_layer entries                */
+    const float *head;     /* [V][E] the output head as stored, or NULL: the
+                              tied wte ("gpt2.s" README, Options: -h stores the
+                              output head in fp16; its values widened here) */
 } orc_weights;
 
 /* ---- scalar math ([P2] "Step 5: Math without a math library") ---------- */

@@ -58,7 +58,7 @@ class _Layer(ctypes.Structure):
 
 class _Weights(ctypes.Structure):
     _fields_ = [("wte", _FP), ("wpe", _FP), ("lnf_w", _FP), ("lnf_b", _FP),
-                ("layers", ctypes.POINTER(_Layer))]
+                ("layers", ctypes.POINTER(_Layer)), ("head", _FP)]
 
 
 def lib():
@@ -290,11 +290,19 @@ def unpack_nibbles(packed, n: int) -> np.ndarray:
 MATRIX_KEYS = ("attn_w", "proj_w", "fc_w", "mlp_proj_w")
 
 
-def stored_weights(weights: dict, wdtype: str) -> dict:
+def stored_weights(weights: dict, wdtype: str, head: str = "f32") -> dict:
     """The weights as a given storage mode holds them, widened back to fp32
     in the checkpoint layout: the 48 block matrices are rounded to fp16 or
     quantised to grouped int4; embeddings, biases, LayerNorm and the tied head
-    stay fp32.  'f32' returns the weights unchanged."""
+    stay fp32.  'f32' returns the weights unchanged.  head='f16' adds the
+    output head stored as fp16 ("gpt2.s" README, Options: -h), a separate
+    matrix: the embedding lookup still reads the fp32 wte."""
+    if head == "f16":
+        out = dict(stored_weights(weights, wdtype))
+        out["head"] = f16_bits_to_f32(f32_to_f16_bits(_f32(weights["wte"])))
+        return out
+    if head != "f32":
+        raise ValueError(f"unknown head dtype {head!r}")
     if wdtype == "f32":
         return weights
     out = dict(weights)
@@ -339,9 +347,11 @@ class _WeightsHolder:
         for i, L in enumerate(weights["layers"]):
             for k in _LAYER_KEYS:
                 setattr(self.layers[i], k, fp(L[k]))
+        head = weights.get("head")
         self.w = _Weights(fp(weights["wte"]), fp(weights["wpe"]),
                           fp(weights["ln_f_w"]), fp(weights["ln_f_b"]),
-                          ctypes.cast(self.layers, ctypes.POINTER(_Layer)))
+                          ctypes.cast(self.layers, ctypes.POINTER(_Layer)),
+                          fp(head) if head is not None else None)
 
 
 class OracleModel:

@@ -36,7 +36,8 @@ def torch_gpt2_logits(cfg, w, tokens):
         f = F.gelu(h @ d(L["fc_w"]) + d(L["fc_b"]), approximate="tanh")
         x = x + f @ d(L["mlp_proj_w"]) + d(L["mlp_proj_b"])
     x = F.layer_norm(x, (E,), d(w["ln_f_w"]), d(w["ln_f_b"]), eps=cfg.ln_eps)
-    return (x @ d(w["wte"]).T).numpy()
+    head = w.get("head", w["wte"])     # a separately stored head, else the tied wte
+    return (x @ d(head).T).numpy()
 
 
 # head_dim 32 (tiny) and head_dim 64 (the GPT-2 head, scale 1/8)
@@ -108,3 +109,32 @@ def test_greedy_teacher_forcing_consistent():
     ids2, logits2 = orc.greedy(cfg, w, p, 16, teacher=ids[:16])
     assert ids2 == ids and np.array_equal(logits, logits2)
     assert ids[0] == int(np.argmax(logits[3]))
+
+
+def test_separately_stored_head():
+    """The output head as a separate stored matrix ("gpt2.s" README, Options:
+    -h stores it in fp16): passing wte itself changes nothing, bit for bit;
+    an fp16-rounded head matches the library forward with that head, while
+    the embedding still reads the fp32 wte."""
+    cfg = synth.TINY
+    w = synth.make_weights(cfg, seed=0)
+    toks = synth.make_prompt(cfg, 12, seed=2)
+    w_same = dict(w, head=np.array(w["wte"], copy=True))
+    w16 = orc.stored_weights(w, "f32", head="f16")
+    assert not np.array_equal(w16["head"], w["wte"])
+    assert np.array_equal(w16["wte"], w["wte"])
+    ref16 = torch_gpt2_logits(cfg, w16, toks)
+    ref32 = torch_gpt2_logits(cfg, w, toks)
+    a, b, c = orc.OracleModel(cfg, w), orc.OracleModel(cfg, w_same), orc.OracleModel(cfg, w16)
+    try:
+        moved = 0.0
+        for pos, t in enumerate(toks):
+            la, _ = a.forward(int(t), pos)
+            lb, _ = b.forward(int(t), pos)
+            lc, _ = c.forward(int(t), pos)
+            assert np.array_equal(la, lb)
+            assert np.abs(lc - ref16[pos]).max() <= 2e-5
+            moved = max(moved, float(np.abs(ref16[pos] - ref32[pos]).max()))
+        assert moved > 1e-5                    # the fp16 head is a different matrix
+    finally:
+        a.close(); b.close(); c.close()
