@@ -61,6 +61,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=120)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--wdtype", choices=["f32", "f16", "int4"], default="f32")
+    p.add_argument("--head", choices=["f32", "f16"], default="f32",
+                   help="LM head storage: the tied fp32 wte (the configurations), or an fp16 copy (README -h)")
     p.add_argument("--e2e-calls", type=int, default=50)
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="CPU time budget of the oracle baseline sample")
@@ -80,8 +82,8 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
-def workload_config(wdtype: str, world: int) -> dict:
-    return {"workload": f"GPT-2 small 124M, {wdtype} block weights, batch 1, {PROMPT_LEN}-token prompt "
+def workload_config(wdtype: str, world: int, head: str = "f32") -> dict:
+    return {"workload": f"GPT-2 small 124M, {wdtype} block weights, {head} LM head, batch 1, {PROMPT_LEN}-token prompt "
                         f"+ {CYCLE} greedy decode steps (positions {PROMPT_LEN}..{PROMPT_LEN + CYCLE - 1}), "
                         "cycled",
             "n_layer": 12, "n_embd": 768, "n_head": 12, "vocab": 50257, "n_positions": 1024,
@@ -183,11 +185,11 @@ def load_traffic():
 
 # ---- CPU oracle timing -------------------------------------------------------
 
-def oracle_sample(cfg, weights, prompt, wdtype, budget_s, max_steps=None):
+def oracle_sample(cfg, weights, prompt, wdtype, budget_s, max_steps=None, head="f32"):
     """Decode passes of the oracle after an untimed prefill; stops after
     ~budget_s seconds (or max_steps).  Returns (passes, seconds)."""
     from oracle import oracle as orc
-    sw = orc.stored_weights(weights, wdtype)
+    sw = orc.stored_weights(weights, wdtype, head=head)
     m = orc.OracleModel(cfg, sw)
     try:
         tok = None
@@ -216,13 +218,13 @@ def run_reference(args):
     cfg = synth.SMALL
     w = synth.make_weights(cfg, 0)
     prompt = synth.make_prompt(cfg, PROMPT_LEN, 1)
-    oracle_sample(cfg, w, prompt, args.wdtype, 1e9, max_steps=min(args.warmup, 3))
-    n, el = oracle_sample(cfg, w, prompt, args.wdtype, 60.0, max_steps=args.steps)
+    oracle_sample(cfg, w, prompt, args.wdtype, 1e9, max_steps=min(args.warmup, 3), head=args.head)
+    n, el = oracle_sample(cfg, w, prompt, args.wdtype, 60.0, max_steps=args.steps, head=args.head)
     value = n / el
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / n,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": workload_config(args.wdtype, 1),
+            "data": "synthetic", "config": workload_config(args.wdtype, 1, args.head),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": f"{n} of the {args.steps} requested decode passes (60 s cap), "
                                        "single-threaded C oracle, after an untimed 10-token prefill"},
@@ -288,7 +290,7 @@ def main():
     w = synth.make_weights(cfg, 0)
     prompt = synth.make_prompt(cfg, PROMPT_LEN, 1)
     dw = binding.upload_weights(w)
-    model = binding.Model(cfg, dw, args.wdtype, path=args.path)
+    model = binding.Model(cfg, dw, args.wdtype, path=args.path, head=args.head)
     del dw
     torch.cuda.empty_cache()
     kps = model.kernels_per_step()
@@ -361,17 +363,17 @@ def main():
         sweep = []
         for (p0, e_a), (p1, e_b) in zip(marks, marks[1:]):
             t = e_a.elapsed_time(e_b) / 1e3 / (p1 - p0)
-            b = roofline.mean_bytes_per_token(cfg, args.wdtype, range(p0, p1))
+            b = roofline.mean_bytes_per_token(cfg, args.wdtype, range(p0, p1), args.head)
             sweep.append({"positions": f"{p0}..{p1 - 1}", "us_per_token": t * 1e6, "tok_s": 1.0 / t,
                           "gbs": b / t / 1e9, "frac": b / t / 1e9 / peaks_s["hbm_gbs"]})
     model.close()
 
     # ---- roofline of the decode pass --------------------------------------
     positions = [PROMPT_LEN + (k % CYCLE) for k in range(CYCLE)]
-    alg = roofline.mean_bytes_per_token(cfg, args.wdtype, positions)
+    alg = roofline.mean_bytes_per_token(cfg, args.wdtype, positions, args.head)
     peaks, peak_kind = measured_peaks()
     achieved = alg / (ms / 1e3 / args.steps) / 1e9
-    traffic = load_traffic().get(path, {}).get(args.wdtype)
+    traffic = load_traffic().get(path, {}).get(args.wdtype if args.head == "f32" else f"{args.wdtype}+f16 head")
     kernel = {
         "cluster": "k_decode_cluster: one cooperative launch per call (one per 60-step cycle here, "
                    "a host-fed pass + 59 device-fed passes), clusters of 4 CTAs, one CTA per SM",
@@ -387,7 +389,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32" if args.wdtype == "f32" else
             f"{args.wdtype} weights, f32 math", "data": "synthetic",
-            "config": dict(workload_config(args.wdtype, world), path=path), "e2e": e2e,
+            "config": dict(workload_config(args.wdtype, world, args.head), path=path), "e2e": e2e,
             "gpu_launches": launches,
             "roofline": roof, "clocks": clocks}
     if sweep is not None:
@@ -395,7 +397,7 @@ def main():
 
     # ---- CPU baseline: the oracle on this host (rank 0, N = 1) ---------------
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n, el = oracle_sample(cfg, w, prompt, args.wdtype, args.cpu_seconds)
+        n, el = oracle_sample(cfg, w, prompt, args.wdtype, args.cpu_seconds, head=args.head)
         line["cpu_baseline"] = {"value": n / el, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": f"{n} greedy decode passes of the same workload (positions "
                                           f"{PROMPT_LEN}..{PROMPT_LEN + CYCLE - 1}) after an untimed "

@@ -146,6 +146,14 @@ int gpt2_create(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
  * used; gpt2_path reports which one a model uses. */
 #define GPT2_FLAG_PER_KERNEL 1
 #define GPT2_FLAG_NO_CLUSTER 2
+/* GPT2_FLAG_HEAD_F16: the tied output head is also stored as fp16 (round to
+ * nearest even), as the "gpt2.s" README's -h option stores it ("Options": the
+ * 48 block matrices and the output head as fp16); the LM head reads that
+ * copy (widened to fp32, products and sums in fp32) while the embedding
+ * lookup still reads the fp32 wte.  Adds n_vocab * n_embd * 2 bytes of device
+ * memory.  Cluster path only: with a flag or device that rules it out,
+ * gpt2_create_ex returns GPT2_ERR_INVALID_ARG. */
+#define GPT2_FLAG_HEAD_F16 4
 int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
                    int32_t flags, void *stream, gpt2_model **out);
 

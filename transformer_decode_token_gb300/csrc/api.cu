@@ -78,7 +78,8 @@ struct gpt2_model {
     size_t p_smem = 0;
     // cluster path (uses the prompt buffer of the persistent path)
     bool cluster = false;
-    uint8_t *cbuf = nullptr;         // tiled matrices, sums, counters, token word, layer table
+    bool head_f16 = false;           // GPT2_FLAG_HEAD_F16: the LM head reads an fp16 copy of wte
+    uint8_t *cbuf = nullptr;         // tiled matrices, fp16 head, sums, keys, layer table
     uint8_t *c_state = nullptr;      // sums + tagged LM-head keys (zeroed together)
     size_t c_state_bytes = 0;
     ClusterArgs cargs{};
@@ -635,6 +636,7 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
     }
     const size_t head_pad = size_t(head_rpc) * grid;
     const size_t o_hc1 = take(head_pad * 4), o_hcb = take(head_pad * 4);
+    const size_t o_h16 = m->head_f16 ? take(size_t(V) * E * 2) : 0;   // the fp16 LM head [V][E]
     const size_t o_state = off;
     const size_t acc_bytes = size_t(2) * L * E * 8 * kClusterAccStride;
     const size_t o_accn = take(acc_bytes), o_accx = take(acc_bytes);
@@ -724,8 +726,20 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
         }
         if (e == cudaSuccess) e = cudaMemsetAsync(B + o_hc1, 0, head_pad * 4, s);
         if (e == cudaSuccess) e = cudaMemsetAsync(B + o_hcb, 0, head_pad * 4, s);
-        if (e == cudaSuccess) e = ln_fold(m->wte, m->lnf_w, m->lnf_b, E, V, reinterpret_cast<float *>(B + o_hc1),
-                                          reinterpret_cast<float *>(B + o_hcb), s);
+        if (m->head_f16) {
+            // the fp16 head, and its LayerNorm fold constants from the stored (rounded) values
+            float *wide = nullptr;
+            if (e == cudaSuccess) e = convert_f16(m->wte, size_t(V) * E, B + o_h16, s);
+            if (e == cudaSuccess) e = cudaMalloc(&wide, size_t(V) * E * 4);
+            if (e == cudaSuccess) e = dequant_to_f32(kWF16, B + o_h16, nullptr, nullptr, E, V, wide, s);
+            if (e == cudaSuccess) e = ln_fold(wide, m->lnf_w, m->lnf_b, E, V, reinterpret_cast<float *>(B + o_hc1),
+                                              reinterpret_cast<float *>(B + o_hcb), s);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+            if (wide) cudaFree(wide);
+        } else if (e == cudaSuccess) {
+            e = ln_fold(m->wte, m->lnf_w, m->lnf_b, E, V, reinterpret_cast<float *>(B + o_hc1),
+                        reinterpret_cast<float *>(B + o_hcb), s);
+        }
         if (e == cudaSuccess) e = cudaStreamSynchronize(s);
         if (tmp) cudaFree(tmp);
         if (d1) cudaFree(d1);
@@ -758,6 +772,8 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
     a.fr = fr;
     a.head_rpc = head_rpc;
     a.pr_rows = pr_rows;
+    a.head_w = m->head_f16 ? static_cast<const void *>(B + o_h16) : static_cast<const void *>(m->wte);
+    a.head_wt = m->head_f16 ? kWF16 : kWF32;
     a.h_c1 = reinterpret_cast<const float *>(B + o_hc1);
     a.h_cb = reinterpret_cast<const float *>(B + o_hcb);
     a.acc_new = reinterpret_cast<long long *>(B + o_accn);
@@ -818,7 +834,7 @@ int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype
     int rc = check_config(cfg, wdtype);
     if (rc != GPT2_OK) return rc;
     if (!w || !w->layers) return GPT2_ERR_INVALID_ARG;
-    if (flags & ~int32_t(GPT2_FLAG_PER_KERNEL | GPT2_FLAG_NO_CLUSTER)) return GPT2_ERR_INVALID_ARG;
+    if (flags & ~int32_t(GPT2_FLAG_PER_KERNEL | GPT2_FLAG_NO_CLUSTER | GPT2_FLAG_HEAD_F16)) return GPT2_ERR_INVALID_ARG;
     int dev;
     TRY_CUDA(cudaGetDevice(&dev));
     cudaDeviceProp prop;
@@ -841,6 +857,7 @@ int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype
     if (!m) return GPT2_ERR_OUT_OF_MEMORY;
     m->cfg = *cfg;
     m->wdtype = wdtype;
+    m->head_f16 = (flags & GPT2_FLAG_HEAD_F16) != 0;
     m->stream = static_cast<cudaStream_t>(stream);
     m->device = dev;
     m->num_sms = prop.multiProcessorCount;
@@ -1030,6 +1047,10 @@ int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype
             m->persistent = false;
             m->ll_base = nullptr;
         }
+    }
+    if (m->head_f16 && !m->cluster) {   // the fp16 head is read only by the cluster kernel
+        free_model(m);
+        return GPT2_ERR_INVALID_ARG;
     }
     // state: the epoch sequence starts at 1 (tagged words are zero)
     DeviceState init{};

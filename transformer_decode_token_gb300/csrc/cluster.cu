@@ -373,7 +373,7 @@ __device__ __forceinline__ Geos make_geos(const ClusterArgs &a, const Role &ro)
         G.b = tile_geo(a.wtype, a.E, a.fr, a.stage_bytes);
     }
     const int r0 = min(a.V, ro.g * a.head_rpc), r1 = min(a.V, r0 + a.head_rpc);
-    G.head = long_geo(kWF32, a.E, r1 - r0, a.stage_bytes);
+    G.head = long_geo(a.head_wt, a.E, r1 - r0, a.stage_bytes);
     G.head_row0 = r0;
     return G;
 }
@@ -390,7 +390,7 @@ __device__ __forceinline__ Seg seg_b(const Role &ro, const Geos &G, const CLayer
 }
 __device__ __forceinline__ Seg seg_head(const ClusterArgs &a, const Geos &G)
 {
-    return long_seg(G.head, a.wte, nullptr, nullptr, G.head_row0);
+    return long_seg(G.head, a.head_w, nullptr, nullptr, G.head_row0);
 }
 
 // ---- producer --------------------------------------------------------------------
@@ -1460,8 +1460,15 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
         CTRACE(s, 201);
         if (!wait_tx_bar(a, c.prm_bar, c.uses_prm, 9000 + int(blockIdx.x))) ok = false;
         TSET(s, 204);
-        canon_rows<kWF32, true>(a, c, G.head, k, kStreamWindow, E, c.x, c.pr, p1, pc, nullptr, G.head_row0, best,
-                                ok, false, a.temperature > 0.f ? (long long)pos * (long long)a.V : -1ll);
+        {
+            const long long sk = a.temperature > 0.f ? (long long)pos * (long long)a.V : -1ll;
+            if (a.head_wt == kWF16)
+                canon_rows<kWF16, true>(a, c, G.head, k, kStreamWindow, E, c.x, c.pr, p1, pc, nullptr, G.head_row0,
+                                        best, ok, false, sk);
+            else
+                canon_rows<kWF32, true>(a, c, G.head, k, kStreamWindow, E, c.x, c.pr, p1, pc, nullptr, G.head_row0,
+                                        best, ok, false, sk);
+        }
         CTRACE(s, 202);
         publish_key(a, sh, seq, best);
         if (s == a.n_steps - 1 && blockIdx.x == 0) {   // the last pass's token: CTA 0 records it

@@ -84,6 +84,8 @@ enum : int32_t { kSetTokPos = 1, kResetOut = 2, kSeedOutWithNext = 4, kClearErr 
 // src is HF [in][out] fp32; writes dst [out][in] in the chosen format.
 cudaError_t repack_f32(const float *src, int in, int out, float *dst, cudaStream_t s);
 cudaError_t repack_f16(const float *src, int in, int out, void *dst, cudaStream_t s);
+// Elementwise fp32 -> fp16 (round to nearest even) of n values, layout unchanged.
+cudaError_t convert_f16(const float *src, size_t n, void *dst, cudaStream_t s);
 // tmp must hold out*in floats.
 cudaError_t repack_int4(const float *src, int in, int out, float *tmp, uint8_t *codes, float *scales,
                         uint8_t *zeros, cudaStream_t s);

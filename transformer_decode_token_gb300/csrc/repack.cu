@@ -13,6 +13,8 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <algorithm>
+
 namespace gpt2 {
 
 template <typename T>
@@ -57,6 +59,21 @@ cudaError_t repack_f32(const float *src, int in, int out, float *dst, cudaStream
 cudaError_t repack_f16(const float *src, int in, int out, void *dst, cudaStream_t s)
 {
     return transpose<__half>(src, in, out, static_cast<__half *>(dst), s);
+}
+
+// Elementwise fp32 -> fp16 (round to nearest even), layout unchanged.
+__global__ void __launch_bounds__(256) k_to_f16(const float *src, size_t n, __half *dst)
+{
+    for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n; i += size_t(gridDim.x) * blockDim.x)
+        dst[i] = __float2half_rn(src[i]);
+}
+
+cudaError_t convert_f16(const float *src, size_t n, void *dst, cudaStream_t s)
+{
+    const size_t blocks = std::min<size_t>((n + 255) / 256, 8192);
+    if (blocks == 0) return cudaSuccess;
+    k_to_f16<<<unsigned(blocks), 256, 0, s>>>(src, n, static_cast<__half *>(dst));
+    return cudaGetLastError();
 }
 
 // One warp per pair of groups (64 inputs of one output row), lane = input.

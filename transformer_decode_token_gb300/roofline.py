@@ -27,12 +27,13 @@ def block_matrix_bytes(cfg, wdtype: str) -> int:
     raise ValueError(wdtype)
 
 
-def bytes_per_token(cfg, wdtype: str, pos: int) -> dict:
-    """Bytes one decode pass at position `pos` must move."""
+def bytes_per_token(cfg, wdtype: str, pos: int, head: str = "f32") -> dict:
+    """Bytes one decode pass at position `pos` must move (head: the LM head's
+    storage, the fp32 tied wte or its fp16 copy)."""
     E, V, L = cfg.n_embd, cfg.vocab_size, cfg.n_layer
     parts = {
         "block_matrices": block_matrix_bytes(cfg, wdtype),
-        "head": V * E * 4,                               # tied wte, fp32 in every mode
+        "head": V * E * (2 if head == "f16" else 4),
         "biases_ln": L * 13 * E * 4 + 2 * E * 4,         # 9E bias + 4E LN per layer, ln_f
         "embedding_rows": 2 * E * 4,                     # wte[token], wpe[pos]
         "logits": V * 4,
@@ -42,9 +43,9 @@ def bytes_per_token(cfg, wdtype: str, pos: int) -> dict:
     return parts
 
 
-def mean_bytes_per_token(cfg, wdtype: str, positions) -> float:
+def mean_bytes_per_token(cfg, wdtype: str, positions, head: str = "f32") -> float:
     positions = list(positions)
-    return sum(bytes_per_token(cfg, wdtype, p)["total"] for p in positions) / len(positions)
+    return sum(bytes_per_token(cfg, wdtype, p, head)["total"] for p in positions) / len(positions)
 
 
 def macs_per_token(cfg) -> int:
