@@ -295,11 +295,17 @@ def stored_weights(weights: dict, wdtype: str, head: str = "f32") -> dict:
     in the checkpoint layout: the 48 block matrices are rounded to fp16 or
     quantised to grouped int4; embeddings, biases, LayerNorm and the tied head
     stay fp32.  'f32' returns the weights unchanged.  head='f16' adds the
-    output head stored as fp16 ("gpt2.s" README, Options: -h), a separate
-    matrix: the embedding lookup still reads the fp32 wte."""
+    output head stored as fp16 ("gpt2.s" README, Options: -h), head='int4'
+    as grouped int4 (the same scheme as the block matrices, groups of 32
+    along n_embd), a separate matrix: the embedding lookup still reads the
+    fp32 wte."""
     if head == "f16":
         out = dict(stored_weights(weights, wdtype))
         out["head"] = f16_bits_to_f32(f32_to_f16_bits(_f32(weights["wte"])))
+        return out
+    if head == "int4":   # wte is already [out][in]; quant_int4 takes the HF [in][out] layout
+        out = dict(stored_weights(weights, wdtype))
+        out["head"] = np.ascontiguousarray(dequant_int4(*quant_int4(np.ascontiguousarray(_f32(weights["wte"]).T))))
         return out
     if head != "f32":
         raise ValueError(f"unknown head dtype {head!r}")

@@ -111,16 +111,17 @@ def test_greedy_teacher_forcing_consistent():
     assert ids[0] == int(np.argmax(logits[3]))
 
 
-def test_separately_stored_head():
+@pytest.mark.parametrize("head", ["f16", "int4"])
+def test_separately_stored_head(head):
     """The output head as a separate stored matrix ("gpt2.s" README, Options:
-    -h stores it in fp16): passing wte itself changes nothing, bit for bit;
-    an fp16-rounded head matches the library forward with that head, while
-    the embedding still reads the fp32 wte."""
+    -h stores it in fp16; or grouped int4): passing wte itself changes
+    nothing, bit for bit; a rounded head matches the library forward with
+    that head, while the embedding still reads the fp32 wte."""
     cfg = synth.TINY
     w = synth.make_weights(cfg, seed=0)
     toks = synth.make_prompt(cfg, 12, seed=2)
     w_same = dict(w, head=np.array(w["wte"], copy=True))
-    w16 = orc.stored_weights(w, "f32", head="f16")
+    w16 = orc.stored_weights(w, "f32", head=head)
     assert not np.array_equal(w16["head"], w["wte"])
     assert np.array_equal(w16["wte"], w["wte"])
     ref16 = torch_gpt2_logits(cfg, w16, toks)
@@ -135,6 +136,6 @@ def test_separately_stored_head():
             assert np.array_equal(la, lb)
             assert np.abs(lc - ref16[pos]).max() <= 2e-5
             moved = max(moved, float(np.abs(ref16[pos] - ref32[pos]).max()))
-        assert moved > 1e-5                    # the fp16 head is a different matrix
+        assert moved > 1e-5                    # the stored head is a different matrix
     finally:
         a.close(); b.close(); c.close()
