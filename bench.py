@@ -61,8 +61,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=120)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--wdtype", choices=["f32", "f16", "int4"], default="f32")
-    p.add_argument("--head", choices=["f32", "f16"], default="f32",
-                   help="LM head storage: the tied fp32 wte (the configurations), or an fp16 copy (README -h)")
+    p.add_argument("--head", choices=["f32", "f16", "int4"], default="f32",
+                   help="LM head storage: the tied fp32 wte (the configurations), an fp16 copy (README -h) or int4")
     p.add_argument("--e2e-calls", type=int, default=50)
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="CPU time budget of the oracle baseline sample")

@@ -154,6 +154,12 @@ int gpt2_create(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
  * memory.  Cluster path only: with a flag or device that rules it out,
  * gpt2_create_ex returns GPT2_ERR_INVALID_ARG. */
 #define GPT2_FLAG_HEAD_F16 4
+/* GPT2_FLAG_HEAD_INT4: the output head stored as grouped asymmetric int4 of
+ * wte's rows (the GPT2_INT4 scheme and layout, groups of 32 along n_embd),
+ * the "next" variant for the int4 mode, where the fp32 head is three quarters
+ * of the bytes; the embedding still reads the fp32 wte.  Cluster path only,
+ * n_embd % 64 == 0; not together with GPT2_FLAG_HEAD_F16. */
+#define GPT2_FLAG_HEAD_INT4 8
 int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
                    int32_t flags, void *stream, gpt2_model **out);
 

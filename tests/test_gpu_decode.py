@@ -361,19 +361,22 @@ def test_sampling_controls():
 
 # ---- the fp16 output head (the README's -h mode) ----------------------------------
 
-@pytest.mark.parametrize("cfg_name,wdtype,n_prompt,n_steps", [("tiny", "f16", 4, 16), ("tiny", "f32", 4, 16),
-                                                              ("small", "f16", 10, 60), ("small", "int4", 10, 30)])
-def test_fp16_head_matches_oracle(cfg_name, wdtype, n_prompt, n_steps):
-    """GPT2_FLAG_HEAD_F16: the LM head reads an fp16 copy of wte (the embedding
-    still reads the fp32 wte); against the oracle run on the same stored
-    weights (block matrices as stored, head rounded to fp16), teacher-forced:
-    logits within 2e-3, ids wherever the oracle's top-2 margin exceeds 1e-3."""
+@pytest.mark.parametrize("cfg_name,wdtype,head,n_prompt,n_steps",
+                         [("tiny", "f16", "f16", 4, 16), ("tiny", "f32", "f16", 4, 16),
+                          ("small", "f16", "f16", 10, 60), ("small", "int4", "f16", 10, 30),
+                          ("tiny", "int4", "int4", 4, 16), ("small", "int4", "int4", 10, 30)])
+def test_stored_head_matches_oracle(cfg_name, wdtype, head, n_prompt, n_steps):
+    """GPT2_FLAG_HEAD_F16 / _INT4: the LM head reads an fp16 or int4 copy of
+    wte (the embedding still reads the fp32 wte); against the oracle run on
+    the same stored weights (block matrices and head as stored),
+    teacher-forced: logits within 2e-3, ids wherever the oracle's top-2 margin
+    exceeds 1e-3."""
     cfg = synth.TINY if cfg_name == "tiny" else synth.SMALL
     w, dw = weights(cfg)
     prompt = synth.make_prompt(cfg, n_prompt, 1)
-    ref_ids, ref_rows = orc.greedy(cfg, orc.stored_weights(w, wdtype, head="f16"), prompt, n_steps)
+    ref_ids, ref_rows = orc.greedy(cfg, orc.stored_weights(w, wdtype, head=head), prompt, n_steps)
     tokens = list(prompt) + ref_ids[:n_steps]
-    m = binding.Model(cfg, dw, wdtype, head="f16")
+    m = binding.Model(cfg, dw, wdtype, head=head)
     try:
         assert m.path() == "cluster"
         rows, ids = teacher_forced(m, tokens)
@@ -382,8 +385,9 @@ def test_fp16_head_matches_oracle(cfg_name, wdtype, n_prompt, n_steps):
     check_rows(rows, ref_rows, ids, 2e-3)
 
 
-def test_fp16_head_needs_the_cluster_kernel():
+def test_stored_head_needs_the_cluster_kernel():
     cfg = synth.TINY
     _, dw = weights(cfg)
-    with pytest.raises(binding.GPT2Error):
-        binding.Model(cfg, dw, "f32", path="per_kernel", head="f16")
+    for head in ("f16", "int4"):
+        with pytest.raises(binding.GPT2Error):
+            binding.Model(cfg, dw, "f32", path="per_kernel", head=head)

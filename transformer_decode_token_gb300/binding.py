@@ -163,8 +163,8 @@ class Model:
                  head: str = "f32"):
         """path: "auto" (cluster kernel where possible, else the persistent
         kernel, else the per-kernel graph), "persistent" (skip the cluster
-        kernel) or "per_kernel".  head: "f32" (the tied wte) or "f16" (an fp16
-        copy for the LM head, GPT2_FLAG_HEAD_F16; cluster kernel only)."""
+        kernel) or "per_kernel".  head: "f32" (the tied wte), "f16" or "int4" (a
+        copy for the LM head, GPT2_FLAG_HEAD_F16 / _INT4; cluster kernel only)."""
         L = lib()
         self.cfg = cfg
         self.wdtype = wdtype
@@ -178,7 +178,7 @@ class Model:
                     dev_weights["ln_f_w"].data_ptr(), dev_weights["ln_f_b"].data_ptr(),
                     ctypes.cast(layers, ctypes.POINTER(LayerWeights)))
         h = ctypes.c_void_p()
-        flags = {"auto": 0, "persistent": 2, "per_kernel": 1}[path] | {"f32": 0, "f16": 4}[head]
+        flags = {"auto": 0, "persistent": 2, "per_kernel": 1}[path] | {"f32": 0, "f16": 4, "int4": 8}[head]
         check(L.gpt2_create_ex(ctypes.byref(c), ctypes.byref(w), WDTYPES[wdtype], flags,
                                _stream_handle(stream), ctypes.byref(h)), "gpt2_create_ex")
         self._h = h

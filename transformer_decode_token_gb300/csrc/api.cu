@@ -79,6 +79,7 @@ struct gpt2_model {
     // cluster path (uses the prompt buffer of the persistent path)
     bool cluster = false;
     bool head_f16 = false;           // GPT2_FLAG_HEAD_F16: the LM head reads an fp16 copy of wte
+    bool head_int4 = false;          // GPT2_FLAG_HEAD_INT4: ... or a grouped int4 copy
     uint8_t *cbuf = nullptr;         // tiled matrices, fp16 head, sums, keys, layer table
     uint8_t *c_state = nullptr;      // sums + tagged LM-head keys (zeroed together)
     size_t c_state_bytes = 0;
@@ -576,7 +577,9 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
     const int n_clusters = H + nfc / kClusterSize, grid = n_clusters * kClusterSize;
     if (grid > 256) return GPT2_ERR_INVALID_ARG;   // each consumer thread polls one CTA's LM-head key
     if (V > (1 << 17)) return GPT2_ERR_INVALID_ARG;   // tagged keys keep 17 bits of the id
-    const int head_rpc = ((V + grid - 1) / grid + 3) / 4 * 4;
+    // LM-head rows per CTA: a multiple of 4 (of 8 for an int4 head, whose shares are padded)
+    const int head_rpc = m->head_int4 ? ((V + grid - 1) / grid + 7) / 8 * 8 : ((V + grid - 1) / grid + 3) / 4 * 4;
+    if (m->head_int4 && E % 64) return GPT2_ERR_INVALID_ARG;
     const int pr_rows = (std::max(std::max(3 * (D / 4), fr), head_rpc) + 3) / 4 * 4;
     const size_t fixed = cluster_fixed_smem(E, D, fr, L, pr_rows);
     const uint32_t ring_offset = uint32_t((fixed + 127) / 128 * 128);
@@ -637,6 +640,10 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
     const size_t head_pad = size_t(head_rpc) * grid;
     const size_t o_hc1 = take(head_pad * 4), o_hcb = take(head_pad * 4);
     const size_t o_h16 = m->head_f16 ? take(size_t(V) * E * 2) : 0;   // the fp16 LM head [V][E]
+    // the int4 LM head, padded to head_pad rows: codes [.][E/2], scales [.][E/32] f32, zero points [.][E/64]
+    const size_t o_h4c = m->head_int4 ? take(head_pad * E / 2) : 0;
+    const size_t o_h4s = m->head_int4 ? take(head_pad * (E / 32) * 4) : 0;
+    const size_t o_h4z = m->head_int4 ? take(head_pad * (E / 64)) : 0;
     const size_t o_state = off;
     const size_t acc_bytes = size_t(2) * L * E * 8 * kClusterAccStride;
     const size_t o_accn = take(acc_bytes), o_accx = take(acc_bytes);
@@ -736,6 +743,21 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
                                               reinterpret_cast<float *>(B + o_hcb), s);
             if (e == cudaSuccess) e = cudaStreamSynchronize(s);
             if (wide) cudaFree(wide);
+        } else if (m->head_int4) {
+            // quantise wte's rows (already [out][in]); padding rows stay zero (scale 0: value 0)
+            float *wide = nullptr;
+            uint8_t *hc = B + o_h4c, *hz = B + o_h4z;
+            float *hs = reinterpret_cast<float *>(B + o_h4s);
+            if (e == cudaSuccess) e = cudaMemsetAsync(hc, 0, head_pad * E / 2, s);
+            if (e == cudaSuccess) e = cudaMemsetAsync(hs, 0, head_pad * (E / 32) * 4, s);
+            if (e == cudaSuccess) e = cudaMemsetAsync(hz, 0, head_pad * (E / 64), s);
+            if (e == cudaSuccess) e = quant_int4_rows(m->wte, E, V, hc, hs, hz, s);
+            if (e == cudaSuccess) e = cudaMalloc(&wide, size_t(V) * E * 4);
+            if (e == cudaSuccess) e = dequant_to_f32(kWI4, hc, hs, hz, E, V, wide, s);
+            if (e == cudaSuccess) e = ln_fold(wide, m->lnf_w, m->lnf_b, E, V, reinterpret_cast<float *>(B + o_hc1),
+                                              reinterpret_cast<float *>(B + o_hcb), s);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+            if (wide) cudaFree(wide);
         } else if (e == cudaSuccess) {
             e = ln_fold(m->wte, m->lnf_w, m->lnf_b, E, V, reinterpret_cast<float *>(B + o_hc1),
                         reinterpret_cast<float *>(B + o_hcb), s);
@@ -772,8 +794,11 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
     a.fr = fr;
     a.head_rpc = head_rpc;
     a.pr_rows = pr_rows;
-    a.head_w = m->head_f16 ? static_cast<const void *>(B + o_h16) : static_cast<const void *>(m->wte);
-    a.head_wt = m->head_f16 ? kWF16 : kWF32;
+    a.head_w = m->head_f16 ? static_cast<const void *>(B + o_h16)
+               : m->head_int4 ? static_cast<const void *>(B + o_h4c) : static_cast<const void *>(m->wte);
+    a.head_s = m->head_int4 ? reinterpret_cast<const float *>(B + o_h4s) : nullptr;
+    a.head_z = m->head_int4 ? B + o_h4z : nullptr;
+    a.head_wt = m->head_f16 ? kWF16 : m->head_int4 ? kWI4 : kWF32;
     a.h_c1 = reinterpret_cast<const float *>(B + o_hc1);
     a.h_cb = reinterpret_cast<const float *>(B + o_hcb);
     a.acc_new = reinterpret_cast<long long *>(B + o_accn);
@@ -834,7 +859,9 @@ int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype
     int rc = check_config(cfg, wdtype);
     if (rc != GPT2_OK) return rc;
     if (!w || !w->layers) return GPT2_ERR_INVALID_ARG;
-    if (flags & ~int32_t(GPT2_FLAG_PER_KERNEL | GPT2_FLAG_NO_CLUSTER | GPT2_FLAG_HEAD_F16)) return GPT2_ERR_INVALID_ARG;
+    if (flags & ~int32_t(GPT2_FLAG_PER_KERNEL | GPT2_FLAG_NO_CLUSTER | GPT2_FLAG_HEAD_F16 | GPT2_FLAG_HEAD_INT4))
+        return GPT2_ERR_INVALID_ARG;
+    if ((flags & GPT2_FLAG_HEAD_F16) && (flags & GPT2_FLAG_HEAD_INT4)) return GPT2_ERR_INVALID_ARG;
     int dev;
     TRY_CUDA(cudaGetDevice(&dev));
     cudaDeviceProp prop;
@@ -858,6 +885,7 @@ int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype
     m->cfg = *cfg;
     m->wdtype = wdtype;
     m->head_f16 = (flags & GPT2_FLAG_HEAD_F16) != 0;
+    m->head_int4 = (flags & GPT2_FLAG_HEAD_INT4) != 0;
     m->stream = static_cast<cudaStream_t>(stream);
     m->device = dev;
     m->num_sms = prop.multiProcessorCount;
@@ -1048,7 +1076,7 @@ int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype
             m->ll_base = nullptr;
         }
     }
-    if (m->head_f16 && !m->cluster) {   // the fp16 head is read only by the cluster kernel
+    if ((m->head_f16 || m->head_int4) && !m->cluster) {   // a separate head is read only by the cluster kernel
         free_model(m);
         return GPT2_ERR_INVALID_ARG;
     }

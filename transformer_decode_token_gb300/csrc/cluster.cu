@@ -372,7 +372,11 @@ __device__ __forceinline__ Geos make_geos(const ClusterArgs &a, const Role &ro)
         G.a = long_geo(a.wtype, a.E, a.fr, a.stage_bytes);
         G.b = tile_geo(a.wtype, a.E, a.fr, a.stage_bytes);
     }
-    const int r0 = min(a.V, ro.g * a.head_rpc), r1 = min(a.V, r0 + a.head_rpc);
+    // an int4 head streams whole padded shares (whole chunks of 8 rows: its
+    // 12-byte zero-point rows need multiples of 4 rows per copy); rows >= V
+    // are read but never stored
+    const int r0 = a.head_wt == kWI4 ? ro.g * a.head_rpc : min(a.V, ro.g * a.head_rpc);
+    const int r1 = a.head_wt == kWI4 ? r0 + a.head_rpc : min(a.V, r0 + a.head_rpc);
     G.head = long_geo(a.head_wt, a.E, r1 - r0, a.stage_bytes);
     G.head_row0 = r0;
     return G;
@@ -390,7 +394,7 @@ __device__ __forceinline__ Seg seg_b(const Role &ro, const Geos &G, const CLayer
 }
 __device__ __forceinline__ Seg seg_head(const ClusterArgs &a, const Geos &G)
 {
-    return long_seg(G.head, a.head_w, nullptr, nullptr, G.head_row0);
+    return long_seg(G.head, a.head_w, a.head_s, a.head_z, G.head_row0);
 }
 
 // ---- producer --------------------------------------------------------------------
@@ -748,12 +752,14 @@ __device__ __forceinline__ void canon_groups(const ClusterArgs &a, const CS &c, 
             const int i = g0 + jr;
             if (LN) t = rstd * fmaf(-mean, c1[i], t) + cb[i];
             if (logit_row0 >= 0) {
-                a.logits[logit_row0 + i] = t;
-                const float score = sample_k0 >= 0 ? sample_score(t, a.temperature, a.seed,
-                                                                  (unsigned long long)(sample_k0 + logit_row0 + i))
-                                                   : t;
-                const unsigned long long key = argmax_key(score, uint32_t(logit_row0 + i));
-                best = key > best ? key : best;
+                if (logit_row0 + i < a.V) {   // (rows >= V: padding of an int4 head)
+                    a.logits[logit_row0 + i] = t;
+                    const float score = sample_k0 >= 0 ? sample_score(t, a.temperature, a.seed,
+                                                                      (unsigned long long)(sample_k0 + logit_row0 + i))
+                                                       : t;
+                    const unsigned long long key = argmax_key(score, uint32_t(logit_row0 + i));
+                    best = key > best ? key : best;
+                }
             } else {
                 out[i] = t;
             }
@@ -1465,6 +1471,9 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
             if (a.head_wt == kWF16)
                 canon_rows<kWF16, true>(a, c, G.head, k, kStreamWindow, E, c.x, c.pr, p1, pc, nullptr, G.head_row0,
                                         best, ok, false, sk);
+            else if (a.head_wt == kWI4)
+                canon_rows<kWI4, true>(a, c, G.head, k, kStreamWindow, E, c.x, c.pr, p1, pc, nullptr, G.head_row0,
+                                       best, ok, false, sk);
             else
                 canon_rows<kWF32, true>(a, c, G.head, k, kStreamWindow, E, c.x, c.pr, p1, pc, nullptr, G.head_row0,
                                         best, ok, false, sk);

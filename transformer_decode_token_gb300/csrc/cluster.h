@@ -62,8 +62,10 @@ struct ClusterArgs {
     float eps, scale;
     int32_t nfc, fr;             // fc CTAs, fc rows (= mlp-proj columns) per fc CTA
     int32_t head_rpc;            // LM-head rows per CTA (a multiple of 4)
-    const void *head_w;          // the LM head's rows [V][E]: the fp32 wte, or its fp16 copy
-    int32_t head_wt;             // their type (kWF32 or kWF16)
+    const void *head_w;          // the LM head's rows [V][E]: the fp32 wte, or its fp16 / int4 copy
+    const float *head_s;         // int4 head: scales [Vp][E/32] (Vp = head_rpc * grid, padding rows zero)
+    const uint8_t *head_z;       // int4 head: zero points [Vp][E/64]
+    int32_t head_wt;             // their type (kWF32, kWF16 or kWI4)
     float temperature;           // token choice: 0 = greedy, > 0 = a draw from softmax(logits / T)
     unsigned long long seed;     // sampling: seed of the counter-based generator
     int32_t pr_rows;             // row slots of the parameter area (a multiple of 4)

@@ -87,6 +87,9 @@ cudaError_t repack_f16(const float *src, int in, int out, void *dst, cudaStream_
 // Elementwise fp32 -> fp16 (round to nearest even) of n values, layout unchanged.
 cudaError_t convert_f16(const float *src, size_t n, void *dst, cudaStream_t s);
 // tmp must hold out*in floats.
+// Grouped int4 of a matrix already in [out][in] layout (the second step of repack_int4).
+cudaError_t quant_int4_rows(const float *Wt, int in, int out, uint8_t *codes, float *scales, uint8_t *zeros,
+                            cudaStream_t s);
 cudaError_t repack_int4(const float *src, int in, int out, float *tmp, uint8_t *codes, float *scales,
                         uint8_t *zeros, cudaStream_t s);
 // Widen a stored matrix to fp32 [out][in].

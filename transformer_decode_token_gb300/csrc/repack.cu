@@ -110,6 +110,16 @@ __global__ void __launch_bounds__(256) k_quant_int4(const float *Wt, int in, int
     if (lane == 0) zeros[size_t(o) * (in / 64) + pj] = uint8_t(zbyte);
 }
 
+cudaError_t quant_int4_rows(const float *Wt, int in, int out, uint8_t *codes, float *scales, uint8_t *zeros,
+                            cudaStream_t s)
+{
+    if (in % 64) return cudaErrorInvalidValue;
+    const long long warps = (long long)out * (in / 64);
+    const long long blocks = (warps + 7) / 8;
+    k_quant_int4<<<unsigned(blocks), 256, 0, s>>>(Wt, in, out, codes, scales, zeros);
+    return cudaGetLastError();
+}
+
 cudaError_t repack_int4(const float *src, int in, int out, float *tmp, uint8_t *codes, float *scales,
                         uint8_t *zeros, cudaStream_t s)
 {

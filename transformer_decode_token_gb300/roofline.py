@@ -33,7 +33,7 @@ def bytes_per_token(cfg, wdtype: str, pos: int, head: str = "f32") -> dict:
     E, V, L = cfg.n_embd, cfg.vocab_size, cfg.n_layer
     parts = {
         "block_matrices": block_matrix_bytes(cfg, wdtype),
-        "head": V * E * (2 if head == "f16" else 4),
+        "head": (V * E // 2 + (V * E // 32) * 4 + V * E // 64) if head == "int4" else V * E * (2 if head == "f16" else 4),
         "biases_ln": L * 13 * E * 4 + 2 * E * 4,         # 9E bias + 4E LN per layer, ln_f
         "embedding_rows": 2 * E * 4,                     # wte[token], wpe[pos]
         "logits": V * 4,
