@@ -235,6 +235,24 @@ def run_reference(args):
 
 # ---- our arm -------------------------------------------------------------------
 
+def reduce_max(v: float, world: int, device: str) -> float:
+    """The largest of the ranks' values (the slowest rank's time); the
+    process group must be initialised when world > 1."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(steps_per_rank: int, world: int, ms_slowest: float) -> float:
+    """Whole-job passes per second: every rank's passes over the slowest
+    rank's time (replicas: each rank runs its own sequence)."""
+    return steps_per_rank * world / (ms_slowest / 1e3)
+
+
 class StepRunner:
     """Queues decode passes that cycle through the 60-step generation."""
 
@@ -280,11 +298,7 @@ def main():
             dist.barrier()
 
     def max_over_ranks(v: float) -> float:
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(v, world, "cuda")
 
     cfg = synth.SMALL
     w = synth.make_weights(cfg, 0)
@@ -321,7 +335,7 @@ def main():
     clocks = sampler.stop(t_begin, t_end)
     model.sync()
     ms = max_over_ranks(e0.elapsed_time(e1))
-    value = args.steps * world / (ms / 1e3)
+    value = job_throughput(args.steps, world, ms)
 
     # ---- end to end through gpt2_generate: host prompt in, host ids out ----
     passes_per_call = PROMPT_LEN + CYCLE
