@@ -808,8 +808,8 @@ __device__ __forceinline__ void canon_rows(const ClusterArgs &a, CS &c, const Ge
                                           bool prewaited = false, long long sample_k0 = -1)
 {
     constexpr int kF4 = UnitOf<WT>::kF4;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int C = g.chunk, nch = g.nch;
+    const int lane = threadIdx.x & 31;
+    const int nch = g.nch;
     const int units = in / UnitOf<WT>::kIn;
     const uint32_t xa = smem_addr(xin), ga = smem_addr(gamma);
     float4 xr[UnitOf<WT>::kPL * kF4];
