@@ -67,3 +67,21 @@ def test_invalid_arguments_are_rejected_on_the_host():
     L.gpt2_destroy(None)
     assert L.gpt2_op_layernorm(None, None, None, 1, 4, 1e-5, None, None) == -1
     assert L.gpt2_op_head_argmax_workspace(50257, 768) >= 16 + 8 * 152
+
+
+def test_new_options_are_rejected_on_the_host():
+    """gpt2_set_sampling and the head flags validate their arguments before
+    any device work: a NULL model, a negative or non-finite temperature,
+    unknown or conflicting create flags."""
+    L = binding.lib()
+    out = ctypes.c_void_p()
+    assert L.gpt2_set_sampling(None, 0.8, 1) == -1
+    assert L.gpt2_set_sampling(None, 0.0, 1) == -1
+    good = binding.Config(2, 128, 4, 64, 512, 1e-5)
+    w = binding.Weights()
+    # unknown flag bit; both head flags at once
+    assert L.gpt2_create_ex(ctypes.byref(good), ctypes.byref(w), 0, 64, None, ctypes.byref(out)) == -1
+    assert L.gpt2_create_ex(ctypes.byref(good), ctypes.byref(w), 0, 4 | 8, None, ctypes.byref(out)) == -1
+    assert L.gpt2_path(None, None) == -1
+    assert L.gpt2_launch_count(None, None) == -1
+
