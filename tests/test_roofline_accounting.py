@@ -47,3 +47,21 @@ def test_bytes_per_token_components():
     assert roofline.bytes_per_token(cfg, "f32", 1023)["kv"] == 12 * 1025 * 2 * 768 * 4
     with pytest.raises(ValueError):
         roofline.block_matrix_bytes(cfg, "int8")
+
+
+def test_stored_head_bytes():
+    """The LM head's bytes with a separately stored head: fp16 is half of the
+    fp32 tied head; int4 is codes (half a byte per weight) + one fp32 scale per
+    32 weights + one 4-bit zero point per 32 weights, as for the block
+    matrices; the rest of the pass does not change."""
+    cfg = synth.SMALL
+    n = cfg.vocab_size * cfg.n_embd
+    f32 = roofline.bytes_per_token(cfg, "int4", 10)
+    f16 = roofline.bytes_per_token(cfg, "int4", 10, head="f16")
+    i4 = roofline.bytes_per_token(cfg, "int4", 10, head="int4")
+    assert f16["head"] * 2 == f32["head"] == 4 * n
+    assert i4["head"] == n // 2 + (n // 32) * 4 + n // 64
+    for k in ("block_matrices", "biases_ln", "embedding_rows", "logits", "kv"):
+        assert f32[k] == f16[k] == i4[k]
+    assert roofline.mean_bytes_per_token(cfg, "f32", [10, 11], head="f16") == pytest.approx(
+        (roofline.bytes_per_token(cfg, "f32", 10, "f16")["total"] + roofline.bytes_per_token(cfg, "f32", 11, "f16")["total"]) / 2)
