@@ -125,8 +125,9 @@ int gpt2_create(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
                 void *stream, gpt2_model **out);
 
 /* gpt2_create with options.  flags = 0 is gpt2_create.  Three paths compute
- * the same pass (the decode forward pass of "The Illustrated GPT-2", "Model
- * Output" and "Self-Attention" sections; greedy choice as in "model.fir"):
+ * the same pass (the node list of the "model.fir" graph file and the model.s
+ * description of the "gpt2.s" README, "Inner Workings"; greedy choice as in
+ * "Let's make GPT-2 in assembly", Step 7):
  *  - cluster (default): one cooperative launch per call of a kernel whose
  *    CTAs form clusters of 4.  One cluster per attention head computes that
  *    head's q, k, v, attention and its share of the output projection,
@@ -140,10 +141,11 @@ int gpt2_create(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
  *    (five GPU-wide exchanges per block).
  *  - per-kernel (GPT2_FLAG_PER_KERNEL, or GPT2_PATH=graph): the captured CUDA
  *    graph of 5 * n_layer + 1 kernels per pass.
- * A path that cannot run on the device or configuration (too few
- * co-resident clusters, n_embd not a multiple of 64 for the cluster kernel,
- * n_embd > 4096 for the persistent kernel) is left out and the next one is
- * used; gpt2_path reports which one a model uses. */
+ * A path that cannot run on the device or configuration is left out and the
+ * next one is used (the cluster kernel needs n_embd a multiple of 64 and at
+ * most 1024, vocab_size <= 131072 and 36 co-resident clusters of 4 CTAs; the
+ * persistent kernel n_embd <= 4096); gpt2_path reports which one a model
+ * uses. */
 #define GPT2_FLAG_PER_KERNEL 1
 #define GPT2_FLAG_NO_CLUSTER 2
 /* GPT2_FLAG_HEAD_F16: the tied output head is also stored as fp16 (round to
