@@ -143,9 +143,9 @@ int gpt2_create(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
  *    graph of 5 * n_layer + 1 kernels per pass.
  * A path that cannot run on the device or configuration is left out and the
  * next one is used (the cluster kernel needs n_embd a multiple of 64 and at
- * most 1024, vocab_size <= 131072 and 36 co-resident clusters of 4 CTAs; the
- * persistent kernel n_embd <= 4096); gpt2_path reports which one a model
- * uses. */
+ * most 1024, vocab_size <= 131072, and enough co-resident clusters of 4 CTAs
+ * for one per head plus the MLP's; the persistent kernel n_embd <= 4096);
+ * gpt2_path reports which one a model uses. */
 #define GPT2_FLAG_PER_KERNEL 1
 #define GPT2_FLAG_NO_CLUSTER 2
 /* GPT2_FLAG_HEAD_F16: the tied output head is also stored as fp16 (round to
