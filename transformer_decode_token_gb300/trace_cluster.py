@@ -31,7 +31,7 @@ FC_PHASES = [("wait for x_new (GPU-wide sum)", 0, 1), ("LN/bias parameters", 1, 
              ("fc rows (LN folded)", 2, 3), ("gelu_new", 3, 4), ("mlp-proj tile", 4, 5),
              ("cluster reduce + add into x", 5, 6)]
 LM_PHASES = [("wait for x (GPU-wide sum)", 200, 201), ("LM-head rows + argmax keys", 201, 202),
-             ("argmax across CTAs, token", 202, 203)]
+             ("publish the tagged argmax key", 202, 203)]
 
 
 def run(wdtype: str, layer: int = 5):
