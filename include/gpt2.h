@@ -210,7 +210,8 @@ int gpt2_argmax(gpt2_model *m, int32_t *token_out);
  * softmax(logits / temperature), in the Gumbel-max form: the token with the
  * highest logit / temperature - log(-log u), u the uniform number of counter
  * position * vocab_size + id from a counter-based SplitMix64 generator with
- * this seed (u = (top 24 bits of the output + 0.5) * 2^-24).  The same seed,
+ * this seed (u = (top 23 bits of the output + 0.5) * 2^-23, strictly inside
+ * (0, 1)).  The same seed,
  * prompt and weights give the same tokens.  The drawn token is what
  * gpt2_argmax returns and what gpt2_decode_greedy / gpt2_generate feed to the
  * next pass; the logits stay the plain ones.  Takes effect from the next

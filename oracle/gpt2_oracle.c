@@ -215,11 +215,19 @@ uint64_t orc_splitmix64(uint64_t seed, uint64_t k)
     return z ^ (z >> 31);
 }
 
-/* A uniform float in (0, 1): the top 24 bits of output k, plus one half,
- * times 2^-24 (exact in fp32). */
+/* A uniform float in the open interval (0, 1) from 64 random bits: the top
+ * 23 bits m, as (m + 1/2) * 2^-23.  2m + 1 < 2^24, so m + 1/2 is exact in
+ * fp32 and the largest value is 1 - 2^-24 < 1 (with 24 bits, m + 1/2 for
+ * m = 2^24 - 1 rounds to 2^24 and the draw would be exactly 1). */
+float orc_uniform_bits(uint64_t z)
+{
+    return ((float)(z >> 41) + 0.5f) * 1.1920928955078125e-7f;
+}
+
+/* Uniform number k of the generator with this seed. */
 float orc_uniform(uint64_t seed, uint64_t k)
 {
-    return ((float)(orc_splitmix64(seed, k) >> 40) + 0.5f) * 5.9604644775390625e-8f;
+    return orc_uniform_bits(orc_splitmix64(seed, k));
 }
 
 /* The Gumbel-max form of a draw from softmax(s / T): score i is

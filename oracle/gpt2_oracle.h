@@ -129,6 +129,7 @@ void orc_dequant_int4(const uint8_t *codes, const float *scales,
  * (0, 1) from it, the Gumbel-max scores s_i / T - log(-log u_i) with
  * u_i = uniform(seed, pos * n + i), and the chosen token (greedy if T == 0). */
 uint64_t orc_splitmix64(uint64_t seed, uint64_t k);
+float orc_uniform_bits(uint64_t z);   /* top 23 bits of z -> (0, 1) */
 float orc_uniform(uint64_t seed, uint64_t k);
 void orc_sample_scores(const float *s, int32_t n, float T, uint64_t seed, int32_t pos, float *out);
 int32_t orc_sample(const float *s, int32_t n, float T, uint64_t seed, int32_t pos);

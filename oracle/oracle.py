@@ -83,6 +83,7 @@ def lib():
             c_u64 = ctypes.c_uint64
             L.orc_splitmix64.restype = c_u64; L.orc_splitmix64.argtypes = [c_u64, c_u64]
             L.orc_uniform.restype = c_f; L.orc_uniform.argtypes = [c_u64, c_u64]
+            L.orc_uniform_bits.restype = c_f; L.orc_uniform_bits.argtypes = [c_u64]
             L.orc_sample_scores.argtypes = [vp, c_i32, c_f, c_u64, c_i32, vp]
             L.orc_sample.restype = c_i32; L.orc_sample.argtypes = [vp, c_i32, c_f, c_u64, c_i32]
             L.orc_create.restype = vp
@@ -203,6 +204,11 @@ def splitmix64(seed: int, k: int) -> int:
 
 def uniform(seed: int, k: int) -> float:
     return float(lib().orc_uniform(seed, k))
+
+
+def uniform_bits(z: int) -> float:
+    """The uniform number that 64 random bits z map to."""
+    return float(lib().orc_uniform_bits(z & (2**64 - 1)))
 
 
 def sample_scores(logits, temperature: float, seed: int, pos: int) -> np.ndarray:

@@ -25,6 +25,20 @@ def test_uniform_numbers_are_uniform_and_inside_the_open_interval():
     assert abs(np.corrcoef(u[:-1], u[1:])[0, 1]) < 0.02
 
 
+def test_uniform_mapping_stays_inside_the_open_interval_at_its_extremes():
+    # the largest and smallest raw outputs: the draw must stay below 1 (a
+    # draw of exactly 1 gives -log(-log u) = +inf, which would win every
+    # argmax) and above 0; the grid is 2^-23 wide, centred in each cell
+    top = orc.uniform_bits(2**64 - 1)
+    assert top < 1.0 and top == 1.0 - 2.0**-24
+    assert orc.uniform_bits(0) == 2.0**-24
+    assert orc.uniform_bits(2**41) == 1.5 * 2.0**-23
+    # every cell of the top 23 bits maps to a distinct value strictly inside
+    for m in (1, 2**22, 2**23 - 2, 2**23 - 1):
+        u = orc.uniform_bits(m << 41)
+        assert 0.0 < u < 1.0 and u == (m + 0.5) * 2.0**-23
+
+
 def test_generator_depends_on_seed_and_counter():
     a = [orc.splitmix64(1, k) for k in range(1000)]
     b = [orc.splitmix64(2, k) for k in range(1000)]

@@ -687,8 +687,9 @@ __device__ __forceinline__ uint32_t stage_addr(const ClusterArgs &a, const CS &c
 // token with the highest logit / T - log(-log u), u = the uniform number of
 // counter pos * V + id from a counter-based SplitMix64 generator (Steele, Lea
 // and Flood, 2014): seed + (k + 1) * 0x9E3779B97F4A7C15 through its output
-// mixer; u = (top 24 bits + 0.5) * 2^-24.  The argmax key is built from that
-// score; the stored logit stays the plain one.
+// mixer; u = (top 23 bits + 0.5) * 2^-23, which lies strictly inside (0, 1)
+// (2m + 1 < 2^24 is exact in fp32).  The argmax key is built from that score;
+// the stored logit stays the plain one.
 __device__ __forceinline__ float sample_score(float logit, float temperature, unsigned long long seed,
                                               unsigned long long k)
 {
@@ -696,7 +697,7 @@ __device__ __forceinline__ float sample_score(float logit, float temperature, un
     z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
     z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
     z ^= z >> 31;
-    const float u = (float(uint32_t(z >> 40)) + 0.5f) * 5.9604644775390625e-8f;
+    const float u = (float(uint32_t(z >> 41)) + 0.5f) * 1.1920928955078125e-7f;
     return logit / temperature - logf(-logf(u));
 }
 
