@@ -1,18 +1,21 @@
 #!/usr/bin/env python
 """GPT-2 124M batch-1 greedy decode throughput on GB300.
 
-Workload (default): GPT-2 small (12 layers, n_embd 768, 12 heads, vocab 50257,
-1024 positions), fp32 weights drawn from N(0, 0.02) with seed 0, a 10-token
-prompt (seed 1) and 60 greedy decode steps at positions 10..69.  With
---wdtype int4 the block matrices are grouped int4 and the workload is a
-10-token prompt + 128 steps; with --wdtype f16 they are fp16 and the workload
-is a 16-token prompt decoded to the full 1024-position cache (1008 steps),
-with tok/s and GB/s also reported per 64 positions ("context_sweep").  A bench
-"step" is one decode pass over one token: embedding, 12 blocks, final
+Headline workload: GPT-2 small (12 layers, n_embd 768, 12 heads, vocab
+50257, 1024 positions), fp32 weights drawn from N(0, 0.02) with seed 0, a
+10-token prompt (seed 1) and 60 greedy decode steps at positions 10..69.  A
+bench "step" is one decode pass over one token: embedding, 12 blocks, final
 LayerNorm, tied head and argmax.  The timed region runs exactly --steps
 passes; they cycle through the workload's generation (each cycle re-enters
 its first position with the generation's first token, the rest are
 device-fed greedy passes), so any step count keeps the workload's positions.
+
+The same run also times the two other single-sequence configurations, each
+over whole cycles of its own generation, and reports them under "variants":
+int4 block matrices (10-token prompt + 128 steps) and fp16 block matrices
+(16-token prompt decoded to the full 1024-position cache, 1008 steps, with
+tok/s and GB/s per 64 positions in "context_sweep").  --wdtype picks one of
+them as the headline instead (then no variants).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--wdtype f32|f16|int4]
   python bench.py --impl reference ...     # the CPU oracle, same metric
@@ -23,6 +26,7 @@ process per GPU, launched by torchrun); the value is the total over ranks.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -41,20 +45,13 @@ UNIT = "tok/s"
 # passes): fp32 10 + 60, int4 10 + 128, fp16 16 + 1008 (to the full
 # 1024-position cache, with tok/s reported per 64 positions).
 WORKLOADS = {"f32": (10, 60), "int4": (10, 128), "f16": (16, 1008)}
-PROMPT_LEN, CYCLE = WORKLOADS["f32"]
 SWEEP_BUCKET = 64
-
-
-def set_workload(wdtype: str):
-    global PROMPT_LEN, CYCLE
-    PROMPT_LEN, CYCLE = WORKLOADS[wdtype]
-L2_BYTES = 129 * 1024 * 1024
 CLOCK_FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
                 "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
                 "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=20000)
@@ -63,13 +60,15 @@ def parse():
     p.add_argument("--wdtype", choices=["f32", "f16", "int4"], default="f32")
     p.add_argument("--head", choices=["f32", "f16", "int4"], default="f32",
                    help="LM head storage: the tied fp32 wte (the configurations), an fp16 copy (README -h) or int4")
+    p.add_argument("--no-variants", action="store_true",
+                   help="time only the headline workload (not the int4 and fp16 configurations)")
     p.add_argument("--e2e-calls", type=int, default=50)
-    p.add_argument("--cpu-seconds", type=float, default=15.0,
-                   help="CPU time budget of the oracle baseline sample")
+    p.add_argument("--cpu-seconds", type=float, default=8.0,
+                   help="CPU time budget of each leg of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--path", choices=["auto", "persistent", "per_kernel"], default="auto",
+    p.add_argument("--path", choices=["auto", "per_kernel"], default="auto",
                    help="auto: the cluster decode kernel where the device allows it")
-    a = p.parse_args()
+    a = p.parse_args(argv)
     if a.warmup < 3:
         p.error("--warmup must be >= 3")
     if a.steps < 1:
@@ -83,14 +82,21 @@ def dist_env():
 
 
 def workload_config(wdtype: str, world: int, head: str = "f32") -> dict:
-    return {"workload": f"GPT-2 small 124M, {wdtype} block weights, {head} LM head, batch 1, {PROMPT_LEN}-token prompt "
-                        f"+ {CYCLE} greedy decode steps (positions {PROMPT_LEN}..{PROMPT_LEN + CYCLE - 1}), "
+    n_prompt, cycle = WORKLOADS[wdtype]
+    return {"workload": f"GPT-2 small 124M, {wdtype} block weights, {head} LM head, batch 1, {n_prompt}-token prompt "
+                        f"+ {cycle} greedy decode steps (positions {n_prompt}..{n_prompt + cycle - 1}), "
                         "cycled",
             "n_layer": 12, "n_embd": 768, "n_head": 12, "vocab": 50257, "n_positions": 1024,
             "batch": 1, "weights": "synthetic N(0,0.02), seed 0; prompt ids uniform, seed 1",
             "l2": "no flush: every step streams all weights (f32 494.6 MB, f16 324.7 MB, int4 209.3 MB) "
                   "through a 129 MB L2",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def timed_positions(wdtype: str, steps: int) -> list:
+    """Positions of the passes a timed region of `steps` passes runs."""
+    n_prompt, cycle = WORKLOADS[wdtype]
+    return [n_prompt + (k % cycle) for k in range(steps)]
 
 
 # ---- clocks ------------------------------------------------------------------
@@ -172,25 +178,42 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def load_traffic():
-    """DRAM bytes per decode pass from the committed ncu summaries, by path and
-    weight type ({path: {wdtype: bytes}}), if any."""
+def kernel_source_sha() -> str:
+    """sha256 prefix of the decode kernel's sources: a traffic figure taken on
+    other sources no longer describes the kernel."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "transformer_decode_token_gb300", "csrc")
+    for name in ("cluster.cu", "cluster.h", "common.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(path: str, key: str):
+    """DRAM bytes per decode pass from the committed ncu summaries
+    (profiles/traffic.json: {path: {key: {"bytes": B, "sources": sha}}}), or
+    None if there is none for the current kernel sources."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
-            return json.load(f)
+            t = json.load(f).get(path, {}).get(key)
     except OSError:
-        return {}
+        return None
+    if not isinstance(t, dict) or t.get("sources") != kernel_source_sha():
+        return None
+    return t.get("bytes")
 
 
 # ---- CPU oracle timing -------------------------------------------------------
 
-def oracle_sample(cfg, weights, prompt, wdtype, budget_s, max_steps=None, head="f32"):
-    """Decode passes of the oracle after an untimed prefill; stops after
-    ~budget_s seconds (or max_steps).  Returns (passes, seconds)."""
+def oracle_sample(cfg, weights, prompt, wdtype, budget_s, max_steps=None, head="f32", omp=False):
+    """Decode passes of the oracle after an untimed prefill, at the
+    workload's positions; stops after ~budget_s seconds (or max_steps).
+    Returns (passes, seconds)."""
     from oracle import oracle as orc
+    n_prompt, cycle = WORKLOADS[wdtype]
     sw = orc.stored_weights(weights, wdtype, head=head)
-    m = orc.OracleModel(cfg, sw)
+    m = orc.OracleModel(cfg, sw, omp=omp)
     try:
         tok = None
         for pos, t in enumerate(prompt):
@@ -198,8 +221,8 @@ def oracle_sample(cfg, weights, prompt, wdtype, budget_s, max_steps=None, head="
         n, pos = 0, len(prompt)
         t0 = time.perf_counter()
         while True:
-            if pos >= PROMPT_LEN + CYCLE:           # keep the workload's positions
-                pos = PROMPT_LEN
+            if pos >= n_prompt + cycle:           # keep the workload's positions
+                pos = n_prompt
             _, tok = m.forward(tok, pos)
             pos += 1
             n += 1
@@ -210,24 +233,36 @@ def oracle_sample(cfg, weights, prompt, wdtype, budget_s, max_steps=None, head="
         m.close()
 
 
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     from transformer_decode_token_gb300 import synth
     cfg = synth.SMALL
+    n_prompt, _ = WORKLOADS[args.wdtype]
     w = synth.make_weights(cfg, 0)
-    prompt = synth.make_prompt(cfg, PROMPT_LEN, 1)
-    oracle_sample(cfg, w, prompt, args.wdtype, 1e9, max_steps=min(args.warmup, 3), head=args.head)
-    n, el = oracle_sample(cfg, w, prompt, args.wdtype, 60.0, max_steps=args.steps, head=args.head)
+    prompt = synth.make_prompt(cfg, n_prompt, 1)
+    cores = host_cores()
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    oracle_sample(cfg, w, prompt, args.wdtype, 1e9, max_steps=min(args.warmup, 3), head=args.head, omp=True)
+    n, el = oracle_sample(cfg, w, prompt, args.wdtype, 60.0, max_steps=args.steps, head=args.head, omp=True)
     value = n / el
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / n,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": workload_config(args.wdtype, 1, args.head),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"{n} of the {args.steps} requested decode passes (60 s cap), "
-                                       "single-threaded C oracle, after an untimed 10-token prefill"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": int(os.environ["OMP_NUM_THREADS"]),
+                             "kind": "oracle",
+                             "sample": f"{n} of the {args.steps} requested decode passes (60 s cap), the C oracle's "
+                                       "OpenMP build (each matrix product's outputs split between the threads), "
+                                       "after an untimed prefill"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -254,36 +289,154 @@ def job_throughput(steps_per_rank: int, world: int, ms_slowest: float) -> float:
 
 
 class StepRunner:
-    """Queues decode passes that cycle through the 60-step generation."""
+    """Queues decode passes that cycle through a workload's generation: a
+    host-fed pass at the first generated position, then device-fed greedy
+    passes up to the cycle's end."""
 
-    def __init__(self, model, first_token: int):
+    def __init__(self, model, first_token: int, n_prompt: int, cycle: int):
         self.m = model
         self.tok0 = first_token
+        self.n_prompt = n_prompt
+        self.cycle = cycle
         self.k = 0
         self.host_steps = 0
 
     def run(self, n: int):
         while n > 0:
-            if self.k % CYCLE == 0:
-                self.m.decode_step(self.tok0, PROMPT_LEN)
+            if self.k % self.cycle == 0:
+                self.m.decode_step(self.tok0, self.n_prompt)
                 self.host_steps += 1
                 self.k += 1
                 n -= 1
             else:
-                c = min(n, CYCLE - self.k % CYCLE)
+                c = min(n, self.cycle - self.k % self.cycle)
                 self.m.decode_greedy(c)
                 self.k += c
                 n -= c
 
 
+KERNEL_DESC = {
+    "cluster": "k_decode_cluster: one cooperative launch per call (a host-fed pass, then one launch of the "
+               "cycle's remaining device-fed passes), clusters of 4 CTAs, one CTA per SM",
+}
+
+
+def measure(torch, cfg, w, wdtype, head, path, steps, warmup, world, local, barrier, max_over_ranks,
+            sweep=False, e2e_calls=0):
+    """Times `steps` decode passes of one workload on a fresh model; returns
+    the workload's fields of the JSON line."""
+    from transformer_decode_token_gb300 import binding, roofline, synth
+    n_prompt, cycle = WORKLOADS[wdtype]
+    prompt = synth.make_prompt(cfg, n_prompt, 1)
+    dw = binding.upload_weights(w)
+    model = binding.Model(cfg, dw, wdtype, path=path, head=head)
+    del dw
+    torch.cuda.empty_cache()
+    out = {}
+    try:
+        kps = model.kernels_per_step()
+        path_used = model.path()
+        model.prefill(prompt)
+        tok0 = model.argmax()
+        runner = StepRunner(model, tok0, n_prompt, cycle)
+        runner.run(warmup)
+        model.sync()
+        runner = StepRunner(model, tok0, n_prompt, cycle)
+        sampler = ClockSampler(gpu_id_for(torch, local))
+        sampler.start()
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        t_begin = time.time()
+        n0 = model.launch_count()
+        e0.record(stream)
+        runner.run(steps)
+        e1.record(stream)
+        launches = model.launch_count() - n0
+        torch.cuda.synchronize()
+        t_end = time.time()
+        barrier()
+        clocks = sampler.stop(t_begin, t_end)
+        model.sync()
+        ms = max_over_ranks(e0.elapsed_time(e1))
+        out["value"] = job_throughput(steps, world, ms)
+        out["ms_per_step"] = ms / steps
+        out["steps"] = steps
+        out["gpu_launches"] = launches
+        out["clocks"] = clocks
+        out["path"] = path_used
+
+        if e2e_calls:
+            # end to end through gpt2_generate: host prompt in, host ids out
+            model.generate(prompt, cycle)
+            barrier()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(e2e_calls):
+                model.generate(prompt, cycle)
+            torch.cuda.synchronize()
+            e2e_s = max_over_ranks(time.perf_counter() - t0)
+            out["e2e"] = {"value": e2e_calls * (n_prompt + cycle) * world / e2e_s, "unit": UNIT,
+                          "h2d_bytes_per_step": n_prompt * 4, "d2h_bytes_per_step": (cycle + 1) * 4,
+                          "generated_tok_s": e2e_calls * (cycle + 1) * world / e2e_s,
+                          "step": f"one gpt2_generate call: {n_prompt}-id host prompt in, {n_prompt} prompt passes "
+                                  f"+ {cycle} greedy passes, {cycle + 1} ids back to host; value counts passes "
+                                  "(prompt and greedy), generated_tok_s counts the ids returned",
+                          "calls": e2e_calls}
+
+        if sweep and cycle >= 2 * SWEEP_BUCKET:
+            # tok/s against context length: one cycle, an event every SWEEP_BUCKET positions
+            peaks_s, _ = measured_peaks()
+            marks = []
+            torch.cuda.synchronize()
+            ev = torch.cuda.Event(enable_timing=True)
+            ev.record(stream)
+            marks.append((n_prompt, ev))
+            model.decode_step(tok0, n_prompt)
+            pos = n_prompt + 1
+            while pos < n_prompt + cycle:
+                n = min(SWEEP_BUCKET - (pos - n_prompt) % SWEEP_BUCKET, n_prompt + cycle - pos)
+                model.decode_greedy(n)
+                pos += n
+                ev = torch.cuda.Event(enable_timing=True)
+                ev.record(stream)
+                marks.append((pos, ev))
+            torch.cuda.synchronize()
+            rows = []
+            for (p0, e_a), (p1, e_b) in zip(marks, marks[1:]):
+                t = e_a.elapsed_time(e_b) / 1e3 / (p1 - p0)
+                b = roofline.mean_bytes_per_token(cfg, wdtype, range(p0, p1), head)
+                rows.append({"positions": f"{p0}..{p1 - 1}", "us_per_token": t * 1e6, "tok_s": 1.0 / t,
+                             "gbs": b / t / 1e9, "frac": b / t / 1e9 / peaks_s["hbm_gbs"]})
+            out["context_sweep"] = rows
+    finally:
+        model.close()
+
+    # roofline of the decode pass over the positions the timed region ran
+    positions = timed_positions(wdtype, steps)
+    alg = roofline.mean_bytes_per_token(cfg, wdtype, positions, head)
+    peaks, peak_kind = measured_peaks()
+    achieved = alg / (out["ms_per_step"] / 1e3) / 1e9
+    key = wdtype if head == "f32" else f"{wdtype}+{head} head"
+    out["roofline"] = {
+        "bound": "hbm",
+        "kernel": KERNEL_DESC.get(path_used, f"decode pass: one CUDA graph of {kps} kernels (PDL-chained)"),
+        "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+        "frac": achieved / peaks["hbm_gbs"], "peak_kind": f"{peak_kind} copy bandwidth",
+        "traffic": load_traffic(path_used, key),
+        "algorithmic_bytes_per_launch": alg,
+        "positions": f"{min(positions)}..{max(positions)} ({len(positions)} passes)"}
+    return out
+
+
 def main():
     args = parse()
-    set_workload(args.wdtype)
     if args.impl == "reference":
         return run_reference(args)
     import torch
     import torch.distributed as dist
-    from transformer_decode_token_gb300 import binding, roofline, synth
+    from transformer_decode_token_gb300 import synth
 
     rank, world, local = dist_env()
     if not torch.cuda.is_available():
@@ -302,120 +455,47 @@ def main():
 
     cfg = synth.SMALL
     w = synth.make_weights(cfg, 0)
-    prompt = synth.make_prompt(cfg, PROMPT_LEN, 1)
-    dw = binding.upload_weights(w)
-    model = binding.Model(cfg, dw, args.wdtype, path=args.path, head=args.head)
-    del dw
-    torch.cuda.empty_cache()
-    kps = model.kernels_per_step()
-    path = model.path()
+    head = measure(torch, cfg, w, args.wdtype, args.head, args.path, args.steps, args.warmup, world, local,
+                   barrier, max_over_ranks, sweep=True, e2e_calls=max(3, min(args.e2e_calls, 3000 // sum(
+                       WORKLOADS[args.wdtype]))))
+    n_prompt, cycle = WORKLOADS[args.wdtype]
+    line = {"metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if args.wdtype == "f32" else f"{args.wdtype} weights, f32 math", "data": "synthetic",
+            "config": workload_config(args.wdtype, world, args.head), "path": head["path"], "e2e": head["e2e"],
+            "gpu_launches": head["gpu_launches"], "roofline": head["roofline"], "clocks": head["clocks"]}
+    if "context_sweep" in head:
+        line["context_sweep"] = head["context_sweep"]
 
-    # ---- device-timed value ----
-    model.prefill(prompt)
-    tok0 = model.argmax()
-    runner = StepRunner(model, tok0)
-    runner.run(args.warmup)
-    model.sync()
-    runner = StepRunner(model, tok0)
-    sampler = ClockSampler(gpu_id_for(torch, local))
-    sampler.start()
-    stream = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
-    t_begin = time.time()
-    n0 = model.launch_count()
-    e0.record(stream)
-    runner.run(args.steps)
-    e1.record(stream)
-    launches = model.launch_count() - n0
-    torch.cuda.synchronize()
-    t_end = time.time()
-    barrier()
-    clocks = sampler.stop(t_begin, t_end)
-    model.sync()
-    ms = max_over_ranks(e0.elapsed_time(e1))
-    value = job_throughput(args.steps, world, ms)
-
-    # ---- end to end through gpt2_generate: host prompt in, host ids out ----
-    passes_per_call = PROMPT_LEN + CYCLE
-    e2e_calls = max(3, min(args.e2e_calls, 3000 // passes_per_call))
-    model.generate(prompt, CYCLE)
-    barrier()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(e2e_calls):
-        model.generate(prompt, CYCLE)
-    torch.cuda.synchronize()
-    e2e_s = max_over_ranks(time.perf_counter() - t0)
-    e2e = {"value": e2e_calls * passes_per_call * world / e2e_s, "unit": UNIT,
-           "h2d_bytes_per_step": PROMPT_LEN * 4, "d2h_bytes_per_step": (CYCLE + 1) * 4,
-           "step": f"one gpt2_generate call: {PROMPT_LEN}-id host prompt, {PROMPT_LEN} prompt passes "
-                   f"+ {CYCLE} greedy passes, {CYCLE + 1} ids back to host; value counts passes",
-           "calls": e2e_calls}
-
-    # ---- tok/s against context length (long workloads): one cycle, an event
-    # every SWEEP_BUCKET positions ----
-    sweep = None
-    if CYCLE >= 2 * SWEEP_BUCKET:
-        peaks_s, _ = measured_peaks()
-        marks = []
-        torch.cuda.synchronize()
-        ev = torch.cuda.Event(enable_timing=True)
-        ev.record(stream)
-        marks.append((PROMPT_LEN, ev))
-        model.decode_step(tok0, PROMPT_LEN)
-        pos = PROMPT_LEN + 1
-        while pos < PROMPT_LEN + CYCLE:
-            n = min(SWEEP_BUCKET - (pos - PROMPT_LEN) % SWEEP_BUCKET, PROMPT_LEN + CYCLE - pos)
-            model.decode_greedy(n)
-            pos += n
-            ev = torch.cuda.Event(enable_timing=True)
-            ev.record(stream)
-            marks.append((pos, ev))
-        torch.cuda.synchronize()
-        sweep = []
-        for (p0, e_a), (p1, e_b) in zip(marks, marks[1:]):
-            t = e_a.elapsed_time(e_b) / 1e3 / (p1 - p0)
-            b = roofline.mean_bytes_per_token(cfg, args.wdtype, range(p0, p1), args.head)
-            sweep.append({"positions": f"{p0}..{p1 - 1}", "us_per_token": t * 1e6, "tok_s": 1.0 / t,
-                          "gbs": b / t / 1e9, "frac": b / t / 1e9 / peaks_s["hbm_gbs"]})
-    model.close()
-
-    # ---- roofline of the decode pass --------------------------------------
-    positions = [PROMPT_LEN + (k % CYCLE) for k in range(CYCLE)]
-    alg = roofline.mean_bytes_per_token(cfg, args.wdtype, positions, args.head)
-    peaks, peak_kind = measured_peaks()
-    achieved = alg / (ms / 1e3 / args.steps) / 1e9
-    traffic = load_traffic().get(path, {}).get(args.wdtype if args.head == "f32" else f"{args.wdtype}+f16 head")
-    kernel = {
-        "cluster": "k_decode_cluster: one cooperative launch per call (one per 60-step cycle here, "
-                   "a host-fed pass + 59 device-fed passes), clusters of 4 CTAs, one CTA per SM",
-        "persistent": "k_decode_persistent: one cooperative launch per call (one per 60-step cycle here, "
-                      "a host-fed pass + 59 device-fed passes), one CTA per SM",
-    }.get(path, f"decode pass: one CUDA graph of {kps} kernels (PDL-chained)")
-    roof = {"bound": "hbm", "kernel": kernel,
-            "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"], "peak_kind": f"{peak_kind} copy bandwidth",
-            "traffic": traffic, "algorithmic_bytes_per_launch": alg}
-
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32" if args.wdtype == "f32" else
-            f"{args.wdtype} weights, f32 math", "data": "synthetic",
-            "config": dict(workload_config(args.wdtype, world, args.head), path=path), "e2e": e2e,
-            "gpu_launches": launches,
-            "roofline": roof, "clocks": clocks}
-    if sweep is not None:
-        line["context_sweep"] = sweep
+    # the other single-sequence configurations, each over whole cycles of its generation
+    if not args.no_variants and args.wdtype == "f32" and args.head == "f32":
+        variants = {}
+        for wd in ("int4", "f16"):
+            cyc = WORKLOADS[wd][1]
+            steps = cyc * max(1, -(-args.steps // cyc))
+            v = measure(torch, cfg, w, wd, "f32", args.path, steps, args.warmup, world, local, barrier,
+                        max_over_ranks, sweep=(wd == "f16"))
+            v["config"] = workload_config(wd, world)
+            v["dtype"] = f"{wd} weights, f32 math"
+            variants[wd] = v
+        line["variants"] = variants
 
     # ---- CPU baseline: the oracle on this host (rank 0, N = 1) ---------------
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n, el = oracle_sample(cfg, w, prompt, args.wdtype, args.cpu_seconds, head=args.head)
-        line["cpu_baseline"] = {"value": n / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                "sample": f"{n} greedy decode passes of the same workload (positions "
-                                          f"{PROMPT_LEN}..{PROMPT_LEN + CYCLE - 1}) after an untimed "
-                                          f"prefill, single-threaded C oracle, ~{args.cpu_seconds:.0f} s"}
+        prompt = synth.make_prompt(cfg, n_prompt, 1)
+        cores = host_cores()
+        os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+        n1, el1 = oracle_sample(cfg, w, prompt, args.wdtype, args.cpu_seconds, head=args.head)
+        nm, elm = oracle_sample(cfg, w, prompt, args.wdtype, args.cpu_seconds, head=args.head, omp=True)
+        line["cpu_baseline"] = {
+            "value": nm / elm, "unit": UNIT, "cores": int(os.environ["OMP_NUM_THREADS"]), "kind": "oracle",
+            "sample": f"{nm} greedy decode passes of the same workload (positions {n_prompt}..{n_prompt + cycle - 1}) "
+                      f"after an untimed prefill, the C oracle's OpenMP build (each matrix product's outputs "
+                      f"split between the threads), ~{args.cpu_seconds:.0f} s",
+            "single_thread": {"value": n1 / el1, "unit": UNIT, "cores": 1,
+                              "sample": f"{n1} passes of the same workload, single-threaded build, "
+                                        f"~{args.cpu_seconds:.0f} s"}}
     if world > 1:
         dist.destroy_process_group()
     if rank == 0:

@@ -10,6 +10,31 @@
 #include <stdlib.h>
 #include <string.h>
 
+/* The CPU baseline's multi-core build (-fopenmp) splits the outputs of each
+ * matrix product between threads, as [P1] "Inner Workings" splits the rows of
+ * each matrix product between its -j workers; each output is still computed
+ * by one thread with the same operations in the same order, so both builds
+ * give the same bits.  Without OpenMP the loops run on one thread. */
+#ifdef _OPENMP
+#include <omp.h>
+#define ORC_PARALLEL _Pragma("omp parallel")
+#define ORC_PARALLEL_FOR _Pragma("omp parallel for schedule(static)")
+static void orc_share(int32_t n, int32_t *lo, int32_t *hi)
+{
+    const int64_t t = omp_get_thread_num(), nt = omp_get_num_threads();
+    *lo = (int32_t)(n * t / nt);
+    *hi = (int32_t)(n * (t + 1) / nt);
+}
+#else
+#define ORC_PARALLEL
+#define ORC_PARALLEL_FOR
+static void orc_share(int32_t n, int32_t *lo, int32_t *hi)
+{
+    *lo = 0;
+    *hi = n;
+}
+#endif
+
 /* ======================================================================== */
 /* Scalar math: [P2] "Step 5: Math without a math library".                */
 /* ======================================================================== */
@@ -127,14 +152,19 @@ void orc_softmax(float *s, int32_t n)
 void orc_linear(const float *x, const float *W, const float *b,
                 int32_t in, int32_t out, float *y)
 {
-    for (int32_t o = 0; o < out; ++o) y[o] = 0.0f;
-    for (int32_t i = 0; i < in; ++i) {
-        const float xi = x[i];
-        const float *row = W + (size_t)i * (size_t)out;
-        for (int32_t o = 0; o < out; ++o) y[o] += xi * row[o];
+    ORC_PARALLEL
+    {
+        int32_t o0, o1;   /* this thread's outputs (all of them on one thread) */
+        orc_share(out, &o0, &o1);
+        for (int32_t o = o0; o < o1; ++o) y[o] = 0.0f;
+        for (int32_t i = 0; i < in; ++i) {
+            const float xi = x[i];
+            const float *row = W + (size_t)i * (size_t)out;
+            for (int32_t o = o0; o < o1; ++o) y[o] += xi * row[o];
+        }
+        if (b)
+            for (int32_t o = o0; o < o1; ++o) y[o] = y[o] + b[o];
     }
-    if (b)
-        for (int32_t o = 0; o < out; ++o) y[o] = y[o] + b[o];
 }
 
 /* Multiply by the transpose of a stored [out][in] matrix: the tied output
@@ -143,6 +173,7 @@ void orc_linear(const float *x, const float *W, const float *b,
 void orc_linear_t(const float *x, const float *W, int32_t in, int32_t out,
                   float *y)
 {
+    ORC_PARALLEL_FOR
     for (int32_t o = 0; o < out; ++o) {
         const float *row = W + (size_t)o * (size_t)in;
         float acc = 0.0f;

@@ -21,8 +21,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gpt2_oracle.c")
 _HDR = os.path.join(_HERE, "gpt2_oracle.h")
 _LIB = os.path.join(_HERE, "liboracle.so")
+_LIB_OMP = os.path.join(_HERE, "liboracle_omp.so")
 _lock = threading.Lock()
 _lib = None
+_lib_omp = None
 
 # -ffp-contract=off: every product and sum rounds separately (GCC contracts
 # a*b+c into an FMA by default on AArch64); no -ffast-math.
@@ -30,15 +32,18 @@ CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
           "-shared", "-Wall"]
 
 
-def build(force: bool = False) -> str:
-    """Compile liboracle.so next to its source (gcc)."""
-    stale = (not os.path.exists(_LIB) or
-             os.path.getmtime(_LIB) < max(os.path.getmtime(_SRC), os.path.getmtime(_HDR)))
+def build(force: bool = False, omp: bool = False) -> str:
+    """Compile liboracle.so next to its source (gcc); omp=True builds the
+    multi-core variant liboracle_omp.so (-fopenmp: each matrix product's
+    outputs split between threads, the same bits as the single-thread build)."""
+    path = _LIB_OMP if omp else _LIB
+    stale = (not os.path.exists(path) or
+             os.path.getmtime(path) < max(os.path.getmtime(_SRC), os.path.getmtime(_HDR)))
     if force or stale:
-        tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"])
-        os.replace(tmp, _LIB)
-    return _LIB
+        tmp = path + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", *CFLAGS, *(["-fopenmp"] if omp else []), "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, path)
+    return path
 
 
 class _Cfg(ctypes.Structure):
@@ -61,11 +66,13 @@ class _Weights(ctypes.Structure):
                 ("layers", ctypes.POINTER(_Layer)), ("head", _FP)]
 
 
-def lib():
-    global _lib
+def lib(omp: bool = False):
+    """The oracle library; omp=True: its multi-core build (OMP_NUM_THREADS,
+    default all host cores)."""
+    global _lib, _lib_omp
     with _lock:
-        if _lib is None:
-            L = ctypes.CDLL(build())
+        if (_lib_omp if omp else _lib) is None:
+            L = ctypes.CDLL(build(omp=omp))
             c_sz, c_i32, c_f = ctypes.c_size_t, ctypes.c_int32, ctypes.c_float
             vp = ctypes.c_void_p
             L.orc_expf.restype = c_f; L.orc_expf.argtypes = [c_f]
@@ -101,8 +108,11 @@ def lib():
             L.orc_dequant_int4.argtypes = [vp, vp, vp, c_i32, c_i32, vp]
             L.orc_pack_nibbles.argtypes = [vp, c_sz, vp]
             L.orc_unpack_nibbles.argtypes = [vp, c_sz, vp]
-            _lib = L
-    return _lib
+            if omp:
+                _lib_omp = L
+            else:
+                _lib = L
+    return _lib_omp if omp else _lib
 
 
 def _p(a: np.ndarray):
@@ -367,29 +377,31 @@ class _WeightsHolder:
 
 
 class OracleModel:
-    """Stateful single-sequence decode with a KV cache."""
+    """Stateful single-sequence decode with a KV cache (omp=True: the
+    multi-core build, for the CPU baseline's timing)."""
 
-    def __init__(self, cfg, weights: dict):
+    def __init__(self, cfg, weights: dict, omp: bool = False):
         self.cfg = cfg
+        self._lib = lib(omp)
         self._c = _cfg_struct(cfg)
         self._h = _WeightsHolder(cfg, weights)
-        self._m = lib().orc_create(ctypes.byref(self._c), ctypes.byref(self._h.w))
+        self._m = self._lib.orc_create(ctypes.byref(self._c), ctypes.byref(self._h.w))
         if not self._m:
             raise ValueError("oracle: invalid config")
 
     def forward(self, token: int, pos: int):
         logits = np.empty(self.cfg.vocab_size, np.float32)
-        r = lib().orc_forward(self._m, int(token), int(pos), _p(logits))
+        r = self._lib.orc_forward(self._m, int(token), int(pos), _p(logits))
         if r < 0:
             raise ValueError(f"oracle: bad token {token} or position {pos}")
         return logits, int(r)
 
     def reset(self):
-        lib().orc_reset(self._m)
+        self._lib.orc_reset(self._m)
 
     def close(self):
         if self._m:
-            lib().orc_destroy(self._m)
+            self._lib.orc_destroy(self._m)
             self._m = None
 
     def __del__(self):

@@ -28,10 +28,9 @@ class FakeModel:
 
 @pytest.mark.parametrize("wdtype", ["f32", "int4", "f16"])
 def test_step_runner_keeps_the_workload_positions(wdtype):
-    bench.set_workload(wdtype)
     prompt_len, cycle = bench.WORKLOADS[wdtype]
     m = FakeModel()
-    r = bench.StepRunner(m, first_token=7)
+    r = bench.StepRunner(m, first_token=7, n_prompt=prompt_len, cycle=cycle)
     steps = 2 * cycle + 5
     r.run(steps - 3)
     r.run(3)                                 # split calls continue the cycle
@@ -47,7 +46,14 @@ def test_step_runner_keeps_the_workload_positions(wdtype):
             assert pos <= prompt_len + cycle  # never past the workload's last position
     assert passes == steps
     assert sum(1 for c in m.calls if c[0] == "step") == 3
-    bench.set_workload("f32")
+    # the roofline averages over exactly the positions these passes ran
+    pos_seen = []
+    for c in m.calls:
+        if c[0] == "step":
+            pos_seen.append(c[2])
+        else:
+            pos_seen.extend(range(pos_seen[-1] + 1, pos_seen[-1] + 1 + c[1]))
+    assert pos_seen == bench.timed_positions(wdtype, steps)
 
 
 def test_workloads_follow_the_configurations():
@@ -55,10 +61,10 @@ def test_workloads_follow_the_configurations():
     assert bench.WORKLOADS["int4"] == (10, 128)
     assert bench.WORKLOADS["f16"] == (16, 1008)
     assert sum(bench.WORKLOADS["f16"]) == 1024      # to the full 1024-position cache
-    bench.set_workload("int4")
     cfg = bench.workload_config("int4", 1, "f32")
     assert "10-token prompt + 128 greedy decode steps (positions 10..137)" in cfg["workload"]
-    bench.set_workload("f32")
+    # the driver's short run (20 steps) times positions 10..29 only
+    assert bench.timed_positions("f32", 20) == list(range(10, 30))
 
 
 def test_job_throughput_counts_every_rank_over_the_slowest_time():
@@ -104,3 +110,40 @@ def test_reference_arm_on_other_ranks_exits_without_work(monkeypatch):
         wdtype, steps, warmup, head = "f32", 5, 3, "f32"
 
     assert bench.run_reference(A()) == 0
+
+
+def test_traffic_figures_are_tied_to_the_kernel_sources(tmp_path, monkeypatch):
+    """A committed DRAM-traffic figure counts only while the kernel sources it
+    was captured on are unchanged."""
+    import json
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    sha = bench.kernel_source_sha()
+    (prof / "traffic.json").write_text(json.dumps(
+        {"cluster": {"f32": {"bytes": 123, "sources": sha}, "int4": {"bytes": 45, "sources": "0" * 16}}}))
+    csrc = tmp_path / "transformer_decode_token_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for name in ("cluster.cu", "cluster.h", "common.cuh"):
+        src = os.path.join(ROOT, "transformer_decode_token_gb300", "csrc", name)
+        (csrc / name).write_bytes(open(src, "rb").read())
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_traffic("cluster", "f32") == 123
+    assert bench.load_traffic("cluster", "int4") is None      # captured on other sources
+    assert bench.load_traffic("cluster", "f16") is None       # never captured
+    (csrc / "cluster.cu").write_bytes(b"changed")
+    assert bench.load_traffic("cluster", "f32") is None
+
+
+def test_reference_arm_reports_the_same_config_as_ours(monkeypatch, capsys):
+    """The reference arm (the oracle) prints the headline's metric, unit and
+    config, so the two lines describe the same workload."""
+    import json
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.setattr(bench, "oracle_sample", lambda *a, **k: (5, 0.5))
+    a = bench.parse(["--impl", "reference", "--steps", "5", "--warmup", "3"])
+    assert bench.run_reference(a) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["config"] == bench.workload_config("f32", 1, "f32")
+    assert line["value"] == pytest.approx(10.0) and line["cpu_baseline"]["kind"] == "oracle"

@@ -10,34 +10,9 @@
 """
 import numpy as np
 import pytest
-import torch
-import torch.nn.functional as F
-
 from oracle import oracle as orc
+from ref64 import torch_gpt2_logits
 from transformer_decode_token_gb300 import synth
-
-
-def torch_gpt2_logits(cfg, w, tokens):
-    """Float64 GPT-2 forward over a whole sequence, from library routines."""
-    d = lambda a: torch.from_numpy(np.asarray(a, np.float32)).double()
-    E, H, D = cfg.n_embd, cfg.n_head, cfg.head_dim
-    t = torch.as_tensor(np.asarray(tokens, np.int64))
-    n = t.numel()
-    x = d(w["wte"])[t] + d(w["wpe"])[:n]
-    for L in w["layers"]:
-        h = F.layer_norm(x, (E,), d(L["ln1_w"]), d(L["ln1_b"]), eps=cfg.ln_eps)
-        qkv = h @ d(L["attn_w"]) + d(L["attn_b"])
-        q, k, v = qkv.split(E, dim=-1)
-        q, k, v = (a.reshape(n, H, D).transpose(0, 1) for a in (q, k, v))
-        a = F.scaled_dot_product_attention(q, k, v, is_causal=True)
-        a = a.transpose(0, 1).reshape(n, E)
-        x = x + a @ d(L["proj_w"]) + d(L["proj_b"])
-        h = F.layer_norm(x, (E,), d(L["ln2_w"]), d(L["ln2_b"]), eps=cfg.ln_eps)
-        f = F.gelu(h @ d(L["fc_w"]) + d(L["fc_b"]), approximate="tanh")
-        x = x + f @ d(L["mlp_proj_w"]) + d(L["mlp_proj_b"])
-    x = F.layer_norm(x, (E,), d(w["ln_f_w"]), d(w["ln_f_b"]), eps=cfg.ln_eps)
-    head = w.get("head", w["wte"])     # a separately stored head, else the tied wte
-    return (x @ d(head).T).numpy()
 
 
 # head_dim 32 (tiny) and head_dim 64 (the GPT-2 head, scale 1/8)
@@ -139,3 +114,29 @@ def test_separately_stored_head(head):
         assert moved > 1e-5                    # the stored head is a different matrix
     finally:
         a.close(); b.close(); c.close()
+
+
+def test_multicore_build_gives_the_same_bits():
+    """The CPU baseline's OpenMP build splits each matrix product's outputs
+    between threads; every output keeps its operations and their order, so
+    the logits are bitwise those of the single-thread build."""
+    import os
+    cfg = synth.TINY
+    w = synth.make_weights(cfg, 0)
+    prompt = synth.make_prompt(cfg, 6, 1)
+    rows = {}
+    old = os.environ.get("OMP_NUM_THREADS")
+    os.environ["OMP_NUM_THREADS"] = "3"        # an uneven split of every output range
+    try:
+        for omp in (False, True):
+            m = orc.OracleModel(cfg, w, omp=omp)
+            try:
+                rows[omp] = np.stack([m.forward(int(t), p)[0] for p, t in enumerate(prompt)])
+            finally:
+                m.close()
+    finally:
+        if old is None:
+            os.environ.pop("OMP_NUM_THREADS", None)
+        else:
+            os.environ["OMP_NUM_THREADS"] = old
+    assert np.array_equal(rows[False].view(np.uint32), rows[True].view(np.uint32))
