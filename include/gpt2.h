@@ -50,6 +50,9 @@ extern "C" {
 #define GPT2_ERR_TIMEOUT            -7  /* a bounded device wait gave up      */
 #define GPT2_ERR_DEVICE_STATE       -8  /* a kernel rejected its inputs       */
 #define GPT2_ERR_OUT_OF_MEMORY      -9  /* device allocation failed           */
+#define GPT2_ERR_RANGE             -10  /* an activation left the range of the
+                                           cluster kernel's fixed-point residual
+                                           sums (|value| > 65000, or NaN)      */
 
 /* ---- configuration ------------------------------------------------------- */
 /* Model shape, as the graph file's config checks and symbols define it
@@ -117,14 +120,16 @@ typedef struct gpt2_model gpt2_model;
  * cache [n_layer][n_head][n_positions][head_dim] — "stored by head", as the
  * "gpt2.s" README's Inner Workings puts it — activations, logits), repacks
  * the weights on the device (transpose to [out][in]; fp16 rounding; int4
- * quantisation), and captures one decode pass into a CUDA graph.
+ * quantisation) and prepares the decode path (gpt2_create_ex: the cluster
+ * kernel's tiled copies and launch shape, or, on the per-kernel path, one
+ * decode pass captured into a CUDA graph).
  * The caller keeps ownership of `w`'s tensors and may free them once this
  * returns.  On success *out owns everything and must be released with
  * gpt2_destroy.  Errors: INVALID_ARG, UNSUPPORTED_DEVICE, OUT_OF_MEMORY, CUDA. */
 int gpt2_create(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
                 void *stream, gpt2_model **out);
 
-/* gpt2_create with options.  flags = 0 is gpt2_create.  Three paths compute
+/* gpt2_create with options.  flags = 0 is gpt2_create.  Two paths compute
  * the same pass (the node list of the "model.fir" graph file and the model.s
  * description of the "gpt2.s" README, "Inner Workings"; greedy choice as in
  * "Let's make GPT-2 in assembly", Step 7):
@@ -135,19 +140,13 @@ int gpt2_create(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
  *    other CTAs own slices of the MLP.  Residual sums between the two groups
  *    are fixed-point integer atomics, so runs are bitwise reproducible; two
  *    GPU-wide exchanges per block.  Greedy steps never return to the host.
- *  - persistent (GPT2_FLAG_NO_CLUSTER, or GPT2_PATH=persistent): one
- *    cooperative launch per call, one CTA per SM, weights streamed through
- *    shared memory, activations passed between CTAs as value+epoch words
- *    (five GPU-wide exchanges per block).
- *  - per-kernel (GPT2_FLAG_PER_KERNEL, or GPT2_PATH=graph): the captured CUDA
- *    graph of 5 * n_layer + 1 kernels per pass.
- * A path that cannot run on the device or configuration is left out and the
- * next one is used (the cluster kernel needs n_embd a multiple of 64 and at
- * most 1024, vocab_size <= 131072, and enough co-resident clusters of 4 CTAs
- * for one per head plus the MLP's; the persistent kernel n_embd <= 4096);
+ *  - per-kernel (GPT2_FLAG_PER_KERNEL): the CUDA graph, captured at create
+ *    time, of 5 * n_layer + 1 kernels per pass.
+ * Where the cluster kernel cannot run (it needs n_embd a multiple of 64 and
+ * at most 1024, vocab_size <= 131072, and enough co-resident clusters of 4
+ * CTAs for one per head plus the MLP's), the per-kernel path is used;
  * gpt2_path reports which one a model uses. */
 #define GPT2_FLAG_PER_KERNEL 1
-#define GPT2_FLAG_NO_CLUSTER 2
 /* GPT2_FLAG_HEAD_F16: the tied output head is also stored as fp16 (round to
  * nearest even), as the "gpt2.s" README's -h option stores it ("Options": the
  * 48 block matrices and the output head as fp16); the LM head reads that
@@ -166,7 +165,6 @@ int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype
                    int32_t flags, void *stream, gpt2_model **out);
 
 #define GPT2_PATH_PER_KERNEL 0
-#define GPT2_PATH_PERSISTENT 1
 #define GPT2_PATH_CLUSTER 2
 int gpt2_path(const gpt2_model *m, int32_t *path);
 
@@ -238,8 +236,21 @@ int gpt2_generate(gpt2_model *m, const int32_t *host_prompt, int32_t n_prompt,
  * and synchronises.  Errors: NOT_READY, INVALID_ARG, CUDA, DEVICE_STATE. */
 int gpt2_copy_logits(gpt2_model *m, float *dst);
 
-/* Waits for the model's queued work; returns a recorded device error if any. */
+/* Waits for the model's queued work; returns a recorded device error if any
+ * (and clears it, with the cluster kernel's exchange state, so the model
+ * stays usable). */
 int gpt2_sync(gpt2_model *m);
+
+/* Time limit of every wait inside the cluster kernel (for a weight stage, a
+ * peer CTA, a GPU-wide sum or the previous pass's token), in nanoseconds of
+ * the GPU's global timer; default 2e9 (2 s).  When a wait runs out the kernel
+ * records GPT2_ERR_TIMEOUT, every CTA skips its remaining work and returns,
+ * and the next synchronising call reports the error ("gpt2.s" README,
+ * Limitations: a worker that stops ends the program with an error instead of
+ * hanging it).  A test hook: a tiny limit makes the first wait that does not
+ * succeed at once give up.  Takes effect from the next call.
+ * Errors: INVALID_ARG (NULL model, or a model on the per-kernel path). */
+int gpt2_set_wait_limit(gpt2_model *m, uint64_t ns);
 
 /* ---- inspection (for parity tests and tools) ---------------------------- */
 
@@ -269,7 +280,7 @@ int gpt2_export_kv(gpt2_model *m, int32_t layer, int32_t n_rows,
                    float *dst_k, float *dst_v);
 
 /* Kernel launches per decode pass: 5 * n_layer + 1 on the per-kernel path,
- * 1 on the persistent path (where one launch runs every pass of a call). */
+ * 1 on the cluster path (where one launch runs every pass of a call). */
 int gpt2_kernels_per_step(const gpt2_model *m, int32_t *count);
 
 /* Total kernel launches this model has issued so far (graph kernels and the
@@ -310,7 +321,8 @@ int gpt2_op_head_argmax(const float *x, const float *ln_w, const float *ln_b,
  *     return GPT2_ERR_INVALID_ARG (the array holds one key per 256 rows).
  *   - The first call on each device looks up the array's device address
  *     (with that device current); make that first call before any stream
- *     capture begins.
+ *     capture begins.  The address is kept with the device's context: after
+ *     cudaDeviceReset the next call looks it up again (again a first call).
  *   - All calls on a device share the array: calls whose kernels can overlap
  *     on the GPU (different streams, different threads) race and must be
  *     serialised by the caller.  Each call clears the counter it needs.

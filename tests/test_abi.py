@@ -85,3 +85,6 @@ def test_new_options_are_rejected_on_the_host():
     assert L.gpt2_path(None, None) == -1
     assert L.gpt2_launch_count(None, None) == -1
 
+    assert L.gpt2_set_wait_limit(None, 0) == -1
+    # the flag that once selected a third path is no longer accepted
+    assert L.gpt2_create_ex(ctypes.byref(good), ctypes.byref(w), 0, 2, None, ctypes.byref(out)) == -1

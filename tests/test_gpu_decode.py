@@ -14,13 +14,13 @@ import pytest
 from oracle import oracle as orc
 from transformer_decode_token_gb300 import binding, synth
 
-from gpu_util import check_rows, max_abs, teacher_forced, top2_margin
+from gpu_util import check_rows, max_abs, rel_l2, teacher_forced, top2_margin
 
 pytestmark = pytest.mark.gpu
 
 TOL = {"f32": (1e-3, 1e-4), "f16": (2e-3, None), "int4": (2e-3, None)}
-PATHS = ["cluster", "persistent", "per_kernel"]
-_BINDING_PATH = {"cluster": "auto", "persistent": "persistent", "per_kernel": "per_kernel"}
+PATHS = ["cluster", "per_kernel"]
+_BINDING_PATH = {"cluster": "auto", "per_kernel": "per_kernel"}
 _cache = {}
 _oracle_cache = {}
 
@@ -86,7 +86,7 @@ def test_small_fp16_full_context(path):
 
 @pytest.mark.parametrize("wdtype", ["f32", "int4"])
 def test_paths_agree(wdtype):
-    """The three paths compute the same pass: the same row dot products up to
+    """The two paths compute the same pass: the same row dot products up to
     summation order (the cluster kernel adds the residual stream as
     fixed-point integers, the others in fp32)."""
     cfg = synth.SMALL
@@ -391,3 +391,132 @@ def test_stored_head_needs_the_cluster_kernel():
     for head in ("f16", "int4"):
         with pytest.raises(binding.GPT2Error):
             binding.Model(cfg, dw, "f32", path="per_kernel", head=head)
+
+
+# ---- inputs that reach the numerically fragile parts -------------------------------
+
+def _stress_parity(cfg, kind, wdtype, n_prompt, n_steps, path):
+    """Teacher-forced parity on a stress input, measured against exact
+    (float64) arithmetic.  With a common offset of 30 the residual stream is
+    ill-conditioned for fp32: LayerNorm divides rounding errors of size
+    ulp(30) ~ 2e-6 by std(x) ~ 0.03, so any fp32 evaluation, the oracle's
+    included, is off from exact arithmetic by ~2e-4 (tiny) to ~3e-3 (GPT-2
+    small) in the logits; the standard tolerance against the oracle then
+    measures the conditioning, not the kernel.  The bar: per step, the CUDA
+    path's distance from the exact logits is at most max(standard tolerance,
+    3 x the oracle's own), element-wise and in relative L2, and its token is
+    the exact argmax wherever the exact top-2 margin exceeds twice that.  A
+    LayerNorm fold that cancels (W.(gamma*x) - mean*W.gamma at |mean| >> std)
+    puts an error of ~3e-4 on every folded row of unit scale (a numpy model of
+    the fold in fp32: ~3e-7 when centred on x[0]), a thousand times the
+    centred fold's."""
+    from ref64 import torch_gpt2_logits
+    w = synth.make_stress_weights(cfg, kind)
+    sw = orc.stored_weights(w, wdtype)
+    dw = binding.upload_weights(w)
+    prompt = synth.make_prompt(cfg, n_prompt, 1)
+    ref_ids, ref_rows = orc.greedy(cfg, sw, prompt, n_steps)
+    tokens = list(prompt) + ref_ids[:n_steps]
+    m = model(cfg, dw, wdtype, path)
+    try:
+        rows, ids = teacher_forced(m, tokens)
+    finally:
+        m.close()
+    atol, rl2 = TOL[wdtype]
+    exact = torch_gpt2_logits(cfg, sw, tokens)
+    for i in range(len(tokens)):
+        tol = max(atol, 3 * max_abs(ref_rows[i], exact[i]))
+        assert max_abs(rows[i], exact[i]) <= tol, f"step {i}"
+        if rl2 is not None:
+            assert rel_l2(rows[i], exact[i]) <= max(rl2, 3 * rel_l2(ref_rows[i], exact[i])), f"step {i}"
+        if top2_margin(exact[i]) > 2 * tol:
+            assert ids[i] == int(np.argmax(exact[i])), f"step {i}: argmax differs"
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("kind", ["offset", "outliers"])
+@pytest.mark.parametrize("cfg_name,n_prompt,n_steps", [("tiny", 4, 16), ("small", 10, 20)])
+def test_large_offset_and_outlier_residuals(cfg_name, n_prompt, n_steps, kind, path):
+    """Residual streams with a common offset of 30 (|mean| ~ 1000 std at the
+    first LayerNorm) or with three dimensions in the thousands: the cluster
+    kernel folds each LayerNorm into the rows that follow it, a difference of
+    two sums that cancels when |mean| >> std, and adds the residual stream in
+    fixed point; fp32 tolerance against the oracle, teacher-forced."""
+    cfg = synth.TINY if cfg_name == "tiny" else synth.SMALL
+    _stress_parity(cfg, kind, "f32", n_prompt, n_steps, path)
+
+
+@pytest.mark.parametrize("wdtype", ["f16", "int4"])
+def test_large_offset_stored_weights(wdtype):
+    _stress_parity(synth.TINY, "offset", wdtype, 4, 16, "cluster")
+
+
+def test_fixed_point_range_is_reported():
+    """A residual value beyond the fixed-point sums' range (|x| ~ 1e5 > 65000)
+    is reported as GPT2_ERR_RANGE by the next synchronising call, not summed
+    as a clamped value with status OK; the model stays usable afterwards."""
+    cfg = synth.TINY
+    dw = binding.upload_weights(synth.make_stress_weights(cfg, "overflow"))
+    m = model(cfg, dw, "f32", "cluster")
+    try:
+        m.decode_step(5, 0)
+        with pytest.raises(binding.GPT2Error) as e:
+            m.sync()
+        assert e.value.name == "RANGE"
+        m.sync()                                         # reported once, then cleared
+    finally:
+        m.close()
+    # the same weights within range (no offset) run clean on a fresh model
+    w, dw = weights(cfg)
+    prompt = synth.make_prompt(cfg, 4, 1)
+    ref_ids, _ = orc.greedy(cfg, w, prompt, 8)
+    m = model(cfg, dw, "f32", "cluster")
+    try:
+        assert m.generate(prompt, 8) == ref_ids
+    finally:
+        m.close()
+
+
+# ---- bounded device waits ------------------------------------------------------------
+
+def test_wait_limit_runs_out_and_the_model_recovers():
+    """Every wait of the cluster kernel is bounded.  With a limit of 0 ns the
+    first wait that does not succeed at once gives up: the kernel records
+    GPT2_ERR_TIMEOUT, every CTA skips its remaining work (the abort word, the
+    producer's drain, the final cluster barrier) and returns, and the next
+    synchronising call reports it within a second.  With the default limit
+    restored, the same model and a fresh one match the oracle again."""
+    import time
+    cfg = synth.TINY
+    w, dw = weights(cfg)
+    prompt = synth.make_prompt(cfg, 4, 1)
+    ref_ids, ref_rows = orc.greedy(cfg, w, prompt, 12)
+    m = model(cfg, dw, "f32", "cluster")
+    try:
+        m.set_wait_limit(0)
+        t0 = time.perf_counter()
+        status = "OK"
+        try:
+            m.generate(prompt, 12)
+        except binding.GPT2Error as e:
+            status = e.name
+        assert status in ("TIMEOUT", "OK")
+        assert time.perf_counter() - t0 < 1.0
+        assert status == "TIMEOUT"                       # the weights cannot all be resident at once
+        m.sync()                                         # the error was reported once and cleared
+        m.set_wait_limit(2_000_000_000)
+        assert m.generate(prompt, 12) == ref_ids
+        assert max_abs(m.logits(), ref_rows[-1]) <= 1e-3
+    finally:
+        m.close()
+    m = model(cfg, dw, "f32", "cluster")
+    try:
+        assert m.generate(prompt, 12) == ref_ids
+    finally:
+        m.close()
+    m = model(cfg, dw, "f32", "per_kernel")
+    try:
+        with pytest.raises(binding.GPT2Error):
+            m.set_wait_limit(0)                          # no cross-CTA waits on that path
+    finally:
+        m.close()

@@ -14,20 +14,21 @@ import numpy as np
 
 from . import build as _build
 
-GPT2_F32, GPT2_F16, GPT2_INT4 = 0, 1, 2
-WDTYPES = {"f32": GPT2_F32, "f16": GPT2_F16, "int4": GPT2_INT4}
+GPT2_F32, GPT2_F16, GPT2_INT4, GPT2_BF16 = 0, 1, 2, 3
+WDTYPES = {"f32": GPT2_F32, "f16": GPT2_F16, "int4": GPT2_INT4, "bf16": GPT2_BF16}
 MAT_ATTN, MAT_PROJ, MAT_FC, MAT_MLP_PROJ = 0, 1, 2, 3
 MATRIX_KEYS = ("attn_w", "proj_w", "fc_w", "mlp_proj_w")   # index = MAT_*
 
 STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED_DEVICE", -3: "TOKEN_RANGE",
           -4: "POSITION_RANGE", -5: "NOT_READY", -6: "CUDA", -7: "TIMEOUT",
-          -8: "DEVICE_STATE", -9: "OUT_OF_MEMORY"}
+          -8: "DEVICE_STATE", -9: "OUT_OF_MEMORY", -10: "RANGE"}
 
 EXPORTED = ("gpt2_create", "gpt2_create_ex", "gpt2_path", "gpt2_launch_count", "gpt2_destroy", "gpt2_reset", "gpt2_decode_step", "gpt2_prefill",
             "gpt2_argmax", "gpt2_decode_greedy", "gpt2_generate", "gpt2_copy_logits", "gpt2_sync",
             "gpt2_matrix_bytes", "gpt2_export_matrix", "gpt2_export_dequant", "gpt2_export_kv",
             "gpt2_kernels_per_step", "gpt2_op_layernorm", "gpt2_op_head_argmax_workspace",
-            "gpt2_op_head_argmax", "gpt2_op_head_argmax_noalloc", "gpt2_set_sampling", "gpt2_strerror")
+            "gpt2_op_head_argmax", "gpt2_op_head_argmax_noalloc", "gpt2_set_sampling", "gpt2_set_wait_limit",
+            "gpt2_strerror")
 
 
 class GPT2Error(RuntimeError):
@@ -114,6 +115,7 @@ def lib(build_if_stale: bool = True, path: str = None):
             L.gpt2_op_head_argmax.argtypes = [vp, vp, vp, f32, vp, i32, i32, vp, vp, vp, sz, vp]
             L.gpt2_op_head_argmax_noalloc.argtypes = [vp, vp, vp, f32, vp, i32, i32, vp, vp, vp]
             L.gpt2_set_sampling.argtypes = [vp, f32, ctypes.c_uint64]
+            L.gpt2_set_wait_limit.argtypes = [vp, ctypes.c_uint64]
             L.gpt2_strerror.argtypes = [ctypes.c_int]
             L.gpt2_strerror.restype = ctypes.c_char_p
             for n in EXPORTED:
@@ -161,9 +163,8 @@ class Model:
 
     def __init__(self, cfg, dev_weights: dict, wdtype: str = "f32", stream=None, path: str = "auto",
                  head: str = "f32"):
-        """path: "auto" (cluster kernel where possible, else the persistent
-        kernel, else the per-kernel graph), "persistent" (skip the cluster
-        kernel) or "per_kernel".  head: "f32" (the tied wte), "f16" or "int4" (a
+        """path: "auto" (the cluster kernel where possible, else the per-kernel
+        graph) or "per_kernel".  head: "f32" (the tied wte), "f16" or "int4" (a
         copy for the LM head, GPT2_FLAG_HEAD_F16 / _INT4; cluster kernel only)."""
         L = lib()
         self.cfg = cfg
@@ -178,7 +179,7 @@ class Model:
                     dev_weights["ln_f_w"].data_ptr(), dev_weights["ln_f_b"].data_ptr(),
                     ctypes.cast(layers, ctypes.POINTER(LayerWeights)))
         h = ctypes.c_void_p()
-        flags = {"auto": 0, "persistent": 2, "per_kernel": 1}[path] | {"f32": 0, "f16": 4, "int4": 8}[head]
+        flags = {"auto": 0, "per_kernel": 1}[path] | {"f32": 0, "f16": 4, "int4": 8}[head]
         check(L.gpt2_create_ex(ctypes.byref(c), ctypes.byref(w), WDTYPES[wdtype], flags,
                                _stream_handle(stream), ctypes.byref(h)), "gpt2_create_ex")
         self._h = h
@@ -209,6 +210,9 @@ class Model:
 
     def set_sampling(self, temperature: float, seed: int = 0):
         check(lib().gpt2_set_sampling(self._h, float(temperature), int(seed) & (2**64 - 1)), "gpt2_set_sampling")
+
+    def set_wait_limit(self, ns: int):
+        check(lib().gpt2_set_wait_limit(self._h, int(ns)), "gpt2_set_wait_limit")
 
     def generate(self, prompt, n_steps: int) -> list:
         p = np.ascontiguousarray(prompt, np.int32)
@@ -264,7 +268,7 @@ class Model:
     def path(self) -> str:
         p = ctypes.c_int32()
         check(lib().gpt2_path(self._h, ctypes.byref(p)), "gpt2_path")
-        return {0: "per_kernel", 1: "persistent", 2: "cluster"}[p.value]
+        return {0: "per_kernel", 2: "cluster"}[p.value]
 
     def launch_count(self) -> int:
         n = ctypes.c_uint64()
@@ -321,3 +325,4 @@ def op_head_argmax_noalloc(x, ln_w, ln_b, eps: float, wte, logits, token, stream
     check(lib().gpt2_op_head_argmax_noalloc(_ptr(x), _ptr(ln_w), _ptr(ln_b), float(eps), _ptr(wte), V, E,
                                             _ptr(logits), _ptr(token), _stream_handle(stream)),
           "gpt2_op_head_argmax_noalloc")
+

@@ -13,7 +13,6 @@
 #include "cluster.h"
 #include "common.cuh"
 #include "kernels.h"
-#include "persistent.h"
 
 using namespace gpt2;
 
@@ -32,13 +31,6 @@ struct LayerDev {
     QMat mat[4];   // GPT2_MAT_ATTN, _PROJ, _FC, _MLP_PROJ
 };
 
-int env_int(const char *name, int dflt)
-{
-    const char *v = std::getenv(name);
-    if (!v || !*v) return dflt;
-    return std::atoi(v);
-}
-
 }  // namespace
 
 struct gpt2_model {
@@ -47,7 +39,6 @@ struct gpt2_model {
     cudaStream_t stream = nullptr;
     int device = 0;
     int num_sms = 0;
-    bool pdl = true;
     // device memory
     uint8_t *arena = nullptr;        // weights
     size_t arena_bytes = 0;
@@ -67,17 +58,9 @@ struct gpt2_model {
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
     int kernels_per_step = 0;
-    // persistent path
-    bool persistent = false;
-    PPhase *d_phases = nullptr;
-    int32_t *prompt_buf = nullptr;
-    uint64_t *ll_base = nullptr;
-    size_t ll_bytes = 0;
-    PersistArgs pargs{};
-    int p_grid = 0;
-    size_t p_smem = 0;
-    // cluster path (uses the prompt buffer of the persistent path)
+    // cluster path: one cooperative launch per call
     bool cluster = false;
+    int32_t *prompt_buf = nullptr;
     bool head_f16 = false;           // GPT2_FLAG_HEAD_F16: the LM head reads an fp16 copy of wte
     bool head_int4 = false;          // GPT2_FLAG_HEAD_INT4: ... or a grouped int4 copy
     uint8_t *cbuf = nullptr;         // tiled matrices, fp16 head, sums, keys, layer table
@@ -95,6 +78,10 @@ struct gpt2_model {
 namespace {
 
 constexpr size_t kAlign = 256;
+// Per-kernel graph path: shared-memory stage budget and stages in flight of
+// each GEMV launch (measured on GB300: 96 KB in up to 4 stages).
+constexpr size_t kGraphStageBudget = 96 * 1024;
+constexpr int kGraphMaxStages = 4;
 size_t aup(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 size_t main_bytes_of(int wdtype, int in, int out)
@@ -167,13 +154,13 @@ int record_pass(gpt2_model *m, cudaStream_t s)
 {
     const gpt2_config &c = m->cfg;
     const int E = c.n_embd, H = c.n_head, D = E / H, P = c.n_positions;
-    const size_t budget = size_t(env_int("GPT2_STAGE_KB", 96)) * 1024;
-    const int max_stages = env_int("GPT2_MAX_STAGES", 4);
+    const size_t budget = kGraphStageBudget;
+    const int max_stages = kGraphMaxStages;
     const int ctas = m->num_sms;
     int kernels = 0;
     bool first = true;
     auto pdl = [&]() {
-        bool p = m->pdl && !first;
+        bool p = !first;
         first = false;
         return p;
     };
@@ -304,250 +291,43 @@ int read_state(gpt2_model *m, DeviceState *hs)
         // report once, then clear so the model stays usable: the error word,
         // the abort word, and every tagged activation (stale epochs)
         TRY_CUDA(cudaMemset(&m->st->err, 0, 3 * sizeof(int32_t)));
-        if (m->ll_base) TRY_CUDA(cudaMemset(m->ll_base, 0, m->ll_bytes));
         if (m->cluster) {   // sums and counters restart with the sequence
             const int32_t one = 1;
             TRY_CUDA(cudaMemset(m->c_state, 0, m->c_state_bytes));
             TRY_CUDA(cudaMemcpy(&m->st->seq, &one, sizeof one, cudaMemcpyHostToDevice));
         }
-        return err == kDevErrTimeout ? GPT2_ERR_TIMEOUT : GPT2_ERR_DEVICE_STATE;
+        return err == kDevErrTimeout ? GPT2_ERR_TIMEOUT : err == kDevErrRange ? GPT2_ERR_RANGE : GPT2_ERR_DEVICE_STATE;
     }
     return GPT2_OK;
 }
 
-int launch_persist(gpt2_model *m, int n_steps, const int32_t *prompt, int n_prompt, int tok_first, int pos0)
+// One launch of the cluster kernel running n_steps passes.
+int launch_cluster_call(gpt2_model *m, int n_steps, const int32_t *prompt, int n_prompt, int tok_first, int pos0)
 {
-    PersistArgs a = m->pargs;
-    a.n_steps = n_steps;
-    a.prompt = prompt;
-    a.n_prompt = n_prompt;
-    a.tok_first = tok_first;
-    a.pos0 = pos0;
-    if (m->cluster) {
-        ClusterArgs c = m->cargs;
-        c.n_steps = n_steps;
-        c.prompt = prompt;
-        c.n_prompt = n_prompt;
-        c.tok_first = tok_first;
-        c.pos0 = pos0;
-        TRY_CUDA(launch_cluster(m->wdtype, c, m->c_clusters, m->c_smem, m->stream));
-    } else {
-        TRY_CUDA(launch_persistent(m->wdtype, a, m->p_grid, m->p_smem, m->stream));
-    }
+    ClusterArgs c = m->cargs;
+    c.n_steps = n_steps;
+    c.prompt = prompt;
+    c.n_prompt = n_prompt;
+    c.tok_first = tok_first;
+    c.pos0 = pos0;
+    TRY_CUDA(launch_cluster(m->wdtype, c, m->c_clusters, m->c_smem, m->stream));
     m->launches += 1;
     return GPT2_OK;
 }
 
 int launch_step(gpt2_model *m, int32_t token, int32_t position)
 {
-    if (m->persistent) return launch_persist(m, 1, nullptr, 1, token, position);
+    if (m->cluster) return launch_cluster_call(m, 1, nullptr, 1, token, position);
     TRY_CUDA(launch_set_state(m->st, token, position, kSetTokPos, m->out_ids, m->stream));
     TRY_CUDA(cudaGraphLaunch(m->exec, m->stream));
     m->launches += 1 + m->kernels_per_step;
     return GPT2_OK;
 }
 
-// Rows of each CTA and rows per ring stage of one persistent GEMV phase.
-void plan_phase(PPhase &ph, int wtype, int grid, uint32_t stage)
-{
-    const int gran = wtype == kWI4 ? 8 : 1;
-    int rpc = (ph.out + grid - 1) / grid;
-    rpc = (rpc + gran - 1) / gran * gran;
-    ph.rpc = rpc;
-    const uint32_t rb = wtype == kWF32 ? uint32_t(ph.in) * 4 : wtype == kWF16 ? uint32_t(ph.in) * 2 : uint32_t(ph.in) / 2;
-    const uint32_t G = uint32_t(ph.in) / 32, zb = uint32_t(ph.in) / 64;
-    auto a16 = [](uint32_t v) { return (v + 15u) / 16u * 16u; };
-    int chunk = std::max(gran, std::min(std::min(rpc, 8), int(stage / std::max(1u, rb)) / gran * gran));
-    for (;; chunk -= gran) {
-        uint32_t total;
-        if (wtype == kWI4) {
-            ph.stage_scale_off = a16(uint32_t(chunk) * rb);
-            ph.stage_zero_off = ph.stage_scale_off + a16(uint32_t(chunk) * G * 4);
-            total = ph.stage_zero_off + uint32_t(chunk) * zb;
-        } else {
-            ph.stage_scale_off = ph.stage_zero_off = 0;
-            total = uint32_t(chunk) * rb;
-        }
-        if (total <= stage || chunk <= gran) break;
-    }
-    ph.chunk_rows = chunk;
-}
-
-// Builds the phase table and launch arguments of the persistent kernel;
-// returns GPT2_OK, or a nonzero status if the path cannot run here (the
-// caller then uses the per-kernel path).
-int setup_persistent(gpt2_model *m, uint64_t *ll, int32_t *prompt_buf, PPhase *d_phases, float *fold)
-{
-    const gpt2_config &c = m->cfg;
-    const int L = c.n_layer, E = c.n_embd, H = c.n_head, D = E / H, V = c.vocab_size;
-    if (E > 4096) return GPT2_ERR_INVALID_ARG;        // LayerNorm pairs held in registers
-    const int F = 4 * E;
-    const uint32_t max_row = m->wdtype == GPT2_F32 ? uint32_t(F) * 4 : m->wdtype == GPT2_F16 ? uint32_t(F) * 2
-                                                                         : 8u * (uint32_t(F) / 2 + uint32_t(F) / 8 + uint32_t(F) / 64 + 32);
-    uint32_t stage = uint32_t(std::max(8, env_int("GPT2_P_STAGE_KB", 24))) * 1024u;
-    stage = std::max(stage, std::max(max_row, uint32_t(E) * 4));
-    stage = (stage + 127u) / 128u * 128u;
-    const int grid = m->num_sms;
-    std::vector<PPhase> ph;
-    ph.reserve(5 * L + 1);
-    int max_rows = 1;
-    for (int l = 0; l < L; ++l) {
-        const LayerDev &Ld = m->layers[l];
-        auto gemv = [&](int mode, const QMat &q, int in_buf, int in_src, int out_buf, const float *lw,
-                        const float *lb, const float *bias, float *c1) {
-            PPhase p{};
-            p.type = kPhGemv;
-            p.mode = mode;
-            p.layer = l;
-            p.in = q.in;
-            p.out = q.out;
-            p.in_buf = in_buf;
-            p.in_src = in_src;
-            p.out_buf = out_buf;
-            p.W = q.w;
-            p.scales = q.scales;
-            p.zeros = q.zeros;
-            p.ln_w = lw;
-            p.ln_b = lb;
-            p.bias = bias;
-            p.c1 = c1;
-            p.c2 = c1 ? c1 + q.out : nullptr;
-            plan_phase(p, m->wdtype, grid, stage);
-            max_rows = std::max(max_rows, p.rpc);
-            ph.push_back(p);
-        };
-        const int base = 5 * l;
-        float *fq = fold + size_t(l) * (3 * E + 4 * E) * 2, *ff = fq + 2 * 3 * E;
-        gemv(l == 0 ? kModeEmbLnBias : kModeLnBias, Ld.mat[GPT2_MAT_ATTN], kBufXA, l == 0 ? -1 : base - 1, kBufQKV,
-             Ld.ln1_w, Ld.ln1_b, Ld.attn_b, fq);
-        PPhase at{};
-        at.type = kPhAttn;
-        at.layer = l;
-        at.in_buf = kBufQKV;
-        at.in_src = base;
-        at.out_buf = kBufATT;
-        ph.push_back(at);
-        gemv(kModeBiasRes, Ld.mat[GPT2_MAT_PROJ], kBufATT, base + 1, kBufXB, nullptr, nullptr, Ld.proj_b, nullptr);
-        gemv(kModeLnBiasGelu, Ld.mat[GPT2_MAT_FC], kBufXB, base + 2, kBufH, Ld.ln2_w, Ld.ln2_b, Ld.fc_b, ff);
-        gemv(kModeBiasRes, Ld.mat[GPT2_MAT_MLP_PROJ], kBufH, base + 3, kBufXA, nullptr, nullptr, Ld.mlp_proj_b,
-             nullptr);
-    }
-    PPhase hd{};
-    hd.type = kPhHead;
-    hd.mode = kModeHead;
-    hd.layer = L;
-    hd.in = E;
-    hd.out = V;
-    hd.in_buf = kBufXA;
-    hd.in_src = 5 * L - 1;
-    hd.out_buf = -1;
-    hd.W = m->wte;
-    hd.ln_w = m->lnf_w;
-    hd.ln_b = m->lnf_b;
-    plan_phase(hd, kWF32, grid, stage);
-    ph.push_back(hd);
-    if (ph.size() > 63) return GPT2_ERR_INVALID_ARG;   // epochs keep the phase in 6 bits
-    // every shared-memory segment before the attention scratch stays 16-byte
-    // aligned (the query is read as float4): round the bias slots to 4
-    max_rows = (max_rows + 3) / 4 * 4;
-    if (max_rows > 512) return GPT2_ERR_INVALID_ARG;   // two bias slots per consumer thread
-    // a stage holds at least one chunk of every phase
-    for (const PPhase &p : ph) {
-        if (p.type == kPhAttn) continue;
-        const int wt = p.type == kPhHead ? int(kWF32) : m->wdtype;
-        const uint32_t rb = wt == kWF32 ? uint32_t(p.in) * 4 : wt == kWF16 ? uint32_t(p.in) * 2 : uint32_t(p.in) / 2;
-        uint32_t need = uint32_t(p.chunk_rows) * rb;
-        if (wt == kWI4) need = p.stage_zero_off + uint32_t(p.chunk_rows) * uint32_t(p.in / 64);
-        if (need > stage) return GPT2_ERR_INVALID_ARG;
-    }
-
-    PersistArgs &a = m->pargs;
-    a = PersistArgs{};
-    a.phases = d_phases;
-    a.n_phases = int(ph.size());
-    for (int b = 0; b < kNumLL; ++b) a.ll[b] = nullptr;
-    a.ll[kBufXA] = ll;
-    a.ll[kBufXB] = ll + E;
-    a.ll[kBufQKV] = ll + 2 * E;
-    a.ll[kBufATT] = ll + 5 * E;
-    a.ll[kBufH] = ll + 6 * E;
-    a.ll_tok = ll + 10 * E;
-    a.kcache = m->kcache;
-    a.vcache = m->vcache;
-    a.logits = m->logits;
-    a.partials = m->partials;
-    a.counter = m->counter;
-    a.out_ids = m->out_ids;
-    a.out_cap = m->out_cap;
-    a.st = m->st;
-    a.wte = m->wte;
-    a.wpe = m->wpe;
-    a.E = E;
-    a.H = H;
-    a.D = D;
-    a.P = c.n_positions;
-    a.V = V;
-    a.scale = float(1.0 / std::sqrt(double(D)));
-    a.eps = c.ln_eps;
-    a.max_rows = max_rows;
-    a.stage_bytes = stage;
-    {
-        const char *fr = std::getenv("GPT2_HEAD_L2_FRAC");
-        float f = fr ? float(std::atof(fr)) : 0.0f;   // measured: no gain on GB300, off by default
-        a.head_l2_frac = f < 0.f ? 0.f : (f > 1.f ? 1.f : f);
-    }
-    a.block_mode = env_int("GPT2_BLOCK_MODE", 0) ? 1 : 0;
-    const size_t fixed = persistent_fixed_smem(E, D, max_rows);
-    a.ring_offset = uint32_t((fixed + 127) / 128 * 128);
-    int optin = 0;
-    TRY_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, m->device));
-    const size_t limit = size_t(optin) - 4096;       // leave room for static shared memory
-    if (a.ring_offset + 2 * size_t(stage) > limit) return GPT2_ERR_INVALID_ARG;
-    int ns = int((limit - a.ring_offset) / stage);
-    ns = std::min(ns, std::min(kMaxRing, std::max(2, env_int("GPT2_P_STAGES", kMaxRing))));
-    if (ns < 5) return GPT2_ERR_INVALID_ARG;   // a warp holds up to 4 stages at once; one more keeps the stream going
-    a.n_stages = ns;
-    m->p_smem = a.ring_offset + size_t(ns) * stage;
-    int blocks = 0;
-    TRY_CUDA(persistent_blocks_per_sm(m->wdtype, D, m->p_smem, limit, &blocks));
-    if (blocks < 1) return GPT2_ERR_INVALID_ARG;
-    int coop = 0;
-    TRY_CUDA(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, m->device));
-    if (!coop) return GPT2_ERR_UNSUPPORTED_DEVICE;
-    // block phases hold their whole row slice: at most kMaxBlockRows rows, in stages that fit the ring
-    for (const PPhase &p : ph) {
-        if (p.type != kPhGemv) continue;
-        if (p.rpc > kMaxBlockRows) return GPT2_ERR_INVALID_ARG;
-        if ((p.rpc + p.chunk_rows - 1) / p.chunk_rows > ns - 1) return GPT2_ERR_INVALID_ARG;
-    }
-    // LayerNorm folded into the QKV and fc matrices, from the weights as stored
-    {
-        float *tmp = nullptr;
-        TRY_CUDA(cudaMalloc(&tmp, size_t(4 * E) * E * 4));
-        cudaError_t e = cudaSuccess;
-        for (const PPhase &p : ph) {
-            if (p.type != kPhGemv || !p.c1 || e != cudaSuccess) continue;
-            e = dequant_to_f32(m->wdtype, p.W, p.scales, p.zeros, p.in, p.out, tmp, m->stream);
-            if (e == cudaSuccess) e = ln_fold(tmp, p.ln_w, p.ln_b, p.in, p.out, const_cast<float *>(p.c1),
-                                              const_cast<float *>(p.c2), m->stream);
-        }
-        if (e == cudaSuccess) e = cudaStreamSynchronize(m->stream);
-        cudaFree(tmp);
-        TRY_CUDA(e);
-    }
-    m->p_grid = grid;
-    TRY_CUDA(cudaMemcpy(d_phases, ph.data(), ph.size() * sizeof(PPhase), cudaMemcpyHostToDevice));
-    m->d_phases = d_phases;
-    m->prompt_buf = prompt_buf;
-    m->ll_base = ll;
-    m->persistent = true;
-    return GPT2_OK;
-}
-
 // Sets up the cluster decode kernel (cluster.cu): tiled copies of the two
 // projection matrices, the fixed-point sums and their counters, and the
 // launch shape.  Returns GPT2_OK, or a nonzero status if the path cannot run
-// here (the caller then keeps the persistent kernel).
+// here (the caller then keeps the per-kernel graph).
 int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
 {
     const gpt2_config &c = m->cfg;
@@ -576,6 +356,9 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
     const int fr = F / nfc;
     const int n_clusters = H + nfc / kClusterSize, grid = n_clusters * kClusterSize;
     if (grid > 256) return GPT2_ERR_INVALID_ARG;   // each consumer thread polls one CTA's LM-head key
+    // a residual-sum word counts its contributions in 8 bits (bits 56..63):
+    // one per head cluster (x after attention), one per fc cluster (x after the MLP)
+    if (H > 255 || nfc / kClusterSize > 255) return GPT2_ERR_INVALID_ARG;
     if (V > (1 << 17)) return GPT2_ERR_INVALID_ARG;   // tagged keys keep 17 bits of the id
     // LM-head rows per CTA: a multiple of 4 (of 8 for an int4 head, whose shares are padded)
     const int head_rpc = m->head_int4 ? ((V + grid - 1) / grid + 7) / 8 * 8 : ((V + grid - 1) / grid + 3) / 4 * 4;
@@ -818,10 +601,10 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
     a.n_stages = ns;
     a.stage_bytes = stage;
     a.ring_offset = ring_offset;
+    a.wait_ns = kWaitLimitNs;
     m->c_clusters = n_clusters;
     m->prompt_buf = prompt_buf;
     m->cluster = true;
-    m->persistent = true;   // one launch per call, like the persistent kernel
     return GPT2_OK;
 }
 
@@ -842,6 +625,7 @@ const char *gpt2_strerror(int status)
     case GPT2_ERR_TIMEOUT: return "a bounded device wait timed out";
     case GPT2_ERR_DEVICE_STATE: return "a kernel rejected its device-side inputs";
     case GPT2_ERR_OUT_OF_MEMORY: return "device out of memory";
+    case GPT2_ERR_RANGE: return "an activation left the range of the fixed-point residual sums";
     default: return "unknown status";
     }
 }
@@ -859,7 +643,7 @@ int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype
     int rc = check_config(cfg, wdtype);
     if (rc != GPT2_OK) return rc;
     if (!w || !w->layers) return GPT2_ERR_INVALID_ARG;
-    if (flags & ~int32_t(GPT2_FLAG_PER_KERNEL | GPT2_FLAG_NO_CLUSTER | GPT2_FLAG_HEAD_F16 | GPT2_FLAG_HEAD_INT4))
+    if (flags & ~int32_t(GPT2_FLAG_PER_KERNEL | GPT2_FLAG_HEAD_F16 | GPT2_FLAG_HEAD_INT4))
         return GPT2_ERR_INVALID_ARG;
     if ((flags & GPT2_FLAG_HEAD_F16) && (flags & GPT2_FLAG_HEAD_INT4)) return GPT2_ERR_INVALID_ARG;
     int dev;
@@ -889,9 +673,7 @@ int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype
     m->stream = static_cast<cudaStream_t>(stream);
     m->device = dev;
     m->num_sms = prop.multiProcessorCount;
-    m->pdl = env_int("GPT2_NO_PDL", 0) == 0;
-    m->max_head_ctas = m->num_sms * std::max(1, env_int("GPT2_HEAD_CTAS_PER_SM", 1));
-    if (m->max_head_ctas > 1024) m->max_head_ctas = 1024;
+    m->max_head_ctas = std::min(m->num_sms, 1024);
 
     const int L = cfg->n_layer, E = cfg->n_embd, H = cfg->n_head, P = cfg->n_positions, V = cfg->vocab_size;
     const int F = 4 * E;
@@ -941,11 +723,7 @@ int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype
     const size_t o_ids = take(size_t(m->out_cap) * 4);
     const size_t o_part = take(size_t(m->max_head_ctas) * 8);
     const size_t o_cnt = take(16);
-    const size_t ll_bytes = (size_t(10) * E + 1) * 8;
-    const size_t o_ll = take(ll_bytes);
     const size_t o_prompt = take(size_t(P) * 4);
-    const size_t o_phases = take(size_t(5 * L + 1) * sizeof(PPhase));
-    const size_t o_fold = take(size_t(L) * (3 * E + 4 * E) * 2 * 4);
     m->work_bytes = off;
 
     cudaError_t e = cudaMalloc(&m->arena, m->arena_bytes);
@@ -1046,34 +824,13 @@ int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype
         free_model(m);
         return rc;
     }
-    const char *path = std::getenv("GPT2_PATH");
-    const bool want_persistent = !(flags & GPT2_FLAG_PER_KERNEL) && !(path && std::strcmp(path, "graph") == 0);
-    const bool want_cluster = want_persistent && !(flags & GPT2_FLAG_NO_CLUSTER) &&
-                              !(path && std::strcmp(path, "persistent") == 0);
-    if (want_cluster) {
+    if (!(flags & GPT2_FLAG_PER_KERNEL)) {
         rc = setup_cluster(m, reinterpret_cast<int32_t *>(W + o_prompt));
-        if (rc != GPT2_OK) {            // keep the persistent kernel
-            if (env_int("GPT2_DEBUG", 0))
-                std::fprintf(stderr, "gpt2: cluster path unavailable (%s: %s)\n", gpt2_strerror(rc),
-                             cudaGetErrorString(cudaGetLastError()));
+        if (rc != GPT2_OK) {            // the per-kernel graph computes the pass instead
             cudaGetLastError();
             if (m->cbuf) cudaFree(m->cbuf);
             m->cbuf = nullptr;
             m->cluster = false;
-            m->persistent = false;
-        }
-    }
-    if (want_persistent && !m->cluster) {
-        m->ll_bytes = ll_bytes;
-        rc = setup_persistent(m, reinterpret_cast<uint64_t *>(W + o_ll), reinterpret_cast<int32_t *>(W + o_prompt),
-                              reinterpret_cast<PPhase *>(W + o_phases), reinterpret_cast<float *>(W + o_fold));
-        if (rc != GPT2_OK) {            // fall back to the per-kernel graph (another GPU path)
-            if (env_int("GPT2_DEBUG", 0))
-                std::fprintf(stderr, "gpt2: persistent path unavailable (%s: %s)\n", gpt2_strerror(rc),
-                             cudaGetErrorString(cudaGetLastError()));
-            cudaGetLastError();
-            m->persistent = false;
-            m->ll_base = nullptr;
         }
     }
     if ((m->head_f16 || m->head_int4) && !m->cluster) {   // a separate head is read only by the cluster kernel
@@ -1108,6 +865,14 @@ int gpt2_set_sampling(gpt2_model *m, float temperature, uint64_t seed)
     return GPT2_OK;
 }
 
+int gpt2_set_wait_limit(gpt2_model *m, uint64_t ns)
+{
+    if (!m) return GPT2_ERR_INVALID_ARG;
+    if (!m->cluster) return GPT2_ERR_INVALID_ARG;   // the per-kernel graph has no cross-CTA waits
+    m->cargs.wait_ns = (unsigned long long)ns;
+    return GPT2_OK;
+}
+
 int gpt2_reset(gpt2_model *m)
 {
     if (!m) return GPT2_ERR_INVALID_ARG;
@@ -1136,9 +901,9 @@ int gpt2_prefill(gpt2_model *m, const int32_t *host_ids, int32_t n)
     for (int i = 0; i < n; ++i)
         if (host_ids[i] < 0 || host_ids[i] >= m->cfg.vocab_size) return GPT2_ERR_TOKEN_RANGE;
     gpt2_reset(m);
-    if (m->persistent) {
+    if (m->cluster) {
         TRY_CUDA(cudaMemcpyAsync(m->prompt_buf, host_ids, size_t(n) * 4, cudaMemcpyHostToDevice, m->stream));
-        int rc = launch_persist(m, n, m->prompt_buf, n, 0, 0);
+        int rc = launch_cluster_call(m, n, m->prompt_buf, n, 0, 0);
         if (rc != GPT2_OK) return rc;
         m->cached = n;
         m->has_step = true;
@@ -1168,8 +933,8 @@ int gpt2_decode_greedy(gpt2_model *m, int32_t n_steps)
     if (!m->has_step) return GPT2_ERR_NOT_READY;
     if ((long long)m->cached + n_steps > m->cfg.n_positions) return GPT2_ERR_POSITION_RANGE;
     if (n_steps == 0) return GPT2_OK;
-    if (m->persistent) {
-        int rc = launch_persist(m, n_steps, nullptr, 0, 0, m->cached);
+    if (m->cluster) {
+        int rc = launch_cluster_call(m, n_steps, nullptr, 0, 0, m->cached);
         if (rc != GPT2_OK) return rc;
     } else {
         for (int i = 0; i < n_steps; ++i) TRY_CUDA(cudaGraphLaunch(m->exec, m->stream));
@@ -1187,12 +952,12 @@ int gpt2_generate(gpt2_model *m, const int32_t *host_prompt, int32_t n_prompt, i
     for (int i = 0; i < n_prompt; ++i)
         if (host_prompt[i] < 0 || host_prompt[i] >= m->cfg.vocab_size) return GPT2_ERR_TOKEN_RANGE;
     int rc;
-    if (m->persistent) {
+    if (m->cluster) {
         gpt2_reset(m);
         TRY_CUDA(launch_set_state(m->st, 0, 0, kResetOut, m->out_ids, m->stream));
         TRY_CUDA(cudaMemcpyAsync(m->prompt_buf, host_prompt, size_t(n_prompt) * 4, cudaMemcpyHostToDevice,
                                  m->stream));
-        rc = launch_persist(m, n_prompt + n_steps, m->prompt_buf, n_prompt, 0, 0);
+        rc = launch_cluster_call(m, n_prompt + n_steps, m->prompt_buf, n_prompt, 0, 0);
         if (rc != GPT2_OK) return rc;
         m->launches += 1;
         m->cached = n_prompt + n_steps;
@@ -1280,7 +1045,7 @@ int gpt2_export_kv(gpt2_model *m, int32_t layer, int32_t n_rows, float *dst_k, f
 int gpt2_kernels_per_step(const gpt2_model *m, int32_t *count)
 {
     if (!m || !count) return GPT2_ERR_INVALID_ARG;
-    *count = m->persistent ? 1 : m->kernels_per_step;
+    *count = m->cluster ? 1 : m->kernels_per_step;
     return GPT2_OK;
 }
 
@@ -1294,7 +1059,7 @@ int gpt2_launch_count(const gpt2_model *m, uint64_t *count)
 int gpt2_path(const gpt2_model *m, int32_t *path)
 {
     if (!m || !path) return GPT2_ERR_INVALID_ARG;
-    *path = m->cluster ? GPT2_PATH_CLUSTER : m->persistent ? GPT2_PATH_PERSISTENT : GPT2_PATH_PER_KERNEL;
+    *path = m->cluster ? GPT2_PATH_CLUSTER : GPT2_PATH_PER_KERNEL;
     return GPT2_OK;
 }
 

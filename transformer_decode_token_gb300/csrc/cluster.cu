@@ -81,8 +81,11 @@ constexpr int kCRing = kClusterRing;
 // number of contributions above.  A reader polls its words until the count
 // is complete: the data is its own arrival flag (one L2 round trip, no
 // counter, no release fence), and integer addition makes the sum independent
-// of the order of the atomics.  |v| < 2^16 keeps each term inside its field
-// (values are clamped there); 2^15 contributions fit.
+// of the order of the atomics.  |v| <= kFixLimit < 2^16 keeps each term in
+// [0, 2^41), so the low field holds 2^15 terms; the count field (bits 56..63)
+// holds at most 255 contributions, which bounds the contributors of one sum
+// (the host checks it).  A value outside the limit (or NaN) is clamped and
+// recorded as a range error, never silently summed.
 constexpr float kFixScale = 16777216.0f;              // 2^24
 constexpr float kFixLimit = 65000.0f;
 constexpr unsigned long long kFixBias = 1ull << 40;
@@ -172,7 +175,7 @@ __device__ __forceinline__ void red_add_i64(long long *p, long long v)
 }
 __device__ __forceinline__ unsigned long long to_word(float v)
 {
-    v = fminf(fmaxf(v, -kFixLimit), kFixLimit);
+    v = fminf(fmaxf(v, -kFixLimit), kFixLimit);   // (fmaxf maps NaN to -kFixLimit)
     return (unsigned long long)(__float2ll_rn(v * kFixScale) + (long long)kFixBias) + (1ull << kCountShift);
 }
 __device__ __forceinline__ int word_count(unsigned long long w) { return int(w >> kCountShift); }
@@ -215,13 +218,19 @@ __device__ __forceinline__ void raise_abort(const ClusterArgs &a, int info)
 }
 
 // One step of a bounded spin: false once the spin must end (abort or timeout).
+// A limit of 0 lets no wait spin: the first one that does not succeed at
+// once gives up (the test of the abort path).
 __device__ __forceinline__ bool keep_waiting(const ClusterArgs &a, Waiter &w, int info)
 {
+    if (a.wait_ns == 0) {
+        raise_abort(a, info);
+        return false;
+    }
     if ((++w.it & 127u) != 0) return true;
     if (aborted(a)) return false;
     const unsigned long long t = global_ns();
     if (w.t0 == 0) w.t0 = t;
-    else if (t - w.t0 > kWaitLimitNs) {
+    else if (t - w.t0 > a.wait_ns) {
         raise_abort(a, info);
         return false;
     }
@@ -565,6 +574,10 @@ __device__ __forceinline__ float4 mul4(const float4 &a, const float4 &b)
 {
     return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w);
 }
+__device__ __forceinline__ float4 sub4(const float4 &a, float k)
+{
+    return make_float4(a.x - k, a.y - k, a.z - k, a.w - k);
+}
 
 // Shifted sum and sum of squares of 4 values (LayerNorm statistics).
 __device__ __forceinline__ void stat4(const float4 &v, float k, float &s, float &q)
@@ -708,8 +721,8 @@ __device__ __forceinline__ float sample_score(float logit, float temperature, un
 template <int WT, bool LN, int RG>
 __device__ __forceinline__ void canon_groups(const ClusterArgs &a, const CS &c, const Geo &g, uint32_t k, int w0,
                                              int w1, int units, const float4 (&xr)[UnitOf<WT>::kPL * UnitOf<WT>::kF4],
-                                             bool &have_stats, float ssum, float ssq, float shift, int in,
-                                             float &mean, float &rstd, const float *c1, const float *cb, float *out,
+                                             bool &have_stats, float ssum, float ssq, int in,
+                                             float &dmean, float &rstd, const float *c1, const float *cb, float *out,
                                              int logit_row0, unsigned long long &best, long long sample_k0)
 {
     constexpr int kF4 = UnitOf<WT>::kF4;
@@ -742,16 +755,15 @@ __device__ __forceinline__ void canon_groups(const ClusterArgs &a, const CS &c, 
                 ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
             }
             const float inv = 1.0f / float(in);
-            const float ms = ssum * inv;
-            mean = shift + ms;
-            rstd = rsqrtf(fmaxf(fmaf(ssq, inv, -ms * ms), 0.f) + a.eps);
+            dmean = ssum * inv;   // mean - shift
+            rstd = rsqrtf(fmaxf(fmaf(ssq, inv, -dmean * dmean), 0.f) + a.eps);
             have_stats = true;
         }
         float t = warp_sum_rows<RG>(acc, lane);
         const int jr = group_row<RG>(lane);
         if (group_writer<RG>(lane) && jr < ng) {
             const int i = g0 + jr;
-            if (LN) t = rstd * fmaf(-mean, c1[i], t) + cb[i];
+            if (LN) t = rstd * fmaf(-dmean, c1[i], t) + cb[i];
             if (logit_row0 >= 0) {
                 if (logit_row0 + i < a.V) {   // (rows >= V: padding of an int4 head)
                     a.logits[logit_row0 + i] = t;
@@ -778,7 +790,10 @@ __device__ __forceinline__ void canon_groups(const ClusterArgs &a, const CS &c, 
 // (logit_row0 >= 0), to the logits and this thread's argmax key.
 //
 // LN: the LayerNorm before the rows is folded into them (see CLayer): each
-// result is rstd * (W.(gamma*x) - mean * c1[i]) + cb[i].
+// result is rstd * (W.(gamma*(x - s)) - (mean - s) * c1[i]) + cb[i], with the
+// shift s = x[0].  Centring on s keeps the two terms of the difference small
+// when the residual stream has a large common offset (|mean| >> std):
+// |mean - s| <= sqrt(n) * std for any x, so the cancellation is bounded.
 // The rows of a window that warp `warp` takes: [w0, w1).
 __device__ __forceinline__ void warp_rows(const Geo &g, int q0, int q1, int &w0, int &w1, int &per)
 {
@@ -814,7 +829,7 @@ __device__ __forceinline__ void canon_rows(const ClusterArgs &a, CS &c, const Ge
     const int units = in / UnitOf<WT>::kIn;
     const uint32_t xa = smem_addr(xin), ga = smem_addr(gamma);
     float4 xr[UnitOf<WT>::kPL * kF4];
-    float mean = 0.f, rstd = 0.f;
+    float dmean = 0.f, rstd = 0.f;
     const float shift = LN ? xin[0] : 0.f;
     float ssum = 0.f, ssq = 0.f;   // this lane's share of the LayerNorm statistics
     {
@@ -831,7 +846,7 @@ __device__ __forceinline__ void canon_rows(const ClusterArgs &a, CS &c, const Ge
                     if (LN) {
                         if ((m * kF4 + f) & 1) stat4(v, shift, s1, q1s);
                         else stat4(v, shift, ssum, ssq);
-                        v = mul4(v, lds_f4(ga + off));
+                        v = mul4(sub4(v, shift), lds_f4(ga + off));
                     }
                 }
                 xr[m * kF4 + f] = v;
@@ -854,10 +869,10 @@ __device__ __forceinline__ void canon_rows(const ClusterArgs &a, CS &c, const Ge
         CSUB(1);
         if (ok && w0 < w1) {
             if (per <= 4)
-                canon_groups<WT, LN, 4>(a, c, g, k, w0, w1, units, xr, have_stats, ssum, ssq, shift, in, mean, rstd,
+                canon_groups<WT, LN, 4>(a, c, g, k, w0, w1, units, xr, have_stats, ssum, ssq, in, dmean, rstd,
                                         c1, cb, out, logit_row0, best, sample_k0);
             else
-                canon_groups<WT, LN, 6>(a, c, g, k, w0, w1, units, xr, have_stats, ssum, ssq, shift, in, mean, rstd,
+                canon_groups<WT, LN, 6>(a, c, g, k, w0, w1, units, xr, have_stats, ssum, ssq, in, dmean, rstd,
                                         c1, cb, out, logit_row0, best, sample_k0);
         }
         CSUB(2);
@@ -1017,13 +1032,14 @@ __device__ __forceinline__ void read_sum(const ClusterArgs &a, CS &c, int count,
 // Adds values[i] (+ extra[base + i] + extra2[i] if extra is given) into
 // sum[base + i], i < n, one contribution per word.  The closing barrier keeps
 // the parameter area (extra2) unchanged until every thread has read it.
-__device__ __forceinline__ void add_sum(long long *sum, int base, const float *values, const float *extra,
-                                        const float *extra2, int n)
+__device__ __forceinline__ void add_sum(const ClusterArgs &a, long long *sum, int base, const float *values,
+                                        const float *extra, const float *extra2, int n)
 {
     const int tid = threadIdx.x;
     for (int i = tid; i < n; i += kCThreads) {
         float v = values[i];
         if (extra) v += extra[base + i] + extra2[i];
+        if (!(fabsf(v) <= kFixLimit)) record_error(a.st, kDevErrRange, base + i);
         red_add_i64(sum + size_t(base + i) * kClusterAccStride, (long long)to_word(v));
     }
     csync();
@@ -1419,7 +1435,7 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                 TSET(s, l * 16 + 11);
                 tile_rows<WT>(a, c, G.b, k, kCRing, D, c.attn, c.outv, ok);
                 CTRACE(s, l * 16 + 6);
-                add_sum(an, ro.r * rq, c.outv, ro.h == 0 ? c.x : nullptr, pb, rq);
+                add_sum(a, an, ro.r * rq, c.outv, ro.h == 0 ? c.x : nullptr, pb, rq);
                 CTRACE(s, l * 16 + 7);
             } else {
                 if (tid == 0) mbar_arrive_expect_tx(c.red_bar, uint32_t(E) * 4u);   // this layer's partial slices
@@ -1454,7 +1470,7 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                         c.outv[i] = ((c.red[i] + c.red[rq + i]) + c.red[2 * rq + i]) + c.red[3 * rq + i];
                     csync();
                 }
-                add_sum(a.acc_next + (size_t(par) * a.L + l) * E * kClusterAccStride, ro.r * rq, c.outv,
+                add_sum(a, a.acc_next + (size_t(par) * a.L + l) * E * kClusterAccStride, ro.r * rq, c.outv,
                         ro.f < kClusterSize ? c.x : nullptr, pb, rq);
                 CTRACE(s, l * 16 + 6);
             }

@@ -46,7 +46,7 @@ struct CLayer {
     const uint8_t *p_z;
     const float *mlp_proj_b;
     // LayerNorm folded into the rows that follow it:
-    //   W.LN(x) + b = rstd * (W.(gamma*x) - mean * c1) + cb,
+    //   W.LN(x) + b = rstd * (W.(gamma*(x-s)) - (mean-s) * c1) + cb  (s = x[0]),
     //   c1 = W.gamma, cb = W.beta + b (from the weights as stored)
     const float *q_c1, *q_cb;    // [3E], in the gathered QKV row order
     const float *f_c1, *f_cb;    // [F]
@@ -85,6 +85,7 @@ struct ClusterArgs {
     int32_t wtype;
     int32_t n_stages;
     uint32_t stage_bytes, ring_offset;
+    unsigned long long wait_ns;  // every device wait gives up after this long (GPT2_ERR_TIMEOUT)
 };
 
 // Dynamic shared memory before the ring.

@@ -11,6 +11,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -27,6 +28,7 @@ enum : int32_t {
     kDevErrBadToken = 2,       // token outside [0, vocab)
     kDevErrBadPosition = 3,    // position outside [0, n_positions)
     kDevErrLaunchShape = 4,    // a kernel found a grid / cluster shape it was not built for
+    kDevErrRange = 5,          // an activation outside the range of the fixed-point residual sums
 };
 
 // Per-model scalars that live in device memory so that a captured graph can
@@ -39,8 +41,8 @@ struct DeviceState {
     int32_t n_out;      // number of ids appended to out_ids
     int32_t err;        // first recorded kDevErr* code (0 = none)
     int32_t err_info;   // where it happened (kernel-specific)
-    int32_t abort;      // persistent kernel: a CTA gave up, every CTA returns
-    int32_t seq;        // persistent kernel: passes run so far + 1 (epoch base)
+    int32_t abort;      // cluster kernel: a CTA gave up, every CTA returns
+    int32_t seq;        // cluster kernel: passes run so far + 1 (epoch base)
 };
 
 __device__ __forceinline__ void record_error(DeviceState *st, int32_t code, int32_t info)

@@ -1,5 +1,5 @@
-// Device-side pieces shared by the per-kernel decode pass and the
-// persistent decode kernel: stored-row layout and the row dot product.
+// Device-side pieces shared by the decode kernels: stored-row layout and the
+// row dot product.
 #pragma once
 
 #include "common.cuh"

@@ -84,6 +84,11 @@ enum : int32_t { kSetTokPos = 1, kResetOut = 2, kSeedOutWithNext = 4, kClearErr 
 // src is HF [in][out] fp32; writes dst [out][in] in the chosen format.
 cudaError_t repack_f32(const float *src, int in, int out, float *dst, cudaStream_t s);
 cudaError_t repack_f16(const float *src, int in, int out, void *dst, cudaStream_t s);
+// src HF [in][out] fp32 -> dst [out][in] bf16 (round to nearest even).
+cudaError_t repack_bf16(const float *src, int in, int out, void *dst, cudaStream_t s);
+// Elementwise split of n fp32 values into bf16 hi = bf16(v), lo = bf16(v - hi)
+// (lo may be null), layout unchanged.
+cudaError_t split_bf16(const float *src, size_t n, void *hi, void *lo, cudaStream_t s);
 // Elementwise fp32 -> fp16 (round to nearest even) of n values, layout unchanged.
 cudaError_t convert_f16(const float *src, size_t n, void *dst, cudaStream_t s);
 // tmp must hold out*in floats.
@@ -92,6 +97,9 @@ cudaError_t quant_int4_rows(const float *Wt, int in, int out, uint8_t *codes, fl
                             cudaStream_t s);
 cudaError_t repack_int4(const float *src, int in, int out, float *tmp, uint8_t *codes, float *scales,
                         uint8_t *zeros, cudaStream_t s);
+// c1[r] = sum_i W[r][i] gamma[i], c2[r] = sum_i W[r][i] beta[i] for W [out][in]
+cudaError_t ln_fold(const float *W, const float *gamma, const float *beta, int in, int out, float *c1, float *c2,
+                    cudaStream_t s);
 // Widen a stored matrix to fp32 [out][in].
 cudaError_t dequant_to_f32(int wtype, const void *W, const float *scales, const uint8_t *zeros, int in,
                            int out, float *dst, cudaStream_t s);

@@ -17,6 +17,8 @@
 // that must start at zero (the arrival counter) before its kernel runs.
 #include "../../include/gpt2.h"
 
+#include <cuda.h>
+
 #include <cstring>
 #include <mutex>
 
@@ -38,10 +40,32 @@ static __device__ __align__(256) unsigned char g_head_scratch[kScratchBytes];
 
 // In host code `g_head_scratch` names a host-side stand-in, not device memory;
 // the device address comes from cudaGetSymbolAddress, looked up once per
-// device with that device current.
+// device with that device current.  The module is loaded into the device's
+// context, so the address is remembered together with that context: after
+// cudaDeviceReset (or any new primary context) the array may sit elsewhere,
+// and the next call looks it up again instead of using a stale address.
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void *g_addr[kMaxDevices] = {};
+CUcontext g_ctx[kMaxDevices] = {};
+
+using CtxGetCurrent = CUresult (*)(CUcontext *);
+
+// The current context, through the driver entry point the runtime hands out
+// (no link against the driver library).
+cudaError_t current_context(CUcontext *ctx)
+{
+    static CtxGetCurrent fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess) return e;
+        if (q != cudaDriverEntryPointSuccess || !p) return cudaErrorNotSupported;
+        fn = reinterpret_cast<CtxGetCurrent>(p);
+    }
+    return fn(ctx) == CUDA_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+}
 
 int scratch_address(void **out)
 {
@@ -53,14 +77,26 @@ int scratch_address(void **out)
     }
     if (dev < 0 || dev >= kMaxDevices) return GPT2_ERR_UNSUPPORTED_DEVICE;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_addr[dev]) {
+    // the first runtime call on a device creates its primary context, so the
+    // lookup comes first and the context is read after it
+    CUcontext ctx = nullptr;
+    if (g_addr[dev]) {
+        e = current_context(&ctx);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return GPT2_ERR_CUDA;
+        }
+    }
+    if (!g_addr[dev] || ctx != g_ctx[dev]) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_head_scratch);
+        if (e == cudaSuccess) e = current_context(&ctx);
         if (e != cudaSuccess || !p) {
             cudaGetLastError();
             return GPT2_ERR_CUDA;
         }
         g_addr[dev] = p;
+        g_ctx[dev] = ctx;
     }
     *out = g_addr[dev];
     return GPT2_OK;

@@ -23,6 +23,8 @@ template <>
 __device__ __forceinline__ float cvt_out<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ __half cvt_out<__half>(float v) { return __float2half_rn(v); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 cvt_out<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
 
 // src [in][out] -> dst [out][in], 32x32 tiles through shared memory.
 template <typename T>
@@ -59,6 +61,33 @@ cudaError_t repack_f32(const float *src, int in, int out, float *dst, cudaStream
 cudaError_t repack_f16(const float *src, int in, int out, void *dst, cudaStream_t s)
 {
     return transpose<__half>(src, in, out, static_cast<__half *>(dst), s);
+}
+
+cudaError_t repack_bf16(const float *src, int in, int out, void *dst, cudaStream_t s)
+{
+    return transpose<__nv_bfloat16>(src, in, out, static_cast<__nv_bfloat16 *>(dst), s);
+}
+
+// Elementwise split of fp32 values into bf16 planes: hi = bf16(v) and
+// lo = bf16(v - hi) (round to nearest even; v - hi is exact in fp32), so that
+// hi + lo keeps about 16 bits of v.  lo may be null (hi only).
+__global__ void __launch_bounds__(256) k_to_bf16(const float *src, size_t n, __nv_bfloat16 *hi, __nv_bfloat16 *lo)
+{
+    for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n; i += size_t(gridDim.x) * blockDim.x) {
+        const float v = src[i];
+        const __nv_bfloat16 h = __float2bfloat16_rn(v);
+        hi[i] = h;
+        if (lo) lo[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+    }
+}
+
+cudaError_t split_bf16(const float *src, size_t n, void *hi, void *lo, cudaStream_t s)
+{
+    const size_t blocks = std::min<size_t>((n + 255) / 256, 8192);
+    if (blocks == 0) return cudaSuccess;
+    k_to_bf16<<<unsigned(blocks), 256, 0, s>>>(src, n, static_cast<__nv_bfloat16 *>(hi),
+                                                static_cast<__nv_bfloat16 *>(lo));
+    return cudaGetLastError();
 }
 
 // Elementwise fp32 -> fp16 (round to nearest even), layout unchanged.
@@ -160,6 +189,35 @@ cudaError_t dequant_to_f32(int wtype, const void *W, const float *scales, const 
     const size_t n = size_t(in) * out;
     const size_t blocks = (n + 255) / 256;
     k_dequant<<<unsigned(blocks), 256, 0, s>>>(wtype, W, scales, zeros, in, out, dst);
+    return cudaGetLastError();
+}
+
+// LayerNorm folded into the rows that follow it (see CLayer in cluster.h):
+// one warp per row of a stored [out][in] matrix, c1 = W.gamma, c2 = W.beta,
+// fixed-order sums.
+__global__ void __launch_bounds__(256) k_ln_fold(const float *W, const float *gamma, const float *beta, int in,
+                                                 int out, float *c1, float *c2)
+{
+    const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (row >= out) return;
+    float a = 0.f, b = 0.f;
+    for (int i = lane; i < in; i += 32) {
+        const float w = W[size_t(row) * in + i];
+        a = fmaf(w, gamma[i], a);
+        b = fmaf(w, beta[i], b);
+    }
+    a = warp_sum(a);
+    b = warp_sum(b);
+    if (lane == 0) {
+        c1[row] = a;
+        c2[row] = b;
+    }
+}
+
+cudaError_t ln_fold(const float *W, const float *gamma, const float *beta, int in, int out, float *c1, float *c2,
+                    cudaStream_t s)
+{
+    k_ln_fold<<<(out + 7) / 8, 256, 0, s>>>(W, gamma, beta, in, out, c1, c2);
     return cudaGetLastError();
 }
 

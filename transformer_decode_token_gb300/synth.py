@@ -84,6 +84,34 @@ def make_weights(cfg: GPT2Config, seed: int = 0) -> dict:
     return w
 
 
+# Stress inputs: the recipe's weights with a shifted distribution, to reach
+# parts of a decode path that N(0, 0.02) weights never exercise.
+#   "offset":   wpe + 30 in every dimension: the residual stream carries a
+#               common offset of 30 through every block, so |mean(x)| is
+#               about a thousand times std(x) at the first LayerNorm;
+#   "outliers": three dimensions get +400 in every MLP output bias, so those
+#               residual values grow into the thousands (one block adds 400);
+#   "overflow": wpe + 1e5 in every dimension (residual values of 1e5).
+STRESS_KINDS = ("offset", "outliers", "overflow")
+
+
+def make_stress_weights(cfg: GPT2Config, kind: str, seed: int = 0) -> dict:
+    if kind not in STRESS_KINDS:
+        raise ValueError(f"unknown stress kind {kind!r}")
+    w = make_weights(cfg, seed)
+    if kind == "offset":
+        w["wpe"] = w["wpe"] + np.float32(30.0)
+    elif kind == "overflow":
+        w["wpe"] = w["wpe"] + np.float32(1e5)
+    else:
+        dims = [1, cfg.n_embd // 2 + 3, cfg.n_embd - 5]
+        for L in w["layers"]:
+            b = L["mlp_proj_b"].copy()
+            b[dims] += np.float32(400.0)
+            L["mlp_proj_b"] = b
+    return w
+
+
 def make_prompt(cfg: GPT2Config, n: int, seed: int = 1) -> np.ndarray:
     rng = np.random.Generator(np.random.PCG64(seed))
     return rng.integers(0, cfg.vocab_size, size=n, dtype=np.int64).astype(np.int32)
