@@ -86,7 +86,8 @@ typedef struct gpt2_config {
 typedef enum gpt2_wdtype {
     GPT2_F32  = 0,
     GPT2_F16  = 1,
-    GPT2_INT4 = 2
+    GPT2_INT4 = 2,
+    GPT2_BF16 = 3     /* batched models only (gpt2_create_batch)          */
 } gpt2_wdtype;
 
 /* One block's tensors, DEVICE pointers to fp32, in the checkpoint's HF
@@ -333,6 +334,91 @@ int gpt2_op_head_argmax_noalloc(const float *x, const float *ln_w, const float *
                                 float eps, const float *wte, int32_t vocab,
                                 int32_t n_embd, float *logits, int32_t *dev_token,
                                 void *stream);
+
+/* ---- batched decoding ------------------------------------------------------ */
+
+/* A batched model decodes up to max_batch independent sequences together,
+ * one token of each per step.  Each step is, for every sequence of the batch,
+ * the decode pass above (the graph file's node list; the model.s description
+ * of the "gpt2.s" README, "Inner Workings"; greedy choice as in "Let's make
+ * GPT-2 in assembly", Step 7) over that sequence's own KV cache; with many
+ * sequences the linears become dense matrix products, which run on the tensor
+ * cores (tcgen05, bf16 operands, fp32 accumulators in tensor memory).
+ *   - Weights: GPT2_BF16 only.  The 48 block matrices are stored as bf16
+ *     [out][in] (round to nearest even) and the tied head as a bf16 copy of
+ *     wte; embeddings, biases, LayerNorm parameters and the KV cache stay
+ *     fp32.  Activations enter each product as two bf16 parts (x = hi + lo,
+ *     lo = bf16(x - hi)), so products use about 16 bits of x; sums are fp32.
+ *   - Cache: [n_layer][max_batch][n_head][n_positions][head_dim] fp32, one
+ *     slot per sequence; sequences have independent lengths (ragged).
+ *   - One step is a CUDA graph of 8 * n_layer + 4 kernels captured at create
+ *     time; steps are asynchronous on the model's stream.
+ * Errors as for the single-sequence calls. */
+typedef struct gpt2_batch gpt2_batch;
+
+/* max_batch in [1, 64].  Same weights argument and ownership as gpt2_create.
+ * Errors: INVALID_ARG (wdtype other than GPT2_BF16, shapes: n_embd % 64,
+ * head_dim in {32, 64, 128}), UNSUPPORTED_DEVICE, OUT_OF_MEMORY, CUDA. */
+int gpt2_create_batch(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
+                      int32_t max_batch, void *stream, gpt2_batch **out);
+void gpt2_destroy_batch(gpt2_batch *m);
+
+/* One step: sequence b (b < n) consumes host tokens[b] at host positions[b]
+ * (append at its cached length, or rewind to a smaller position, as in
+ * gpt2_decode_step); positions[b] == -1 leaves sequence b out of this step
+ * (its cache is untouched).  If dev_logits is not NULL it receives the
+ * model's device buffer of [max_batch][vocab_size] fp32 logits (rows of
+ * sequences left out are not meaningful), valid until the next step. */
+int gpt2_decode_batch(gpt2_batch *m, const int32_t *tokens, const int32_t *positions,
+                      int32_t n, const float **dev_logits);
+
+/* Resets every sequence, then consumes the ragged prompts: sequence b's
+ * lens[b] ids follow one another in the host array ids (sequence 0 first),
+ * one position per step; afterwards each sequence's greedy choice after its
+ * last prompt token is available (gpt2_argmax_batch). */
+int gpt2_prefill_batch(gpt2_batch *m, const int32_t *ids, const int32_t *lens, int32_t n);
+
+/* n_steps device-resident greedy steps for every sequence with a cached
+ * prefix: each continues at its own length with its last choice; the host is
+ * not involved between steps.  Errors: NOT_READY, POSITION_RANGE (a sequence
+ * would pass n_positions), INVALID_ARG. */
+int gpt2_decode_batch_greedy(gpt2_batch *m, int32_t n_steps);
+
+/* The greedy choice of the last step for sequences 0..n-1 (synchronises). */
+int gpt2_argmax_batch(gpt2_batch *m, int32_t *host_ids, int32_t n);
+
+/* The tokens chosen by the passes at positions first_pos .. first_pos +
+ * n_pos - 1, [n_pos][max_batch] int32, copied to host memory (an entry of a
+ * sequence that never ran that position is not meaningful); synchronises. */
+int gpt2_batch_ids(gpt2_batch *m, int32_t first_pos, int32_t n_pos, int32_t *host_ids);
+
+/* Copies the logits of sequences 0..n-1 ([n][vocab_size] fp32) of the last
+ * step to host or device memory; synchronises. */
+int gpt2_copy_logits_batch(gpt2_batch *m, int32_t n, float *dst);
+
+/* Copies the cached K and V rows 0..n_rows-1 of one layer and sequence,
+ * [n_head][n_rows][head_dim] fp32 each, to host or device memory. */
+int gpt2_export_kv_batch(gpt2_batch *m, int32_t layer, int32_t seq, int32_t n_rows,
+                         float *dst_k, float *dst_v);
+
+/* Kernels per step and kernel launches so far (any pointer may be NULL). */
+int gpt2_batch_info(const gpt2_batch *m, int32_t *kernels_per_step, uint64_t *launches);
+
+/* Waits for the model's queued work; returns (and clears) a recorded device
+ * error. */
+int gpt2_sync_batch(gpt2_batch *m);
+
+/* The batched path's tensor-core linear on caller buffers: Y[r][o] =
+ * sum_k W[o][k] * X[r][k] for r < n, W a DEVICE bf16 [M][K] matrix (16-byte
+ * aligned), X DEVICE fp32 [n][K], Y DEVICE fp32 [n][M]; n <= 64, K % 64 == 0.
+ * X enters as hi + lo bf16 parts, sums are fp32 (the graph file's linear node
+ * with bf16 weights).  workspace (DEVICE, 256-byte aligned) holds
+ * gpt2_op_linear_bf16_workspace(M, n, K) bytes and may not be used by another
+ * call in flight.  Asynchronous on `stream`.  Errors: INVALID_ARG,
+ * UNSUPPORTED_DEVICE, CUDA. */
+size_t gpt2_op_linear_bf16_workspace(int32_t M, int32_t n, int32_t K);
+int gpt2_op_linear_bf16(const void *W, const float *X, int32_t M, int32_t n, int32_t K,
+                        float *Y, void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---- errors ------------------------------------------------------------- */
 const char *gpt2_strerror(int status);

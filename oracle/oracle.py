@@ -319,6 +319,10 @@ def stored_weights(weights: dict, wdtype: str, head: str = "f32") -> dict:
         out = dict(stored_weights(weights, wdtype))
         out["head"] = f16_bits_to_f32(f32_to_f16_bits(_f32(weights["wte"])))
         return out
+    if head == "bf16":   # the batched path's head: a bf16 copy of wte (round to nearest even)
+        out = dict(stored_weights(weights, wdtype))
+        out["head"] = bf16_bits_to_f32(f32_to_bf16_bits(_f32(weights["wte"])))
+        return out
     if head == "int4":   # wte is already [out][in]; quant_int4 takes the HF [in][out] layout
         out = dict(stored_weights(weights, wdtype))
         out["head"] = np.ascontiguousarray(dequant_int4(*quant_int4(np.ascontiguousarray(_f32(weights["wte"]).T))))
@@ -422,14 +426,15 @@ def forward_full(cfg, weights: dict, tokens) -> np.ndarray:
     return out
 
 
-def greedy(cfg, weights: dict, prompt, n_steps: int, teacher=None, temperature: float = 0.0, seed: int = 0):
+def greedy(cfg, weights: dict, prompt, n_steps: int, teacher=None, temperature: float = 0.0, seed: int = 0,
+           omp: bool = False):
     """Prefill the prompt one token at a time (positions 0..n-1), then run
     ``n_steps`` decode passes.  Returns (ids, logits): ids[i] is the token
     chosen after pass n-1+i (so ids has n_steps + 1 entries): the greedy
     argmax, or with temperature > 0 the draw of sample(); logits has one row
     per pass (n + n_steps rows).  Decode pass i consumes ids[i], or
     teacher[i] when ``teacher`` is given (teacher forcing)."""
-    m = OracleModel(cfg, weights)
+    m = OracleModel(cfg, weights, omp=omp)
     try:
         prompt = [int(t) for t in prompt]
         rows = []

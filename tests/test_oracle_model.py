@@ -86,10 +86,11 @@ def test_greedy_teacher_forcing_consistent():
     assert ids[0] == int(np.argmax(logits[3]))
 
 
-@pytest.mark.parametrize("head", ["f16", "int4"])
+@pytest.mark.parametrize("head", ["f16", "int4", "bf16"])
 def test_separately_stored_head(head):
     """The output head as a separate stored matrix ("gpt2.s" README, Options:
-    -h stores it in fp16; or grouped int4): passing wte itself changes
+    -h stores it in fp16; or grouped int4; or bf16, the batched path's
+    head): passing wte itself changes
     nothing, bit for bit; a rounded head matches the library forward with
     that head, while the embedding still reads the fp32 wte."""
     cfg = synth.TINY

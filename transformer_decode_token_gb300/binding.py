@@ -28,7 +28,10 @@ EXPORTED = ("gpt2_create", "gpt2_create_ex", "gpt2_path", "gpt2_launch_count", "
             "gpt2_matrix_bytes", "gpt2_export_matrix", "gpt2_export_dequant", "gpt2_export_kv",
             "gpt2_kernels_per_step", "gpt2_op_layernorm", "gpt2_op_head_argmax_workspace",
             "gpt2_op_head_argmax", "gpt2_op_head_argmax_noalloc", "gpt2_set_sampling", "gpt2_set_wait_limit",
-            "gpt2_strerror")
+            "gpt2_create_batch", "gpt2_destroy_batch", "gpt2_decode_batch", "gpt2_prefill_batch",
+            "gpt2_decode_batch_greedy", "gpt2_argmax_batch", "gpt2_batch_ids", "gpt2_copy_logits_batch",
+            "gpt2_export_kv_batch", "gpt2_batch_info", "gpt2_sync_batch", "gpt2_op_linear_bf16_workspace",
+            "gpt2_op_linear_bf16", "gpt2_strerror")
 
 
 class GPT2Error(RuntimeError):
@@ -116,10 +119,27 @@ def lib(build_if_stale: bool = True, path: str = None):
             L.gpt2_op_head_argmax_noalloc.argtypes = [vp, vp, vp, f32, vp, i32, i32, vp, vp, vp]
             L.gpt2_set_sampling.argtypes = [vp, f32, ctypes.c_uint64]
             L.gpt2_set_wait_limit.argtypes = [vp, ctypes.c_uint64]
+            L.gpt2_create_batch.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), i32, i32, vp,
+                                            ctypes.POINTER(vp)]
+            L.gpt2_destroy_batch.argtypes = [vp]
+            L.gpt2_destroy_batch.restype = None
+            L.gpt2_decode_batch.argtypes = [vp, pi32, pi32, i32, ctypes.POINTER(vp)]
+            L.gpt2_prefill_batch.argtypes = [vp, pi32, pi32, i32]
+            L.gpt2_decode_batch_greedy.argtypes = [vp, i32]
+            L.gpt2_argmax_batch.argtypes = [vp, pi32, i32]
+            L.gpt2_batch_ids.argtypes = [vp, i32, i32, pi32]
+            L.gpt2_copy_logits_batch.argtypes = [vp, i32, vp]
+            L.gpt2_export_kv_batch.argtypes = [vp, i32, i32, i32, vp, vp]
+            L.gpt2_batch_info.argtypes = [vp, pi32, ctypes.POINTER(ctypes.c_uint64)]
+            L.gpt2_sync_batch.argtypes = [vp]
+            L.gpt2_op_linear_bf16_workspace.argtypes = [i32, i32, i32]
+            L.gpt2_op_linear_bf16_workspace.restype = sz
+            L.gpt2_op_linear_bf16.argtypes = [vp, vp, i32, i32, i32, vp, vp, sz, vp]
             L.gpt2_strerror.argtypes = [ctypes.c_int]
             L.gpt2_strerror.restype = ctypes.c_char_p
             for n in EXPORTED:
-                if n not in ("gpt2_destroy", "gpt2_op_head_argmax_workspace", "gpt2_strerror"):
+                if n not in ("gpt2_destroy", "gpt2_destroy_batch", "gpt2_op_head_argmax_workspace",
+                             "gpt2_op_linear_bf16_workspace", "gpt2_strerror"):
                     getattr(L, n).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -326,3 +346,104 @@ def op_head_argmax_noalloc(x, ln_w, ln_b, eps: float, wte, logits, token, stream
                                             _ptr(logits), _ptr(token), _stream_handle(stream)),
           "gpt2_op_head_argmax_noalloc")
 
+
+# ---- batched decoding ----------------------------------------------------------
+
+def _i32(a):
+    a = np.ascontiguousarray(a, np.int32)
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+class BatchModel:
+    """Up to max_batch independent sequences decoded together (bf16 weights,
+    tensor-core linears); see gpt2_create_batch in include/gpt2.h."""
+
+    def __init__(self, cfg, dev_weights: dict, max_batch: int, wdtype: str = "bf16", stream=None):
+        L = lib()
+        self.cfg = cfg
+        self.max_batch = max_batch
+        c = Config(cfg.n_layer, cfg.n_embd, cfg.n_head, cfg.n_positions, cfg.vocab_size, cfg.ln_eps)
+        layers = (LayerWeights * cfg.n_layer)()
+        for i, Lw in enumerate(dev_weights["layers"]):
+            for k in _LAYER_KEYS:
+                setattr(layers[i], k, Lw[k].data_ptr())
+        w = Weights(dev_weights["wte"].data_ptr(), dev_weights["wpe"].data_ptr(),
+                    dev_weights["ln_f_w"].data_ptr(), dev_weights["ln_f_b"].data_ptr(),
+                    ctypes.cast(layers, ctypes.POINTER(LayerWeights)))
+        h = ctypes.c_void_p()
+        check(L.gpt2_create_batch(ctypes.byref(c), ctypes.byref(w), WDTYPES[wdtype], int(max_batch),
+                                  _stream_handle(stream), ctypes.byref(h)), "gpt2_create_batch")
+        self._h = h
+
+    def decode(self, tokens, positions) -> int:
+        t, tp = _i32(tokens)
+        p, pp = _i32(positions)
+        assert t.size == p.size
+        d = ctypes.c_void_p()
+        check(lib().gpt2_decode_batch(self._h, tp, pp, t.size, ctypes.byref(d)), "gpt2_decode_batch")
+        return d.value
+
+    def prefill(self, prompts):
+        lens, lp = _i32([len(q) for q in prompts])
+        ids, ip = _i32(np.concatenate([np.asarray(q, np.int32) for q in prompts]))
+        check(lib().gpt2_prefill_batch(self._h, ip, lp, lens.size), "gpt2_prefill_batch")
+
+    def decode_greedy(self, n_steps: int):
+        check(lib().gpt2_decode_batch_greedy(self._h, int(n_steps)), "gpt2_decode_batch_greedy")
+
+    def argmax(self, n: int) -> list:
+        out = np.zeros(n, np.int32)
+        check(lib().gpt2_argmax_batch(self._h, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), n),
+              "gpt2_argmax_batch")
+        return out.tolist()
+
+    def ids(self, first_pos: int, n_pos: int) -> np.ndarray:
+        out = np.zeros((n_pos, self.max_batch), np.int32)
+        check(lib().gpt2_batch_ids(self._h, first_pos, n_pos, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))),
+              "gpt2_batch_ids")
+        return out
+
+    def logits(self, n: int) -> np.ndarray:
+        out = np.empty((n, self.cfg.vocab_size), np.float32)
+        check(lib().gpt2_copy_logits_batch(self._h, n, _ptr(out)), "gpt2_copy_logits_batch")
+        return out
+
+    def export_kv(self, layer: int, seq: int, n_rows: int):
+        H, D = self.cfg.n_head, self.cfg.n_embd // self.cfg.n_head
+        k = np.empty((H, n_rows, D), np.float32)
+        v = np.empty((H, n_rows, D), np.float32)
+        check(lib().gpt2_export_kv_batch(self._h, layer, seq, n_rows, _ptr(k), _ptr(v)), "gpt2_export_kv_batch")
+        return k, v
+
+    def info(self):
+        k, n = ctypes.c_int32(), ctypes.c_uint64()
+        check(lib().gpt2_batch_info(self._h, ctypes.byref(k), ctypes.byref(n)), "gpt2_batch_info")
+        return int(k.value), int(n.value)
+
+    def sync(self):
+        check(lib().gpt2_sync_batch(self._h), "gpt2_sync_batch")
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().gpt2_destroy_batch(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def op_linear_bf16(W_bf16, X, stream=None):
+    """Y = X . W^T on the tensor cores: W a CUDA bf16 [M][K] tensor, X a CUDA
+    fp32 [n][K] tensor (n <= 64); returns a new CUDA fp32 [n][M] tensor."""
+    import torch
+    M, K = W_bf16.shape
+    n = X.shape[0]
+    Y = torch.empty((n, M), dtype=torch.float32, device=X.device)
+    ws_bytes = int(lib().gpt2_op_linear_bf16_workspace(M, n, K))
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=X.device)
+    check(lib().gpt2_op_linear_bf16(_ptr(W_bf16), _ptr(X), M, n, K, _ptr(Y), _ptr(ws), ws_bytes,
+                                    _stream_handle(stream)), "gpt2_op_linear_bf16")
+    return Y

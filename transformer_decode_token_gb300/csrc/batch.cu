@@ -1,0 +1,974 @@
+// Batched decode: the decode pass for up to 64 independent sequences at once,
+// one token each per step, with bf16 block matrices and head on the tensor
+// cores.
+//
+// Every step is the per-token pass of the "model.fir" graph file's node list
+// (and the model.s description of the "gpt2.s" README, "Inner Workings"),
+// applied to each sequence of the batch: embedding, 12 pre-LN blocks, the
+// final LayerNorm, the tied head and the greedy choice ("Let's make GPT-2 in
+// assembly", Step 7).  With 64 sequences the four linears of a block and the
+// head become dense contractions of the stored weights with 64 activation
+// rows (tc_gemm.cu); attention stays per sequence over that sequence's own
+// (ragged) KV cache.  One step is a CUDA graph of 8 kernels per block + 4,
+// chained by programmatic dependent launch:
+//   k_b_ln     residual add (fixed-order sum of the previous linear's split-K
+//              shares + bias), or the embedding; LayerNorm; the bf16 hi/lo
+//              B operand of the next linear
+//   tc_gemm    QKV / out-projection / fc / MLP projection / head
+//   k_b_attn   q, k, v of one (sequence, head) from the QKV shares, k and v
+//              appended at the sequence's position, softmax(q.k / sqrt(D))
+//              over positions 0..pos, the weighted sum of v
+//   k_b_gelu   fc shares + bias, gelu_new, the B operand of the MLP projection
+//   k_b_argmax greedy choice per sequence; k_b_advance feeds it to the next step
+// The KV cache and all activations are fp32; a sequence whose position is -1
+// is inactive for the step (no cache row written, its outputs ignored).
+#include "../../include/gpt2.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_gemm.h"
+
+using namespace gpt2;
+
+namespace {
+
+constexpr int kBT = 256;   // threads of the elementwise / attention kernels
+
+__device__ __forceinline__ void put_hi_lo(__nv_bfloat16 *b_op, int row, int ld, int i, float y)
+{
+    const __nv_bfloat16 h = __float2bfloat16_rn(y);
+    b_op[size_t(row) * ld + i] = h;
+    b_op[size_t(kTcMaxRows + row) * ld + i] = __float2bfloat16_rn(y - __bfloat162float(h));
+}
+
+// Sum of `v` over the CTA in a fixed order (warp butterflies, then the warps'
+// sums in warp order): every run gives the same bits.
+__device__ __forceinline__ float block_sum(float v, float *red)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    v = warp_sum(v);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = 0.f;
+    for (int w = 0; w < int(blockDim.x >> 5); ++w) t += red[w];
+    return t;
+}
+__device__ __forceinline__ float block_max(float v, float *red)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    v = warp_max(v);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = red[0];
+    for (int w = 1; w < int(blockDim.x >> 5); ++w) t = fmaxf(t, red[w]);
+    return t;
+}
+
+struct BLnArgs {
+    float *x;                       // [rows][E] residual stream
+    const float *parts;             // [splits][rows][E] shares of the linear before (mode 1)
+    int32_t splits;
+    const float *bias;              // its bias [E]
+    const int32_t *tok, *pos;       // mode 0: the embedding of tok at pos
+    const float *wte, *wpe;
+    const float *gamma, *beta;
+    float eps;
+    int32_t E, rows, V, P;
+    __nv_bfloat16 *out;             // [128][E] hi/lo B operand
+    int32_t mode;                   // 0: x = wte[tok] + wpe[pos]; 1: x += sum(parts) + bias
+    DeviceState *st;
+};
+
+// One CTA per row: the residual stream update, then LayerNorm ("model.fir"
+// kernel g2.layernorm: mean, biased variance, (x - mean) / sqrt(var + eps) *
+// gamma + beta) into the next linear's B operand.
+__global__ void __launch_bounds__(kBT) k_b_ln(const BLnArgs a)
+{
+    extern __shared__ float xs[];   // [E]
+    __shared__ float red[kBT / 32];
+    const int b = blockIdx.x, E = a.E;
+    pdl_wait();
+    if (a.mode == 0) {
+        int t = a.tok[b], p = a.pos[b];
+        if (t < 0 || t >= a.V || p >= a.P) {
+            if (threadIdx.x == 0 && p >= 0) record_error(a.st, t < 0 || t >= a.V ? kDevErrBadToken : kDevErrBadPosition, b);
+            t = min(max(t, 0), a.V - 1);
+        }
+        p = min(max(p, 0), a.P - 1);
+        for (int i = threadIdx.x; i < E; i += kBT) {
+            const float v = a.wte[size_t(t) * E + i] + a.wpe[size_t(p) * E + i];
+            xs[i] = v;
+            a.x[size_t(b) * E + i] = v;
+        }
+    } else {
+        for (int i = threadIdx.x; i < E; i += kBT) {
+            float s = 0.f;
+            for (int k = 0; k < a.splits; ++k) s += a.parts[(size_t(k) * a.rows + b) * E + i];
+            const float v = a.x[size_t(b) * E + i] + (s + a.bias[i]);
+            xs[i] = v;
+            a.x[size_t(b) * E + i] = v;
+        }
+    }
+    float s = 0.f;
+    for (int i = threadIdx.x; i < E; i += kBT) s += xs[i];
+    const float mean = block_sum(s, red) / float(E);
+    float q = 0.f;
+    for (int i = threadIdx.x; i < E; i += kBT) {
+        const float d = xs[i] - mean;
+        q = fmaf(d, d, q);
+    }
+    const float var = block_sum(q, red) / float(E);
+    const float rstd = 1.0f / sqrtf(var + a.eps);
+    for (int i = threadIdx.x; i < E; i += kBT)
+        put_hi_lo(a.out, b, E, i, (xs[i] - mean) * rstd * a.gamma[i] + a.beta[i]);
+    pdl_launch_dependents();
+}
+
+struct BAttnArgs {
+    const float *parts;             // [splits][rows][3E] QKV shares
+    int32_t splits;
+    const float *bias;              // [3E]
+    float *kc, *vc;                 // this layer's cache: [slots][H][P][D]
+    const int32_t *pos;             // [rows]; -1: inactive
+    int32_t E, H, P, rows, slots;
+    int32_t append;                 // 1: this row's k, v are written at pos here
+    float scale;
+    __nv_bfloat16 *out;             // [128][E] hi/lo B operand of the output projection
+};
+
+// One CTA per (row, head).  Scores: D/4 threads per cached row (a float4 of
+// the head dimension each), several rows per pass, shuffles within the row's
+// threads; softmax over positions 0..pos (max subtracted); the weighted sum of
+// v with the same thread layout, partial sums combined in a fixed order.
+template <int D>
+__global__ void __launch_bounds__(kBT) k_b_attn(const BAttnArgs a)
+{
+    constexpr int LPR = D / 4;               // threads per row
+    constexpr int RPP = kBT / LPR;           // rows per pass
+    constexpr int U = 4;                     // passes in flight
+    extern __shared__ float sc[];            // [P] scores, then probabilities
+    __shared__ float red[kBT / 32];
+    __shared__ __align__(16) float qkv[3 * D];
+    __shared__ __align__(16) float part[RPP][D];
+    const int b = blockIdx.x, h = blockIdx.y, E = a.E;
+    const int g = threadIdx.x / LPR, l = threadIdx.x % LPR;
+    pdl_wait();
+    const int pos = a.pos[b];
+    if (pos < 0 || pos >= a.P) {             // inactive row: zero output
+        for (int d = threadIdx.x; d < D; d += kBT) put_hi_lo(a.out, b, E, h * D + d, 0.f);
+        pdl_launch_dependents();
+        return;
+    }
+    const int slot = a.slots == 1 ? 0 : b;
+    float *kh = a.kc + (size_t(slot) * a.H + h) * a.P * D;
+    float *vh = a.vc + (size_t(slot) * a.H + h) * a.P * D;
+    for (int t = threadIdx.x; t < 3 * D; t += kBT) {
+        const int part_ = t / D, d = t % D;
+        const int j = part_ * E + h * D + d;
+        float s = 0.f;
+        for (int k = 0; k < a.splits; ++k) s += a.parts[(size_t(k) * a.rows + b) * 3 * E + j];
+        s += a.bias[j];
+        qkv[t] = s;
+        if (a.append && part_ == 1) kh[size_t(pos) * D + d] = s;
+        if (a.append && part_ == 2) vh[size_t(pos) * D + d] = s;
+    }
+    __syncthreads();
+    const int n = pos + 1;
+    const float4 q4 = reinterpret_cast<const float4 *>(qkv)[l];
+    for (int j0 = 0; j0 < n; j0 += RPP * U) {
+        float4 k4[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * RPP + g;
+            k4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j < n)
+                k4[u] = (a.append && j == pos) ? reinterpret_cast<const float4 *>(qkv + D)[l]
+                                               : reinterpret_cast<const float4 *>(kh + size_t(j) * D)[l];
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float d = fmaf(q4.x, k4[u].x, fmaf(q4.y, k4[u].y, fmaf(q4.z, k4[u].z, q4.w * k4[u].w)));
+#pragma unroll
+            for (int o = LPR / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+            const int j = j0 + u * RPP + g;
+            if (l == 0 && j < n) sc[j] = d * a.scale;
+        }
+    }
+    __syncthreads();
+    float m = -INFINITY;
+    for (int j = threadIdx.x; j < n; j += kBT) m = fmaxf(m, sc[j]);
+    m = block_max(m, red);
+    float sum = 0.f;
+    for (int j = threadIdx.x; j < n; j += kBT) {
+        const float p = expf(sc[j] - m);
+        sc[j] = p;
+        sum += p;
+    }
+    sum = block_sum(sum, red);   // (its barriers also publish sc)
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j0 = 0; j0 < n; j0 += RPP * U) {
+        float4 v4[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * RPP + g;
+            v4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j < n)
+                v4[u] = (a.append && j == pos) ? reinterpret_cast<const float4 *>(qkv + 2 * D)[l]
+                                               : reinterpret_cast<const float4 *>(vh + size_t(j) * D)[l];
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * RPP + g;
+            const float p = j < n ? sc[j] : 0.f;
+            acc.x = fmaf(p, v4[u].x, acc.x);
+            acc.y = fmaf(p, v4[u].y, acc.y);
+            acc.z = fmaf(p, v4[u].z, acc.z);
+            acc.w = fmaf(p, v4[u].w, acc.w);
+        }
+    }
+    reinterpret_cast<float4 *>(part[g])[l] = acc;
+    __syncthreads();
+    for (int d = threadIdx.x; d < D; d += kBT) {
+        float o = 0.f;
+        for (int r = 0; r < RPP; ++r) o += part[r][d];
+        put_hi_lo(a.out, b, E, h * D + d, o / sum);
+    }
+    pdl_launch_dependents();
+}
+
+struct BGeluArgs {
+    const float *parts;             // [splits][rows][F]
+    int32_t splits;
+    const float *bias;              // [F]
+    int32_t F, rows;
+    __nv_bfloat16 *out;             // [128][F]
+};
+
+__global__ void __launch_bounds__(kBT) k_b_gelu(const BGeluArgs a)
+{
+    const int b = blockIdx.x, f = blockIdx.y * kBT + threadIdx.x;
+    pdl_wait();
+    if (f < a.F) {
+        float s = 0.f;
+        for (int k = 0; k < a.splits; ++k) s += a.parts[(size_t(k) * a.rows + b) * a.F + f];
+        put_hi_lo(a.out, b, a.F, f, gelu_new(s + a.bias[f]));
+    }
+    pdl_launch_dependents();
+}
+
+struct BArgmaxArgs {
+    const float *logits;            // [rows][V]
+    int32_t V, rows, P;
+    const int32_t *pos;
+    int32_t *next_tok;              // [rows]
+    int32_t *out_ids;               // [P][rows]: the token chosen by the pass at each position
+};
+
+__global__ void __launch_bounds__(1024) k_b_argmax(const BArgmaxArgs a)
+{
+    __shared__ unsigned long long keys[32];
+    const int b = blockIdx.x;
+    pdl_wait();
+    unsigned long long best = 0ull;
+    for (int i = threadIdx.x; i < a.V; i += 1024) {
+        const unsigned long long k = argmax_key(a.logits[size_t(b) * a.V + i], uint32_t(i));
+        best = k > best ? k : best;
+    }
+    best = warp_max_u64(best);
+    if ((threadIdx.x & 31) == 0) keys[threadIdx.x >> 5] = best;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long m = 0ull;
+        for (int w = 0; w < 32; ++w) m = keys[w] > m ? keys[w] : m;
+        const int p = a.pos[b];
+        if (p >= 0 && p < a.P) {
+            const int32_t tok = argmax_key_index(m);
+            a.next_tok[b] = tok;
+            a.out_ids[size_t(p) * a.rows + b] = tok;
+        }
+    }
+    pdl_launch_dependents();
+}
+
+// Feeds each active row's choice to the next step, one position further.
+__global__ void k_b_advance(int32_t *tok, int32_t *pos, const int32_t *next_tok, int rows, int P, DeviceState *st)
+{
+    pdl_wait();
+    const int b = threadIdx.x;
+    if (b < rows && pos[b] >= 0) {
+        tok[b] = next_tok[b];
+        pos[b] = pos[b] + 1 < P ? pos[b] + 1 : -1;   // a full cache stops the row
+    }
+}
+
+// X [n][K] fp32 -> the hi/lo B operand [128][K] (stand-alone linear).
+__global__ void k_b_split_rows(const float *X, int n, int K, __nv_bfloat16 *out)
+{
+    const int r = blockIdx.x;
+    for (int i = threadIdx.x; i < K; i += blockDim.x) put_hi_lo(out, r, K, i, X[size_t(r) * K + i]);
+}
+
+// Y [n][M] = sum over splits of the shares (stand-alone linear).
+__global__ void k_b_sum_splits(const float *parts, int splits, int n, int M, float *Y)
+{
+    const size_t total = size_t(n) * M;
+    for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < total; i += size_t(gridDim.x) * blockDim.x) {
+        float s = 0.f;
+        for (int k = 0; k < splits; ++k) s += parts[size_t(k) * total + i];
+        Y[i] = s;
+    }
+}
+
+cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, void **args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+// K splits of a linear: as many CTAs as the GPU has SMs, about, each with a
+// whole number of 64-input chunks and every split non-empty.
+void plan_splits(int M, int K, int sms, int *splits, int *cps)
+{
+    const int tiles = (M + kTcM - 1) / kTcM, chunks = K / kTcK;
+    int want = std::max(1, std::min(chunks, sms / std::max(1, tiles)));
+    int c = (chunks + want - 1) / want;
+    *cps = c;
+    *splits = (chunks + c - 1) / c;
+}
+
+struct Linear {
+    CUtensorMap a_map;              // the stored weights [planes * M][K] bf16
+    int M, K, splits, cps;
+};
+
+}  // namespace
+
+struct gpt2_batch {
+    gpt2_config cfg{};
+    int wdtype = GPT2_BF16;
+    int max_batch = 0;
+    cudaStream_t stream = nullptr;
+    int num_sms = 0;
+    uint8_t *arena = nullptr;       // weights
+    uint8_t *work = nullptr;        // cache, activations, shares, state
+    // weights
+    float *wte = nullptr, *wpe = nullptr, *lnf_w = nullptr, *lnf_b = nullptr;
+    struct Layer {
+        float *ln1_w, *ln1_b, *attn_b, *proj_b, *ln2_w, *ln2_b, *fc_b, *mlp_proj_b;
+        void *w[4];                 // bf16 [out][in]: QKV, out-projection, fc, MLP projection
+        Linear lin[4];
+    };
+    std::vector<Layer> layers;
+    void *head = nullptr;           // bf16 copy of wte [V][E]
+    Linear head_lin{};
+    // work
+    float *kc = nullptr, *vc = nullptr;                   // [L][slots][H][P][D]
+    float *x = nullptr;                                   // [64][E]
+    __nv_bfloat16 *b_e = nullptr, *b_a = nullptr, *b_f = nullptr;   // [128][E], [128][E], [128][F]
+    CUtensorMap map_e{}, map_a{}, map_f{};
+    float *p_qkv = nullptr, *p_o = nullptr, *p_fc = nullptr, *p_p = nullptr, *logits = nullptr;
+    int32_t *tok = nullptr, *pos = nullptr, *next_tok = nullptr, *out_ids = nullptr;
+    DeviceState *st = nullptr;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    int kernels_per_step = 0;
+    std::vector<int> cached;        // host view: cached length of each sequence
+    bool has_step = false;
+    unsigned long long launches = 0;
+    unsigned long long wait_ns = kWaitLimitNs;
+};
+
+namespace {
+
+int cuda_rc(cudaError_t e)
+{
+    if (e == cudaSuccess) return GPT2_OK;
+    cudaGetLastError();
+    return e == cudaErrorMemoryAllocation ? GPT2_ERR_OUT_OF_MEMORY : GPT2_ERR_CUDA;
+}
+#define BTRY(expr)                                   \
+    do {                                             \
+        cudaError_t _e = (expr);                     \
+        if (_e != cudaSuccess) return cuda_rc(_e);   \
+    } while (0)
+
+size_t a256(size_t v) { return (v + 255) / 256 * 256; }
+
+bool dev_ptr(const void *p)
+{
+    if (!p) return false;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+cudaError_t run_linear(const gpt2_batch *m, const Linear &L, const CUtensorMap &b_map, float *parts, cudaStream_t s,
+                       bool pdl)
+{
+    TcGemmArgs a;
+    a.M = L.M;
+    a.K = L.K;
+    a.n_rows = m->max_batch;
+    a.a_planes = 1;
+    a.chunks_per_split = L.cps;
+    a.partials = parts;
+    a.st = m->st;
+    a.wait_ns = m->wait_ns;
+    return tc_gemm_launch(L.a_map, b_map, a, L.splits, s, pdl);
+}
+
+// Records one batched step on stream s (under capture).
+int record_step(gpt2_batch *m, cudaStream_t s)
+{
+    const gpt2_config &c = m->cfg;
+    const int E = c.n_embd, H = c.n_head, D = E / H, F = 4 * E, R = m->max_batch, P = c.n_positions;
+    const int V = c.vocab_size, L = c.n_layer, slots = m->max_batch;
+    int kernels = 0;
+    bool first = true;
+    auto pdl = [&]() {
+        const bool p = !first;
+        first = false;
+        return p;
+    };
+    const size_t ln_smem = size_t(E) * 4;
+    for (int l = 0; l < L; ++l) {
+        const gpt2_batch::Layer &Ly = m->layers[l];
+        BLnArgs ln{};
+        ln.x = m->x;
+        ln.E = E;
+        ln.rows = R;
+        ln.V = V;
+        ln.P = P;
+        ln.eps = c.ln_eps;
+        ln.st = m->st;
+        ln.out = m->b_e;
+        ln.gamma = Ly.ln1_w;
+        ln.beta = Ly.ln1_b;
+        if (l == 0) {
+            ln.mode = 0;
+            ln.tok = m->tok;
+            ln.pos = m->pos;
+            ln.wte = m->wte;
+            ln.wpe = m->wpe;
+        } else {
+            ln.mode = 1;
+            ln.parts = m->p_p;
+            ln.splits = m->layers[l - 1].lin[3].splits;
+            ln.bias = m->layers[l - 1].mlp_proj_b;
+        }
+        void *a1[] = {&ln};
+        BTRY(launch_pdl(reinterpret_cast<const void *>(k_b_ln), dim3(R), dim3(kBT), ln_smem, s, pdl(), a1));
+        BTRY(run_linear(m, Ly.lin[0], m->map_e, m->p_qkv, s, pdl()));
+        BAttnArgs at{};
+        at.parts = m->p_qkv;
+        at.splits = Ly.lin[0].splits;
+        at.bias = Ly.attn_b;
+        at.kc = m->kc + size_t(l) * slots * H * P * D;
+        at.vc = m->vc + size_t(l) * slots * H * P * D;
+        at.pos = m->pos;
+        at.E = E;
+        at.H = H;
+        at.P = P;
+        at.rows = R;
+        at.slots = slots;
+        at.append = 1;
+        at.scale = float(1.0 / std::sqrt(double(D)));
+        at.out = m->b_a;
+        void *a2[] = {&at};
+        const void *afn = D == 32 ? reinterpret_cast<const void *>(k_b_attn<32>)
+                          : D == 64 ? reinterpret_cast<const void *>(k_b_attn<64>)
+                                    : reinterpret_cast<const void *>(k_b_attn<128>);
+        BTRY(launch_pdl(afn, dim3(R, H), dim3(kBT), size_t(P) * 4, s, pdl(), a2));
+        BTRY(run_linear(m, Ly.lin[1], m->map_a, m->p_o, s, pdl()));
+        ln.mode = 1;
+        ln.parts = m->p_o;
+        ln.splits = Ly.lin[1].splits;
+        ln.bias = Ly.proj_b;
+        ln.gamma = Ly.ln2_w;
+        ln.beta = Ly.ln2_b;
+        void *a3[] = {&ln};
+        BTRY(launch_pdl(reinterpret_cast<const void *>(k_b_ln), dim3(R), dim3(kBT), ln_smem, s, pdl(), a3));
+        BTRY(run_linear(m, Ly.lin[2], m->map_e, m->p_fc, s, pdl()));
+        BGeluArgs ge{};
+        ge.parts = m->p_fc;
+        ge.splits = Ly.lin[2].splits;
+        ge.bias = Ly.fc_b;
+        ge.F = F;
+        ge.rows = R;
+        ge.out = m->b_f;
+        void *a4[] = {&ge};
+        BTRY(launch_pdl(reinterpret_cast<const void *>(k_b_gelu), dim3(R, (F + kBT - 1) / kBT), dim3(kBT), 0, s,
+                        pdl(), a4));
+        BTRY(run_linear(m, Ly.lin[3], m->map_f, m->p_p, s, pdl()));
+        kernels += 8;
+    }
+    BLnArgs ln{};
+    ln.x = m->x;
+    ln.E = E;
+    ln.rows = R;
+    ln.V = V;
+    ln.P = P;
+    ln.eps = c.ln_eps;
+    ln.st = m->st;
+    ln.out = m->b_e;
+    ln.mode = 1;
+    ln.parts = m->p_p;
+    ln.splits = m->layers[L - 1].lin[3].splits;
+    ln.bias = m->layers[L - 1].mlp_proj_b;
+    ln.gamma = m->lnf_w;
+    ln.beta = m->lnf_b;
+    void *a5[] = {&ln};
+    BTRY(launch_pdl(reinterpret_cast<const void *>(k_b_ln), dim3(R), dim3(kBT), ln_smem, s, pdl(), a5));
+    BTRY(run_linear(m, m->head_lin, m->map_e, m->logits, s, pdl()));
+    BArgmaxArgs am{};
+    am.logits = m->logits;
+    am.V = V;
+    am.rows = R;
+    am.P = P;
+    am.pos = m->pos;
+    am.next_tok = m->next_tok;
+    am.out_ids = m->out_ids;
+    void *a6[] = {&am};
+    BTRY(launch_pdl(reinterpret_cast<const void *>(k_b_argmax), dim3(R), dim3(1024), 0, s, pdl(), a6));
+    int32_t *tk = m->tok, *ps = m->pos;
+    const int32_t *nt = m->next_tok;
+    int rows = R, pp = P;
+    DeviceState *st = m->st;
+    void *a7[] = {&tk, &ps, &nt, &rows, &pp, &st};
+    BTRY(launch_pdl(reinterpret_cast<const void *>(k_b_advance), dim3(1), dim3(kTcMaxRows), 0, s, pdl(), a7));
+    m->kernels_per_step = kernels + 4;
+    return GPT2_OK;
+}
+
+int build_step_graph(gpt2_batch *m)
+{
+    cudaStream_t cs;
+    BTRY(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
+    cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) {
+        cudaStreamDestroy(cs);
+        return cuda_rc(e);
+    }
+    const int rc = record_step(m, cs);
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(cs, &g);
+    cudaStreamDestroy(cs);
+    if (rc != GPT2_OK) {
+        if (g) cudaGraphDestroy(g);
+        return rc;
+    }
+    if (e != cudaSuccess) return cuda_rc(e);
+    m->graph = g;
+    BTRY(cudaGraphInstantiate(&m->exec, g, 0));
+    return GPT2_OK;
+}
+
+void free_batch(gpt2_batch *m)
+{
+    if (!m) return;
+    if (m->exec) cudaGraphExecDestroy(m->exec);
+    if (m->graph) cudaGraphDestroy(m->graph);
+    if (m->arena) cudaFree(m->arena);
+    if (m->work) cudaFree(m->work);
+    delete m;
+}
+
+int read_batch_state(gpt2_batch *m)
+{
+    BTRY(cudaStreamSynchronize(m->stream));
+    DeviceState hs;
+    BTRY(cudaMemcpy(&hs, m->st, sizeof hs, cudaMemcpyDeviceToHost));
+    if (hs.err != kDevErrNone) {
+        BTRY(cudaMemset(&m->st->err, 0, 3 * sizeof(int32_t)));
+        return hs.err == kDevErrTimeout ? GPT2_ERR_TIMEOUT : GPT2_ERR_DEVICE_STATE;
+    }
+    return GPT2_OK;
+}
+
+int set_linear(Linear &L, const void *w, int M, int K, int sms)
+{
+    L.M = M;
+    L.K = K;
+    plan_splits(M, K, sms, &L.splits, &L.cps);
+    return tc_make_tmap(&L.a_map, w, uint64_t(M), uint64_t(K)) == 0 ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gpt2_create_batch(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype, int32_t max_batch, void *stream,
+                      gpt2_batch **out)
+{
+    if (!out) return GPT2_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!cfg || !w || !w->layers) return GPT2_ERR_INVALID_ARG;
+    if (wdtype != GPT2_BF16) return GPT2_ERR_INVALID_ARG;
+    if (max_batch < 1 || max_batch > kTcMaxRows) return GPT2_ERR_INVALID_ARG;
+    const int L = cfg->n_layer, E = cfg->n_embd, H = cfg->n_head, P = cfg->n_positions, V = cfg->vocab_size;
+    if (L < 1 || H < 1 || P < 1 || V < 1 || E < 64 || E % 64 || E % H) return GPT2_ERR_INVALID_ARG;
+    const int D = E / H, F = 4 * E;
+    if (D != 32 && D != 64 && D != 128) return GPT2_ERR_INVALID_ARG;
+    if (!(cfg->ln_eps > 0.f) || !std::isfinite(cfg->ln_eps)) return GPT2_ERR_INVALID_ARG;
+    if ((long long)V * E > (1ll << 31) - 1 || (long long)P * 4 > 48 * 1024) return GPT2_ERR_INVALID_ARG;
+    int dev;
+    BTRY(cudaGetDevice(&dev));
+    cudaDeviceProp prop;
+    BTRY(cudaGetDeviceProperties(&prop, dev));
+    if (!(prop.major == 10 && prop.minor == 3)) return GPT2_ERR_UNSUPPORTED_DEVICE;
+    const float *top[4] = {w->wte, w->wpe, w->ln_f_w, w->ln_f_b};
+    for (const float *p : top)
+        if (!dev_ptr(p)) return GPT2_ERR_INVALID_ARG;
+    for (int l = 0; l < L; ++l) {
+        const gpt2_layer_weights &Lw = w->layers[l];
+        const float *ps[12] = {Lw.ln1_w, Lw.ln1_b, Lw.attn_w, Lw.attn_b, Lw.proj_w, Lw.proj_b,
+                               Lw.ln2_w, Lw.ln2_b, Lw.fc_w,   Lw.fc_b,   Lw.mlp_proj_w, Lw.mlp_proj_b};
+        for (const float *p : ps)
+            if (!dev_ptr(p)) return GPT2_ERR_INVALID_ARG;
+    }
+    BTRY(tc_gemm_init());
+
+    gpt2_batch *m = new (std::nothrow) gpt2_batch();
+    if (!m) return GPT2_ERR_OUT_OF_MEMORY;
+    m->cfg = *cfg;
+    m->max_batch = max_batch;
+    m->stream = static_cast<cudaStream_t>(stream);
+    m->num_sms = prop.multiProcessorCount;
+    m->cached.assign(max_batch, 0);
+    const int mat_in[4] = {E, E, E, F}, mat_out[4] = {3 * E, E, F, E};
+    // ---- weights ----
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += a256(bytes);
+        return o;
+    };
+    const size_t o_wte = take(size_t(V) * E * 4), o_wpe = take(size_t(P) * E * 4);
+    const size_t o_lnf_w = take(size_t(E) * 4), o_lnf_b = take(size_t(E) * 4);
+    const size_t o_head = take(size_t(V) * E * 2);
+    struct LO {
+        size_t p[8], w[4];
+    };
+    std::vector<LO> lo(L);
+    const int psz[8] = {E, E, 3 * E, E, E, E, F, E};
+    for (int l = 0; l < L; ++l) {
+        for (int k = 0; k < 8; ++k) lo[l].p[k] = take(size_t(psz[k]) * 4);
+        for (int k = 0; k < 4; ++k) lo[l].w[k] = take(size_t(mat_in[k]) * mat_out[k] * 2);
+    }
+    const size_t arena_bytes = off;
+    // ---- work ----
+    off = 0;
+    const size_t kv = size_t(L) * max_batch * H * P * D * 4;
+    const size_t o_k = take(kv), o_v = take(kv);
+    const size_t o_x = take(size_t(kTcMaxRows) * E * 4);
+    const size_t o_be = take(size_t(2 * kTcMaxRows) * E * 2), o_ba = take(size_t(2 * kTcMaxRows) * E * 2);
+    const size_t o_bf = take(size_t(2 * kTcMaxRows) * F * 2);
+    int sp[4], cps[4];
+    for (int k = 0; k < 4; ++k) plan_splits(mat_out[k], mat_in[k], m->num_sms, &sp[k], &cps[k]);
+    const size_t o_pq = take(size_t(sp[0]) * max_batch * 3 * E * 4), o_po = take(size_t(sp[1]) * max_batch * E * 4);
+    const size_t o_pf = take(size_t(sp[2]) * max_batch * F * 4), o_pp = take(size_t(sp[3]) * max_batch * E * 4);
+    const size_t o_lg = take(size_t(max_batch) * V * 4);
+    const size_t o_tok = take(size_t(kTcMaxRows) * 4), o_pos = take(size_t(kTcMaxRows) * 4);
+    const size_t o_nt = take(size_t(kTcMaxRows) * 4), o_ids = take(size_t(P) * max_batch * 4);
+    const size_t o_st = take(sizeof(DeviceState));
+    const size_t work_bytes = off;
+    cudaError_t e = cudaMalloc(&m->arena, arena_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&m->work, work_bytes);
+    if (e != cudaSuccess) {
+        free_batch(m);
+        return cuda_rc(e);
+    }
+    uint8_t *A = m->arena, *W = m->work;
+    m->wte = reinterpret_cast<float *>(A + o_wte);
+    m->wpe = reinterpret_cast<float *>(A + o_wpe);
+    m->lnf_w = reinterpret_cast<float *>(A + o_lnf_w);
+    m->lnf_b = reinterpret_cast<float *>(A + o_lnf_b);
+    m->head = A + o_head;
+    m->layers.resize(L);
+    cudaStream_t s = m->stream;
+    int rc = GPT2_OK;
+#define BCK(expr)                        \
+    do {                                 \
+        cudaError_t _e2 = (expr);        \
+        if (_e2 != cudaSuccess) {        \
+            rc = cuda_rc(_e2);           \
+            goto fail;                   \
+        }                                \
+    } while (0)
+    BCK(cudaMemsetAsync(m->work, 0, work_bytes, s));
+    BCK(cudaMemcpyAsync(m->wte, w->wte, size_t(V) * E * 4, cudaMemcpyDeviceToDevice, s));
+    BCK(cudaMemcpyAsync(m->wpe, w->wpe, size_t(P) * E * 4, cudaMemcpyDeviceToDevice, s));
+    BCK(cudaMemcpyAsync(m->lnf_w, w->ln_f_w, size_t(E) * 4, cudaMemcpyDeviceToDevice, s));
+    BCK(cudaMemcpyAsync(m->lnf_b, w->ln_f_b, size_t(E) * 4, cudaMemcpyDeviceToDevice, s));
+    BCK(split_bf16(w->wte, size_t(V) * E, m->head, nullptr, s));   // the head's bf16 copy (the embedding reads fp32)
+    for (int l = 0; l < L; ++l) {
+        const gpt2_layer_weights &src = w->layers[l];
+        gpt2_batch::Layer &d = m->layers[l];
+        float **pp[8] = {&d.ln1_w, &d.ln1_b, &d.attn_b, &d.proj_b, &d.ln2_w, &d.ln2_b, &d.fc_b, &d.mlp_proj_b};
+        const float *ps[8] = {src.ln1_w, src.ln1_b, src.attn_b, src.proj_b, src.ln2_w, src.ln2_b, src.fc_b,
+                              src.mlp_proj_b};
+        for (int k = 0; k < 8; ++k) {
+            *pp[k] = reinterpret_cast<float *>(A + lo[l].p[k]);
+            BCK(cudaMemcpyAsync(*pp[k], ps[k], size_t(psz[k]) * 4, cudaMemcpyDeviceToDevice, s));
+        }
+        const float *sm[4] = {src.attn_w, src.proj_w, src.fc_w, src.mlp_proj_w};
+        for (int k = 0; k < 4; ++k) {
+            d.w[k] = A + lo[l].w[k];
+            BCK(repack_bf16(sm[k], mat_in[k], mat_out[k], d.w[k], s));
+            rc = set_linear(d.lin[k], d.w[k], mat_out[k], mat_in[k], m->num_sms);
+            if (rc != GPT2_OK) goto fail;
+        }
+    }
+    rc = set_linear(m->head_lin, m->head, V, E, m->num_sms);
+    if (rc != GPT2_OK) goto fail;
+    m->head_lin.splits = 1;                       // whole logits from one pass over K
+    m->head_lin.cps = E / kTcK;
+    m->kc = reinterpret_cast<float *>(W + o_k);
+    m->vc = reinterpret_cast<float *>(W + o_v);
+    m->x = reinterpret_cast<float *>(W + o_x);
+    m->b_e = reinterpret_cast<__nv_bfloat16 *>(W + o_be);
+    m->b_a = reinterpret_cast<__nv_bfloat16 *>(W + o_ba);
+    m->b_f = reinterpret_cast<__nv_bfloat16 *>(W + o_bf);
+    m->p_qkv = reinterpret_cast<float *>(W + o_pq);
+    m->p_o = reinterpret_cast<float *>(W + o_po);
+    m->p_fc = reinterpret_cast<float *>(W + o_pf);
+    m->p_p = reinterpret_cast<float *>(W + o_pp);
+    m->logits = reinterpret_cast<float *>(W + o_lg);
+    m->tok = reinterpret_cast<int32_t *>(W + o_tok);
+    m->pos = reinterpret_cast<int32_t *>(W + o_pos);
+    m->next_tok = reinterpret_cast<int32_t *>(W + o_nt);
+    m->out_ids = reinterpret_cast<int32_t *>(W + o_ids);
+    m->st = reinterpret_cast<DeviceState *>(W + o_st);
+    if (tc_make_tmap(&m->map_e, m->b_e, 2 * kTcMaxRows, uint64_t(E)) ||
+        tc_make_tmap(&m->map_a, m->b_a, 2 * kTcMaxRows, uint64_t(E)) ||
+        tc_make_tmap(&m->map_f, m->b_f, 2 * kTcMaxRows, uint64_t(F))) {
+        rc = GPT2_ERR_CUDA;
+        goto fail;
+    }
+    {
+        std::vector<int32_t> neg(kTcMaxRows, -1);   // every row inactive until a call feeds it
+        BCK(cudaMemcpyAsync(m->pos, neg.data(), neg.size() * 4, cudaMemcpyHostToDevice, s));
+        BCK(cudaStreamSynchronize(s));
+    }
+    rc = build_step_graph(m);
+    if (rc != GPT2_OK) goto fail;
+    *out = m;
+    return GPT2_OK;
+fail:
+    cudaStreamSynchronize(s);
+    free_batch(m);
+    return rc;
+#undef BCK
+}
+
+void gpt2_destroy_batch(gpt2_batch *m)
+{
+    if (!m) return;
+    cudaStreamSynchronize(m->stream);
+    free_batch(m);
+}
+
+int gpt2_decode_batch(gpt2_batch *m, const int32_t *tokens, const int32_t *positions, int32_t n,
+                      const float **dev_logits)
+{
+    if (!m || !tokens || !positions || n < 1 || n > m->max_batch) return GPT2_ERR_INVALID_ARG;
+    const gpt2_config &c = m->cfg;
+    std::vector<int32_t> t(kTcMaxRows, 0), p(kTcMaxRows, -1);
+    for (int b = 0; b < n; ++b) {
+        if (positions[b] == -1) continue;          // this sequence sits the step out
+        if (tokens[b] < 0 || tokens[b] >= c.vocab_size) return GPT2_ERR_TOKEN_RANGE;
+        if (positions[b] < 0 || positions[b] >= c.n_positions || positions[b] > m->cached[b])
+            return GPT2_ERR_POSITION_RANGE;
+        t[b] = tokens[b];
+        p[b] = positions[b];
+    }
+    BTRY(cudaMemcpyAsync(m->tok, t.data(), t.size() * 4, cudaMemcpyHostToDevice, m->stream));
+    BTRY(cudaMemcpyAsync(m->pos, p.data(), p.size() * 4, cudaMemcpyHostToDevice, m->stream));
+    BTRY(cudaGraphLaunch(m->exec, m->stream));
+    m->launches += m->kernels_per_step;
+    for (int b = 0; b < n; ++b)
+        if (p[b] >= 0) m->cached[b] = p[b] + 1;
+    m->has_step = true;
+    if (dev_logits) *dev_logits = m->logits;
+    return GPT2_OK;
+}
+
+int gpt2_prefill_batch(gpt2_batch *m, const int32_t *ids, const int32_t *lens, int32_t n)
+{
+    if (!m || !ids || !lens || n < 1 || n > m->max_batch) return GPT2_ERR_INVALID_ARG;
+    int max_len = 0;
+    size_t total = 0;
+    for (int b = 0; b < n; ++b) {
+        if (lens[b] < 1 || lens[b] > m->cfg.n_positions) return GPT2_ERR_POSITION_RANGE;
+        max_len = std::max(max_len, int(lens[b]));
+        total += size_t(lens[b]);
+    }
+    for (size_t i = 0; i < total; ++i)
+        if (ids[i] < 0 || ids[i] >= m->cfg.vocab_size) return GPT2_ERR_TOKEN_RANGE;
+    std::fill(m->cached.begin(), m->cached.end(), 0);
+    std::vector<size_t> start(n, 0);
+    for (int b = 1; b < n; ++b) start[b] = start[b - 1] + size_t(lens[b - 1]);
+    std::vector<int32_t> t(n), p(n);
+    for (int step = 0; step < max_len; ++step) {
+        for (int b = 0; b < n; ++b) {
+            const bool on = step < lens[b];
+            t[b] = on ? ids[start[b] + step] : 0;
+            p[b] = on ? step : -1;
+        }
+        const int rc = gpt2_decode_batch(m, t.data(), p.data(), n, nullptr);
+        if (rc != GPT2_OK) return rc;
+    }
+    return GPT2_OK;
+}
+
+int gpt2_decode_batch_greedy(gpt2_batch *m, int32_t n_steps)
+{
+    if (!m || n_steps < 0) return GPT2_ERR_INVALID_ARG;
+    if (!m->has_step) return GPT2_ERR_NOT_READY;
+    for (int b = 0; b < m->max_batch; ++b)
+        if (m->cached[b] > 0 && m->cached[b] + n_steps > m->cfg.n_positions) return GPT2_ERR_POSITION_RANGE;
+    if (n_steps == 0) return GPT2_OK;
+    // every sequence with a cached prefix continues from its own length with
+    // its last choice
+    std::vector<int32_t> p(kTcMaxRows, -1);
+    for (int b = 0; b < m->max_batch; ++b)
+        if (m->cached[b] > 0) p[b] = m->cached[b];
+    BTRY(cudaMemcpyAsync(m->pos, p.data(), p.size() * 4, cudaMemcpyHostToDevice, m->stream));
+    BTRY(cudaMemcpyAsync(m->tok, m->next_tok, size_t(kTcMaxRows) * 4, cudaMemcpyDeviceToDevice, m->stream));
+    for (int i = 0; i < n_steps; ++i) BTRY(cudaGraphLaunch(m->exec, m->stream));
+    m->launches += (unsigned long long)n_steps * m->kernels_per_step;
+    for (int b = 0; b < m->max_batch; ++b)
+        if (m->cached[b] > 0) m->cached[b] += n_steps;
+    return GPT2_OK;
+}
+
+int gpt2_argmax_batch(gpt2_batch *m, int32_t *host_ids, int32_t n)
+{
+    if (!m || !host_ids || n < 1 || n > m->max_batch) return GPT2_ERR_INVALID_ARG;
+    if (!m->has_step) return GPT2_ERR_NOT_READY;
+    const int rc = read_batch_state(m);
+    if (rc != GPT2_OK) return rc;
+    BTRY(cudaMemcpy(host_ids, m->next_tok, size_t(n) * 4, cudaMemcpyDeviceToHost));
+    return GPT2_OK;
+}
+
+int gpt2_batch_ids(gpt2_batch *m, int32_t first_pos, int32_t n_pos, int32_t *host_ids)
+{
+    if (!m || !host_ids || first_pos < 0 || n_pos < 0 || first_pos + n_pos > m->cfg.n_positions)
+        return GPT2_ERR_INVALID_ARG;
+    const int rc = read_batch_state(m);
+    if (rc != GPT2_OK) return rc;
+    BTRY(cudaMemcpy(host_ids, m->out_ids + size_t(first_pos) * m->max_batch, size_t(n_pos) * m->max_batch * 4,
+                    cudaMemcpyDeviceToHost));
+    return GPT2_OK;
+}
+
+int gpt2_copy_logits_batch(gpt2_batch *m, int32_t n, float *dst)
+{
+    if (!m || !dst || n < 1 || n > m->max_batch) return GPT2_ERR_INVALID_ARG;
+    if (!m->has_step) return GPT2_ERR_NOT_READY;
+    BTRY(cudaMemcpyAsync(dst, m->logits, size_t(n) * m->cfg.vocab_size * 4, cudaMemcpyDefault, m->stream));
+    return read_batch_state(m);
+}
+
+int gpt2_export_kv_batch(gpt2_batch *m, int32_t layer, int32_t seq, int32_t n_rows, float *dst_k, float *dst_v)
+{
+    if (!m || layer < 0 || layer >= m->cfg.n_layer || seq < 0 || seq >= m->max_batch) return GPT2_ERR_INVALID_ARG;
+    const int H = m->cfg.n_head, D = m->cfg.n_embd / H, P = m->cfg.n_positions;
+    if (n_rows < 0 || n_rows > P) return GPT2_ERR_INVALID_ARG;
+    for (int h = 0; h < H; ++h) {
+        const size_t src = ((size_t(layer) * m->max_batch + seq) * H + h) * P * D;
+        const size_t bytes = size_t(n_rows) * D * 4;
+        if (dst_k) BTRY(cudaMemcpyAsync(dst_k + size_t(h) * n_rows * D, m->kc + src, bytes, cudaMemcpyDefault, m->stream));
+        if (dst_v) BTRY(cudaMemcpyAsync(dst_v + size_t(h) * n_rows * D, m->vc + src, bytes, cudaMemcpyDefault, m->stream));
+    }
+    BTRY(cudaStreamSynchronize(m->stream));
+    return GPT2_OK;
+}
+
+int gpt2_batch_info(const gpt2_batch *m, int32_t *kernels_per_step, uint64_t *launches)
+{
+    if (!m) return GPT2_ERR_INVALID_ARG;
+    if (kernels_per_step) *kernels_per_step = m->kernels_per_step;
+    if (launches) *launches = m->launches;
+    return GPT2_OK;
+}
+
+int gpt2_sync_batch(gpt2_batch *m)
+{
+    if (!m) return GPT2_ERR_INVALID_ARG;
+    return read_batch_state(m);
+}
+
+// ---- the stand-alone tensor-core linear ------------------------------------
+
+size_t gpt2_op_linear_bf16_workspace(int32_t M, int32_t n, int32_t K)
+{
+    if (M < 1 || K < kTcK || n < 1) return 0;
+    int sp, cps;
+    plan_splits(M, K, 148, &sp, &cps);
+    return a256(size_t(2 * kTcMaxRows) * K * 2) + a256(size_t(K / kTcK) * n * M * 4);
+}
+
+int gpt2_op_linear_bf16(const void *W, const float *X, int32_t M, int32_t n, int32_t K, float *Y, void *workspace,
+                        size_t workspace_bytes, void *stream)
+{
+    if (!W || !X || !Y || !workspace) return GPT2_ERR_INVALID_ARG;
+    if (M < 1 || n < 1 || n > kTcMaxRows || K < kTcK || K % kTcK) return GPT2_ERR_INVALID_ARG;
+    if ((long long)M * K > (1ll << 31) - 1) return GPT2_ERR_INVALID_ARG;
+    if (workspace_bytes < gpt2_op_linear_bf16_workspace(M, n, K)) return GPT2_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(W) % 16 || reinterpret_cast<uintptr_t>(workspace) % 256)
+        return GPT2_ERR_INVALID_ARG;
+    int dev, sms;
+    BTRY(cudaGetDevice(&dev));
+    cudaDeviceProp prop;
+    BTRY(cudaGetDeviceProperties(&prop, dev));
+    if (!(prop.major == 10 && prop.minor == 3)) return GPT2_ERR_UNSUPPORTED_DEVICE;
+    sms = prop.multiProcessorCount;
+    BTRY(tc_gemm_init());
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    __nv_bfloat16 *bop = static_cast<__nv_bfloat16 *>(workspace);
+    float *parts = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + a256(size_t(2 * kTcMaxRows) * K * 2));
+    Linear L;
+    if (set_linear(L, W, M, K, sms) != GPT2_OK) return GPT2_ERR_CUDA;
+    CUtensorMap bmap;
+    if (tc_make_tmap(&bmap, bop, 2 * kTcMaxRows, uint64_t(K))) return GPT2_ERR_CUDA;
+    BTRY(cudaMemsetAsync(bop, 0, size_t(2 * kTcMaxRows) * K * 2, s));
+    k_b_split_rows<<<n, 256, 0, s>>>(X, n, K, bop);
+    BTRY(cudaGetLastError());
+    TcGemmArgs a;
+    a.M = M;
+    a.K = K;
+    a.n_rows = n;
+    a.a_planes = 1;
+    a.chunks_per_split = L.cps;
+    a.partials = parts;
+    a.st = nullptr;
+    a.wait_ns = kWaitLimitNs;
+    BTRY(tc_gemm_launch(L.a_map, bmap, a, L.splits, s, false));
+    k_b_sum_splits<<<std::min(4096, (n * M + 255) / 256), 256, 0, s>>>(parts, L.splits, n, M, Y);
+    BTRY(cudaGetLastError());
+    return GPT2_OK;
+}
+
+}  // extern "C"
