@@ -14,8 +14,12 @@ The same run also times the two other single-sequence configurations, each
 over whole cycles of its own generation, and reports them under "variants":
 int4 block matrices (10-token prompt + 128 steps) and fp16 block matrices
 (16-token prompt decoded to the full 1024-position cache, 1008 steps, with
-tok/s and GB/s per 64 positions in "context_sweep").  --wdtype picks one of
-them as the headline instead (then no variants).
+tok/s and GB/s per 64 positions in "context_sweep"), and the batched
+configuration: 64 independent sequences with bf16 weights on the tensor
+cores, prompts of 32..512 tokens prefilled untimed, then 64 device-fed
+greedy steps of all 64 sequences (aggregate tok/s = 64 x steps / time).
+--wdtype picks one of the single-sequence configurations as the headline
+instead (then no variants).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--wdtype f32|f16|int4]
   python bench.py --impl reference ...     # the CPU oracle, same metric
@@ -46,6 +50,9 @@ UNIT = "tok/s"
 # 1024-position cache, with tok/s reported per 64 positions).
 WORKLOADS = {"f32": (10, 60), "int4": (10, 128), "f16": (16, 1008)}
 SWEEP_BUCKET = 64
+# The batched configuration: 64 independent sequences, bf16 weights, prompts
+# of uniform length in [32, 512] (seed 2), 64 greedy steps per sequence.
+BATCH, BATCH_PROMPT, BATCH_STEPS = 64, (32, 512), 64
 CLOCK_FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
                 "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
                 "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
@@ -430,6 +437,112 @@ def measure(torch, cfg, w, wdtype, head, path, steps, warmup, world, local, barr
     return out
 
 
+def measure_batch(torch, cfg, w, steps, warmup, world, local, barrier, max_over_ranks):
+    """The batched configuration on a fresh batched model: an untimed prefill
+    of the 64 ragged prompts, then 64 device-resident greedy steps timed;
+    repeated (each after a fresh prefill) until `steps` steps are timed."""
+    from transformer_decode_token_gb300 import binding, roofline, synth
+    prompts = synth.make_batch_prompts(cfg, BATCH, *BATCH_PROMPT, seed=2)
+    lens = [len(q) for q in prompts]
+    dw = binding.upload_weights(w)
+    m = binding.BatchModel(cfg, dw, BATCH)
+    del dw
+    torch.cuda.empty_cache()
+    try:
+        kps, _ = m.info()
+        m.prefill(prompts)
+        m.decode_greedy(min(warmup, BATCH_STEPS))
+        m.sync()
+        cycles = max(1, -(-steps // BATCH_STEPS))
+        stream = torch.cuda.current_stream()
+        ms = 0.0
+        launches = 0
+        sampler = ClockSampler(gpu_id_for(torch, local))
+        sampler.start()
+        t_begin = time.time()
+        for _ in range(cycles):
+            m.prefill(prompts)
+            m.sync()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            barrier()
+            torch.cuda.synchronize()
+            n0 = m.info()[1]
+            e0.record(stream)
+            m.decode_greedy(BATCH_STEPS)
+            e1.record(stream)
+            launches += m.info()[1] - n0
+            torch.cuda.synchronize()
+            ms += e0.elapsed_time(e1)
+        t_end = time.time()
+        clocks = sampler.stop(t_begin, t_end)
+        m.sync()
+    finally:
+        m.close()
+    ms = max_over_ranks(ms)
+    n_steps = cycles * BATCH_STEPS
+    # bytes and flops of the timed steps: step t runs every sequence at lens + t
+    alg = sum(roofline.batched_bytes_per_step(cfg, [L + t for L in lens])["total"] for t in range(BATCH_STEPS))
+    alg /= BATCH_STEPS
+    flops = roofline.batched_flops_per_step(cfg, BATCH)
+    peaks, peak_kind = measured_peaks()
+    step_s = ms / 1e3 / n_steps
+    achieved = alg / step_s / 1e9
+    return {
+        "value": BATCH * world / step_s, "unit": UNIT, "ms_per_step": ms / n_steps, "steps": n_steps,
+        "gpu_launches": launches, "clocks": clocks, "dtype": "bf16 weights, f32 math (bf16 x bf16 tensor-core "
+                                                                "products of hi/lo activation parts, fp32 sums)",
+        "config": {"workload": f"GPT-2 small 124M, batched: {BATCH} sequences, bf16 block weights and head, "
+                               f"prompts uniform in [{BATCH_PROMPT[0]}, {BATCH_PROMPT[1]}] tokens (seed 2), "
+                               f"{BATCH_STEPS} greedy decode steps per sequence (prefill untimed)",
+                   "batch": BATCH, "prompt_tokens": sum(lens), "weights": "synthetic N(0,0.02), seed 0"},
+        "roofline": {"bound": "hbm", "kernel": f"one batched step: a CUDA graph of {kps} kernels (tcgen05 linears, "
+                                               "ragged attention, LayerNorm/gelu/argmax), PDL-chained",
+                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "peak_kind": f"{peak_kind} copy bandwidth",
+                     "traffic": None, "algorithmic_bytes_per_launch": alg,
+                     "tensor_tflops": flops / step_s / 1e12,
+                     "tensor_frac": flops / step_s / 1e12 / peaks.get("bf16_tflops", 1900.0),
+                     "note": "bytes: weights once per step + each sequence's KV rows 0..p, embedding and logits "
+                             "rows; flops: 2 x 64 x the linears' and head's multiply-adds (the hi/lo parts "
+                             "double the tensor work actually issued)"},
+    }
+
+
+def measure_prefill(torch, cfg, w, lengths=(2, 4, 8, 10, 16, 64), reps=10):
+    """gpt2_prefill of prompts of several lengths (fp32 weights), on the tensor
+    cores (the default on the cluster path) and as single-token passes of the
+    cluster kernel (one launch of n passes): device time per call."""
+    from transformer_decode_token_gb300 import binding, synth
+    out = {}
+    stream = torch.cuda.current_stream()
+    dw = binding.upload_weights(w)
+    for name, tc in (("tensor_cores", True), ("single_token_passes", False)):
+        m = binding.Model(cfg, dw, "f32", tc_prefill=tc)
+        try:
+            row = {}
+            for n in lengths:
+                prompt = synth.make_prompt(cfg, n, 1)
+                m.prefill(prompt)
+                m.sync()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(reps):
+                    m.prefill(prompt)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                m.sync()
+                row[str(n)] = e0.elapsed_time(e1) / reps
+            out[name] = row
+        finally:
+            m.close()
+    del dw
+    torch.cuda.empty_cache()
+    out["unit"] = "ms per gpt2_prefill call"
+    out["note"] = ("tensor cores: the prompt's positions as the rows of one batched step (up to 64 per step); "
+                   "single-token passes: one cluster-kernel launch running n passes")
+    return out
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -479,7 +592,10 @@ def main():
             v["config"] = workload_config(wd, world)
             v["dtype"] = f"{wd} weights, f32 math"
             variants[wd] = v
+        variants["batch64_bf16"] = measure_batch(torch, cfg, w, args.steps, args.warmup, world, local, barrier,
+                                                 max_over_ranks)
         line["variants"] = variants
+        line["prefill"] = measure_prefill(torch, cfg, w)
 
     # ---- CPU baseline: the oracle on this host (rank 0, N = 1) ---------------
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -162,6 +162,16 @@ int gpt2_create(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
  * of the bytes; the embedding still reads the fp32 wte.  Cluster path only,
  * n_embd % 64 == 0; not together with GPT2_FLAG_HEAD_F16. */
 #define GPT2_FLAG_HEAD_INT4 8
+/* Prompts (gpt2_prefill, gpt2_generate) on the cluster path run, by default,
+ * on the tensor cores: the prompt's positions become the rows of one batched
+ * step (see gpt2_create_batch), up to 64 positions per step, with the stored
+ * block matrices and head held again as bf16 hi + lo planes (about 16 bits of
+ * each weight, fp32 sums; greedy choice; 340 MB more for GPT-2 small's block
+ * matrices, plus the head's planes).  Prompts of fewer than 5 tokens (where
+ * single-token passes are faster), or a model with a sampling temperature,
+ * use single-token passes.  GPT2_FLAG_NO_TC_PREFILL keeps every prompt on
+ * single-token passes. */
+#define GPT2_FLAG_NO_TC_PREFILL 16
 int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
                    int32_t flags, void *stream, gpt2_model **out);
 

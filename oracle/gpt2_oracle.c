@@ -352,6 +352,21 @@ void orc_reset(orc_model *m)
     if (m) m->cached = 0;
 }
 
+/* Copies the cached K and V rows 0..n_rows-1 of one layer, [H][n_rows][D]
+ * each (a copy of the cache the decode passes fill, for inspection). */
+int32_t orc_export_kv(const orc_model *m, int32_t layer, int32_t n_rows, float *k, float *v)
+{
+    const orc_config *c = &m->cfg;
+    const int32_t H = c->n_head, D = c->n_embd / H, P = c->n_positions;
+    if (layer < 0 || layer >= c->n_layer || n_rows < 0 || n_rows > m->cached) return -1;
+    for (int32_t h = 0; h < H; ++h) {
+        const size_t src = ((size_t)layer * H + h) * P * D, dst = (size_t)h * n_rows * D;
+        memcpy(k + dst, m->k_cache + src, sizeof(float) * (size_t)n_rows * D);
+        memcpy(v + dst, m->v_cache + src, sizeof(float) * (size_t)n_rows * D);
+    }
+    return 0;
+}
+
 int32_t orc_forward(orc_model *m, int32_t token, int32_t pos, float *logits)
 {
     const orc_config *c = &m->cfg;

@@ -134,6 +134,9 @@ float orc_uniform(uint64_t seed, uint64_t k);
 void orc_sample_scores(const float *s, int32_t n, float T, uint64_t seed, int32_t pos, float *out);
 int32_t orc_sample(const float *s, int32_t n, float T, uint64_t seed, int32_t pos);
 
+/* The cached K and V rows 0..n_rows-1 of one layer, [H][n_rows][D] each. */
+int32_t orc_export_kv(const orc_model *m, int32_t layer, int32_t n_rows, float *k, float *v);
+
 /* nibble helpers (for the round-trip pin) */
 void orc_pack_nibbles(const uint8_t *vals, size_t n, uint8_t *packed);
 void orc_unpack_nibbles(const uint8_t *packed, size_t n, uint8_t *vals);

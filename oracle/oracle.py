@@ -99,6 +99,8 @@ def lib(omp: bool = False):
             L.orc_reset.argtypes = [vp]
             L.orc_forward.restype = c_i32
             L.orc_forward.argtypes = [vp, c_i32, c_i32, vp]
+            L.orc_export_kv.restype = c_i32
+            L.orc_export_kv.argtypes = [vp, c_i32, c_i32, vp, vp]
             L.orc_forward_full.restype = c_i32
             L.orc_forward_full.argtypes = [ctypes.POINTER(_Cfg), ctypes.POINTER(_Weights),
                                            vp, c_i32, vp]
@@ -399,6 +401,15 @@ class OracleModel:
         if r < 0:
             raise ValueError(f"oracle: bad token {token} or position {pos}")
         return logits, int(r)
+
+    def export_kv(self, layer: int, n_rows: int):
+        """The cached K and V rows 0..n_rows-1 of one layer, [H][n_rows][D] each."""
+        H, D = self.cfg.n_head, self.cfg.n_embd // self.cfg.n_head
+        k = np.empty((H, n_rows, D), np.float32)
+        v = np.empty((H, n_rows, D), np.float32)
+        if self._lib.orc_export_kv(self._m, layer, n_rows, _p(k), _p(v)) != 0:
+            raise ValueError("oracle: bad layer or row count")
+        return k, v
 
     def reset(self):
         self._lib.orc_reset(self._m)

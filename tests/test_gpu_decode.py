@@ -520,3 +520,74 @@ def test_wait_limit_runs_out_and_the_model_recovers():
             m.set_wait_limit(0)                          # no cross-CTA waits on that path
     finally:
         m.close()
+
+
+# ---- prompts on the tensor cores ----------------------------------------------------
+
+@pytest.mark.parametrize("wdtype", ["f32", "f16", "int4"])
+@pytest.mark.parametrize("cfg_name,n", [("tiny", 5), ("tiny", 13), ("tiny", 64), ("small", 10), ("small", 100)])
+def test_tc_prefill_matches_oracle(cfg_name, n, wdtype):
+    """gpt2_prefill on the cluster path runs the prompt's positions as the
+    rows of one batched tensor-core step (two for more than 64): every
+    position's K and V in every layer, and the last position's logits and
+    choice, against the oracle on the same stored weights; then greedy
+    passes continue from the state it leaves (the cluster kernel's first
+    pass reads the choice as its token)."""
+    cfg = synth.TINY if cfg_name == "tiny" else synth.SMALL
+    if n > cfg.n_positions:
+        pytest.skip("prompt longer than the context")
+    w, dw = weights(cfg)
+    sw = orc.stored_weights(w, wdtype)
+    prompt = synth.make_prompt(cfg, n, 7)
+    om = orc.OracleModel(cfg, sw, omp=True)
+    try:
+        for p, t in enumerate(prompt):
+            ref_last, ref_tok = om.forward(int(t), p)
+        ref_kv = [om.export_kv(l, n) for l in range(cfg.n_layer)]
+    finally:
+        om.close()
+    atol = TOL[wdtype][0]
+    m = model(cfg, dw, wdtype, "cluster")
+    try:
+        m.prefill(prompt)
+        assert max_abs(m.logits(), ref_last) <= atol
+        if top2_margin(ref_last) > 1e-3:
+            assert m.argmax() == ref_tok
+        for l in range(cfg.n_layer):
+            k, v = m.export_kv(l, n)
+            assert max_abs(k, ref_kv[l][0]) <= atol, f"layer {l} K"
+            assert max_abs(v, ref_kv[l][1]) <= atol, f"layer {l} V"
+        # greedy passes continue from the state the prefill leaves
+        if n + 3 <= cfg.n_positions:
+            m.decode_greedy(3)
+            m.sync()
+            ref_ids, ref_rows = orc.greedy(cfg, sw, prompt, 3, omp=True)
+            if all(top2_margin(ref_rows[n - 1 + i]) > 1e-3 for i in range(4)):
+                assert m.argmax() == ref_ids[3]
+    finally:
+        m.close()
+
+
+def test_tc_prefill_agrees_with_single_token_passes():
+    """The two prefill paths leave the same cache and logits (within the fp32
+    tolerance) and the same greedy continuation."""
+    cfg = synth.SMALL
+    w, dw = weights(cfg)
+    prompt = synth.make_prompt(cfg, 20, 9)
+    out = {}
+    for name, flags in (("tc", "auto"), ("passes", "no_tc")):
+        m = binding.Model(cfg, dw, "f32", path="auto", tc_prefill=(flags == "auto"))
+        try:
+            ids = m.generate(prompt, 8)
+            k, v = m.export_kv(cfg.n_layer - 1, 28)
+            out[name] = (ids, m.logits(), k, v)
+        finally:
+            m.close()
+    assert max_abs(out["tc"][1], out["passes"][1]) <= 1e-3
+    assert max_abs(out["tc"][2], out["passes"][2]) <= 1e-3
+    assert max_abs(out["tc"][3], out["passes"][3]) <= 1e-3
+    ref_ids, ref_rows = orc.greedy(cfg, w, prompt, 8, omp=True)
+    for i, (a, b) in enumerate(zip(out["tc"][0], ref_ids)):
+        if top2_margin(ref_rows[len(prompt) - 1 + i]) <= 1e-3:
+            break
+        assert a == b

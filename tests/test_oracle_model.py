@@ -141,3 +141,35 @@ def test_multicore_build_gives_the_same_bits():
         else:
             os.environ["OMP_NUM_THREADS"] = old
     assert np.array_equal(rows[False].view(np.uint32), rows[True].view(np.uint32))
+
+
+def test_export_kv_layout():
+    """The oracle's cache accessor returns, for layer 0, row p of head h = the
+    k and v slices of LN1(wte[t] + wpe[p]) . W_attn + b_attn (float64 torch
+    routines), laid out [head][row][head_dim]."""
+    import torch
+    import torch.nn.functional as F
+    cfg = synth.TINY
+    w = synth.make_weights(cfg, seed=0)
+    toks = synth.make_prompt(cfg, 7, seed=3)
+    m = orc.OracleModel(cfg, w)
+    try:
+        for p, t in enumerate(toks):
+            m.forward(int(t), p)
+        k, v = m.export_kv(0, len(toks))
+    finally:
+        m.close()
+    d = lambda a: torch.from_numpy(np.asarray(a, np.float32)).double()
+    E, H, D = cfg.n_embd, cfg.n_head, cfg.head_dim
+    L0 = w["layers"][0]
+    x = d(w["wte"])[torch.as_tensor(np.asarray(toks, np.int64))] + d(w["wpe"])[:len(toks)]
+    qkv = F.layer_norm(x, (E,), d(L0["ln1_w"]), d(L0["ln1_b"]), eps=cfg.ln_eps) @ d(L0["attn_w"]) + d(L0["attn_b"])
+    kr = qkv[:, E:2 * E].reshape(len(toks), H, D).transpose(0, 1).numpy()
+    vr = qkv[:, 2 * E:].reshape(len(toks), H, D).transpose(0, 1).numpy()
+    assert np.abs(k - kr).max() <= 1e-5 and np.abs(v - vr).max() <= 1e-5
+    with pytest.raises(ValueError):
+        m2 = orc.OracleModel(cfg, w)
+        try:
+            m2.export_kv(0, 1)                       # nothing cached yet
+        finally:
+            m2.close()

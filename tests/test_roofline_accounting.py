@@ -65,3 +65,23 @@ def test_stored_head_bytes():
         assert f32[k] == f16[k] == i4[k]
     assert roofline.mean_bytes_per_token(cfg, "f32", [10, 11], head="f16") == pytest.approx(
         (roofline.bytes_per_token(cfg, "f32", 10, "f16")["total"] + roofline.bytes_per_token(cfg, "f32", 11, "f16")["total"]) / 2)
+
+
+def test_batched_step_bytes():
+    """One batched step streams every stored weight once for the whole batch
+    (bf16: half the fp32 block bytes the pages print, and a bf16 head of half
+    the tied head), and per sequence its own embedding rows, logits row and
+    KV rows; a batch of one is a single-sequence pass with those weights."""
+    cfg = synth.SMALL
+    one = roofline.batched_bytes_per_step(cfg, [37])
+    assert one["block_matrices"] == 339_738_624 // 2
+    assert one["head"] == 154_389_504 // 2
+    single = roofline.bytes_per_token(cfg, "bf16", 37)
+    for k in ("block_matrices", "biases_ln", "embedding_rows", "logits", "kv"):
+        assert one[k] == single[k]
+    pos = [40, 300, 511]
+    many = roofline.batched_bytes_per_step(cfg, pos)
+    assert many["block_matrices"] == one["block_matrices"] and many["head"] == one["head"]
+    assert many["kv"] == sum(roofline.bytes_per_token(cfg, "f32", p)["kv"] for p in pos)
+    assert many["logits"] == 3 * cfg.vocab_size * 4
+    assert roofline.batched_flops_per_step(cfg, 64) == 2 * 64 * roofline.macs_per_token(cfg)

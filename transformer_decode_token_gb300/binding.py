@@ -182,10 +182,11 @@ class Model:
     """One GPT-2 decode model on the current CUDA device."""
 
     def __init__(self, cfg, dev_weights: dict, wdtype: str = "f32", stream=None, path: str = "auto",
-                 head: str = "f32"):
+                 head: str = "f32", tc_prefill: bool = True):
         """path: "auto" (the cluster kernel where possible, else the per-kernel
         graph) or "per_kernel".  head: "f32" (the tied wte), "f16" or "int4" (a
-        copy for the LM head, GPT2_FLAG_HEAD_F16 / _INT4; cluster kernel only)."""
+        copy for the LM head, GPT2_FLAG_HEAD_F16 / _INT4; cluster kernel only).
+        tc_prefill=False: prompts as single-token passes (GPT2_FLAG_NO_TC_PREFILL)."""
         L = lib()
         self.cfg = cfg
         self.wdtype = wdtype
@@ -199,7 +200,7 @@ class Model:
                     dev_weights["ln_f_w"].data_ptr(), dev_weights["ln_f_b"].data_ptr(),
                     ctypes.cast(layers, ctypes.POINTER(LayerWeights)))
         h = ctypes.c_void_p()
-        flags = {"auto": 0, "per_kernel": 1}[path] | {"f32": 0, "f16": 4, "int4": 8}[head]
+        flags = {"auto": 0, "per_kernel": 1}[path] | {"f32": 0, "f16": 4, "int4": 8}[head] | (0 if tc_prefill else 16)
         check(L.gpt2_create_ex(ctypes.byref(c), ctypes.byref(w), WDTYPES[wdtype], flags,
                                _stream_handle(stream), ctypes.byref(h)), "gpt2_create_ex")
         self._h = h

@@ -10,6 +10,7 @@
 #include <new>
 #include <vector>
 
+#include "batch.h"
 #include "cluster.h"
 #include "common.cuh"
 #include "kernels.h"
@@ -61,6 +62,9 @@ struct gpt2_model {
     // cluster path: one cooperative launch per call
     bool cluster = false;
     int32_t *prompt_buf = nullptr;
+    // prompts on the tensor cores: the prompt's positions as the rows of one
+    // batched step (cluster path, greedy)
+    gpt2_batch *pre = nullptr;
     bool head_f16 = false;           // GPT2_FLAG_HEAD_F16: the LM head reads an fp16 copy of wte
     bool head_int4 = false;          // GPT2_FLAG_HEAD_INT4: ... or a grouped int4 copy
     uint8_t *cbuf = nullptr;         // tiled matrices, fp16 head, sums, keys, layer table
@@ -78,6 +82,11 @@ struct gpt2_model {
 namespace {
 
 constexpr size_t kAlign = 256;
+// Prompts of at least this many tokens run on the tensor cores (the
+// prefill engine), shorter ones as single-token passes of the cluster kernel
+// (measured on GB300, GPT-2 small fp32: one engine step takes ~0.62 ms for up
+// to 64 positions, a pass ~0.148 ms, so the engine wins from 5 tokens).
+constexpr int kTcPrefillMin = 5;
 // Per-kernel graph path: shared-memory stage budget and stages in flight of
 // each GEMV launch (measured on GB300: 96 KB in up to 4 stages).
 constexpr size_t kGraphStageBudget = 96 * 1024;
@@ -274,6 +283,7 @@ int build_graph(gpt2_model *m)
 void free_model(gpt2_model *m)
 {
     if (!m) return;
+    if (m->pre) prefill_engine_destroy(m->pre);
     if (m->exec) cudaGraphExecDestroy(m->exec);
     if (m->graph) cudaGraphDestroy(m->graph);
     if (m->arena) cudaFree(m->arena);
@@ -313,6 +323,13 @@ int launch_cluster_call(gpt2_model *m, int n_steps, const int32_t *prompt, int n
     TRY_CUDA(launch_cluster(m->wdtype, c, m->c_clusters, m->c_smem, m->stream));
     m->launches += 1;
     return GPT2_OK;
+}
+
+// Whether a prompt of n tokens runs on the tensor cores (greedy only: a
+// temperature draw of the first token is the cluster kernel's).
+bool use_tc_prefill(const gpt2_model *m, int n)
+{
+    return m->pre && n >= kTcPrefillMin && !(m->cargs.temperature > 0.f);
 }
 
 int launch_step(gpt2_model *m, int32_t token, int32_t position)
@@ -643,7 +660,7 @@ int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype
     int rc = check_config(cfg, wdtype);
     if (rc != GPT2_OK) return rc;
     if (!w || !w->layers) return GPT2_ERR_INVALID_ARG;
-    if (flags & ~int32_t(GPT2_FLAG_PER_KERNEL | GPT2_FLAG_HEAD_F16 | GPT2_FLAG_HEAD_INT4))
+    if (flags & ~int32_t(GPT2_FLAG_PER_KERNEL | GPT2_FLAG_HEAD_F16 | GPT2_FLAG_HEAD_INT4 | GPT2_FLAG_NO_TC_PREFILL))
         return GPT2_ERR_INVALID_ARG;
     if ((flags & GPT2_FLAG_HEAD_F16) && (flags & GPT2_FLAG_HEAD_INT4)) return GPT2_ERR_INVALID_ARG;
     int dev;
@@ -833,6 +850,39 @@ int gpt2_create_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype
             m->cluster = false;
         }
     }
+    if (m->cluster && !(flags & GPT2_FLAG_NO_TC_PREFILL)) {
+        // the prefill engine: the stored matrices and head as bf16 hi + lo planes
+        std::vector<const float *> params(size_t(L) * 8);
+        for (int l = 0; l < L; ++l) {
+            const LayerDev &d = m->layers[l];
+            const float *pv[8] = {d.ln1_w, d.ln1_b, d.attn_b, d.proj_b, d.ln2_w, d.ln2_b, d.fc_b, d.mlp_proj_b};
+            for (int k = 0; k < 8; ++k) params[size_t(l) * 8 + k] = pv[k];
+        }
+        PrefillSrc ps;
+        ps.wte = m->wte;
+        ps.wpe = m->wpe;
+        ps.lnf_w = m->lnf_w;
+        ps.lnf_b = m->lnf_b;
+        ps.params = params.data();
+        ps.kc = m->kcache;
+        ps.vc = m->vcache;
+        ps.matrix = [m](int l, int k, float *dst, cudaStream_t st) {
+            const QMat &q = m->layers[l].mat[k];
+            return dequant_to_f32(m->wdtype, q.w, q.scales, q.zeros, q.in, q.out, dst, st);
+        };
+        ps.head = [m](float *dst, cudaStream_t st) {
+            const ClusterArgs &a = m->cargs;
+            if (a.head_wt == kWF32)
+                return cudaMemcpyAsync(dst, m->wte, size_t(m->cfg.vocab_size) * m->cfg.n_embd * 4,
+                                       cudaMemcpyDeviceToDevice, st);
+            return dequant_to_f32(a.head_wt, a.head_w, a.head_s, a.head_z, m->cfg.n_embd, m->cfg.vocab_size, dst, st);
+        };
+        rc = prefill_engine_create(m->cfg, ps, m->stream, m->num_sms, &m->pre);
+        if (rc != GPT2_OK) {
+            free_model(m);
+            return rc;
+        }
+    }
     if ((m->head_f16 || m->head_int4) && !m->cluster) {   // a separate head is read only by the cluster kernel
         free_model(m);
         return GPT2_ERR_INVALID_ARG;
@@ -901,6 +951,14 @@ int gpt2_prefill(gpt2_model *m, const int32_t *host_ids, int32_t n)
     for (int i = 0; i < n; ++i)
         if (host_ids[i] < 0 || host_ids[i] >= m->cfg.vocab_size) return GPT2_ERR_TOKEN_RANGE;
     gpt2_reset(m);
+    if (use_tc_prefill(m, n)) {
+        int rc = prefill_engine_run(m->pre, host_ids, n, m->st, m->out_ids, m->out_cap, m->logits, m->stream,
+                                    &m->launches);
+        if (rc != GPT2_OK) return rc;
+        m->cached = n;
+        m->has_step = true;
+        return GPT2_OK;
+    }
     if (m->cluster) {
         TRY_CUDA(cudaMemcpyAsync(m->prompt_buf, host_ids, size_t(n) * 4, cudaMemcpyHostToDevice, m->stream));
         int rc = launch_cluster_call(m, n, m->prompt_buf, n, 0, 0);
@@ -955,11 +1013,18 @@ int gpt2_generate(gpt2_model *m, const int32_t *host_prompt, int32_t n_prompt, i
     if (m->cluster) {
         gpt2_reset(m);
         TRY_CUDA(launch_set_state(m->st, 0, 0, kResetOut, m->out_ids, m->stream));
-        TRY_CUDA(cudaMemcpyAsync(m->prompt_buf, host_prompt, size_t(n_prompt) * 4, cudaMemcpyHostToDevice,
-                                 m->stream));
-        rc = launch_cluster_call(m, n_prompt + n_steps, m->prompt_buf, n_prompt, 0, 0);
-        if (rc != GPT2_OK) return rc;
         m->launches += 1;
+        if (use_tc_prefill(m, n_prompt)) {
+            // the prompt on the tensor cores, then the greedy passes in one launch
+            rc = prefill_engine_run(m->pre, host_prompt, n_prompt, m->st, m->out_ids, m->out_cap, m->logits,
+                                    m->stream, &m->launches);
+            if (rc == GPT2_OK && n_steps > 0) rc = launch_cluster_call(m, n_steps, nullptr, 0, 0, n_prompt);
+        } else {
+            TRY_CUDA(cudaMemcpyAsync(m->prompt_buf, host_prompt, size_t(n_prompt) * 4, cudaMemcpyHostToDevice,
+                                     m->stream));
+            rc = launch_cluster_call(m, n_prompt + n_steps, m->prompt_buf, n_prompt, 0, 0);
+        }
+        if (rc != GPT2_OK) return rc;
         m->cached = n_prompt + n_steps;
         m->has_step = true;
     } else {

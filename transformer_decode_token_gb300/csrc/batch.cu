@@ -11,15 +11,19 @@
 // rows (tc_gemm.cu); attention stays per sequence over that sequence's own
 // (ragged) KV cache.  One step is a CUDA graph of 8 kernels per block + 4,
 // chained by programmatic dependent launch:
-//   k_b_ln     residual add (fixed-order sum of the previous linear's split-K
-//              shares + bias), or the embedding; LayerNorm; the bf16 hi/lo
-//              B operand of the next linear
-//   tc_gemm    QKV / out-projection / fc / MLP projection / head
+//   k_b_ln     residual add (the previous linear's split-K shares summed in a
+//              fixed order, + bias), or the embedding; LayerNorm; the bf16
+//              hi/lo B operand of the next linear
+//   tc_gemm    QKV / out-projection / fc / MLP projection / head: fp32 shares
+//              of the K splits
 //   k_b_attn   q, k, v of one (sequence, head) from the QKV shares, k and v
 //              appended at the sequence's position, softmax(q.k / sqrt(D))
 //              over positions 0..pos, the weighted sum of v
 //   k_b_gelu   fc shares + bias, gelu_new, the B operand of the MLP projection
 //   k_b_argmax greedy choice per sequence; k_b_advance feeds it to the next step
+// When the rows are positions of one sequence (a prompt on the tensor cores),
+// k_b_append writes every row's k and v into the cache before the attention
+// reads them (9 kernels per block).
 // The KV cache and all activations are fp32; a sequence whose position is -1
 // is inactive for the step (no cache row written, its outputs ignored).
 #include "../../include/gpt2.h"
@@ -27,9 +31,11 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <functional>
 #include <new>
 #include <vector>
 
+#include "batch.h"
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_gemm.h"
@@ -72,6 +78,20 @@ __device__ __forceinline__ float block_max(float v, float *red)
     return t;
 }
 
+// Sum of the K-split shares of element i of row b ([splits][rows][n]), in
+// split order, with every share's load in flight at once.
+__device__ __forceinline__ float sum_shares(const float *parts, int splits, int rows, int n, int b, int i)
+{
+    float v[kTcMaxSplits];
+#pragma unroll
+    for (int k = 0; k < kTcMaxSplits; ++k) v[k] = k < splits ? parts[(size_t(k) * rows + b) * n + i] : 0.f;
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < kTcMaxSplits; ++k)
+        if (k < splits) s += v[k];
+    return s;
+}
+
 struct BLnArgs {
     float *x;                       // [rows][E] residual stream
     const float *parts;             // [splits][rows][E] shares of the linear before (mode 1)
@@ -110,9 +130,7 @@ __global__ void __launch_bounds__(kBT) k_b_ln(const BLnArgs a)
         }
     } else {
         for (int i = threadIdx.x; i < E; i += kBT) {
-            float s = 0.f;
-            for (int k = 0; k < a.splits; ++k) s += a.parts[(size_t(k) * a.rows + b) * E + i];
-            const float v = a.x[size_t(b) * E + i] + (s + a.bias[i]);
+            const float v = a.x[size_t(b) * E + i] + (sum_shares(a.parts, a.splits, a.rows, E, b, i) + a.bias[i]);
             xs[i] = v;
             a.x[size_t(b) * E + i] = v;
         }
@@ -173,9 +191,7 @@ __global__ void __launch_bounds__(kBT) k_b_attn(const BAttnArgs a)
     for (int t = threadIdx.x; t < 3 * D; t += kBT) {
         const int part_ = t / D, d = t % D;
         const int j = part_ * E + h * D + d;
-        float s = 0.f;
-        for (int k = 0; k < a.splits; ++k) s += a.parts[(size_t(k) * a.rows + b) * 3 * E + j];
-        s += a.bias[j];
+        const float s = sum_shares(a.parts, a.splits, a.rows, 3 * E, b, j) + a.bias[j];
         qkv[t] = s;
         if (a.append && part_ == 1) kh[size_t(pos) * D + d] = s;
         if (a.append && part_ == 2) vh[size_t(pos) * D + d] = s;
@@ -256,10 +272,25 @@ __global__ void __launch_bounds__(kBT) k_b_gelu(const BGeluArgs a)
 {
     const int b = blockIdx.x, f = blockIdx.y * kBT + threadIdx.x;
     pdl_wait();
-    if (f < a.F) {
-        float s = 0.f;
-        for (int k = 0; k < a.splits; ++k) s += a.parts[(size_t(k) * a.rows + b) * a.F + f];
-        put_hi_lo(a.out, b, a.F, f, gelu_new(s + a.bias[f]));
+    if (f < a.F) put_hi_lo(a.out, b, a.F, f, gelu_new(sum_shares(a.parts, a.splits, a.rows, a.F, b, f) + a.bias[f]));
+    pdl_launch_dependents();
+}
+
+// k and v of every row (QKV shares + bias) into the cache at the row's
+// position, before any row's attention reads them: the rows of one step are
+// then positions of one sequence (slot 0).
+__global__ void __launch_bounds__(kBT) k_b_append(const BAttnArgs a, int D)
+{
+    const int b = blockIdx.x, E = a.E;
+    pdl_wait();
+    const int pos = a.pos[b];
+    if (pos >= 0 && pos < a.P) {
+        const int slot = a.slots == 1 ? 0 : b;
+        for (int t = blockIdx.y * kBT + threadIdx.x; t < 2 * E; t += gridDim.y * kBT) {
+            const int part_ = 1 + t / E, hd = t % E, h = hd / D, d = hd % D, j = part_ * E + hd;
+            const float v = sum_shares(a.parts, a.splits, a.rows, 3 * E, b, j) + a.bias[j];
+            (part_ == 1 ? a.kc : a.vc)[((size_t(slot) * a.H + h) * a.P + pos) * D + d] = v;
+        }
     }
     pdl_launch_dependents();
 }
@@ -342,20 +373,23 @@ cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, size_t smem, cudaS
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-// K splits of a linear: as many CTAs as the GPU has SMs, about, each with a
-// whole number of 64-input chunks and every split non-empty.
+// K splits of a linear (the CTAs of one cluster, at most kTcMaxSplits): as
+// many CTAs as the GPU has SMs, about, each with a whole number of 64-input
+// chunks and every split non-empty.
 void plan_splits(int M, int K, int sms, int *splits, int *cps)
 {
     const int tiles = (M + kTcM - 1) / kTcM, chunks = K / kTcK;
-    int want = std::max(1, std::min(chunks, sms / std::max(1, tiles)));
+    // (at most ~128 CTAs: the clusters of a launch then fit the GPU at once)
+    const int cap = std::min(sms, 128);
+    int want = std::max(1, std::min(std::min(chunks, kTcMaxSplits), cap / std::max(1, tiles)));
     int c = (chunks + want - 1) / want;
     *cps = c;
     *splits = (chunks + c - 1) / c;
 }
 
 struct Linear {
-    CUtensorMap a_map;              // the stored weights [planes * M][K] bf16
-    int M, K, splits, cps;
+    CUtensorMap a_map;              // the stored weights [planes][plane_rows][K] bf16
+    int M, K, splits, cps, plane_rows;
 };
 
 }  // namespace
@@ -363,7 +397,10 @@ struct Linear {
 struct gpt2_batch {
     gpt2_config cfg{};
     int wdtype = GPT2_BF16;
-    int max_batch = 0;
+    int max_batch = 0;              // activation rows per step
+    int planes = 1;                 // bf16 planes per stored matrix (2: hi + lo of fp32 weights)
+    int slots = 1;                  // cache slots: one per row (sequences), or 1 (positions of one sequence)
+    bool own_cache = true;
     cudaStream_t stream = nullptr;
     int num_sms = 0;
     uint8_t *arena = nullptr;       // weights
@@ -376,14 +413,15 @@ struct gpt2_batch {
         Linear lin[4];
     };
     std::vector<Layer> layers;
-    void *head = nullptr;           // bf16 copy of wte [V][E]
+    void *head = nullptr;           // bf16 planes of the head [planes][Vp][E] (rows V..Vp zero)
     Linear head_lin{};
     // work
     float *kc = nullptr, *vc = nullptr;                   // [L][slots][H][P][D]
     float *x = nullptr;                                   // [64][E]
     __nv_bfloat16 *b_e = nullptr, *b_a = nullptr, *b_f = nullptr;   // [128][E], [128][E], [128][F]
     CUtensorMap map_e{}, map_a{}, map_f{};
-    float *p_qkv = nullptr, *p_o = nullptr, *p_fc = nullptr, *p_p = nullptr, *logits = nullptr;
+    float *p_qkv = nullptr, *p_o = nullptr, *p_fc = nullptr, *p_p = nullptr;   // K-split shares
+    float *logits = nullptr;                                                  // [rows][V]
     int32_t *tok = nullptr, *pos = nullptr, *next_tok = nullptr, *out_ids = nullptr;
     DeviceState *st = nullptr;
     cudaGraph_t graph = nullptr;
@@ -429,7 +467,8 @@ cudaError_t run_linear(const gpt2_batch *m, const Linear &L, const CUtensorMap &
     a.M = L.M;
     a.K = L.K;
     a.n_rows = m->max_batch;
-    a.a_planes = 1;
+    a.a_planes = m->planes;
+    a.a_plane_rows = L.plane_rows;
     a.chunks_per_split = L.cps;
     a.partials = parts;
     a.st = m->st;
@@ -442,7 +481,7 @@ int record_step(gpt2_batch *m, cudaStream_t s)
 {
     const gpt2_config &c = m->cfg;
     const int E = c.n_embd, H = c.n_head, D = E / H, F = 4 * E, R = m->max_batch, P = c.n_positions;
-    const int V = c.vocab_size, L = c.n_layer, slots = m->max_batch;
+    const int V = c.vocab_size, L = c.n_layer, slots = m->slots;
     int kernels = 0;
     bool first = true;
     auto pdl = [&]() {
@@ -464,12 +503,12 @@ int record_step(gpt2_batch *m, cudaStream_t s)
         ln.out = m->b_e;
         ln.gamma = Ly.ln1_w;
         ln.beta = Ly.ln1_b;
+        ln.tok = m->tok;
+        ln.pos = m->pos;
+        ln.wte = m->wte;
+        ln.wpe = m->wpe;
         if (l == 0) {
             ln.mode = 0;
-            ln.tok = m->tok;
-            ln.pos = m->pos;
-            ln.wte = m->wte;
-            ln.wpe = m->wpe;
         } else {
             ln.mode = 1;
             ln.parts = m->p_p;
@@ -491,9 +530,15 @@ int record_step(gpt2_batch *m, cudaStream_t s)
         at.P = P;
         at.rows = R;
         at.slots = slots;
-        at.append = 1;
+        at.append = slots == 1 ? 0 : 1;   // one sequence: every row's k, v first (k_b_append)
         at.scale = float(1.0 / std::sqrt(double(D)));
         at.out = m->b_a;
+        if (slots == 1) {
+            int dd = D;
+            void *ap[] = {&at, &dd};
+            BTRY(launch_pdl(reinterpret_cast<const void *>(k_b_append), dim3(R, 2), dim3(kBT), 0, s, pdl(), ap));
+            ++kernels;
+        }
         void *a2[] = {&at};
         const void *afn = D == 32 ? reinterpret_cast<const void *>(k_b_attn<32>)
                           : D == 64 ? reinterpret_cast<const void *>(k_b_attn<64>)
@@ -556,7 +601,7 @@ int record_step(gpt2_batch *m, cudaStream_t s)
     DeviceState *st = m->st;
     void *a7[] = {&tk, &ps, &nt, &rows, &pp, &st};
     BTRY(launch_pdl(reinterpret_cast<const void *>(k_b_advance), dim3(1), dim3(kTcMaxRows), 0, s, pdl(), a7));
-    m->kernels_per_step = kernels + 4;
+    m->kernels_per_step = kernels + 4;   // + final LayerNorm, head, argmax, advance
     return GPT2_OK;
 }
 
@@ -605,57 +650,56 @@ int read_batch_state(gpt2_batch *m)
     return GPT2_OK;
 }
 
-int set_linear(Linear &L, const void *w, int M, int K, int sms)
+int set_linear(Linear &L, const void *w, int M, int K, int sms, int planes = 1, int plane_rows = 0)
 {
     L.M = M;
     L.K = K;
+    L.plane_rows = plane_rows > 0 ? plane_rows : M;
     plan_splits(M, K, sms, &L.splits, &L.cps);
-    return tc_make_tmap(&L.a_map, w, uint64_t(M), uint64_t(K)) == 0 ? GPT2_OK : GPT2_ERR_CUDA;
+    return tc_make_tmap(&L.a_map, w, uint64_t(L.plane_rows) * planes, uint64_t(K)) == 0 ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
-}  // namespace
+// What an engine is built from (device pointers, read during the build only
+// unless stated).  The block matrices come either in the checkpoint's HF
+// [in][out] layout (hf = true) or as fp32 [out][in] (hf = false); a head
+// source of [V][E].  borrow: wte and wpe are used in place for the embedding
+// (their owner keeps them alive); kc, vc: an external cache (else own).
+struct EngineSrc {
+    const float *wte, *wpe, *lnf_w, *lnf_b, *head;
+    struct Layer {
+        const float *p[8];   // ln1_w, ln1_b, attn_b, proj_b, ln2_w, ln2_b, fc_b, mlp_proj_b
+        const float *w[4];   // QKV, out-projection, fc, MLP projection
+    };
+    std::vector<Layer> layers;
+    bool hf = true;
+    bool borrow = false;
+    float *kc = nullptr, *vc = nullptr;
+    int planes = 1, slots = 1, rows = kTcMaxRows;
+    // in place of w[] / head: write the fp32 [out][in] matrix (or the [V][E]
+    // head) into dst
+    std::function<cudaError_t(int, int, float *, cudaStream_t)> matrix;
+    std::function<cudaError_t(float *, cudaStream_t)> head_fn;
+};
 
-extern "C" {
-
-int gpt2_create_batch(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype, int32_t max_batch, void *stream,
-                      gpt2_batch **out)
+int engine_build(gpt2_batch *m, const gpt2_config &cfg, const EngineSrc &src, cudaStream_t stream, int sms)
 {
-    if (!out) return GPT2_ERR_INVALID_ARG;
-    *out = nullptr;
-    if (!cfg || !w || !w->layers) return GPT2_ERR_INVALID_ARG;
-    if (wdtype != GPT2_BF16) return GPT2_ERR_INVALID_ARG;
-    if (max_batch < 1 || max_batch > kTcMaxRows) return GPT2_ERR_INVALID_ARG;
-    const int L = cfg->n_layer, E = cfg->n_embd, H = cfg->n_head, P = cfg->n_positions, V = cfg->vocab_size;
-    if (L < 1 || H < 1 || P < 1 || V < 1 || E < 64 || E % 64 || E % H) return GPT2_ERR_INVALID_ARG;
+    const int L = cfg.n_layer, E = cfg.n_embd, H = cfg.n_head, P = cfg.n_positions, V = cfg.vocab_size;
     const int D = E / H, F = 4 * E;
-    if (D != 32 && D != 64 && D != 128) return GPT2_ERR_INVALID_ARG;
-    if (!(cfg->ln_eps > 0.f) || !std::isfinite(cfg->ln_eps)) return GPT2_ERR_INVALID_ARG;
-    if ((long long)V * E > (1ll << 31) - 1 || (long long)P * 4 > 48 * 1024) return GPT2_ERR_INVALID_ARG;
-    int dev;
-    BTRY(cudaGetDevice(&dev));
-    cudaDeviceProp prop;
-    BTRY(cudaGetDeviceProperties(&prop, dev));
-    if (!(prop.major == 10 && prop.minor == 3)) return GPT2_ERR_UNSUPPORTED_DEVICE;
-    const float *top[4] = {w->wte, w->wpe, w->ln_f_w, w->ln_f_b};
-    for (const float *p : top)
-        if (!dev_ptr(p)) return GPT2_ERR_INVALID_ARG;
-    for (int l = 0; l < L; ++l) {
-        const gpt2_layer_weights &Lw = w->layers[l];
-        const float *ps[12] = {Lw.ln1_w, Lw.ln1_b, Lw.attn_w, Lw.attn_b, Lw.proj_w, Lw.proj_b,
-                               Lw.ln2_w, Lw.ln2_b, Lw.fc_w,   Lw.fc_b,   Lw.mlp_proj_w, Lw.mlp_proj_b};
-        for (const float *p : ps)
-            if (!dev_ptr(p)) return GPT2_ERR_INVALID_ARG;
-    }
     BTRY(tc_gemm_init());
-
-    gpt2_batch *m = new (std::nothrow) gpt2_batch();
-    if (!m) return GPT2_ERR_OUT_OF_MEMORY;
-    m->cfg = *cfg;
-    m->max_batch = max_batch;
-    m->stream = static_cast<cudaStream_t>(stream);
-    m->num_sms = prop.multiProcessorCount;
-    m->cached.assign(max_batch, 0);
+    m->cfg = cfg;
+    m->max_batch = src.rows;
+    m->planes = src.planes;
+    m->slots = src.slots;
+    m->own_cache = src.kc == nullptr;
+    m->stream = stream;
+    m->num_sms = sms;
+    m->cached.assign(src.rows, 0);
     const int mat_in[4] = {E, E, E, F}, mat_out[4] = {3 * E, E, F, E};
+    const int pl = src.planes;
+    // rows of one plane: a multiple of the tile height when there are two
+    // planes (a tile never reads into the next plane; padding rows are zero)
+    auto plane_rows = [&](int M) { return pl > 1 ? (M + kTcM - 1) / kTcM * kTcM : M; };
+    const int Vp = plane_rows(V);
     // ---- weights ----
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -663,9 +707,9 @@ int gpt2_create_batch(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdt
         off += a256(bytes);
         return o;
     };
-    const size_t o_wte = take(size_t(V) * E * 4), o_wpe = take(size_t(P) * E * 4);
+    const size_t o_wte = src.borrow ? 0 : take(size_t(V) * E * 4), o_wpe = src.borrow ? 0 : take(size_t(P) * E * 4);
     const size_t o_lnf_w = take(size_t(E) * 4), o_lnf_b = take(size_t(E) * 4);
-    const size_t o_head = take(size_t(V) * E * 2);
+    const size_t o_head = take(size_t(pl) * Vp * E * 2);
     struct LO {
         size_t p[8], w[4];
     };
@@ -673,78 +717,108 @@ int gpt2_create_batch(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdt
     const int psz[8] = {E, E, 3 * E, E, E, E, F, E};
     for (int l = 0; l < L; ++l) {
         for (int k = 0; k < 8; ++k) lo[l].p[k] = take(size_t(psz[k]) * 4);
-        for (int k = 0; k < 4; ++k) lo[l].w[k] = take(size_t(mat_in[k]) * mat_out[k] * 2);
+        for (int k = 0; k < 4; ++k) lo[l].w[k] = take(size_t(pl) * plane_rows(mat_out[k]) * mat_in[k] * 2);
     }
     const size_t arena_bytes = off;
     // ---- work ----
     off = 0;
-    const size_t kv = size_t(L) * max_batch * H * P * D * 4;
-    const size_t o_k = take(kv), o_v = take(kv);
+    const size_t kv = m->own_cache ? size_t(L) * src.slots * H * P * D * 4 : 0;
+    const size_t o_k = m->own_cache ? take(kv) : 0, o_v = m->own_cache ? take(kv) : 0;
     const size_t o_x = take(size_t(kTcMaxRows) * E * 4);
     const size_t o_be = take(size_t(2 * kTcMaxRows) * E * 2), o_ba = take(size_t(2 * kTcMaxRows) * E * 2);
     const size_t o_bf = take(size_t(2 * kTcMaxRows) * F * 2);
     int sp[4], cps[4];
-    for (int k = 0; k < 4; ++k) plan_splits(mat_out[k], mat_in[k], m->num_sms, &sp[k], &cps[k]);
-    const size_t o_pq = take(size_t(sp[0]) * max_batch * 3 * E * 4), o_po = take(size_t(sp[1]) * max_batch * E * 4);
-    const size_t o_pf = take(size_t(sp[2]) * max_batch * F * 4), o_pp = take(size_t(sp[3]) * max_batch * E * 4);
-    const size_t o_lg = take(size_t(max_batch) * V * 4);
+    for (int k = 0; k < 4; ++k) plan_splits(mat_out[k], mat_in[k], sms, &sp[k], &cps[k]);
+    const size_t o_pq = take(size_t(sp[0]) * src.rows * 3 * E * 4), o_po = take(size_t(sp[1]) * src.rows * E * 4);
+    const size_t o_pf = take(size_t(sp[2]) * src.rows * F * 4), o_pp = take(size_t(sp[3]) * src.rows * E * 4);
+    const size_t o_lg = take(size_t(src.rows) * V * 4);
     const size_t o_tok = take(size_t(kTcMaxRows) * 4), o_pos = take(size_t(kTcMaxRows) * 4);
-    const size_t o_nt = take(size_t(kTcMaxRows) * 4), o_ids = take(size_t(P) * max_batch * 4);
+    const size_t o_nt = take(size_t(kTcMaxRows) * 4), o_ids = take(size_t(P) * src.rows * 4);
     const size_t o_st = take(sizeof(DeviceState));
     const size_t work_bytes = off;
+    const size_t tmp_elems = size_t(F) * E > size_t(Vp) * E ? size_t(F) * E : size_t(Vp) * E;
+    float *tmp = nullptr;
     cudaError_t e = cudaMalloc(&m->arena, arena_bytes);
     if (e == cudaSuccess) e = cudaMalloc(&m->work, work_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&tmp, tmp_elems * 4);
     if (e != cudaSuccess) {
-        free_batch(m);
+        if (tmp) cudaFree(tmp);
         return cuda_rc(e);
     }
     uint8_t *A = m->arena, *W = m->work;
-    m->wte = reinterpret_cast<float *>(A + o_wte);
-    m->wpe = reinterpret_cast<float *>(A + o_wpe);
-    m->lnf_w = reinterpret_cast<float *>(A + o_lnf_w);
-    m->lnf_b = reinterpret_cast<float *>(A + o_lnf_b);
-    m->head = A + o_head;
-    m->layers.resize(L);
-    cudaStream_t s = m->stream;
+    cudaStream_t s = stream;
+    // the bf16 planes of one fp32 [rows][K] matrix (rows of each plane padded
+    // to prow, padding zero)
+    auto planes_of = [&](const float *w_oi, int rows, int K, int prow, void *dst) -> cudaError_t {
+        __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(dst);
+        cudaError_t r = cudaSuccess;
+        if (prow > rows) r = cudaMemsetAsync(d, 0, size_t(pl) * prow * K * 2, s);
+        if (r == cudaSuccess)
+            r = split_bf16(w_oi, size_t(rows) * K, d, pl > 1 ? d + size_t(prow) * K : nullptr, s);
+        return r;
+    };
     int rc = GPT2_OK;
-#define BCK(expr)                        \
+#define ECK(expr)                        \
     do {                                 \
         cudaError_t _e2 = (expr);        \
         if (_e2 != cudaSuccess) {        \
             rc = cuda_rc(_e2);           \
-            goto fail;                   \
+            goto done;                   \
         }                                \
     } while (0)
-    BCK(cudaMemsetAsync(m->work, 0, work_bytes, s));
-    BCK(cudaMemcpyAsync(m->wte, w->wte, size_t(V) * E * 4, cudaMemcpyDeviceToDevice, s));
-    BCK(cudaMemcpyAsync(m->wpe, w->wpe, size_t(P) * E * 4, cudaMemcpyDeviceToDevice, s));
-    BCK(cudaMemcpyAsync(m->lnf_w, w->ln_f_w, size_t(E) * 4, cudaMemcpyDeviceToDevice, s));
-    BCK(cudaMemcpyAsync(m->lnf_b, w->ln_f_b, size_t(E) * 4, cudaMemcpyDeviceToDevice, s));
-    BCK(split_bf16(w->wte, size_t(V) * E, m->head, nullptr, s));   // the head's bf16 copy (the embedding reads fp32)
+    ECK(cudaMemsetAsync(m->work, 0, work_bytes, s));
+    if (src.borrow) {
+        m->wte = const_cast<float *>(src.wte);
+        m->wpe = const_cast<float *>(src.wpe);
+    } else {
+        m->wte = reinterpret_cast<float *>(A + o_wte);
+        m->wpe = reinterpret_cast<float *>(A + o_wpe);
+        ECK(cudaMemcpyAsync(m->wte, src.wte, size_t(V) * E * 4, cudaMemcpyDeviceToDevice, s));
+        ECK(cudaMemcpyAsync(m->wpe, src.wpe, size_t(P) * E * 4, cudaMemcpyDeviceToDevice, s));
+    }
+    m->lnf_w = reinterpret_cast<float *>(A + o_lnf_w);
+    m->lnf_b = reinterpret_cast<float *>(A + o_lnf_b);
+    ECK(cudaMemcpyAsync(m->lnf_w, src.lnf_w, size_t(E) * 4, cudaMemcpyDeviceToDevice, s));
+    ECK(cudaMemcpyAsync(m->lnf_b, src.lnf_b, size_t(E) * 4, cudaMemcpyDeviceToDevice, s));
+    m->head = A + o_head;
+    if (src.head_fn) {
+        ECK(src.head_fn(tmp, s));
+        ECK(planes_of(tmp, V, E, Vp, m->head));
+        ECK(cudaStreamSynchronize(s));
+    } else {
+        ECK(planes_of(src.head, V, E, Vp, m->head));   // the embedding reads the fp32 wte
+    }
+    m->layers.resize(L);
     for (int l = 0; l < L; ++l) {
-        const gpt2_layer_weights &src = w->layers[l];
+        const EngineSrc::Layer &sl = src.layers[l];
         gpt2_batch::Layer &d = m->layers[l];
         float **pp[8] = {&d.ln1_w, &d.ln1_b, &d.attn_b, &d.proj_b, &d.ln2_w, &d.ln2_b, &d.fc_b, &d.mlp_proj_b};
-        const float *ps[8] = {src.ln1_w, src.ln1_b, src.attn_b, src.proj_b, src.ln2_w, src.ln2_b, src.fc_b,
-                              src.mlp_proj_b};
         for (int k = 0; k < 8; ++k) {
             *pp[k] = reinterpret_cast<float *>(A + lo[l].p[k]);
-            BCK(cudaMemcpyAsync(*pp[k], ps[k], size_t(psz[k]) * 4, cudaMemcpyDeviceToDevice, s));
+            ECK(cudaMemcpyAsync(*pp[k], sl.p[k], size_t(psz[k]) * 4, cudaMemcpyDeviceToDevice, s));
         }
-        const float *sm[4] = {src.attn_w, src.proj_w, src.fc_w, src.mlp_proj_w};
         for (int k = 0; k < 4; ++k) {
             d.w[k] = A + lo[l].w[k];
-            BCK(repack_bf16(sm[k], mat_in[k], mat_out[k], d.w[k], s));
-            rc = set_linear(d.lin[k], d.w[k], mat_out[k], mat_in[k], m->num_sms);
-            if (rc != GPT2_OK) goto fail;
+            const float *w_oi = sl.w[k];
+            if (src.matrix) {
+                ECK(src.matrix(l, k, tmp, s));
+                w_oi = tmp;
+            } else if (src.hf) {   // [in][out] -> [out][in]
+                ECK(repack_f32(sl.w[k], mat_in[k], mat_out[k], tmp, s));
+                w_oi = tmp;
+            }
+            ECK(planes_of(w_oi, mat_out[k], mat_in[k], plane_rows(mat_out[k]), d.w[k]));
+            ECK(cudaStreamSynchronize(s));   // tmp is reused
+            rc = set_linear(d.lin[k], d.w[k], mat_out[k], mat_in[k], sms, pl, plane_rows(mat_out[k]));
+            if (rc != GPT2_OK) goto done;
         }
     }
-    rc = set_linear(m->head_lin, m->head, V, E, m->num_sms);
-    if (rc != GPT2_OK) goto fail;
+    rc = set_linear(m->head_lin, m->head, V, E, sms, pl, Vp);
+    if (rc != GPT2_OK) goto done;
     m->head_lin.splits = 1;                       // whole logits from one pass over K
     m->head_lin.cps = E / kTcK;
-    m->kc = reinterpret_cast<float *>(W + o_k);
-    m->vc = reinterpret_cast<float *>(W + o_v);
+    m->kc = m->own_cache ? reinterpret_cast<float *>(W + o_k) : src.kc;
+    m->vc = m->own_cache ? reinterpret_cast<float *>(W + o_v) : src.vc;
     m->x = reinterpret_cast<float *>(W + o_x);
     m->b_e = reinterpret_cast<__nv_bfloat16 *>(W + o_be);
     m->b_a = reinterpret_cast<__nv_bfloat16 *>(W + o_ba);
@@ -763,22 +837,171 @@ int gpt2_create_batch(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdt
         tc_make_tmap(&m->map_a, m->b_a, 2 * kTcMaxRows, uint64_t(E)) ||
         tc_make_tmap(&m->map_f, m->b_f, 2 * kTcMaxRows, uint64_t(F))) {
         rc = GPT2_ERR_CUDA;
-        goto fail;
+        goto done;
     }
     {
         std::vector<int32_t> neg(kTcMaxRows, -1);   // every row inactive until a call feeds it
-        BCK(cudaMemcpyAsync(m->pos, neg.data(), neg.size() * 4, cudaMemcpyHostToDevice, s));
-        BCK(cudaStreamSynchronize(s));
+        ECK(cudaMemcpyAsync(m->pos, neg.data(), neg.size() * 4, cudaMemcpyHostToDevice, s));
+        ECK(cudaStreamSynchronize(s));
     }
     rc = build_step_graph(m);
-    if (rc != GPT2_OK) goto fail;
+done:
+    cudaStreamSynchronize(s);
+    cudaFree(tmp);
+    return rc;
+#undef ECK
+}
+
+// Shape checks common to every engine.
+int engine_shape_ok(const gpt2_config *cfg)
+{
+    const int L = cfg->n_layer, E = cfg->n_embd, H = cfg->n_head, P = cfg->n_positions, V = cfg->vocab_size;
+    if (L < 1 || H < 1 || P < 1 || V < 1 || E < 64 || E % 64 || E % H) return GPT2_ERR_INVALID_ARG;
+    const int D = E / H;
+    if (D != 32 && D != 64 && D != 128) return GPT2_ERR_INVALID_ARG;
+    if (!(cfg->ln_eps > 0.f) || !std::isfinite(cfg->ln_eps)) return GPT2_ERR_INVALID_ARG;
+    if ((long long)V * E > (1ll << 31) - 1 || (long long)P * 4 > 48 * 1024) return GPT2_ERR_INVALID_ARG;
+    return GPT2_OK;
+}
+
+// The single model's device state after a prefill through the engine (what
+// its own prefill leaves): the choice after the last position is the next
+// token, appended to the generated ids.
+__global__ void k_seed_after_prefill(const int32_t *next_tok, int row, DeviceState *st, int32_t *out_ids,
+                                     int out_cap, int n)
+{
+    const int32_t tok = next_tok[row];
+    st->next_tok = tok;
+    st->tok = tok;
+    st->pos = n;
+    const int32_t k = st->n_out;
+    if (out_ids && k >= 0 && k < out_cap) out_ids[k] = tok;
+    st->n_out = k + 1;
+}
+
+}  // namespace
+
+namespace gpt2 {
+
+int prefill_engine_create(const gpt2_config &cfg, const PrefillSrc &ps, cudaStream_t s, int sms, gpt2_batch **out)
+{
+    *out = nullptr;
+    int rc = engine_shape_ok(&cfg);
+    if (rc != GPT2_OK) return rc;
+    EngineSrc src;
+    src.wte = ps.wte;
+    src.wpe = ps.wpe;
+    src.lnf_w = ps.lnf_w;
+    src.lnf_b = ps.lnf_b;
+    src.head = nullptr;
+    src.head_fn = ps.head;
+    src.matrix = ps.matrix;
+    src.layers.resize(cfg.n_layer);
+    for (int l = 0; l < cfg.n_layer; ++l)
+        for (int k = 0; k < 8; ++k) src.layers[l].p[k] = ps.params[l * 8 + k];
+    src.hf = false;
+    src.borrow = true;
+    src.kc = ps.kc;
+    src.vc = ps.vc;
+    src.planes = 2;
+    src.slots = 1;
+    src.rows = kTcMaxRows;
+    gpt2_batch *e = new (std::nothrow) gpt2_batch();
+    if (!e) return GPT2_ERR_OUT_OF_MEMORY;
+    rc = engine_build(e, cfg, src, s, sms);
+    if (rc != GPT2_OK) {
+        free_batch(e);
+        return rc;
+    }
+    *out = e;
+    return GPT2_OK;
+}
+
+int prefill_engine_run(gpt2_batch *e, const int32_t *ids, int n, DeviceState *st, int32_t *out_ids, int out_cap,
+                       float *logits, cudaStream_t s, unsigned long long *launches)
+{
+    if (!e || n < 1 || n > e->cfg.n_positions) return GPT2_ERR_INVALID_ARG;
+    std::vector<int32_t> t(kTcMaxRows), p(kTcMaxRows);
+    int last = 0;
+    for (int c0 = 0; c0 < n; c0 += kTcMaxRows) {
+        const int rows = std::min(kTcMaxRows, n - c0);
+        for (int r = 0; r < kTcMaxRows; ++r) {
+            t[r] = r < rows ? ids[c0 + r] : 0;
+            p[r] = r < rows ? c0 + r : -1;
+        }
+        BTRY(cudaMemcpyAsync(e->tok, t.data(), t.size() * 4, cudaMemcpyHostToDevice, s));
+        BTRY(cudaMemcpyAsync(e->pos, p.data(), p.size() * 4, cudaMemcpyHostToDevice, s));
+        BTRY(cudaGraphLaunch(e->exec, s));
+        e->launches += e->kernels_per_step;
+        if (launches) *launches += e->kernels_per_step;
+        last = rows - 1;
+    }
+    k_seed_after_prefill<<<1, 1, 0, s>>>(e->next_tok, last, st, out_ids, out_cap, n);
+    BTRY(cudaGetLastError());
+    if (launches) *launches += 1;
+    BTRY(cudaMemcpyAsync(logits, e->logits + size_t(last) * e->cfg.vocab_size, size_t(e->cfg.vocab_size) * 4,
+                         cudaMemcpyDeviceToDevice, s));
+    return GPT2_OK;
+}
+
+void prefill_engine_destroy(gpt2_batch *e) { free_batch(e); }
+
+}  // namespace gpt2
+
+extern "C" {
+
+int gpt2_create_batch(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype, int32_t max_batch, void *stream,
+                      gpt2_batch **out)
+{
+    if (!out) return GPT2_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!cfg || !w || !w->layers) return GPT2_ERR_INVALID_ARG;
+    if (wdtype != GPT2_BF16) return GPT2_ERR_INVALID_ARG;
+    if (max_batch < 1 || max_batch > kTcMaxRows) return GPT2_ERR_INVALID_ARG;
+    int rc = engine_shape_ok(cfg);
+    if (rc != GPT2_OK) return rc;
+    int dev;
+    BTRY(cudaGetDevice(&dev));
+    cudaDeviceProp prop;
+    BTRY(cudaGetDeviceProperties(&prop, dev));
+    if (!(prop.major == 10 && prop.minor == 3)) return GPT2_ERR_UNSUPPORTED_DEVICE;
+    const float *top[4] = {w->wte, w->wpe, w->ln_f_w, w->ln_f_b};
+    for (const float *p : top)
+        if (!dev_ptr(p)) return GPT2_ERR_INVALID_ARG;
+    EngineSrc src;
+    src.wte = w->wte;
+    src.wpe = w->wpe;
+    src.lnf_w = w->ln_f_w;
+    src.lnf_b = w->ln_f_b;
+    src.head = w->wte;                // the tied head, stored as its bf16 copy
+    src.layers.resize(cfg->n_layer);
+    for (int l = 0; l < cfg->n_layer; ++l) {
+        const gpt2_layer_weights &Lw = w->layers[l];
+        const float *ps[12] = {Lw.ln1_w, Lw.ln1_b, Lw.attn_w, Lw.attn_b, Lw.proj_w, Lw.proj_b,
+                               Lw.ln2_w, Lw.ln2_b, Lw.fc_w,   Lw.fc_b,   Lw.mlp_proj_w, Lw.mlp_proj_b};
+        for (const float *p : ps)
+            if (!dev_ptr(p)) return GPT2_ERR_INVALID_ARG;
+        EngineSrc::Layer &sl = src.layers[l];
+        const float *pv[8] = {Lw.ln1_w, Lw.ln1_b, Lw.attn_b, Lw.proj_b, Lw.ln2_w, Lw.ln2_b, Lw.fc_b, Lw.mlp_proj_b};
+        for (int k = 0; k < 8; ++k) sl.p[k] = pv[k];
+        sl.w[0] = Lw.attn_w;
+        sl.w[1] = Lw.proj_w;
+        sl.w[2] = Lw.fc_w;
+        sl.w[3] = Lw.mlp_proj_w;
+    }
+    src.hf = true;
+    src.planes = 1;
+    src.slots = max_batch;
+    src.rows = max_batch;
+    gpt2_batch *m = new (std::nothrow) gpt2_batch();
+    if (!m) return GPT2_ERR_OUT_OF_MEMORY;
+    rc = engine_build(m, *cfg, src, static_cast<cudaStream_t>(stream), prop.multiProcessorCount);
+    if (rc != GPT2_OK) {
+        free_batch(m);
+        return rc;
+    }
     *out = m;
     return GPT2_OK;
-fail:
-    cudaStreamSynchronize(s);
-    free_batch(m);
-    return rc;
-#undef BCK
 }
 
 void gpt2_destroy_batch(gpt2_batch *m)
@@ -925,9 +1148,8 @@ int gpt2_sync_batch(gpt2_batch *m)
 size_t gpt2_op_linear_bf16_workspace(int32_t M, int32_t n, int32_t K)
 {
     if (M < 1 || K < kTcK || n < 1) return 0;
-    int sp, cps;
-    plan_splits(M, K, 148, &sp, &cps);
-    return a256(size_t(2 * kTcMaxRows) * K * 2) + a256(size_t(K / kTcK) * n * M * 4);
+    // the hi/lo B operand, then the K splits' shares (at most kTcMaxSplits)
+    return a256(size_t(2 * kTcMaxRows) * K * 2) + a256(size_t(kTcMaxSplits) * n * M * 4);
 }
 
 int gpt2_op_linear_bf16(const void *W, const float *X, int32_t M, int32_t n, int32_t K, float *Y, void *workspace,
@@ -961,6 +1183,7 @@ int gpt2_op_linear_bf16(const void *W, const float *X, int32_t M, int32_t n, int
     a.K = K;
     a.n_rows = n;
     a.a_planes = 1;
+    a.a_plane_rows = M;
     a.chunks_per_split = L.cps;
     a.partials = parts;
     a.st = nullptr;

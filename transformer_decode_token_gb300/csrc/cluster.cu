@@ -91,6 +91,9 @@ constexpr float kFixLimit = 65000.0f;
 constexpr unsigned long long kFixBias = 1ull << 40;
 constexpr int kCountShift = 56;
 constexpr uint32_t kKvWin = 8192;          // K/V rows of this CTA's positions held in shared memory
+// Attention: up to this many positions per CTA, one lane per head dimension
+// (pairs of positions per warp); more, one lane per position (32 per tile).
+constexpr int kLanePerDimMax = 48;
 constexpr uint32_t kBarBytes = 512;        // mbarriers at the start of shared memory
 
 // Shared-memory layout before the ring (byte offsets): barriers, x, LN(x),
@@ -192,7 +195,12 @@ struct Sh {
 
 // Shared-memory views of a consumer thread.
 struct CS {
-    uint64_t *full, *empty, *qkv_bar, *att_bar, *kv_bar, *prm_bar, *red_bar, *x_bar;
+    uint64_t *full, *empty, *kv_bar, *prm_bar;
+    // the barriers of the cluster exchanges come in pairs, used alternately
+    // (exchange n on barrier n & 1): a CTA of the cluster can run one exchange
+    // ahead of another, and its stores then complete on the other barrier of
+    // the pair, never on the phase this CTA is still waiting for
+    uint64_t *qkv_bar, *att_bar, *red_bar, *x_bar;
     float *x, *qkv, *part, *attn, *hloc, *outv, *red, *kvw;
     float *pr;                 // this layer's LayerNorm parameters and bias slices
     const CLayer *layers;      // the layer table, copied to shared memory
@@ -214,12 +222,14 @@ __device__ __forceinline__ bool aborted(const ClusterArgs &a) { return ld_relaxe
 __device__ __forceinline__ void raise_abort(const ClusterArgs &a, int info)
 {
     record_error(a.st, kDevErrTimeout, info);
-    atomicExch(&a.st->abort, 1);
+    atomicMax(&a.st->abort, 1);   // (never lowers the level 2 of keep_waiting_landing)
 }
 
 // One step of a bounded spin: false once the spin must end (abort or timeout).
 // A limit of 0 lets no wait spin: the first one that does not succeed at
-// once gives up (the test of the abort path).
+// once gives up (the test of the abort path).  Used by the waits for data
+// that may never come once the pass is abandoned: ring stages, GPU-wide sums,
+// the previous pass's token, free ring slots.
 __device__ __forceinline__ bool keep_waiting(const ClusterArgs &a, Waiter &w, int info)
 {
     if (a.wait_ns == 0) {
@@ -232,6 +242,29 @@ __device__ __forceinline__ bool keep_waiting(const ClusterArgs &a, Waiter &w, in
     if (w.t0 == 0) w.t0 = t;
     else if (t - w.t0 > a.wait_ns) {
         raise_abort(a, info);
+        return false;
+    }
+    return true;
+}
+
+// The same for waits on writes into this CTA's shared memory that have been
+// issued and will land whatever happens (bulk copies of parameters and K/V
+// rows, st.async stores from the cluster's CTAs, which send every exchange
+// even on the abort path): they never give up early, so no write into shared
+// memory is still in flight when the CTA leaves and no barrier is re-armed
+// with a phase pending; only the fixed limit ends them.
+// If one of these ever runs out (a fault, not an abandoned pass), the abort
+// word goes to 2 and every such wait then ends at once, so the kernel still
+// returns within about one limit.
+__device__ __forceinline__ bool keep_waiting_landing(const ClusterArgs &a, Waiter &w, int info)
+{
+    if ((++w.it & 127u) != 0) return true;
+    if (ld_relaxed_i32(&a.st->abort) >= 2) return false;
+    const unsigned long long t = global_ns();
+    if (w.t0 == 0) w.t0 = t;
+    else if (t - w.t0 > kWaitLimitNs) {
+        record_error(a.st, kDevErrTimeout, info);
+        atomicMax(&a.st->abort, 2);
         return false;
     }
     return true;
@@ -258,16 +291,30 @@ __device__ __forceinline__ bool wait_stage(const ClusterArgs &a, const CS &c, ui
 }
 
 // Bounded wait on a barrier of this CTA that completes by transaction bytes
-// (bulk copies, or stores from CTAs of the cluster).
+// (bulk copies, or stores from CTAs of the cluster): always waited out (see
+// keep_waiting_landing).
+__device__ __forceinline__ bool wait_phase(const ClusterArgs &a, uint64_t *bar, uint32_t par, int info)
+{
+    if (mbar_test_wait(bar, par)) return true;
+    Waiter w;
+    while (!try_wait_cluster(bar, par))
+        if (!keep_waiting_landing(a, w, info)) return false;
+    return true;
+}
+// One barrier, one phase per use (this CTA's bulk copies).
 __device__ __forceinline__ bool wait_tx_bar(const ClusterArgs &a, uint64_t *bar, uint32_t &uses, int info)
 {
     const uint32_t par = uses & 1u;
     ++uses;
-    if (mbar_test_wait(bar, par)) return true;
-    Waiter w;
-    while (!try_wait_cluster(bar, par))
-        if (!keep_waiting(a, w, info)) return false;
-    return true;
+    return wait_phase(a, bar, par, info);
+}
+// A pair of barriers used alternately (cluster exchanges): use n waits for
+// phase (n / 2) & 1 of barrier n & 1.
+__device__ __forceinline__ uint64_t *pair_bar(uint64_t *bars, uint32_t uses) { return bars + (uses & 1u); }
+__device__ __forceinline__ bool wait_pair(const ClusterArgs &a, uint64_t *bars, uint32_t &uses, int info)
+{
+    const uint32_t n = uses++;
+    return wait_phase(a, bars + (n & 1u), (n >> 1) & 1u, info);
 }
 
 // ---- roles and row segments ---------------------------------------------------
@@ -412,6 +459,7 @@ __device__ __forceinline__ void stream_seg(const ClusterArgs &a, const Geo &g, c
 {
     const int C = g.chunk;
     for (int rs = 0; rs < g.rows && ok; rs += C) {
+        const uint64_t p = pol;
         const int n = min(C, g.rows - rs);
         const uint32_t st = k & (kCRing - 1);
         if (k >= uint32_t(kCRing)) {
@@ -422,13 +470,22 @@ __device__ __forceinline__ void stream_seg(const ClusterArgs &a, const Geo &g, c
                 __nanosleep(32);   // the ring is full: leave the issue slots to the consumer warps
             }
             if (!ok) break;
+            // the stage's previous copy has landed (consumers that gave up on
+            // it may have released it early): never re-arm a pending phase
+            Waiter w2;
+            while (!mbar_try_wait(&full[st], par))
+                if (!keep_waiting_landing(a, w2, 2100 + int(blockIdx.x))) {
+                    ok = false;
+                    break;
+                }
+            if (!ok) break;
         }
         uint8_t *dst = ring + size_t(st) * a.stage_bytes;
         const uint32_t b0 = uint32_t(n) * g.rb, b1 = uint32_t(n) * g.srb, b2 = uint32_t(n) * g.zrb;
         mbar_arrive_expect_tx(&full[st], b0 + b1 + b2);
-        bulk_g2s_hint(dst, sg.main + size_t(rs) * g.rb, b0, &full[st], pol);
-        if (b1) bulk_g2s_hint(dst + g.soff, sg.sc + size_t(rs) * g.srb, b1, &full[st], pol);
-        if (b2) bulk_g2s_hint(dst + g.zoff, sg.zp + size_t(rs) * g.zrb, b2, &full[st], pol);
+        bulk_g2s_hint(dst, sg.main + size_t(rs) * g.rb, b0, &full[st], p);
+        if (b1) bulk_g2s_hint(dst + g.soff, sg.sc + size_t(rs) * g.srb, b1, &full[st], p);
+        if (b2) bulk_g2s_hint(dst + g.zoff, sg.zp + size_t(rs) * g.zrb, b2, &full[st], p);
         ++k;
     }
 }
@@ -523,50 +580,74 @@ __device__ __forceinline__ RowAddr row_addr(uint32_t stage, const Geo &g, int rr
     return r;
 }
 
-// Unit c of a canonical row dotted with its inputs xu[0..kF4).  int4: the 8
-// codes q of word c, (q - z) taken exactly as (2^23 + q) - (2^23 + z), summed
-// in two chains, times the group's scale.
+// Packed pairs of fp32 values (low word first) and the paired fp32 operations
+// (fma/sub .f32x2: two IEEE operations per instruction).
+using F2 = unsigned long long;
+__device__ __forceinline__ F2 pack2(float a, float b)
+{
+    F2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float sum2(F2 r)
+{
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+    return a + b;
+}
+__device__ __forceinline__ F2 fma2(F2 a, F2 b, F2 c)
+{
+    F2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ F2 sub2(F2 a, F2 b)
+{
+    F2 d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ void lds_f2x2(uint32_t a, F2 &lo, F2 &hi)
+{
+    asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(lo), "=l"(hi) : "r"(a));
+}
+__device__ __forceinline__ F2 half2_f2(uint32_t h)
+{
+    const float2 p = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    return pack2(p.x, p.y);
+}
+
+// Unit c of a canonical row dotted with its inputs, in pairs: xu[0..2 kF4)
+// hold the unit's inputs two by two; acc is a pair of partial sums.  int4:
+// the 8 codes q of word c, (q - z) taken exactly as (2^23 + q) - (2^23 + z),
+// the pairs' sums times the group's scale.
 template <int WT>
-__device__ __forceinline__ float canon_unit(const RowAddr &ra, int c, const float4 *xu, float acc)
+__device__ __forceinline__ F2 canon_unit(const RowAddr &ra, int c, const F2 *xu, F2 acc)
 {
     if (WT == kWF32) {
-        const float4 v = lds_f4(ra.m + 16u * uint32_t(c));
-        const float4 x0 = xu[0];
-        return fmaf(v.w, x0.w, fmaf(v.z, x0.z, fmaf(v.y, x0.y, fmaf(v.x, x0.x, acc))));
+        F2 w0, w1;
+        lds_f2x2(ra.m + 16u * uint32_t(c), w0, w1);
+        return fma2(w1, xu[1], fma2(w0, xu[0], acc));
     } else if (WT == kWF16) {
         const uint4 u = lds_u4(ra.m + 16u * uint32_t(c));
-        const float4 x0 = xu[0], x1 = xu[1];
-        const float2 p0 = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
-        const float2 p1 = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
-        const float2 p2 = __half22float2(*reinterpret_cast<const __half2 *>(&u.z));
-        const float2 p3 = __half22float2(*reinterpret_cast<const __half2 *>(&u.w));
-        acc = fmaf(p0.x, x0.x, acc);
-        acc = fmaf(p0.y, x0.y, acc);
-        acc = fmaf(p1.x, x0.z, acc);
-        acc = fmaf(p1.y, x0.w, acc);
-        acc = fmaf(p2.x, x1.x, acc);
-        acc = fmaf(p2.y, x1.y, acc);
-        acc = fmaf(p3.x, x1.z, acc);
-        return fmaf(p3.y, x1.w, acc);
+        acc = fma2(half2_f2(u.x), xu[0], acc);
+        acc = fma2(half2_f2(u.y), xu[1], acc);
+        acc = fma2(half2_f2(u.z), xu[2], acc);
+        return fma2(half2_f2(u.w), xu[3], acc);
     } else {
         // word c: inputs 8c..8c+7 of group c / 4; byte b of the word holds
         // inputs 2b (low nibble) and 2b + 1
         const uint32_t q = lds_u32(ra.m + 4u * uint32_t(c));
         const int grp = c >> 2;
         const float s = lds_f(ra.s + 4u * uint32_t(grp));
-        const int z = int(lds_u8(ra.z + uint32_t(grp >> 1)) >> ((grp & 1) * 4)) & 15;
-        const float zf = 8388608.0f + float(z);
+        const uint32_t z = (lds_u8(ra.z + uint32_t(grp >> 1)) >> ((grp & 1) * 4)) & 15u;
+        const float zf = __uint_as_float(0x4B000000u | z);   // 2^23 + z, exactly
+        const F2 zz = pack2(zf, zf);
         const uint32_t lo = q & 0x0F0F0F0Fu, hi = (q >> 4) & 0x0F0F0F0Fu;
-        const float4 xa = xu[0], xb = xu[1];
-        float d0 = (byte_f23(lo, 0) - zf) * xa.x;
-        float d1 = (byte_f23(hi, 0) - zf) * xa.y;
-        d0 = fmaf(byte_f23(lo, 1) - zf, xa.z, d0);
-        d1 = fmaf(byte_f23(hi, 1) - zf, xa.w, d1);
-        d0 = fmaf(byte_f23(lo, 2) - zf, xb.x, d0);
-        d1 = fmaf(byte_f23(hi, 2) - zf, xb.y, d1);
-        d0 = fmaf(byte_f23(lo, 3) - zf, xb.z, d0);
-        d1 = fmaf(byte_f23(hi, 3) - zf, xb.w, d1);
-        return fmaf(s, d0 + d1, acc);
+        F2 d = 0ull;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) d = fma2(sub2(pack2(byte_f23(lo, b), byte_f23(hi, b)), zz), xu[b], d);
+        return fma2(pack2(s, s), d, acc);
     }
 }
 
@@ -718,9 +799,9 @@ __device__ __forceinline__ float sample_score(float logit, float temperature, un
 // last group repeats its first row in the empty slots, whose sums are not
 // stored: no per-row branches in the loop), lanes over the column units; each
 // lane's inputs (x * gamma) are in registers, xr[m] for unit lane + 32 m.
-template <int WT, bool LN, int RG>
+template <int WT, bool LN, int RG, bool GELU>
 __device__ __forceinline__ void canon_groups(const ClusterArgs &a, const CS &c, const Geo &g, uint32_t k, int w0,
-                                             int w1, int units, const float4 (&xr)[UnitOf<WT>::kPL * UnitOf<WT>::kF4],
+                                             int w1, int units, const F2 (&xr)[UnitOf<WT>::kPL * UnitOf<WT>::kF4 * 2],
                                              bool &have_stats, float ssum, float ssq, int in,
                                              float &dmean, float &rstd, const float *c1, const float *cb, float *out,
                                              int logit_row0, unsigned long long &best, long long sample_k0)
@@ -736,17 +817,20 @@ __device__ __forceinline__ void canon_groups(const ClusterArgs &a, const CS &c, 
             const int q = chunk_of(g, i);
             ra[j] = row_addr(stage_addr(a, c, k + uint32_t(q)), g, i - q * C);
         }
-        float acc[RG];
+        F2 acc2[RG];
 #pragma unroll
-        for (int j = 0; j < RG; ++j) acc[j] = 0.f;
+        for (int j = 0; j < RG; ++j) acc2[j] = 0ull;
 #pragma unroll
         for (int m = 0; m < UnitOf<WT>::kPL; ++m) {
             const int u = lane + 32 * m;
             if (u < units) {
 #pragma unroll
-                for (int j = 0; j < RG; ++j) acc[j] = canon_unit<WT>(ra[j], u, &xr[m * kF4], acc[j]);
+                for (int j = 0; j < RG; ++j) acc2[j] = canon_unit<WT>(ra[j], u, &xr[m * kF4 * 2], acc2[j]);
             }
         }
+        float acc[RG];
+#pragma unroll
+        for (int j = 0; j < RG; ++j) acc[j] = sum2(acc2[j]);
         if (LN && !have_stats) {
             // the statistics' butterfly runs here, after the first group's loads
 #pragma unroll
@@ -774,7 +858,7 @@ __device__ __forceinline__ void canon_groups(const ClusterArgs &a, const CS &c, 
                     best = key > best ? key : best;
                 }
             } else {
-                out[i] = t;
+                out[i] = GELU ? gelu_new(t) : t;
             }
         }
     }
@@ -817,7 +901,7 @@ __device__ __forceinline__ void prewait_rows(const ClusterArgs &a, const CS &c, 
             if (ok && !wait_stage(a, c, k + uint32_t(q))) ok = false;
 }
 
-template <int WT, bool LN>
+template <int WT, bool LN, bool GELU = false>
 __device__ __forceinline__ void canon_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &k, int win, int in,
                                           const float *xin, const float *gamma, const float *c1, const float *cb,
                                           float *out, int logit_row0, unsigned long long &best, bool &ok,
@@ -828,7 +912,7 @@ __device__ __forceinline__ void canon_rows(const ClusterArgs &a, CS &c, const Ge
     const int nch = g.nch;
     const int units = in / UnitOf<WT>::kIn;
     const uint32_t xa = smem_addr(xin), ga = smem_addr(gamma);
-    float4 xr[UnitOf<WT>::kPL * kF4];
+    F2 xr[UnitOf<WT>::kPL * kF4 * 2];
     float dmean = 0.f, rstd = 0.f;
     const float shift = LN ? xin[0] : 0.f;
     float ssum = 0.f, ssq = 0.f;   // this lane's share of the LayerNorm statistics
@@ -849,7 +933,8 @@ __device__ __forceinline__ void canon_rows(const ClusterArgs &a, CS &c, const Ge
                         v = mul4(sub4(v, shift), lds_f4(ga + off));
                     }
                 }
-                xr[m * kF4 + f] = v;
+                xr[(m * kF4 + f) * 2] = pack2(v.x, v.y);
+                xr[(m * kF4 + f) * 2 + 1] = pack2(v.z, v.w);
             }
         }
         ssum += s1;
@@ -867,13 +952,16 @@ __device__ __forceinline__ void canon_rows(const ClusterArgs &a, CS &c, const Ge
                 if (ok && !wait_stage(a, c, k + uint32_t(q))) ok = false;
         }
         CSUB(1);
-        if (ok && w0 < w1) {
+        // the row groups' shuffles need the whole warp: a lane whose wait gave
+        // up (the pass is being abandoned) takes its warp out of the work
+        const bool wok = __all_sync(0xffffffffu, ok);
+        if (wok && w0 < w1) {
             if (per <= 4)
-                canon_groups<WT, LN, 4>(a, c, g, k, w0, w1, units, xr, have_stats, ssum, ssq, in, dmean, rstd,
-                                        c1, cb, out, logit_row0, best, sample_k0);
+                canon_groups<WT, LN, 4, GELU>(a, c, g, k, w0, w1, units, xr, have_stats, ssum, ssq, in, dmean, rstd,
+                                              c1, cb, out, logit_row0, best, sample_k0);
             else
-                canon_groups<WT, LN, 6>(a, c, g, k, w0, w1, units, xr, have_stats, ssum, ssq, in, dmean, rstd,
-                                        c1, cb, out, logit_row0, best, sample_k0);
+                canon_groups<WT, LN, 6, GELU>(a, c, g, k, w0, w1, units, xr, have_stats, ssum, ssq, in, dmean, rstd,
+                                              c1, cb, out, logit_row0, best, sample_k0);
         }
         CSUB(2);
         window_release(c, k, q0, q1);   // its barrier also publishes out[]
@@ -988,7 +1076,7 @@ __device__ __forceinline__ void read_sum(const ClusterArgs &a, CS &c, int count,
 {
     const int tid = threadIdx.x, rq = a.E / kClusterSize;
     const int r = int(blockIdx.x) % kClusterSize;
-    if (tid == 0) mbar_arrive_expect_tx(c.x_bar, uint32_t(a.E) * 4u);
+    if (tid == 0) mbar_arrive_expect_tx(pair_bar(c.x_bar, c.uses_x), uint32_t(a.E) * 4u);
     constexpr int kW = kMaxPerThread / kClusterSize;   // words per thread
     unsigned long long v[kW];
 #pragma unroll
@@ -1014,7 +1102,7 @@ __device__ __forceinline__ void read_sum(const ClusterArgs &a, CS &c, int count,
         }
     }
     if (fence) __threadfence();
-    const uint32_t xbar = smem_addr(c.x_bar);
+    const uint32_t xbar = smem_addr(pair_bar(c.x_bar, c.uses_x));
 #pragma unroll
     for (int j = 0; j < kW; ++j) {
         const int t = tid + j * kCThreads;
@@ -1026,7 +1114,7 @@ __device__ __forceinline__ void read_sum(const ClusterArgs &a, CS &c, int count,
                 st_async_f32(mapa(dsm, uint32_t(dst)), val, mapa(xbar, uint32_t(dst)));
         }
     }
-    if (!wait_tx_bar(a, c.x_bar, c.uses_x, 5500 + int(blockIdx.x))) ok = false;
+    if (!wait_pair(a, c.x_bar, c.uses_x, 5500 + int(blockIdx.x))) ok = false;
 }
 
 // Adds values[i] (+ extra[base + i] + extra2[i] if extra is given) into
@@ -1066,102 +1154,128 @@ __device__ void attention(const ClusterArgs &a, CS &c, int l, int h, int r, int 
     if (n_pre > 0) {
         const uint32_t par = c.uses_kv & 1u;
         ++c.uses_kv;
-        Waiter w;
-        while (ok && !mbar_try_wait(c.kv_bar, par))
-            if (!keep_waiting(a, w, 4000 + int(blockIdx.x))) ok = false;
+        Waiter w;   // the bulk copies of this CTA's K/V rows always land: waited out
+        while (!mbar_try_wait(c.kv_bar, par))
+            if (!keep_waiting_landing(a, w, 4000 + int(blockIdx.x))) {
+                ok = false;
+                break;
+            }
     }
-    // this CTA's positions, split over warps; online softmax in 32-position
-    // tiles.  Up to 32 positions take one warp, which sends its partial state
-    // directly (no merge across warps).
+    // this CTA's positions, spread over all warps.  Few positions (short
+    // contexts): warp w takes positions j0 + w, j0 + w + 8, ..., two at a time,
+    // each lane holding DPL consecutive dimensions, the score a butterfly over
+    // the warp.  Many positions: warp w takes a contiguous block, 32 positions
+    // at a time with one lane per position (online softmax per tile).  Either
+    // way each warp keeps its own state (max, sum, unnormalised output),
+    // merged over the warps in a fixed order below.
     const int cnt = max(0, j1 - j0);
-    const bool single = cnt <= 32;
-    const int per = single ? 32 : (cnt + kCWarps - 1) / kCWarps;
-    const int w0 = j0 + warp * per, w1 = min(j1, w0 + per);
+    const bool lpd = cnt <= kLanePerDimMax;
     float m = -INFINITY, lsum = 0.f, o[DPL];
 #pragma unroll
     for (int i = 0; i < DPL; ++i) o[i] = 0.f;
-    const float4 *q4 = reinterpret_cast<const float4 *>(c.qkv);
     auto krow = [&](int j) -> const float * {
         return j == pos ? c.qkv + D : (j - j0 < n_pre ? kw + size_t(j - j0) * D : kh + size_t(j) * D);
     };
     auto vrow = [&](int j) -> const float * {
         return j == pos ? c.qkv + 2 * D : (j - j0 < n_pre ? vw + size_t(j - j0) * D : vh + size_t(j) * D);
     };
-    for (int base = w0; base < w1 && ok; base += 32) {
-        const int j = base + lane;
-        const bool valid = j < w1;
-        float sc = -INFINITY;
-        if (valid) {
-            // lane j starts at unit j: the rows of a quarter-warp, 4 D bytes
-            // apart, then fall in different shared-memory banks
-            const float4 *kr = reinterpret_cast<const float4 *>(krow(j));
-            float d0 = 0.f, d1 = 0.f;
+    const bool wok = __all_sync(0xffffffffu, ok);   // the loops' shuffles need the whole warp
+    if (lpd) {
+        float qv[DPL];
 #pragma unroll
-            for (int i = 0; i < D / 4; i += 2) {
-                const int u0 = (i + lane) & (D / 4 - 1), u1 = (i + 1 + lane) & (D / 4 - 1);
-                const float4 k0 = kr[u0], k1 = kr[u1], qa = q4[u0], qb = q4[u1];
-                d0 = fmaf(qa.x, k0.x, fmaf(qa.y, k0.y, fmaf(qa.z, k0.z, fmaf(qa.w, k0.w, d0))));
-                d1 = fmaf(qb.x, k1.x, fmaf(qb.y, k1.y, fmaf(qb.z, k1.z, fmaf(qb.w, k1.w, d1))));
-            }
-            sc = (d0 + d1) * a.scale;
-        }
-        const float mn = fmaxf(m, warp_max(sc));
-        const float corr = expf(m - mn);
-        const float p = valid ? expf(sc - mn) : 0.f;
-        lsum = fmaf(lsum, corr, warp_sum(p));
+        for (int i = 0; i < DPL; ++i) qv[i] = c.qkv[lane * DPL + i];
+        for (int ja = j0 + warp; ja < j1 && wok; ja += 2 * kCWarps) {
+            const int jb = ja + kCWarps;
+            const bool hb = jb < j1;
+            const float *ka = krow(ja), *kb = krow(hb ? jb : ja);
+            float sa = 0.f, sb = 0.f;
 #pragma unroll
-        for (int i = 0; i < DPL; ++i) o[i] *= corr;
-        // sum of p_j v_j, 8 positions at a time: their value rows are loaded
-        // before any is used, so the loads (shared or global) overlap
-        const int cntt = min(32, w1 - base);
-        for (int i0 = 0; i0 < cntt; i0 += 8) {
-            float pv[8], vv[8][DPL];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int i = min(i0 + u, cntt - 1);
-                pv[u] = __shfl_sync(0xffffffffu, p, i);
-                const float *vr = vrow(base + i);
-#pragma unroll
-                for (int dd = 0; dd < DPL; ++dd) vv[u][dd] = vr[lane + 32 * dd];
+            for (int i = 0; i < DPL; ++i) {
+                sa = fmaf(qv[i], ka[lane * DPL + i], sa);
+                sb = fmaf(qv[i], kb[lane * DPL + i], sb);
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (i0 + u < cntt) {
-#pragma unroll
-                    for (int dd = 0; dd < DPL; ++dd) o[dd] = fmaf(pv[u], vv[u][dd], o[dd]);
-                }
-        }
-        m = mn;
-    }
-    // this CTA's (max, sum, unnormalised output) to every CTA of the cluster;
-    // the stores complete on each receiver's att_bar
-    const uint32_t slot = smem_addr(c.part + size_t(r) * (D + 4));
-    const uint32_t abar = smem_addr(c.att_bar);
-    if (single) {
-        if (warp == 0) {
-#pragma unroll
-            for (int dd = 0; dd < DPL; ++dd) {
-                const uint32_t off = uint32_t(lane + 32 * dd + 4) * 4u;
-#pragma unroll
-                for (int dst = 0; dst < kClusterSize; ++dst)
-                    st_async_f32(mapa(slot + off, uint32_t(dst)), o[dd], mapa(abar, uint32_t(dst)));
+            for (int off = 16; off > 0; off >>= 1) {
+                sa += __shfl_xor_sync(0xffffffffu, sa, off);
+                sb += __shfl_xor_sync(0xffffffffu, sb, off);
             }
-            if (lane < 2) {
-                const float v = lane == 0 ? (lsum > 0.f ? m : -INFINITY) : lsum;
+            sa *= a.scale;
+            sb = hb ? sb * a.scale : -INFINITY;
+            const float mn = fmaxf(m, fmaxf(sa, sb));
+            const float corr = expf(m - mn);          // 0 on the first positions (m = -inf)
+            const float pa = expf(sa - mn), pb = hb ? expf(sb - mn) : 0.f;
+            lsum = fmaf(lsum, corr, pa + pb);
+            const float *va = vrow(ja), *vb = vrow(hb ? jb : ja);
 #pragma unroll
-                for (int dst = 0; dst < kClusterSize; ++dst)
-                    st_async_f32(mapa(slot + uint32_t(lane) * 4u, uint32_t(dst)), v, mapa(abar, uint32_t(dst)));
-            }
+            for (int i = 0; i < DPL; ++i)
+                o[i] = fmaf(pb, vb[lane * DPL + i], fmaf(pa, va[lane * DPL + i], o[i] * corr));
+            m = mn;
         }
     } else {
-        // merge the warps through shared scratch (outv), then send
+        const int per = (cnt + kCWarps - 1) / kCWarps;
+        const int w0 = j0 + warp * per, w1 = min(j1, w0 + per);
+        const float4 *q4 = reinterpret_cast<const float4 *>(c.qkv);
+        for (int base = w0; base < w1 && wok; base += 32) {
+            const int j = base + lane;
+            const bool valid = j < w1;
+            float sc = -INFINITY;
+            if (valid) {
+                // lane j starts at unit j: the rows of a quarter-warp, 4 D
+                // bytes apart, then fall in different shared-memory banks
+                const float4 *kr = reinterpret_cast<const float4 *>(krow(j));
+                float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+                for (int i = 0; i < D / 4; i += 2) {
+                    const int u0 = (i + lane) & (D / 4 - 1), u1 = (i + 1 + lane) & (D / 4 - 1);
+                    const float4 k0 = kr[u0], k1 = kr[u1], qa = q4[u0], qb = q4[u1];
+                    d0 = fmaf(qa.x, k0.x, fmaf(qa.y, k0.y, fmaf(qa.z, k0.z, fmaf(qa.w, k0.w, d0))));
+                    d1 = fmaf(qb.x, k1.x, fmaf(qb.y, k1.y, fmaf(qb.z, k1.z, fmaf(qb.w, k1.w, d1))));
+                }
+                sc = (d0 + d1) * a.scale;
+            }
+            const float mn = fmaxf(m, warp_max(sc));
+            const float corr = expf(m - mn);
+            const float p = valid ? expf(sc - mn) : 0.f;
+            lsum = fmaf(lsum, corr, warp_sum(p));
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) o[i] *= corr;
+            // sum of p_j v_j, 8 positions at a time: their value rows are
+            // loaded before any is used, so the loads overlap; lane holds
+            // dimensions lane + 32 i here
+            const int cntt = min(32, w1 - base);
+            for (int i0 = 0; i0 < cntt; i0 += 8) {
+                float pv[8], vv[8][DPL];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = min(i0 + u, cntt - 1);
+                    pv[u] = __shfl_sync(0xffffffffu, p, i);
+                    const float *vr = vrow(base + i);
+#pragma unroll
+                    for (int dd = 0; dd < DPL; ++dd) vv[u][dd] = vr[lane + 32 * dd];
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (i0 + u < cntt) {
+#pragma unroll
+                        for (int dd = 0; dd < DPL; ++dd) o[dd] = fmaf(pv[u], vv[u][dd], o[dd]);
+                    }
+            }
+            m = mn;
+        }
+    }
+    // merge the warps through shared scratch (outv), then send this CTA's
+    // (max, sum, unnormalised output) to every CTA of the cluster; the stores
+    // complete on each receiver's att_bar
+    const uint32_t slot = smem_addr(c.part + size_t(r) * (D + 4));
+    const uint32_t abar = smem_addr(pair_bar(c.att_bar, c.uses_att));
+    {
         float *wm = c.outv, *wl = c.outv + kCWarps, *wo = c.outv + 2 * kCWarps;
         if (lane == 0) {
             wm[warp] = m;
             wl[warp] = lsum;
         }
 #pragma unroll
-        for (int i = 0; i < DPL; ++i) wo[warp * D + lane + 32 * i] = o[i];
+        for (int i = 0; i < DPL; ++i) wo[warp * D + (lpd ? lane * DPL + i : lane + 32 * i)] = o[i];
         csync();
         for (int t = tid; t < D + 2; t += kCThreads) {
             float M = -INFINITY;
@@ -1182,7 +1296,7 @@ __device__ void attention(const ClusterArgs &a, CS &c, int l, int h, int r, int 
                 st_async_f32(mapa(slot + off, uint32_t(dst)), v, mapa(abar, uint32_t(dst)));
         }
     }
-    if (!wait_tx_bar(a, c.att_bar, c.uses_att, 6000 + int(blockIdx.x))) ok = false;
+    if (!wait_pair(a, c.att_bar, c.uses_att, 6000 + int(blockIdx.x))) ok = false;
     // combine the 4 ranks in rank order (every CTA gets the same bits)
     for (int t = tid; t < D; t += kCThreads) {
         float M = -INFINITY;
@@ -1377,8 +1491,8 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
             issue_params(a, c, ro, G, &L);
             if (ro.head) {
                 if (tid == 0) {   // this layer's phases of the two cluster exchanges
-                    mbar_arrive_expect_tx(c.qkv_bar, 3u * D * 4u);
-                    mbar_arrive_expect_tx(c.att_bar, uint32_t(kClusterSize) * (D + 2) * 4u);
+                    mbar_arrive_expect_tx(pair_bar(c.qkv_bar, c.uses_qkv), 3u * D * 4u);
+                    mbar_arrive_expect_tx(pair_bar(c.att_bar, c.uses_att), uint32_t(kClusterSize) * (D + 2) * 4u);
                 }
                 prefetch_kv<D>(a, c, l, ro.h, ro.r, pos);
                 prewait_rows(a, c, G.a, k, kCRing, ok);   // this layer's QKV rows, while x is on its way
@@ -1416,7 +1530,7 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                 canon_rows<WT, true>(a, c, G.a, k, kCRing, E, c.x, c.pr, p1, pc, c.outv, -1, best, ok, true);
                 CTRACE(s, l * 16 + 3);   // (the window's closing barrier published c.outv)
                 {
-                    const uint32_t qbar = smem_addr(c.qkv_bar);
+                    const uint32_t qbar = smem_addr(pair_bar(c.qkv_bar, c.uses_qkv));
                     for (int t = tid; t < 3 * q4; t += kCThreads) {
                         const int part = t / q4, d = ro.r * q4 + t % q4;
                         const float v = c.outv[t];
@@ -1426,7 +1540,7 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                             st_async_f32(mapa(dsm, uint32_t(dst)), v, mapa(qbar, uint32_t(dst)));
                     }
                 }
-                if (!wait_tx_bar(a, c.qkv_bar, c.uses_qkv, 8000 + int(blockIdx.x))) ok = false;
+                if (!wait_pair(a, c.qkv_bar, c.uses_qkv, 8000 + int(blockIdx.x))) ok = false;
                 CTRACE(s, l * 16 + 4);
                 attention<D>(a, c, l, ro.h, ro.r, pos, ok);
                 csync();   // publishes c.attn; the attention scratch in c.outv is free again
@@ -1438,7 +1552,7 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                 add_sum(a, an, ro.r * rq, c.outv, ro.h == 0 ? c.x : nullptr, pb, rq);
                 CTRACE(s, l * 16 + 7);
             } else {
-                if (tid == 0) mbar_arrive_expect_tx(c.red_bar, uint32_t(E) * 4u);   // this layer's partial slices
+                if (tid == 0) mbar_arrive_expect_tx(pair_bar(c.red_bar, c.uses_red), uint32_t(E) * 4u);   // this layer's partial slices
                 prewait_rows(a, c, G.a, k, kCRing, ok);   // this layer's fc rows, while x_new is on its way
                 read_sum(a, c, a.H, an, ok, l == 0);
                 if (l == 0) zero_other_parity(a, par);
@@ -1446,10 +1560,10 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                 if (!wait_tx_bar(a, c.prm_bar, c.uses_prm, 9000 + int(blockIdx.x))) ok = false;
                 CTRACE(s, l * 16 + 2);
                 TSET(s, l * 16 + 8);
-                canon_rows<WT, true>(a, c, G.a, k, kCRing, E, c.x, c.pr, p1, pc, c.outv, -1, best, ok, true);
+                // fc rows with gelu_new applied as they are written (the
+                // window's closing barrier publishes c.hloc)
+                canon_rows<WT, true, true>(a, c, G.a, k, kCRing, E, c.x, c.pr, p1, pc, c.hloc, -1, best, ok, true);
                 CTRACE(s, l * 16 + 3);
-                for (int t = tid; t < a.fr; t += kCThreads) c.hloc[t] = gelu_new(c.outv[t]);
-                csync();
                 CTRACE(s, l * 16 + 4);
                 TSET(s, l * 16 + 11);
                 tile_rows<WT>(a, c, G.b, k, kCRing, a.fr, c.hloc, c.outv, ok);
@@ -1458,14 +1572,14 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                 // slice r of all four (in rank order) and adds that once
                 {
                     const int q = rq / 4;   // float4 per slice
-                    const uint32_t rbar = smem_addr(c.red_bar);
+                    const uint32_t rbar = smem_addr(pair_bar(c.red_bar, c.uses_red));
                     const float4 *o4 = reinterpret_cast<const float4 *>(c.outv);
                     for (int t = tid; t < kClusterSize * q; t += kCThreads) {
                         const int dst = t / q, u = t % q;
                         const uint32_t slot = smem_addr(c.red + ro.r * rq + u * 4);
                         st_async_f32x4(mapa(slot, uint32_t(dst)), o4[dst * q + u], mapa(rbar, uint32_t(dst)));
                     }
-                    if (!wait_tx_bar(a, c.red_bar, c.uses_red, 9500 + int(blockIdx.x))) ok = false;
+                    if (!wait_pair(a, c.red_bar, c.uses_red, 9500 + int(blockIdx.x))) ok = false;
                     for (int i = tid; i < rq; i += kCThreads)
                         c.outv[i] = ((c.red[i] + c.red[rq + i]) + c.red[2 * rq + i]) + c.red[3 * rq + i];
                     csync();
@@ -1532,12 +1646,12 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kCAll, 1)
     CS c;
     c.full = reinterpret_cast<uint64_t *>(smem);
     c.empty = c.full + kCRing;
-    c.qkv_bar = c.empty + kCRing;
-    c.att_bar = c.qkv_bar + 1;
-    c.kv_bar = c.qkv_bar + 2;
-    c.prm_bar = c.qkv_bar + 3;
+    c.qkv_bar = c.empty + kCRing;   // pairs: qkv, att, red, x; then kv, prm
+    c.att_bar = c.qkv_bar + 2;
     c.red_bar = c.qkv_bar + 4;
-    c.x_bar = c.qkv_bar + 5;
+    c.x_bar = c.qkv_bar + 6;
+    c.kv_bar = c.qkv_bar + 8;
+    c.prm_bar = c.qkv_bar + 9;
     c.red = reinterpret_cast<float *>(smem + lo.red);
     c.x = reinterpret_cast<float *>(smem + lo.x);
     c.qkv = reinterpret_cast<float *>(smem + lo.qkv);
@@ -1568,12 +1682,14 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kCAll, 1)
             mbar_init(&c.full[i], 1);
             mbar_init(&c.empty[i], 1);
         }
-        mbar_init(c.qkv_bar, 1);   // + the bytes of the 4 ranks' stores
-        mbar_init(c.att_bar, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(c.qkv_bar + i, 1);   // + the bytes of the 4 ranks' stores
+            mbar_init(c.att_bar + i, 1);
+            mbar_init(c.red_bar + i, 1);   // + the bytes of the cluster's four partial slices
+            mbar_init(c.x_bar + i, 1);     // + the bytes of x, a quarter from each CTA of the cluster
+        }
         mbar_init(c.kv_bar, 1);
         mbar_init(c.prm_bar, 1);
-        mbar_init(c.red_bar, 1);   // + the bytes of the cluster's four partial slices
-        mbar_init(c.x_bar, 1);     // + the bytes of x, a quarter from each CTA of the cluster
         mbar_init_fence();
 #ifdef GPT2_CTRACE
         twait = 0;

@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
             const int plane = i / nk, kc = kc0 + i % nk;
             const uint32_t st = base + uint32_t(i) * kStageBytes;
             mbar_arrive_expect_tx(&full[i], kStageBytes);
-            tma_load_2d(st, &a_map, kc * kTcK, plane * a.M + m0, &full[i]);
+            tma_load_2d(st, &a_map, kc * kTcK, plane * a.a_plane_rows + m0, &full[i]);
         }
         pdl_wait();
         for (int i = 0; i < pre; ++i) {
@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
             const int plane = i / nk, kc = kc0 + i % nk;
             const uint32_t st = base + uint32_t(s) * kStageBytes;
             mbar_arrive_expect_tx(&full[s], kStageBytes);
-            tma_load_2d(st, &a_map, kc * kTcK, plane * a.M + m0, &full[s]);
+            tma_load_2d(st, &a_map, kc * kTcK, plane * a.a_plane_rows + m0, &full[s]);
             tma_load_2d(st + kTileA, &b_map, kc * kTcK, 0, &full[s]);
             issued = i + 1;
         }

@@ -21,6 +21,7 @@ constexpr int kTcK = 64;
 constexpr int kTcMaxRows = 64;          // activation rows (sequences or positions) per call
 constexpr int kTcStages = 4;            // shared-memory pipeline depth
 constexpr int kTcThreads = 128;         // 4 warps: TMA producer, MMA issuer, then all four read TMEM
+constexpr int kTcMaxSplits = 8;         // K splits of one linear (the consumers sum at most this many shares)
 
 // Activations as the MMA's B operand: a bf16 [128][K] matrix whose row r < 64
 // is bf16(x_r) and row 64 + r is bf16(x_r - bf16(x_r)), so that
@@ -31,6 +32,7 @@ struct TcGemmArgs {
     int32_t M, K;              // weight rows and inputs (K % 64 == 0)
     int32_t n_rows;            // activation rows that are stored (<= 64)
     int32_t a_planes;          // 1 or 2
+    int32_t a_plane_rows;      // rows from one plane to the next (>= M, a multiple of 128 when a_planes > 1)
     int32_t chunks_per_split;  // 64-input chunks of K per CTA (grid.y = splits)
     float *partials;           // [splits][n_rows][M]: this split's share of Y (hi + lo summed)
     DeviceState *st;           // where a wait that runs out is recorded

@@ -43,6 +43,32 @@ def bytes_per_token(cfg, wdtype: str, pos: int, head: str = "f32") -> dict:
     return parts
 
 
+def batched_bytes_per_step(cfg, positions, wdtype: str = "bf16", head: str = "bf16") -> dict:
+    """Bytes one step of the batched path must move: every stored weight once
+    for the whole batch (block matrices and head), the small fp32 parameters,
+    and per sequence at position p its embedding rows, its logits row and
+    its KV rows (read 0..p, write p)."""
+    E, V, L = cfg.n_embd, cfg.vocab_size, cfg.n_layer
+    positions = list(positions)
+    n = len(positions)
+    head_bytes = V * E * {"f32": 4, "f16": 2, "bf16": 2}[head]
+    parts = {
+        "block_matrices": block_matrix_bytes(cfg, wdtype),
+        "head": head_bytes,
+        "biases_ln": L * 13 * E * 4 + 2 * E * 4,
+        "embedding_rows": n * 2 * E * 4,
+        "logits": n * V * 4,
+        "kv": sum(L * 2 * E * 4 * (p + 2) for p in positions),
+    }
+    parts["total"] = sum(parts.values())
+    return parts
+
+
+def batched_flops_per_step(cfg, n_seq: int) -> int:
+    """Multiply-adds x 2 of the linears and the head for n_seq sequences."""
+    return 2 * n_seq * macs_per_token(cfg)
+
+
 def mean_bytes_per_token(cfg, wdtype: str, positions, head: str = "f32") -> float:
     positions = list(positions)
     return sum(bytes_per_token(cfg, wdtype, p, head)["total"] for p in positions) / len(positions)
