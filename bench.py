@@ -18,10 +18,10 @@ tok/s and GB/s per 64 positions in "context_sweep"), and the batched
 configuration: 64 independent sequences with bf16 weights on the tensor
 cores, prompts of 32..512 tokens prefilled untimed, then 64 device-fed
 greedy steps of all 64 sequences (aggregate tok/s = 64 x steps / time).
---wdtype picks one of the single-sequence configurations as the headline
-instead (then no variants).
+--wdtype picks one of the other configurations as the headline instead
+(then no variants): f16, int4, or bf16 for the batched one.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--wdtype f32|f16|int4]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--wdtype f32|f16|int4|bf16]
   python bench.py --impl reference ...     # the CPU oracle, same metric
 
 Prints one JSON line on rank 0.  N > 1 runs N independent replicas (one
@@ -64,7 +64,8 @@ def parse(argv=None):
     p.add_argument("--steps", type=int, default=20000)
     p.add_argument("--warmup", type=int, default=120)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--wdtype", choices=["f32", "f16", "int4"], default="f32")
+    p.add_argument("--wdtype", choices=["f32", "f16", "int4", "bf16"], default="f32",
+                   help="the headline configuration; bf16 = the batched one (64 sequences, tensor cores)")
     p.add_argument("--head", choices=["f32", "f16", "int4"], default="f32",
                    help="LM head storage: the tied fp32 wte (the configurations), an fp16 copy (README -h) or int4")
     p.add_argument("--no-variants", action="store_true",
@@ -216,9 +217,14 @@ def load_traffic(path: str, key: str):
 def oracle_sample(cfg, weights, prompt, wdtype, budget_s, max_steps=None, head="f32", omp=False):
     """Decode passes of the oracle after an untimed prefill, at the
     workload's positions; stops after ~budget_s seconds (or max_steps).
-    Returns (passes, seconds)."""
+    bf16 (the batched configuration): one of its sequences, the given prompt
+    followed by its greedy steps, with the weights and head that
+    configuration stores.  Returns (passes, seconds)."""
     from oracle import oracle as orc
-    n_prompt, cycle = WORKLOADS[wdtype]
+    if wdtype == "bf16":
+        n_prompt, cycle, head = len(prompt), BATCH_STEPS, "bf16"
+    else:
+        n_prompt, cycle = WORKLOADS[wdtype]
     sw = orc.stored_weights(weights, wdtype, head=head)
     m = orc.OracleModel(cfg, sw, omp=omp)
     try:
@@ -253,9 +259,16 @@ def run_reference(args):
         return 0
     from transformer_decode_token_gb300 import synth
     cfg = synth.SMALL
-    n_prompt, _ = WORKLOADS[args.wdtype]
     w = synth.make_weights(cfg, 0)
-    prompt = synth.make_prompt(cfg, n_prompt, 1)
+    if args.wdtype == "bf16":   # one sequence of the batched workload (the oracle runs one at a time)
+        prompt = min(synth.make_batch_prompts(cfg, BATCH, *BATCH_PROMPT, seed=2), key=len)
+        config = {"workload": f"GPT-2 small 124M, batched configuration ({BATCH} sequences, bf16 block weights "
+                              f"and head, prompts of {BATCH_PROMPT[0]}..{BATCH_PROMPT[1]} tokens, {BATCH_STEPS} "
+                              "greedy steps); the oracle decodes its shortest sequence",
+                  "batch": BATCH, "weights": "synthetic N(0,0.02), seed 0"}
+    else:
+        prompt = synth.make_prompt(cfg, WORKLOADS[args.wdtype][0], 1)
+        config = workload_config(args.wdtype, 1, args.head)
     cores = host_cores()
     os.environ.setdefault("OMP_NUM_THREADS", str(cores))
     oracle_sample(cfg, w, prompt, args.wdtype, 1e9, max_steps=min(args.warmup, 3), head=args.head, omp=True)
@@ -263,8 +276,9 @@ def run_reference(args):
     value = n / el
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / n,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": workload_config(args.wdtype, 1, args.head),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if args.wdtype == "f32" else f"{args.wdtype} weights, f32 math",
+            "data": "synthetic", "config": config,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": int(os.environ["OMP_NUM_THREADS"]),
                              "kind": "oracle",
                              "sample": f"{n} of the {args.steps} requested decode passes (60 s cap), the C oracle's "
@@ -437,10 +451,14 @@ def measure(torch, cfg, w, wdtype, head, path, steps, warmup, world, local, barr
     return out
 
 
-def measure_batch(torch, cfg, w, steps, warmup, world, local, barrier, max_over_ranks):
+def measure_batch(torch, cfg, w, steps, warmup, world, local, barrier, max_over_ranks, e2e_calls=0,
+                  exact=False):
     """The batched configuration on a fresh batched model: an untimed prefill
     of the 64 ragged prompts, then 64 device-resident greedy steps timed;
-    repeated (each after a fresh prefill) until `steps` steps are timed."""
+    repeated (each after a fresh prefill) until `steps` steps are timed,
+    rounded up to whole cycles unless `exact`.
+    With e2e_calls > 0, also that many whole generations through the ABI
+    with host buffers (prompts in, every generated id out), wall clock."""
     from transformer_decode_token_gb300 import binding, roofline, synth
     prompts = synth.make_batch_prompts(cfg, BATCH, *BATCH_PROMPT, seed=2)
     lens = [len(q) for q in prompts]
@@ -453,48 +471,75 @@ def measure_batch(torch, cfg, w, steps, warmup, world, local, barrier, max_over_
         m.prefill(prompts)
         m.decode_greedy(min(warmup, BATCH_STEPS))
         m.sync()
-        cycles = max(1, -(-steps // BATCH_STEPS))
+        # whole cycles of the generation, or exactly `steps` steps (the last
+        # cycle cut short) when this is the line's own workload
+        n_total = steps if exact else BATCH_STEPS * max(1, -(-steps // BATCH_STEPS))
+        cycles = [min(BATCH_STEPS, n_total - i) for i in range(0, n_total, BATCH_STEPS)]
         stream = torch.cuda.current_stream()
         ms = 0.0
         launches = 0
         sampler = ClockSampler(gpu_id_for(torch, local))
         sampler.start()
         t_begin = time.time()
-        for _ in range(cycles):
+        for i, n_cyc in enumerate(cycles):
             m.prefill(prompts)
             m.sync()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             barrier()
             torch.cuda.synchronize()
+            if i == 0:   # the first cycle's steps are what `ncu --profile-from-start off` captures
+                torch.cuda.profiler.start()
             n0 = m.info()[1]
             e0.record(stream)
-            m.decode_greedy(BATCH_STEPS)
+            m.decode_greedy(n_cyc)
             e1.record(stream)
             launches += m.info()[1] - n0
             torch.cuda.synchronize()
+            if i == 0:
+                torch.cuda.profiler.stop()
             ms += e0.elapsed_time(e1)
         t_end = time.time()
         clocks = sampler.stop(t_begin, t_end)
         m.sync()
+        e2e = None
+        if e2e_calls > 0:
+            p0, p1 = min(lens), max(lens) + BATCH_STEPS
+            barrier()
+            t0 = time.perf_counter()
+            for _ in range(e2e_calls):
+                m.prefill(prompts)
+                m.decode_greedy(BATCH_STEPS)
+                ids = m.ids(p0, p1 - p0)
+            el = max_over_ranks(time.perf_counter() - t0)
+            e2e = {"value": BATCH * BATCH_STEPS * e2e_calls * world / el, "unit": UNIT,
+                   "h2d_bytes_per_step": (sum(lens) + BATCH) * 4 / BATCH_STEPS,
+                   "d2h_bytes_per_step": ids.nbytes / BATCH_STEPS,
+                   "calls": e2e_calls,
+                   "what": f"gpt2_prefill_batch (host prompts) + gpt2_decode_batch_greedy({BATCH_STEPS}) + "
+                           "gpt2_batch_ids (host ids) per call, wall clock, prefill included; value = generated "
+                           "tokens / time"}
     finally:
         m.close()
     ms = max_over_ranks(ms)
-    n_steps = cycles * BATCH_STEPS
-    # bytes and flops of the timed steps: step t runs every sequence at lens + t
-    alg = sum(roofline.batched_bytes_per_step(cfg, [L + t for L in lens])["total"] for t in range(BATCH_STEPS))
-    alg /= BATCH_STEPS
+    n_steps = sum(cycles)
+    # bytes and flops of the timed steps: step t of a cycle runs every sequence at lens + t
+    per_t = [roofline.batched_bytes_per_step(cfg, [L + t for L in lens])["total"] for t in range(BATCH_STEPS)]
+    alg = sum(sum(per_t[:n]) for n in cycles) / n_steps
     flops = roofline.batched_flops_per_step(cfg, BATCH)
     peaks, peak_kind = measured_peaks()
     step_s = ms / 1e3 / n_steps
     achieved = alg / step_s / 1e9
-    return {
+    out = {
         "value": BATCH * world / step_s, "unit": UNIT, "ms_per_step": ms / n_steps, "steps": n_steps,
         "gpu_launches": launches, "clocks": clocks, "dtype": "bf16 weights, f32 math (bf16 x bf16 tensor-core "
                                                                 "products of hi/lo activation parts, fp32 sums)",
         "config": {"workload": f"GPT-2 small 124M, batched: {BATCH} sequences, bf16 block weights and head, "
                                f"prompts uniform in [{BATCH_PROMPT[0]}, {BATCH_PROMPT[1]}] tokens (seed 2), "
                                f"{BATCH_STEPS} greedy decode steps per sequence (prefill untimed)",
-                   "batch": BATCH, "prompt_tokens": sum(lens), "weights": "synthetic N(0,0.02), seed 0"},
+                   "batch": BATCH, "prompt_tokens": sum(lens), "weights": "synthetic N(0,0.02), seed 0",
+                   "l2": "no flush: every step streams 247 MB of bf16 weights and ~1.4 GB of KV rows through a "
+                         "129 MB L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": f"one batched step: a CUDA graph of {kps} kernels (tcgen05 linears, "
                                                "ragged attention, LayerNorm/gelu/argmax), PDL-chained",
                      "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -506,6 +551,9 @@ def measure_batch(torch, cfg, w, steps, warmup, world, local, barrier, max_over_
                              "rows; flops: 2 x 64 x the linears' and head's multiply-adds (the hi/lo parts "
                              "double the tensor work actually issued)"},
     }
+    if e2e is not None:
+        out["e2e"] = e2e
+    return out
 
 
 def measure_prefill(torch, cfg, w, lengths=(2, 4, 8, 10, 16, 64), reps=10):
@@ -543,6 +591,35 @@ def measure_prefill(torch, cfg, w, lengths=(2, 4, 8, 10, 16, 64), reps=10):
     return out
 
 
+def batch_main(args, torch, dist, cfg, w, rank, world, local, barrier, max_over_ranks):
+    """--wdtype bf16: the batched configuration as the line's own workload
+    (exactly --steps timed steps)."""
+    from transformer_decode_token_gb300 import synth
+    b = measure_batch(torch, cfg, w, args.steps, args.warmup, world, local, barrier, max_over_ranks,
+                      e2e_calls=max(1, min(args.e2e_calls, 5)), exact=True)
+    line = {"metric": METRIC, "value": b["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": b["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": b["dtype"], "data": "synthetic",
+            "config": b["config"], "path": "batched (tcgen05)", "e2e": b["e2e"],
+            "gpu_launches": b["gpu_launches"], "roofline": b["roofline"], "clocks": b["clocks"]}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        prompts = synth.make_batch_prompts(cfg, BATCH, *BATCH_PROMPT, seed=2)
+        prompt = min(prompts, key=len)
+        cores = host_cores()
+        os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+        n, el = oracle_sample(cfg, w, prompt, "bf16", args.cpu_seconds, omp=True)
+        line["cpu_baseline"] = {
+            "value": n / el, "unit": UNIT, "cores": int(os.environ["OMP_NUM_THREADS"]), "kind": "oracle",
+            "sample": f"{n} greedy decode passes of the batched workload's shortest sequence ({len(prompt)}-token "
+                      f"prompt, untimed prefill), bf16-stored weights and head, the C oracle's OpenMP build; "
+                      f"the oracle runs one sequence at a time, ~{args.cpu_seconds:.0f} s"}
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -568,6 +645,8 @@ def main():
 
     cfg = synth.SMALL
     w = synth.make_weights(cfg, 0)
+    if args.wdtype == "bf16":
+        return batch_main(args, torch, dist, cfg, w, rank, world, local, barrier, max_over_ranks)
     head = measure(torch, cfg, w, args.wdtype, args.head, args.path, args.steps, args.warmup, world, local,
                    barrier, max_over_ranks, sweep=True, e2e_calls=max(3, min(args.e2e_calls, 3000 // sum(
                        WORKLOADS[args.wdtype]))))

@@ -28,8 +28,15 @@ HEAD_PHASES = [("wait for x (GPU-wide sum)", 0, 1), ("LN/bias parameters", 1, 2)
                ("QKV rows (LN folded)", 2, 3), ("q,k,v exchange in cluster", 3, 4),
                ("attention", 4, 5), ("out-proj tile", 5, 6), ("add into x_new", 6, 7)]
 FC_PHASES = [("wait for x_new (GPU-wide sum)", 0, 1), ("LN/bias parameters", 1, 2),
-             ("fc rows (LN folded)", 2, 3), ("gelu_new", 3, 4), ("mlp-proj tile", 4, 5),
+             ("fc rows + gelu_new (LN folded)", 2, 3), ("mlp-proj tile", 4, 5),
              ("cluster reduce + add into x", 5, 6)]
+# inside the dot-product phases (slot offsets 8..10: canonical rows, 11 and 13: tile rows)
+HEAD_SUB = [("QKV: x*gamma to registers + LN stat shares", 2, 8), ("QKV: ring-stage waits", 8, 9),
+            ("QKV: row groups (dot products, butterflies)", 9, 10), ("QKV: window barrier", 10, 3),
+            ("out-proj: rows", 11, 13), ("out-proj: window barrier", 13, 6)]
+FC_SUB = [("fc: x*gamma to registers + LN stat shares", 2, 8), ("fc: ring-stage waits", 8, 9),
+          ("fc: row groups (dot products, gelu_new)", 9, 10), ("fc: window barrier", 10, 3),
+          ("mlp-proj: rows", 11, 13), ("mlp-proj: window barrier", 13, 5)]
 LM_PHASES = [("wait for x (GPU-wide sum)", 200, 201), ("LM-head rows + argmax keys", 201, 202),
              ("publish the tagged argmax key", 202, 203)]
 
@@ -68,6 +75,8 @@ def run(wdtype: str, layer: int = 5):
     out["head_cluster_us"] = {n: med_us(range(n_head), s0, s1, layer * 16) for n, s0, s1 in HEAD_PHASES}
     out["fc_us"] = {n: med_us(range(n_head, grid), s0, s1, layer * 16) for n, s0, s1 in FC_PHASES}
     out["lm_head_us"] = {n: med_us(range(grid), s0, s1, 0) for n, s0, s1 in LM_PHASES}
+    out["head_cluster_sub_us"] = {n: med_us(range(n_head), s0, s1, layer * 16) for n, s0, s1 in HEAD_SUB}
+    out["fc_sub_us"] = {n: med_us(range(n_head, grid), s0, s1, layer * 16) for n, s0, s1 in FC_SUB}
     t0 = a[:grid, 0, 0, 0].min()
     out["pass_us"] = float(a[:grid, 0, 203, 0].max() - t0) / 1e3
     out["layer_us"] = float(np.median(a[:n_head, 0, (layer + 1) * 16 + 1, 0] - a[:n_head, 0, layer * 16 + 1, 0])) / 1e3
@@ -83,10 +92,10 @@ def main():
     out = run(a.wdtype, a.layer)
     print(f"cluster kernel, GPT-2 small {out['wdtype']}, {out['ctas']} CTAs ({out['head_ctas']} in head clusters); "
           f"layer {out['layer']}: {out['layer_us']:.2f} us per layer (head-CTA x arrival to x arrival)")
-    for grp in ("head_cluster_us", "fc_us", "lm_head_us"):
+    for grp in ("head_cluster_us", "fc_us", "lm_head_us", "head_cluster_sub_us", "fc_sub_us"):
         print(f"  {grp}:")
         for n, v in out[grp].items():
-            print(f"    {n:34s} {v:7.2f} us")
+            print(f"    {n:46s} {v:7.2f} us")
     if a.json:
         with open(a.json, "w") as f:
             json.dump(out, f, indent=1)
