@@ -671,8 +671,9 @@ def main():
             v["config"] = workload_config(wd, world)
             v["dtype"] = f"{wd} weights, f32 math"
             variants[wd] = v
-        variants["batch64_bf16"] = measure_batch(torch, cfg, w, args.steps, args.warmup, world, local, barrier,
-                                                 max_over_ranks)
+        # (at most 10 cycles: each cycle re-runs the untimed prefill of all 64 prompts)
+        variants["batch64_bf16"] = measure_batch(torch, cfg, w, min(args.steps, 10 * BATCH_STEPS), args.warmup,
+                                                 world, local, barrier, max_over_ranks)
         line["variants"] = variants
         line["prefill"] = measure_prefill(torch, cfg, w)
 

@@ -127,6 +127,20 @@ def test_tiny_batch_full_and_kv_cache():
         m.close()
 
 
+def test_tiny_batch_long_contexts_span_attention_chunks():
+    """Tiny model with 256 positions: prompts of 40..230 tokens, so a
+    sequence's attention covers up to four chunks of 64 positions (each
+    chunk's softmax merged with the others'), 12 steps across chunk
+    boundaries; every sequence checked."""
+    import dataclasses
+    cfg = dataclasses.replace(synth.TINY, n_positions=256)
+    prompts = synth.make_batch_prompts(cfg, 9, 40, 230, seed=4)
+    prompts[0] = prompts[0][:60]    # crosses the 64-position boundary during the steps
+    prompts[1] = prompts[1][:128]   # starts exactly on a boundary
+    m, _ = run_batch(cfg, prompts, 12, list(range(9)))
+    m.close()
+
+
 def test_small_batch_of_64_ragged_prompts():
     """GPT-2 small, 64 sequences with prompts of 32..512 tokens (the batched
     workload's shape), 3 teacher-forced steps; the oracle checks the three

@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kBT) k_b_attn(const BAttnArgs a)
 {
     constexpr int LPR = D / 4;               // threads per row
     constexpr int RPP = kBT / LPR;           // rows per pass
-    constexpr int U = 4;                     // passes in flight
+    constexpr int U = 8;                     // passes in flight
     extern __shared__ float sc[];            // [P] scores, then probabilities
     __shared__ float red[kBT / 32];
     __shared__ __align__(16) float qkv[3 * D];
@@ -218,6 +218,19 @@ __global__ void __launch_bounds__(kBT) k_b_attn(const BAttnArgs a)
             if (l == 0 && j < n) sc[j] = d * a.scale;
         }
     }
+    // the first value rows are loaded while the softmax is taken
+    float4 v4[U];
+    auto load_v = [&](int j0) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * RPP + g;
+            v4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j < n)
+                v4[u] = (a.append && j == pos) ? reinterpret_cast<const float4 *>(qkv + 2 * D)[l]
+                                               : reinterpret_cast<const float4 *>(vh + size_t(j) * D)[l];
+        }
+    };
+    load_v(0);
     __syncthreads();
     float m = -INFINITY;
     for (int j = threadIdx.x; j < n; j += kBT) m = fmaxf(m, sc[j]);
@@ -231,15 +244,7 @@ __global__ void __launch_bounds__(kBT) k_b_attn(const BAttnArgs a)
     sum = block_sum(sum, red);   // (its barriers also publish sc)
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j0 = 0; j0 < n; j0 += RPP * U) {
-        float4 v4[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int j = j0 + u * RPP + g;
-            v4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (j < n)
-                v4[u] = (a.append && j == pos) ? reinterpret_cast<const float4 *>(qkv + 2 * D)[l]
-                                               : reinterpret_cast<const float4 *>(vh + size_t(j) * D)[l];
-        }
+        if (j0 > 0) load_v(j0);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int j = j0 + u * RPP + g;

@@ -1012,11 +1012,20 @@ __device__ __forceinline__ float tile_unit(const RowAddr &ra, uint32_t us, int u
     }
 }
 
+// Tile rows of exactly 64 columns (the head's slice of the output
+// projection) run with the unit loop unrolled.
+template <int WT>
+constexpr int kTileUnroll = WT == kWF32 ? 16 : WT == kWF16 ? 8 : 2;
+
 // Dot products of the tile rows of a segment (cols columns) with vin: one
 // thread per row, which waits for its row's stage; 16-byte units of row r are
 // stored at u ^ (r & m), so the threads of a quarter-warp read different
-// banks.  out[row] for every row.
-template <int WT>
+// banks.  out[row] for every row.  Rows of exactly UX units run with the unit
+// loop unrolled (every load of a row in flight at once); with XREG (fp32,
+// several rows per thread) the UX float4 of inputs are loaded into registers
+// once.  The sums are taken in the same order on every path (each unit's
+// fused products, then even units, odd units, and the two).
+template <int WT, int UX, bool XREG>
 __device__ __forceinline__ void tile_rows(const ClusterArgs &a, CS &c, const Geo &g, uint32_t &k, int win, int cols,
                                           const float *vin, float *out, bool &ok)
 {
@@ -1026,6 +1035,12 @@ __device__ __forceinline__ void tile_rows(const ClusterArgs &a, CS &c, const Geo
     const int m = (U & (U - 1)) == 0 ? min(U, 8) - 1 : 0;
     const int C = g.chunk, nch = g.nch;
     const uint32_t v4 = smem_addr(vin);
+    constexpr bool kReg = XREG && WT == kWF32;
+    float4 xv[kReg ? UX : 1];
+    if (kReg && U == UX) {
+#pragma unroll
+        for (int u = 0; u < (kReg ? UX : 1); ++u) xv[u] = lds_f4(v4 + 16u * uint32_t(u));
+    }
     for (int q0 = 0; q0 < nch; q0 += win) {
         const int q1 = min(nch, q0 + win);
         const int r1 = min(g.rows, q1 * C);
@@ -1040,11 +1055,27 @@ __device__ __forceinline__ void tile_rows(const ClusterArgs &a, CS &c, const Geo
                 const RowAddr ra = row_addr(stage_addr(a, c, k + uint32_t(q)), g, row - q * C);
                 const int sw = row & m;
                 float acc0 = 0.f, acc1 = 0.f;
+                if (U == UX) {
+#pragma unroll
+                    for (int u = 0; u < UX; ++u) {
+                        float part;
+                        if constexpr (kReg) {
+                            const float4 w = lds_f4(ra.m + 16u * uint32_t(u ^ sw));
+                            const float4 x = xv[u];
+                            part = fmaf(w.w, x.w, fmaf(w.z, x.z, w.y * x.y)) + w.x * x.x;
+                        } else {
+                            part = tile_unit<WT>(ra, uint32_t(u ^ sw), u, v4);
+                        }
+                        if (u & 1) acc1 += part;
+                        else acc0 += part;
+                    }
+                } else {
 #pragma unroll 2
-                for (int u = 0; u < U; ++u) {
-                    const float part = tile_unit<WT>(ra, uint32_t(u ^ sw), u, v4);
-                    if (u & 1) acc1 += part;
-                    else acc0 += part;
+                    for (int u = 0; u < U; ++u) {
+                        const float part = tile_unit<WT>(ra, uint32_t(u ^ sw), u, v4);
+                        if (u & 1) acc1 += part;
+                        else acc0 += part;
+                    }
                 }
                 out[row] = acc0 + acc1;
             }
@@ -1547,7 +1578,7 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                 CTRACE(s, l * 16 + 5);
                 // the head's slice of the output projection, rows rank*E/4.. (+ x + bias once, by head 0)
                 TSET(s, l * 16 + 11);
-                tile_rows<WT>(a, c, G.b, k, kCRing, D, c.attn, c.outv, ok);
+                tile_rows<WT, kTileUnroll<WT>, false>(a, c, G.b, k, kCRing, D, c.attn, c.outv, ok);
                 CTRACE(s, l * 16 + 6);
                 add_sum(a, an, ro.r * rq, c.outv, ro.h == 0 ? c.x : nullptr, pb, rq);
                 CTRACE(s, l * 16 + 7);
@@ -1566,7 +1597,7 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                 CTRACE(s, l * 16 + 3);
                 CTRACE(s, l * 16 + 4);
                 TSET(s, l * 16 + 11);
-                tile_rows<WT>(a, c, G.b, k, kCRing, a.fr, c.hloc, c.outv, ok);
+                tile_rows<WT, 8, false>(a, c, G.b, k, kCRing, a.fr, c.hloc, c.outv, ok);
                 CTRACE(s, l * 16 + 5);
                 // the cluster's four partial vectors meet first: rank r sums
                 // slice r of all four (in rank order) and adds that once
