@@ -374,8 +374,9 @@ int setup_cluster(gpt2_model *m, int32_t *prompt_buf)
     const int n_clusters = H + nfc / kClusterSize, grid = n_clusters * kClusterSize;
     if (grid > 256) return GPT2_ERR_INVALID_ARG;   // each consumer thread polls one CTA's LM-head key
     // a residual-sum word counts its contributions in 8 bits (bits 56..63):
-    // one per head cluster (x after attention), one per fc cluster (x after the MLP)
-    if (H > 255 || nfc / kClusterSize > 255) return GPT2_ERR_INVALID_ARG;
+    // one per head cluster (x after attention), one per fc cluster (x after the
+    // MLP), or one per fc CTA where those add their partials directly (int4)
+    if (H > 255 || (wt == kWI4 ? nfc : nfc / kClusterSize) > 255) return GPT2_ERR_INVALID_ARG;
     if (V > (1 << 17)) return GPT2_ERR_INVALID_ARG;   // tagged keys keep 17 bits of the id
     // LM-head rows per CTA: a multiple of 4 (of 8 for an int4 head, whose shares are padded)
     const int head_rpc = m->head_int4 ? ((V + grid - 1) / grid + 7) / 8 * 8 : ((V + grid - 1) / grid + 3) / 4 * 4;

@@ -160,104 +160,155 @@ struct BAttnArgs {
     int32_t append;                 // 1: this row's k, v are written at pos here
     float scale;
     __nv_bfloat16 *out;             // [128][E] hi/lo B operand of the output projection
+    DeviceState *st;
 };
 
-// One CTA per (row, head).  Scores: D/4 threads per cached row (a float4 of
-// the head dimension each), several rows per pass, shuffles within the row's
-// threads; softmax over positions 0..pos (max subtracted); the weighted sum of
-// v with the same thread layout, partial sums combined in a fixed order.
+constexpr int kAttnRows = 32;       // cache rows per stage
+constexpr int kAttnStages = 3;
+
+// Dynamic shared memory of k_b_attn: the stages, then the scores [P].
+__host__ __device__ constexpr size_t attn_smem(int D, int P)
+{
+    return size_t(kAttnStages) * kAttnRows * D * 4 + size_t(P) * 4;
+}
+
+// One CTA per (row, head).  The row's cached K rows, then its V rows, stream
+// through a ring of shared-memory stages by bulk copies (thread 0 refills a
+// stage once every thread is done with it), so each CTA keeps kAttnStages
+// copies in flight.  Scores: D/4 threads per cached row (a float4 of the
+// head dimension each), shuffles within the row's threads; softmax over
+// positions 0..pos (max subtracted); the weighted sum of v with the same
+// thread layout, the row groups' partial sums combined in a fixed order.
+// When this kernel appends (decode), row pos is this token's k, v (from the
+// shares, kept in shared memory) and the cache supplies rows 0..pos-1.
 template <int D>
 __global__ void __launch_bounds__(kBT) k_b_attn(const BAttnArgs a)
 {
     constexpr int LPR = D / 4;               // threads per row
     constexpr int RPP = kBT / LPR;           // rows per pass
-    constexpr int U = 8;                     // passes in flight
-    extern __shared__ float sc[];            // [P] scores, then probabilities
+    constexpr int NPS = kAttnRows / RPP;     // passes per stage
+    constexpr uint32_t kRowB = D * 4, kStageB = kAttnRows * kRowB;
+    static_assert(kAttnRows % RPP == 0 && LPR <= 32, "thread layout");
+    extern __shared__ __align__(128) uint8_t dyn[];   // [stages][kAttnRows][D], then scores [P]
+    float *sc = reinterpret_cast<float *>(dyn + size_t(kAttnStages) * kStageB);
+    __shared__ __align__(8) uint64_t full[kAttnStages];
     __shared__ float red[kBT / 32];
     __shared__ __align__(16) float qkv[3 * D];
     __shared__ __align__(16) float part[RPP][D];
     const int b = blockIdx.x, h = blockIdx.y, E = a.E;
-    const int g = threadIdx.x / LPR, l = threadIdx.x % LPR;
+    const int tid = threadIdx.x, g = tid / LPR, l = tid % LPR;
+    if (tid == 0) {
+        for (int i = 0; i < kAttnStages; ++i) mbar_init(&full[i], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
     pdl_wait();
     const int pos = a.pos[b];
     if (pos < 0 || pos >= a.P) {             // inactive row: zero output
-        for (int d = threadIdx.x; d < D; d += kBT) put_hi_lo(a.out, b, E, h * D + d, 0.f);
+        for (int d = tid; d < D; d += kBT) put_hi_lo(a.out, b, E, h * D + d, 0.f);
         pdl_launch_dependents();
         return;
     }
     const int slot = a.slots == 1 ? 0 : b;
     float *kh = a.kc + (size_t(slot) * a.H + h) * a.P * D;
     float *vh = a.vc + (size_t(slot) * a.H + h) * a.P * D;
-    for (int t = threadIdx.x; t < 3 * D; t += kBT) {
-        const int part_ = t / D, d = t % D;
-        const int j = part_ * E + h * D + d;
-        const float s = sum_shares(a.parts, a.splits, a.rows, 3 * E, b, j) + a.bias[j];
-        qkv[t] = s;
-        if (a.append && part_ == 1) kh[size_t(pos) * D + d] = s;
-        if (a.append && part_ == 2) vh[size_t(pos) * D + d] = s;
-    }
-    __syncthreads();
     const int n = pos + 1;
-    const float4 q4 = reinterpret_cast<const float4 *>(qkv)[l];
-    for (int j0 = 0; j0 < n; j0 += RPP * U) {
-        float4 k4[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int j = j0 + u * RPP + g;
-            k4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (j < n)
-                k4[u] = (a.append && j == pos) ? reinterpret_cast<const float4 *>(qkv + D)[l]
-                                               : reinterpret_cast<const float4 *>(kh + size_t(j) * D)[l];
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            float d = fmaf(q4.x, k4[u].x, fmaf(q4.y, k4[u].y, fmaf(q4.z, k4[u].z, q4.w * k4[u].w)));
-#pragma unroll
-            for (int o = LPR / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-            const int j = j0 + u * RPP + g;
-            if (l == 0 && j < n) sc[j] = d * a.scale;
-        }
-    }
-    // the first value rows are loaded while the softmax is taken
-    float4 v4[U];
-    auto load_v = [&](int j0) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int j = j0 + u * RPP + g;
-            v4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (j < n)
-                v4[u] = (a.append && j == pos) ? reinterpret_cast<const float4 *>(qkv + 2 * D)[l]
-                                               : reinterpret_cast<const float4 *>(vh + size_t(j) * D)[l];
+    const int nk = a.append ? pos : n;                    // rows read from the cache
+    const int m = (nk + kAttnRows - 1) / kAttnRows;        // stages of K, then as many of V
+    // chunk q of the stream (K chunks 0..m-1, then V chunks) into stage q % kAttnStages
+    auto issue = [&](int q) {
+        const bool isv = q >= m;
+        const int r0 = (isv ? q - m : q) * kAttnRows, rows = min(kAttnRows, nk - r0);
+        uint64_t *bar = &full[q % kAttnStages];
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // after the stage's generic reads
+        mbar_arrive_expect_tx(bar, uint32_t(rows) * kRowB);
+        bulk_g2s(dyn + size_t(q % kAttnStages) * kStageB, (isv ? vh : kh) + size_t(r0) * D, uint32_t(rows) * kRowB,
+                 bar);
+    };
+    if (tid == 0)
+        for (int q = 0; q < min(kAttnStages, 2 * m); ++q) issue(q);
+    bool good = true;   // (the copies always land; a wait that runs out is recorded)
+    auto wait_chunk = [&](int q) {
+        if (!mbar_wait_bounded(&full[q % kAttnStages], uint32_t(q / kAttnStages) & 1u) && good) {
+            good = false;
+            if (l == 0) record_error(a.st, kDevErrTimeout, 14000 + b);
         }
     };
-    load_v(0);
+    // q, k, v from the QKV shares; k and v appended to the cache
+    for (int t = tid; t < (a.append ? 3 * D : D); t += kBT) {
+        const int part_ = t / D, d = t % D;
+        const int j = part_ * E + h * D + d;
+        const float v = sum_shares(a.parts, a.splits, a.rows, 3 * E, b, j) + a.bias[j];
+        qkv[t] = v;
+        if (part_ == 1) kh[size_t(pos) * D + d] = v;
+        if (part_ == 2) vh[size_t(pos) * D + d] = v;
+    }
     __syncthreads();
-    float m = -INFINITY;
-    for (int j = threadIdx.x; j < n; j += kBT) m = fmaxf(m, sc[j]);
-    m = block_max(m, red);
+    const float4 q4 = reinterpret_cast<const float4 *>(qkv)[l];
+    auto dot_row = [&](const float4 k4) {
+        float d = fmaf(q4.x, k4.x, fmaf(q4.y, k4.y, fmaf(q4.z, k4.z, q4.w * k4.w)));
+#pragma unroll
+        for (int o = LPR / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+        return d;
+    };
+    for (int c = 0; c < m; ++c) {
+        wait_chunk(c);
+        const float *stg = reinterpret_cast<const float *>(dyn + size_t(c % kAttnStages) * kStageB);
+#pragma unroll
+        for (int u = 0; u < NPS; ++u) {
+            const int r = u * RPP + g, j = c * kAttnRows + r;
+            const float d = dot_row(reinterpret_cast<const float4 *>(stg + r * D)[l]);
+            if (l == 0 && j < nk) sc[j] = d * a.scale;
+        }
+        __syncthreads();   // the stage is free again
+        if (tid == 0 && c + kAttnStages < 2 * m) issue(c + kAttnStages);
+    }
+    if (a.append && tid < 32) {   // row pos: this token's k (warp 0; group 0 holds the sum)
+        const float d = dot_row(reinterpret_cast<const float4 *>(qkv + D)[l]);
+        if (tid == 0) sc[pos] = d * a.scale;
+    }
+    __syncthreads();
+    float mx = -INFINITY;
+    for (int j = tid; j < n; j += kBT) mx = fmaxf(mx, sc[j]);
+    mx = block_max(mx, red);
     float sum = 0.f;
-    for (int j = threadIdx.x; j < n; j += kBT) {
-        const float p = expf(sc[j] - m);
+    for (int j = tid; j < n; j += kBT) {
+        const float p = expf(sc[j] - mx);
         sc[j] = p;
         sum += p;
     }
     sum = block_sum(sum, red);   // (its barriers also publish sc)
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j0 = 0; j0 < n; j0 += RPP * U) {
-        if (j0 > 0) load_v(j0);
+    for (int c = 0; c < m; ++c) {
+        const int q = m + c;
+        wait_chunk(q);
+        const float *stg = reinterpret_cast<const float *>(dyn + size_t(q % kAttnStages) * kStageB);
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int j = j0 + u * RPP + g;
-            const float p = j < n ? sc[j] : 0.f;
-            acc.x = fmaf(p, v4[u].x, acc.x);
-            acc.y = fmaf(p, v4[u].y, acc.y);
-            acc.z = fmaf(p, v4[u].z, acc.z);
-            acc.w = fmaf(p, v4[u].w, acc.w);
+        for (int u = 0; u < NPS; ++u) {
+            const int r = u * RPP + g, j = c * kAttnRows + r;
+            if (j < nk) {
+                const float p = sc[j];
+                const float4 v4 = reinterpret_cast<const float4 *>(stg + r * D)[l];
+                acc.x = fmaf(p, v4.x, acc.x);
+                acc.y = fmaf(p, v4.y, acc.y);
+                acc.z = fmaf(p, v4.z, acc.z);
+                acc.w = fmaf(p, v4.w, acc.w);
+            }
         }
+        __syncthreads();
+        if (tid == 0 && q + kAttnStages < 2 * m) issue(q + kAttnStages);
+    }
+    if (a.append && g == 0) {   // row pos: this token's v
+        const float p = sc[pos];
+        const float4 v4 = reinterpret_cast<const float4 *>(qkv + 2 * D)[l];
+        acc.x = fmaf(p, v4.x, acc.x);
+        acc.y = fmaf(p, v4.y, acc.y);
+        acc.z = fmaf(p, v4.z, acc.z);
+        acc.w = fmaf(p, v4.w, acc.w);
     }
     reinterpret_cast<float4 *>(part[g])[l] = acc;
     __syncthreads();
-    for (int d = threadIdx.x; d < D; d += kBT) {
+    for (int d = tid; d < D; d += kBT) {
         float o = 0.f;
         for (int r = 0; r < RPP; ++r) o += part[r][d];
         put_hi_lo(a.out, b, E, h * D + d, o / sum);
@@ -538,6 +589,7 @@ int record_step(gpt2_batch *m, cudaStream_t s)
         at.append = slots == 1 ? 0 : 1;   // one sequence: every row's k, v first (k_b_append)
         at.scale = float(1.0 / std::sqrt(double(D)));
         at.out = m->b_a;
+        at.st = m->st;
         if (slots == 1) {
             int dd = D;
             void *ap[] = {&at, &dd};
@@ -548,7 +600,7 @@ int record_step(gpt2_batch *m, cudaStream_t s)
         const void *afn = D == 32 ? reinterpret_cast<const void *>(k_b_attn<32>)
                           : D == 64 ? reinterpret_cast<const void *>(k_b_attn<64>)
                                     : reinterpret_cast<const void *>(k_b_attn<128>);
-        BTRY(launch_pdl(afn, dim3(R, H), dim3(kBT), size_t(P) * 4, s, pdl(), a2));
+        BTRY(launch_pdl(afn, dim3(R, H), dim3(kBT), attn_smem(D, P), s, pdl(), a2));
         BTRY(run_linear(m, Ly.lin[1], m->map_a, m->p_o, s, pdl()));
         ln.mode = 1;
         ln.parts = m->p_o;
@@ -691,6 +743,12 @@ int engine_build(gpt2_batch *m, const gpt2_config &cfg, const EngineSrc &src, cu
     const int L = cfg.n_layer, E = cfg.n_embd, H = cfg.n_head, P = cfg.n_positions, V = cfg.vocab_size;
     const int D = E / H, F = 4 * E;
     BTRY(tc_gemm_init());
+    {
+        const void *afn = D == 32 ? reinterpret_cast<const void *>(k_b_attn<32>)
+                          : D == 64 ? reinterpret_cast<const void *>(k_b_attn<64>)
+                                    : reinterpret_cast<const void *>(k_b_attn<128>);
+        BTRY(cudaFuncSetAttribute(afn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(attn_smem(D, P))));
+    }
     m->cfg = cfg;
     m->max_batch = src.rows;
     m->planes = src.planes;

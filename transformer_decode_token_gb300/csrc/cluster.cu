@@ -1460,6 +1460,16 @@ __device__ __forceinline__ void record_token(const ClusterArgs &a, int s, uint32
     }
 }
 
+// How the fc CTAs' MLP-projection partials reach the residual sum: summed
+// over the cluster first (distributed shared memory, then one contribution
+// per fc cluster and word), or, with int4 weights (measured faster there),
+// each fc CTA adding its whole partial vector (one contribution per fc CTA).
+__device__ __forceinline__ bool mlp_direct(const ClusterArgs &a) { return a.wtype == kWI4; }
+__device__ __forceinline__ int mlp_contributions(const ClusterArgs &a)
+{
+    return mlp_direct(a) ? a.nfc : a.nfc / kClusterSize;
+}
+
 // Bulk copies of what a CTA needs besides weights in one layer
 // (L != nullptr) or in the LM head (L == nullptr) into the parameter area
 // c.pr: gamma [E], the fold vectors c1 and cb of its rows [pr_rows each], and
@@ -1492,12 +1502,17 @@ __device__ __forceinline__ void issue_params(const ClusterArgs &a, CS &c, const 
     } else {
         const uint32_t rv = uint32_t(a.fr) * 4u, qv = ev / kClusterSize;
         const size_t r0 = size_t(ro.f) * a.fr;
-        const bool first = ro.f < kClusterSize;   // fc cluster 0 adds x and the bias, a slice per rank
-        mbar_arrive_expect_tx(c.prm_bar, ev + 2u * rv + (first ? qv : 0u));
+        // x and the bias are added once: by fc cluster 0, a slice per rank
+        // (or, adding partials directly, by fc CTA 0, all of them)
+        const bool direct = mlp_direct(a);
+        const bool first = direct ? ro.f == 0 : ro.f < kClusterSize;
+        const uint32_t bv = direct ? ev : qv;
+        mbar_arrive_expect_tx(c.prm_bar, ev + 2u * rv + (first ? bv : 0u));
         bulk_g2s(pg, L->ln2_w, ev, c.prm_bar);
         bulk_g2s(p1, L->f_c1 + r0, rv, c.prm_bar);
         bulk_g2s(pc, L->f_cb + r0, rv, c.prm_bar);
-        if (first) bulk_g2s(pb, L->mlp_proj_b + size_t(ro.r) * (E / kClusterSize), qv, c.prm_bar);
+        if (first)
+            bulk_g2s(pb, L->mlp_proj_b + (direct ? size_t(0) : size_t(ro.r) * (E / kClusterSize)), bv, c.prm_bar);
     }
 }
 
@@ -1549,7 +1564,7 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                     zero_other_parity(a, par);
                     csync();
                 } else {
-                    read_sum(a, c, a.nfc / kClusterSize,
+                    read_sum(a, c, mlp_contributions(a),
                              a.acc_next + (size_t(par) * a.L + (l - 1)) * E * kClusterAccStride, ok);
                 }
                 CTRACE(s, l * 16 + 1);
@@ -1583,7 +1598,8 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                 add_sum(a, an, ro.r * rq, c.outv, ro.h == 0 ? c.x : nullptr, pb, rq);
                 CTRACE(s, l * 16 + 7);
             } else {
-                if (tid == 0) mbar_arrive_expect_tx(pair_bar(c.red_bar, c.uses_red), uint32_t(E) * 4u);   // this layer's partial slices
+                if (tid == 0 && WT != kWI4)   // this layer's partial slices (see mlp_direct)
+                    mbar_arrive_expect_tx(pair_bar(c.red_bar, c.uses_red), uint32_t(E) * 4u);
                 prewait_rows(a, c, G.a, k, kCRing, ok);   // this layer's fc rows, while x_new is on its way
                 read_sum(a, c, a.H, an, ok, l == 0);
                 if (l == 0) zero_other_parity(a, par);
@@ -1599,31 +1615,36 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                 TSET(s, l * 16 + 11);
                 tile_rows<WT, 8, false>(a, c, G.b, k, kCRing, a.fr, c.hloc, c.outv, ok);
                 CTRACE(s, l * 16 + 5);
-                // the cluster's four partial vectors meet first: rank r sums
-                // slice r of all four (in rank order) and adds that once
-                {
-                    const int q = rq / 4;   // float4 per slice
-                    const uint32_t rbar = smem_addr(pair_bar(c.red_bar, c.uses_red));
-                    const float4 *o4 = reinterpret_cast<const float4 *>(c.outv);
-                    for (int t = tid; t < kClusterSize * q; t += kCThreads) {
-                        const int dst = t / q, u = t % q;
-                        const uint32_t slot = smem_addr(c.red + ro.r * rq + u * 4);
-                        st_async_f32x4(mapa(slot, uint32_t(dst)), o4[dst * q + u], mapa(rbar, uint32_t(dst)));
+                if constexpr (WT == kWI4) {   // (mlp_direct)
+                    add_sum(a, a.acc_next + (size_t(par) * a.L + l) * E * kClusterAccStride, 0, c.outv,
+                            ro.f == 0 ? c.x : nullptr, pb, E);
+                } else {
+                    // the cluster's four partial vectors meet first: rank r sums
+                    // slice r of all four (in rank order) and adds that once
+                    {
+                        const int q = rq / 4;   // float4 per slice
+                        const uint32_t rbar = smem_addr(pair_bar(c.red_bar, c.uses_red));
+                        const float4 *o4 = reinterpret_cast<const float4 *>(c.outv);
+                        for (int t = tid; t < kClusterSize * q; t += kCThreads) {
+                            const int dst = t / q, u = t % q;
+                            const uint32_t slot = smem_addr(c.red + ro.r * rq + u * 4);
+                            st_async_f32x4(mapa(slot, uint32_t(dst)), o4[dst * q + u], mapa(rbar, uint32_t(dst)));
+                        }
+                        if (!wait_pair(a, c.red_bar, c.uses_red, 9500 + int(blockIdx.x))) ok = false;
+                        for (int i = tid; i < rq; i += kCThreads)
+                            c.outv[i] = ((c.red[i] + c.red[rq + i]) + c.red[2 * rq + i]) + c.red[3 * rq + i];
+                        csync();
                     }
-                    if (!wait_pair(a, c.red_bar, c.uses_red, 9500 + int(blockIdx.x))) ok = false;
-                    for (int i = tid; i < rq; i += kCThreads)
-                        c.outv[i] = ((c.red[i] + c.red[rq + i]) + c.red[2 * rq + i]) + c.red[3 * rq + i];
-                    csync();
+                    add_sum(a, a.acc_next + (size_t(par) * a.L + l) * E * kClusterAccStride, ro.r * rq, c.outv,
+                            ro.f < kClusterSize ? c.x : nullptr, pb, rq);
                 }
-                add_sum(a, a.acc_next + (size_t(par) * a.L + l) * E * kClusterAccStride, ro.r * rq, c.outv,
-                        ro.f < kClusterSize ? c.x : nullptr, pb, rq);
                 CTRACE(s, l * 16 + 6);
             }
         }
         // LM head (every CTA)
         CTRACE(s, 200);
         issue_params(a, c, ro, G, nullptr);
-        read_sum(a, c, a.nfc / kClusterSize, a.acc_next + (size_t(par) * a.L + (a.L - 1)) * E * kClusterAccStride,
+        read_sum(a, c, mlp_contributions(a), a.acc_next + (size_t(par) * a.L + (a.L - 1)) * E * kClusterAccStride,
                  ok);
         CTRACE(s, 201);
         if (!wait_tx_bar(a, c.prm_bar, c.uses_prm, 9000 + int(blockIdx.x))) ok = false;
