@@ -495,11 +495,15 @@ __device__ void producer(const ClusterArgs &a, const CLayer *layers, const Role 
 {
     uint32_t k = 0;
     bool ok = true;
+    // L2 policies: the LM head and fp32 / fp16 block matrices stream through
+    // (evict first); int4 block matrices (54 MB for GPT-2 small) fit L2 and
+    // are kept there across passes (evict last)
     const uint64_t pol = l2_evict_first_policy();
+    const uint64_t pol_blk = a.wtype == kWI4 ? l2_evict_last_policy() : pol;
     for (int s = 0; s < a.n_steps && ok; ++s) {
         for (int l = 0; l < a.L && ok; ++l) {
-            stream_seg(a, G.a, seg_a(ro, G, layers[l]), ring, full, empty, k, ok, pol);
-            if (ok) stream_seg(a, G.b, seg_b(ro, G, layers[l]), ring, full, empty, k, ok, pol);
+            stream_seg(a, G.a, seg_a(ro, G, layers[l]), ring, full, empty, k, ok, pol_blk);
+            if (ok) stream_seg(a, G.b, seg_b(ro, G, layers[l]), ring, full, empty, k, ok, pol_blk);
         }
         if (ok) stream_seg(a, G.head, seg_head(a, G), ring, full, empty, k, ok, pol);
     }
@@ -1012,10 +1016,13 @@ __device__ __forceinline__ float tile_unit(const RowAddr &ra, uint32_t us, int u
     }
 }
 
-// Tile rows of exactly 64 columns (the head's slice of the output
-// projection) run with the unit loop unrolled.
+// Tile rows run with the unit loop unrolled at their usual widths: 64
+// columns (the head's slice of the output projection) and 32 (an fc CTA's
+// slice of the MLP projection in GPT-2 small); other widths take the loop.
 template <int WT>
 constexpr int kTileUnroll = WT == kWF32 ? 16 : WT == kWF16 ? 8 : 2;
+template <int WT>
+constexpr int kFcTileUnits = WT == kWF32 ? 8 : WT == kWF16 ? 4 : 1;
 
 // Dot products of the tile rows of a segment (cols columns) with vin: one
 // thread per row, which waits for its row's stage; 16-byte units of row r are
@@ -1613,7 +1620,7 @@ __device__ void consumer(const ClusterArgs &a, CS &c, Sh &sh, const Role &ro, co
                 CTRACE(s, l * 16 + 3);
                 CTRACE(s, l * 16 + 4);
                 TSET(s, l * 16 + 11);
-                tile_rows<WT, 8, false>(a, c, G.b, k, kCRing, a.fr, c.hloc, c.outv, ok);
+                tile_rows<WT, kFcTileUnits<WT>, false>(a, c, G.b, k, kCRing, a.fr, c.hloc, c.outv, ok);
                 CTRACE(s, l * 16 + 5);
                 if constexpr (WT == kWI4) {   // (mlp_direct)
                     add_sum(a, a.acc_next + (size_t(par) * a.L + l) * E * kClusterAccStride, 0, c.outv,

@@ -141,6 +141,14 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy()
     return pol;
 }
 
+// L2 policy: keep (evict last).
+__device__ __forceinline__ uint64_t l2_evict_last_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
 // global to this CTA's shared memory, completing on `bar` (tx bytes).
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
