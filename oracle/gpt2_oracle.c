@@ -301,6 +301,8 @@ struct orc_model {
     orc_weights w;
     float *k_cache, *v_cache;     /* [L][H][P][D] each */
     int32_t cached;               /* rows 0..cached-1 of the cache are valid */
+    int32_t kv_bf16;              /* the cache holds k, v rounded to bf16 */
+    uint16_t *kv16;               /* [2E] scratch for that rounding */
     float *x, *norm, *qkv, *attn, *mix, *fc, *act;
 };
 
@@ -331,8 +333,9 @@ orc_model *orc_create(const orc_config *cfg, const orc_weights *w)
     m->mix = (float *)calloc(E, sizeof(float));
     m->fc = (float *)calloc(F, sizeof(float));
     m->act = (float *)calloc(F, sizeof(float));
+    m->kv16 = (uint16_t *)calloc(2 * E, sizeof(uint16_t));
     if (!m->k_cache || !m->v_cache || !m->x || !m->norm || !m->qkv ||
-        !m->attn || !m->mix || !m->fc || !m->act) {
+        !m->attn || !m->mix || !m->fc || !m->act || !m->kv16) {
         orc_destroy(m);
         return NULL;
     }
@@ -344,12 +347,21 @@ void orc_destroy(orc_model *m)
     if (!m) return;
     free(m->k_cache); free(m->v_cache); free(m->x); free(m->norm);
     free(m->qkv); free(m->attn); free(m->mix); free(m->fc); free(m->act);
+    free(m->kv16);
     free(m);
 }
 
 void orc_reset(orc_model *m)
 {
     if (m) m->cached = 0;
+}
+
+/* The batched configuration's KV variant: every k and v row is rounded to
+ * bf16 (round to nearest even) when it enters the cache, and attention reads
+ * the cached values, this position's included.  q stays fp32. */
+void orc_set_kv_bf16(orc_model *m, int32_t on)
+{
+    if (m) m->kv_bf16 = on ? 1 : 0;
 }
 
 /* Copies the cached K and V rows 0..n_rows-1 of one layer, [H][n_rows][D]
@@ -387,6 +399,10 @@ int32_t orc_forward(orc_model *m, int32_t token, int32_t pos, float *logits)
         float *vc = m->v_cache + (size_t)l * H * P * D;
         orc_layernorm(m->x, L->ln1_w, L->ln1_b, E, eps, m->norm);
         orc_linear(m->norm, L->attn_w, L->attn_b, E, 3 * E, m->qkv);
+        if (m->kv_bf16) {   /* k | v as the cache will hold them */
+            orc_f32_to_bf16(m->qkv + E, m->kv16, 2 * (size_t)E);
+            orc_bf16_to_f32(m->kv16, m->qkv + E, 2 * (size_t)E);
+        }
         orc_attn_decode(m->qkv, pos, H, D, P, kc, vc, m->attn);
         orc_linear(m->attn, L->proj_w, L->proj_b, E, E, m->mix);
         for (int32_t e = 0; e < E; ++e) m->x[e] = m->x[e] + m->mix[e];

@@ -98,6 +98,8 @@ void       orc_reset(orc_model *m);
 /* One decode step: token at position pos (pos must be <= cached length).
  * Writes V logits and returns the greedy argmax. Returns -1 on bad input. */
 int32_t    orc_forward(orc_model *m, int32_t token, int32_t pos, float *logits);
+/* Cache k, v rounded to bf16 (RNE) from now on (0: fp32, the default). */
+void       orc_set_kv_bf16(orc_model *m, int32_t on);
 /* The same model evaluated from scratch for a whole sequence with a causal
  * mask and no cache: logits_all is [n][V]. Returns 0, or -1 on bad input. */
 int32_t    orc_forward_full(const orc_config *cfg, const orc_weights *w,

@@ -97,6 +97,8 @@ def lib(omp: bool = False):
             L.orc_create.argtypes = [ctypes.POINTER(_Cfg), ctypes.POINTER(_Weights)]
             L.orc_destroy.argtypes = [vp]
             L.orc_reset.argtypes = [vp]
+            L.orc_set_kv_bf16.restype = None
+            L.orc_set_kv_bf16.argtypes = [vp, c_i32]
             L.orc_forward.restype = c_i32
             L.orc_forward.argtypes = [vp, c_i32, c_i32, vp]
             L.orc_export_kv.restype = c_i32
@@ -384,9 +386,12 @@ class _WeightsHolder:
 
 class OracleModel:
     """Stateful single-sequence decode with a KV cache (omp=True: the
-    multi-core build, for the CPU baseline's timing)."""
+    multi-core build, for the CPU baseline's timing; kv="bf16": the cache
+    holds k and v rounded to bf16, the batched configuration's KV variant)."""
 
-    def __init__(self, cfg, weights: dict, omp: bool = False):
+    def __init__(self, cfg, weights: dict, omp: bool = False, kv: str = "f32"):
+        if kv not in ("f32", "bf16"):
+            raise ValueError(f"unknown KV cache type {kv!r}")
         self.cfg = cfg
         self._lib = lib(omp)
         self._c = _cfg_struct(cfg)
@@ -394,6 +399,7 @@ class OracleModel:
         self._m = self._lib.orc_create(ctypes.byref(self._c), ctypes.byref(self._h.w))
         if not self._m:
             raise ValueError("oracle: invalid config")
+        self._lib.orc_set_kv_bf16(self._m, 1 if kv == "bf16" else 0)
 
     def forward(self, token: int, pos: int):
         logits = np.empty(self.cfg.vocab_size, np.float32)
@@ -438,14 +444,15 @@ def forward_full(cfg, weights: dict, tokens) -> np.ndarray:
 
 
 def greedy(cfg, weights: dict, prompt, n_steps: int, teacher=None, temperature: float = 0.0, seed: int = 0,
-           omp: bool = False):
+           omp: bool = False, kv: str = "f32"):
     """Prefill the prompt one token at a time (positions 0..n-1), then run
     ``n_steps`` decode passes.  Returns (ids, logits): ids[i] is the token
     chosen after pass n-1+i (so ids has n_steps + 1 entries): the greedy
     argmax, or with temperature > 0 the draw of sample(); logits has one row
     per pass (n + n_steps rows).  Decode pass i consumes ids[i], or
-    teacher[i] when ``teacher`` is given (teacher forcing)."""
-    m = OracleModel(cfg, weights, omp=omp)
+    teacher[i] when ``teacher`` is given (teacher forcing).  kv: the cache's
+    element type (OracleModel)."""
+    m = OracleModel(cfg, weights, omp=omp, kv=kv)
     try:
         prompt = [int(t) for t in prompt]
         rows = []

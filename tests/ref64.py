@@ -8,8 +8,11 @@ import torch
 import torch.nn.functional as F
 
 
-def torch_gpt2_logits(cfg, w, tokens):
-    """Float64 GPT-2 forward over a whole sequence, from library routines."""
+def torch_gpt2_logits(cfg, w, tokens, kv_round=None):
+    """Float64 GPT-2 forward over a whole sequence, from library routines.
+    kv_round="bf16": k and v rounded through fp32 to bf16 (torch's own
+    round-to-nearest-even conversion) before the attention, as a bf16 KV
+    cache holds them."""
     d = lambda a: torch.from_numpy(np.asarray(a, np.float32)).double()
     E, H, D = cfg.n_embd, cfg.n_head, cfg.head_dim
     t = torch.as_tensor(np.asarray(tokens, np.int64))
@@ -19,6 +22,8 @@ def torch_gpt2_logits(cfg, w, tokens):
         h = F.layer_norm(x, (E,), d(L["ln1_w"]), d(L["ln1_b"]), eps=cfg.ln_eps)
         qkv = h @ d(L["attn_w"]) + d(L["attn_b"])
         q, k, v = qkv.split(E, dim=-1)
+        if kv_round == "bf16":
+            k, v = (a.float().bfloat16().double() for a in (k, v))
         q, k, v = (a.reshape(n, H, D).transpose(0, 1) for a in (q, k, v))
         a = F.scaled_dot_product_attention(q, k, v, is_causal=True)
         a = a.transpose(0, 1).reshape(n, E)

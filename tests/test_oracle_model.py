@@ -173,3 +173,48 @@ def test_export_kv_layout():
             m2.export_kv(0, 1)                       # nothing cached yet
         finally:
             m2.close()
+
+
+def test_bf16_kv_cache_holds_rounded_rows():
+    """bf16 KV mode: every cached value is a bf16 number (low 16 bits zero),
+    and layer 0's rows are exactly torch's bf16 rounding of the fp32 mode's
+    rows (layer 0 sees the same inputs in both modes)."""
+    import torch
+    cfg = synth.TINY
+    w = synth.make_weights(cfg, seed=0)
+    toks = synth.make_prompt(cfg, 9, seed=3)
+    kv = {}
+    for mode in ("f32", "bf16"):
+        m = orc.OracleModel(cfg, w, kv=mode)
+        try:
+            for p, t in enumerate(toks):
+                m.forward(int(t), p)
+            kv[mode] = [m.export_kv(l, len(toks)) for l in range(cfg.n_layer)]
+        finally:
+            m.close()
+    for l in range(cfg.n_layer):
+        for a in kv["bf16"][l]:
+            assert not np.any(a.view(np.uint32) & 0xFFFF)
+    for a32, a16 in zip(kv["f32"][0], kv["bf16"][0]):
+        rounded = torch.from_numpy(a32).bfloat16().float().numpy()
+        assert np.array_equal(a16.view(np.uint32), rounded.view(np.uint32))
+
+
+@pytest.mark.parametrize("cfg", [synth.TINY, CFG64], ids=["tiny", "d64"])
+def test_bf16_kv_decode_matches_library_float64_forward(cfg):
+    """The bf16 KV mode against the float64 library forward whose k and v are
+    rounded to bf16: far closer to it than to the unrounded forward (the
+    rounding changes the logits by ~1e-3, a pass that skipped it or rounded
+    q instead would sit as far from the rounded reference)."""
+    w = synth.make_weights(cfg, seed=0)
+    toks = synth.make_prompt(cfg, 20, seed=1)
+    ref_r = torch_gpt2_logits(cfg, w, toks, kv_round="bf16")
+    ref_f = torch_gpt2_logits(cfg, w, toks)
+    m = orc.OracleModel(cfg, w, kv="bf16")
+    try:
+        got = np.stack([m.forward(int(t), p)[0] for p, t in enumerate(toks)])
+    finally:
+        m.close()
+    d_r, d_f = np.abs(got - ref_r).max(), np.abs(got - ref_f).max()
+    assert d_r <= 2e-5, d_r
+    assert d_r * 10 <= d_f, (d_r, d_f)
