@@ -17,11 +17,12 @@ int4 block matrices (10-token prompt + 128 steps) and fp16 block matrices
 tok/s and GB/s per 64 positions in "context_sweep"), and the batched
 configuration: 64 independent sequences with bf16 weights on the tensor
 cores, prompts of 32..512 tokens prefilled untimed, then 64 device-fed
-greedy steps of all 64 sequences (aggregate tok/s = 64 x steps / time).
+greedy steps of all 64 sequences (aggregate tok/s = 64 x steps / time),
+with an fp32 and with a bf16 KV cache.
 --wdtype picks one of the other configurations as the headline instead
 (then no variants): f16, int4, or bf16 for the batched one.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--wdtype f32|f16|int4|bf16]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--wdtype f32|f16|int4|bf16] [--kv f32|bf16]
   python bench.py --impl reference ...     # the CPU oracle, same metric
 
 Prints one JSON line on rank 0.  N > 1 runs N independent replicas (one
@@ -68,6 +69,8 @@ def parse(argv=None):
                    help="the headline configuration; bf16 = the batched one (64 sequences, tensor cores)")
     p.add_argument("--head", choices=["f32", "f16", "int4"], default="f32",
                    help="LM head storage: the tied fp32 wte (the configurations), an fp16 copy (README -h) or int4")
+    p.add_argument("--kv", choices=["f32", "bf16"], default="f32",
+                   help="with --wdtype bf16: the KV cache's element type")
     p.add_argument("--no-variants", action="store_true",
                    help="time only the headline workload (not the int4 and fp16 configurations)")
     p.add_argument("--e2e-calls", type=int, default=50)
@@ -214,7 +217,7 @@ def load_traffic(path: str, key: str):
 
 # ---- CPU oracle timing -------------------------------------------------------
 
-def oracle_sample(cfg, weights, prompt, wdtype, budget_s, max_steps=None, head="f32", omp=False):
+def oracle_sample(cfg, weights, prompt, wdtype, budget_s, max_steps=None, head="f32", omp=False, kv="f32"):
     """Decode passes of the oracle after an untimed prefill, at the
     workload's positions; stops after ~budget_s seconds (or max_steps).
     bf16 (the batched configuration): one of its sequences, the given prompt
@@ -226,7 +229,7 @@ def oracle_sample(cfg, weights, prompt, wdtype, budget_s, max_steps=None, head="
     else:
         n_prompt, cycle = WORKLOADS[wdtype]
     sw = orc.stored_weights(weights, wdtype, head=head)
-    m = orc.OracleModel(cfg, sw, omp=omp)
+    m = orc.OracleModel(cfg, sw, omp=omp, kv=kv)
     try:
         tok = None
         for pos, t in enumerate(prompt):
@@ -271,8 +274,9 @@ def run_reference(args):
         config = workload_config(args.wdtype, 1, args.head)
     cores = host_cores()
     os.environ.setdefault("OMP_NUM_THREADS", str(cores))
-    oracle_sample(cfg, w, prompt, args.wdtype, 1e9, max_steps=min(args.warmup, 3), head=args.head, omp=True)
-    n, el = oracle_sample(cfg, w, prompt, args.wdtype, 60.0, max_steps=args.steps, head=args.head, omp=True)
+    kv = args.kv if args.wdtype == "bf16" else "f32"
+    oracle_sample(cfg, w, prompt, args.wdtype, 1e9, max_steps=min(args.warmup, 3), head=args.head, omp=True, kv=kv)
+    n, el = oracle_sample(cfg, w, prompt, args.wdtype, 60.0, max_steps=args.steps, head=args.head, omp=True, kv=kv)
     value = n / el
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / n,
@@ -452,18 +456,19 @@ def measure(torch, cfg, w, wdtype, head, path, steps, warmup, world, local, barr
 
 
 def measure_batch(torch, cfg, w, steps, warmup, world, local, barrier, max_over_ranks, e2e_calls=0,
-                  exact=False):
+                  exact=False, kv="f32"):
     """The batched configuration on a fresh batched model: an untimed prefill
     of the 64 ragged prompts, then 64 device-resident greedy steps timed;
     repeated (each after a fresh prefill) until `steps` steps are timed,
     rounded up to whole cycles unless `exact`.
     With e2e_calls > 0, also that many whole generations through the ABI
-    with host buffers (prompts in, every generated id out), wall clock."""
+    with host buffers (prompts in, every generated id out), wall clock.
+    kv: the cache's element type ("bf16": GPT2_BATCH_KV_BF16)."""
     from transformer_decode_token_gb300 import binding, roofline, synth
     prompts = synth.make_batch_prompts(cfg, BATCH, *BATCH_PROMPT, seed=2)
     lens = [len(q) for q in prompts]
     dw = binding.upload_weights(w)
-    m = binding.BatchModel(cfg, dw, BATCH)
+    m = binding.BatchModel(cfg, dw, BATCH, kv=kv)
     del dw
     torch.cuda.empty_cache()
     try:
@@ -523,7 +528,7 @@ def measure_batch(torch, cfg, w, steps, warmup, world, local, barrier, max_over_
     ms = max_over_ranks(ms)
     n_steps = sum(cycles)
     # bytes and flops of the timed steps: step t of a cycle runs every sequence at lens + t
-    per_t = [roofline.batched_bytes_per_step(cfg, [L + t for L in lens])["total"] for t in range(BATCH_STEPS)]
+    per_t = [roofline.batched_bytes_per_step(cfg, [L + t for L in lens], kv=kv)["total"] for t in range(BATCH_STEPS)]
     alg = sum(sum(per_t[:n]) for n in cycles) / n_steps
     flops = roofline.batched_flops_per_step(cfg, BATCH)
     peaks, peak_kind = measured_peaks()
@@ -531,9 +536,11 @@ def measure_batch(torch, cfg, w, steps, warmup, world, local, barrier, max_over_
     achieved = alg / step_s / 1e9
     out = {
         "value": BATCH * world / step_s, "unit": UNIT, "ms_per_step": ms / n_steps, "steps": n_steps,
-        "gpu_launches": launches, "clocks": clocks, "dtype": "bf16 weights, f32 math (bf16 x bf16 tensor-core "
-                                                                "products of hi/lo activation parts, fp32 sums)",
+        "gpu_launches": launches, "clocks": clocks,
+        "dtype": "bf16 weights" + (", bf16 KV cache" if kv == "bf16" else "") + ", f32 math (bf16 x bf16 "
+                 "tensor-core products of hi/lo activation parts, fp32 sums)",
         "config": {"workload": f"GPT-2 small 124M, batched: {BATCH} sequences, bf16 block weights and head, "
+                               f"{'bf16' if kv == 'bf16' else 'fp32'} KV cache, "
                                f"prompts uniform in [{BATCH_PROMPT[0]}, {BATCH_PROMPT[1]}] tokens (seed 2), "
                                f"{BATCH_STEPS} greedy decode steps per sequence (prefill untimed)",
                    "batch": BATCH, "prompt_tokens": sum(lens), "weights": "synthetic N(0,0.02), seed 0",
@@ -547,8 +554,8 @@ def measure_batch(torch, cfg, w, steps, warmup, world, local, barrier, max_over_
                      "traffic": None, "algorithmic_bytes_per_launch": alg,
                      "tensor_tflops": flops / step_s / 1e12,
                      "tensor_frac": flops / step_s / 1e12 / peaks.get("bf16_tflops", 1900.0),
-                     "note": "bytes: weights once per step + each sequence's KV rows 0..p, embedding and logits "
-                             "rows; flops: 2 x 64 x the linears' and head's multiply-adds (the hi/lo parts "
+                     "note": f"bytes: weights once per step + each sequence's KV rows 0..p ({kv}), embedding and "
+                             "logits rows; flops: 2 x 64 x the linears' and head's multiply-adds (the hi/lo parts "
                              "double the tensor work actually issued)"},
     }
     if e2e is not None:
@@ -596,7 +603,7 @@ def batch_main(args, torch, dist, cfg, w, rank, world, local, barrier, max_over_
     (exactly --steps timed steps)."""
     from transformer_decode_token_gb300 import synth
     b = measure_batch(torch, cfg, w, args.steps, args.warmup, world, local, barrier, max_over_ranks,
-                      e2e_calls=max(1, min(args.e2e_calls, 5)), exact=True)
+                      e2e_calls=max(1, min(args.e2e_calls, 5)), exact=True, kv=args.kv)
     line = {"metric": METRIC, "value": b["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": b["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": b["dtype"], "data": "synthetic",
@@ -607,7 +614,7 @@ def batch_main(args, torch, dist, cfg, w, rank, world, local, barrier, max_over_
         prompt = min(prompts, key=len)
         cores = host_cores()
         os.environ.setdefault("OMP_NUM_THREADS", str(cores))
-        n, el = oracle_sample(cfg, w, prompt, "bf16", args.cpu_seconds, omp=True)
+        n, el = oracle_sample(cfg, w, prompt, "bf16", args.cpu_seconds, omp=True, kv=args.kv)
         line["cpu_baseline"] = {
             "value": n / el, "unit": UNIT, "cores": int(os.environ["OMP_NUM_THREADS"]), "kind": "oracle",
             "sample": f"{n} greedy decode passes of the batched workload's shortest sequence ({len(prompt)}-token "
@@ -672,8 +679,9 @@ def main():
             v["dtype"] = f"{wd} weights, f32 math"
             variants[wd] = v
         # (at most 10 cycles: each cycle re-runs the untimed prefill of all 64 prompts)
-        variants["batch64_bf16"] = measure_batch(torch, cfg, w, min(args.steps, 10 * BATCH_STEPS), args.warmup,
-                                                 world, local, barrier, max_over_ranks)
+        for name, kv in (("batch64_bf16", "f32"), ("batch64_bf16_kvbf16", "bf16")):
+            variants[name] = measure_batch(torch, cfg, w, min(args.steps, 10 * BATCH_STEPS), args.warmup, world,
+                                           local, barrier, max_over_ranks, kv=kv)
         line["variants"] = variants
         line["prefill"] = measure_prefill(torch, cfg, w)
 

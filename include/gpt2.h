@@ -357,7 +357,7 @@ int gpt2_op_head_argmax_noalloc(const float *x, const float *ln_w, const float *
  *   - Weights: GPT2_BF16 only.  The 48 block matrices are stored as bf16
  *     [out][in] (round to nearest even) and the tied head as a bf16 copy of
  *     wte; embeddings, biases, LayerNorm parameters and the KV cache stay
- *     fp32.  Activations enter each product as two bf16 parts (x = hi + lo,
+ *     fp32 (the cache: bf16 with GPT2_BATCH_KV_BF16).  Activations enter each product as two bf16 parts (x = hi + lo,
  *     lo = bf16(x - hi)), so products use about 16 bits of x; sums are fp32.
  *   - Cache: [n_layer][max_batch][n_head][n_positions][head_dim] fp32, one
  *     slot per sequence; sequences have independent lengths (ragged).
@@ -371,6 +371,16 @@ typedef struct gpt2_batch gpt2_batch;
  * head_dim in {32, 64, 128}), UNSUPPORTED_DEVICE, OUT_OF_MEMORY, CUDA. */
 int gpt2_create_batch(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
                       int32_t max_batch, void *stream, gpt2_batch **out);
+/* GPT2_BATCH_KV_BF16: the cache holds k and v rounded to bf16 (round to
+ * nearest even) when they are written, [n_layer][max_batch][n_head]
+ * [n_positions][head_dim] bf16; attention reads the cached values, the
+ * current position's included (q, the scores and the softmax stay fp32).
+ * Halves the cache's memory and the bytes a step reads from it. */
+#define GPT2_BATCH_KV_BF16 1u
+/* gpt2_create_batch with options: flags is 0 or GPT2_BATCH_KV_BF16 (other
+ * bits: INVALID_ARG). */
+int gpt2_create_batch_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
+                         int32_t max_batch, uint32_t flags, void *stream, gpt2_batch **out);
 void gpt2_destroy_batch(gpt2_batch *m);
 
 /* One step: sequence b (b < n) consumes host tokens[b] at host positions[b]
@@ -407,7 +417,8 @@ int gpt2_batch_ids(gpt2_batch *m, int32_t first_pos, int32_t n_pos, int32_t *hos
 int gpt2_copy_logits_batch(gpt2_batch *m, int32_t n, float *dst);
 
 /* Copies the cached K and V rows 0..n_rows-1 of one layer and sequence,
- * [n_head][n_rows][head_dim] fp32 each, to host or device memory. */
+ * [n_head][n_rows][head_dim] fp32 each (a bf16 cache widened exactly), to
+ * host or device memory; synchronises. */
 int gpt2_export_kv_batch(gpt2_batch *m, int32_t layer, int32_t seq, int32_t n_rows,
                          float *dst_k, float *dst_v);
 

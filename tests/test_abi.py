@@ -88,3 +88,7 @@ def test_new_options_are_rejected_on_the_host():
     assert L.gpt2_set_wait_limit(None, 0) == -1
     # the flag that once selected a third path is no longer accepted
     assert L.gpt2_create_ex(ctypes.byref(good), ctypes.byref(w), 0, 2, None, ctypes.byref(out)) == -1
+    # batched models: unknown option bits, NULL arguments
+    assert L.gpt2_create_batch_ex(ctypes.byref(good), ctypes.byref(w), 3, 4, 2, None, ctypes.byref(out)) == -1
+    assert L.gpt2_create_batch_ex(None, None, 3, 4, 1, None, ctypes.byref(out)) == -1
+    assert L.gpt2_create_batch_ex(ctypes.byref(good), ctypes.byref(w), 3, 4, 1, None, None) == -1

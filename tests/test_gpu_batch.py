@@ -7,7 +7,9 @@ a bf16 copy of wte (the embedding still reads the fp32 wte).  Activations
 enter each tensor-core product as bf16 hi + lo parts (about 16 bits), sums
 are fp32, so the stored-weight tolerance applies: logits within 2e-3 abs,
 ids wherever the oracle's top-2 margin exceeds 1e-3.  The oracle's chosen
-ids are fed to both sides (teacher forcing).
+ids are fed to both sides (teacher forcing).  With the bf16 KV cache
+(GPT2_BATCH_KV_BF16) the oracle runs its bf16 KV mode: k and v rounded to
+bf16 as the cache stores them.
 """
 import numpy as np
 import pytest
@@ -54,7 +56,7 @@ def oracle_weights(w):
     return orc.stored_weights(w, "bf16", head="bf16")
 
 
-def run_batch(cfg, prompts, n_steps, check_seqs):
+def run_batch(cfg, prompts, n_steps, check_seqs, kv="f32"):
     """Prefill the ragged prompts, then n_steps teacher-forced steps (every
     sequence fed the oracle's greedy ids); compares the logits of the
     sequences in check_seqs with the oracle at every step."""
@@ -63,8 +65,8 @@ def run_batch(cfg, prompts, n_steps, check_seqs):
     B = len(prompts)
     ref = {}
     for b in check_seqs:
-        ref[b] = orc.greedy(cfg, sw, prompts[b], n_steps, omp=True)
-    m = binding.BatchModel(cfg, binding.upload_weights(w), B)
+        ref[b] = orc.greedy(cfg, sw, prompts[b], n_steps, omp=True, kv=kv)
+    m = binding.BatchModel(cfg, binding.upload_weights(w), B, kv=kv)
     try:
         m.prefill(prompts)
         first = m.argmax(B)
@@ -93,12 +95,13 @@ def run_batch(cfg, prompts, n_steps, check_seqs):
         raise
 
 
-def test_tiny_batch_ragged():
+@pytest.mark.parametrize("kv", ["f32", "bf16"])
+def test_tiny_batch_ragged(kv):
     """Tiny model, 13 sequences with prompts of 3..20 tokens, 10 steps; every
     sequence checked."""
     cfg = synth.TINY
     prompts = synth.make_batch_prompts(cfg, 13, 3, 20, seed=2)
-    m, _ = run_batch(cfg, prompts, 10, list(range(13)))
+    m, _ = run_batch(cfg, prompts, 10, list(range(13)), kv=kv)
     m.close()
 
 
@@ -127,7 +130,8 @@ def test_tiny_batch_full_and_kv_cache():
         m.close()
 
 
-def test_tiny_batch_long_contexts_span_attention_chunks():
+@pytest.mark.parametrize("kv", ["f32", "bf16"])
+def test_tiny_batch_long_contexts_span_attention_chunks(kv):
     """Tiny model with 256 positions: prompts of 40..230 tokens, so a
     sequence's attention covers up to four chunks of 64 positions (each
     chunk's softmax merged with the others'), 12 steps across chunk
@@ -137,19 +141,48 @@ def test_tiny_batch_long_contexts_span_attention_chunks():
     prompts = synth.make_batch_prompts(cfg, 9, 40, 230, seed=4)
     prompts[0] = prompts[0][:60]    # crosses the 64-position boundary during the steps
     prompts[1] = prompts[1][:128]   # starts exactly on a boundary
-    m, _ = run_batch(cfg, prompts, 12, list(range(9)))
+    m, _ = run_batch(cfg, prompts, 12, list(range(9)), kv=kv)
     m.close()
 
 
-def test_small_batch_of_64_ragged_prompts():
+@pytest.mark.parametrize("kv", ["f32", "bf16"])
+def test_small_batch_of_64_ragged_prompts(kv):
     """GPT-2 small, 64 sequences with prompts of 32..512 tokens (the batched
     workload's shape), 3 teacher-forced steps; the oracle checks the three
     sequences with the shortest prompts (it runs each whole prompt)."""
     cfg = synth.SMALL
     prompts = synth.make_batch_prompts(cfg, 64, 32, 512, seed=2)
     order = np.argsort([len(q) for q in prompts])
-    m, _ = run_batch(cfg, prompts, 3, [int(i) for i in order[:3]])
+    m, _ = run_batch(cfg, prompts, 3, [int(i) for i in order[:3]], kv=kv)
     m.close()
+
+
+def test_bf16_kv_cache_rows():
+    """With the bf16 cache every stored k, v is a bf16 number, within one
+    bf16 rounding of the oracle's bf16 KV mode: the two round fp32 values
+    computed in different orders (and from hi + lo activation parts), which
+    differ by up to a few 1e-6, so values near zero may land a few bf16 steps
+    apart (the 1e-5 absolute term); a row of another sequence or position
+    would be off by O(0.1)."""
+    cfg = synth.TINY
+    prompts = synth.make_batch_prompts(cfg, 6, 5, 30, seed=7)
+    m, _ = run_batch(cfg, prompts, 4, [2], kv="bf16")
+    try:
+        w = synth.make_weights(cfg, 0)
+        om = orc.OracleModel(cfg, oracle_weights(w), kv="bf16")
+        try:
+            for p, t in enumerate(prompts[2]):
+                om.forward(int(t), p)
+            for layer in range(cfg.n_layer):
+                rk, rv = om.export_kv(layer, len(prompts[2]))
+                k, v = m.export_kv(layer, 2, len(prompts[2]))
+                for got, ref in ((k, rk), (v, rv)):
+                    assert not np.any(got.view(np.uint32) & 0xFFFF)
+                    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -7 + 1e-5)
+        finally:
+            om.close()
+    finally:
+        m.close()
 
 
 def test_batch_greedy_matches_host_fed_steps():

@@ -85,3 +85,8 @@ def test_batched_step_bytes():
     assert many["kv"] == sum(roofline.bytes_per_token(cfg, "f32", p)["kv"] for p in pos)
     assert many["logits"] == 3 * cfg.vocab_size * 4
     assert roofline.batched_flops_per_step(cfg, 64) == 2 * 64 * roofline.macs_per_token(cfg)
+    # a bf16 cache: the pages' fp32 KV bytes (the 75.5 MB cache at 1024 rows) halved, the rest unchanged
+    half = roofline.batched_bytes_per_step(cfg, pos, kv="bf16")
+    assert 2 * half["kv"] == many["kv"]
+    assert all(half[k] == many[k] for k in ("block_matrices", "head", "biases_ln", "embedding_rows", "logits"))
+    assert roofline.batched_bytes_per_step(cfg, [1022], kv="bf16")["kv"] * 2 == 12 * 2 * 768 * 4 * 1024

@@ -28,7 +28,7 @@ EXPORTED = ("gpt2_create", "gpt2_create_ex", "gpt2_path", "gpt2_launch_count", "
             "gpt2_matrix_bytes", "gpt2_export_matrix", "gpt2_export_dequant", "gpt2_export_kv",
             "gpt2_kernels_per_step", "gpt2_op_layernorm", "gpt2_op_head_argmax_workspace",
             "gpt2_op_head_argmax", "gpt2_op_head_argmax_noalloc", "gpt2_set_sampling", "gpt2_set_wait_limit",
-            "gpt2_create_batch", "gpt2_destroy_batch", "gpt2_decode_batch", "gpt2_prefill_batch",
+            "gpt2_create_batch", "gpt2_create_batch_ex", "gpt2_destroy_batch", "gpt2_decode_batch", "gpt2_prefill_batch",
             "gpt2_decode_batch_greedy", "gpt2_argmax_batch", "gpt2_batch_ids", "gpt2_copy_logits_batch",
             "gpt2_export_kv_batch", "gpt2_batch_info", "gpt2_sync_batch", "gpt2_op_linear_bf16_workspace",
             "gpt2_op_linear_bf16", "gpt2_strerror")
@@ -121,6 +121,8 @@ def lib(build_if_stale: bool = True, path: str = None):
             L.gpt2_set_wait_limit.argtypes = [vp, ctypes.c_uint64]
             L.gpt2_create_batch.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), i32, i32, vp,
                                             ctypes.POINTER(vp)]
+            L.gpt2_create_batch_ex.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), i32, i32,
+                                               ctypes.c_uint32, vp, ctypes.POINTER(vp)]
             L.gpt2_destroy_batch.argtypes = [vp]
             L.gpt2_destroy_batch.restype = None
             L.gpt2_decode_batch.argtypes = [vp, pi32, pi32, i32, ctypes.POINTER(vp)]
@@ -355,11 +357,18 @@ def _i32(a):
     return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
 
 
+BATCH_KV_BF16 = 1
+
+
 class BatchModel:
     """Up to max_batch independent sequences decoded together (bf16 weights,
-    tensor-core linears); see gpt2_create_batch in include/gpt2.h."""
+    tensor-core linears); see gpt2_create_batch in include/gpt2.h.  kv:
+    the cache's element type, "f32" or "bf16" (GPT2_BATCH_KV_BF16)."""
 
-    def __init__(self, cfg, dev_weights: dict, max_batch: int, wdtype: str = "bf16", stream=None):
+    def __init__(self, cfg, dev_weights: dict, max_batch: int, wdtype: str = "bf16", stream=None,
+                 kv: str = "f32"):
+        if kv not in ("f32", "bf16"):
+            raise ValueError(f"unknown KV cache type {kv!r}")
         L = lib()
         self.cfg = cfg
         self.max_batch = max_batch
@@ -372,8 +381,10 @@ class BatchModel:
                     dev_weights["ln_f_w"].data_ptr(), dev_weights["ln_f_b"].data_ptr(),
                     ctypes.cast(layers, ctypes.POINTER(LayerWeights)))
         h = ctypes.c_void_p()
-        check(L.gpt2_create_batch(ctypes.byref(c), ctypes.byref(w), WDTYPES[wdtype], int(max_batch),
-                                  _stream_handle(stream), ctypes.byref(h)), "gpt2_create_batch")
+        check(L.gpt2_create_batch_ex(ctypes.byref(c), ctypes.byref(w), WDTYPES[wdtype], int(max_batch),
+                                     BATCH_KV_BF16 if kv == "bf16" else 0, _stream_handle(stream), ctypes.byref(h)),
+              "gpt2_create_batch_ex")
+        self.kv = kv
         self._h = h
 
     def decode(self, tokens, positions) -> int:

@@ -154,7 +154,7 @@ struct BAttnArgs {
     const float *parts;             // [splits][rows][3E] QKV shares
     int32_t splits;
     const float *bias;              // [3E]
-    float *kc, *vc;                 // this layer's cache: [slots][H][P][D]
+    void *kc, *vc;                  // this layer's cache: [slots][H][P][D], fp32 or bf16
     const int32_t *pos;             // [rows]; -1: inactive
     int32_t E, H, P, rows, slots;
     int32_t append;                 // 1: this row's k, v are written at pos here
@@ -163,13 +163,34 @@ struct BAttnArgs {
     DeviceState *st;
 };
 
-constexpr int kAttnRows = 32;       // cache rows per stage
+constexpr int kAttnStageB = 8192;   // bytes per stage (32 fp32 or 64 bf16 rows of 64 dimensions)
 constexpr int kAttnStages = 3;
 
-// Dynamic shared memory of k_b_attn: the stages, then the scores [P].
-__host__ __device__ constexpr size_t attn_smem(int D, int P)
+// Dynamic shared memory of k_b_attn: the stages, then the scores [P];
+// es = bytes per cache element.
+__host__ __device__ constexpr size_t attn_smem(int D, int P, int es)
 {
-    return size_t(kAttnStages) * kAttnRows * D * 4 + size_t(P) * 4;
+    return size_t(kAttnStages) * kAttnStageB + size_t(P) * 4;
+}
+
+// A cache element from fp32, and 4 consecutive cache elements as fp32.
+__device__ __forceinline__ void kv_put(float *p, float v) { *p = v; }
+__device__ __forceinline__ void kv_put(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
+__device__ __forceinline__ float kv_round(float v, const float *) { return v; }
+__device__ __forceinline__ float kv_round(float v, const __nv_bfloat16 *)
+{
+    return __bfloat162float(__float2bfloat16_rn(v));
+}
+__device__ __forceinline__ float4 kv_load4(const float *row, int l)
+{
+    return reinterpret_cast<const float4 *>(row)[l];
+}
+__device__ __forceinline__ float4 kv_load4(const __nv_bfloat16 *row, int l)
+{
+    const uint2 u = reinterpret_cast<const uint2 *>(row)[l];
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
 }
 
 // One CTA per (row, head).  The row's cached K rows, then its V rows, stream
@@ -180,16 +201,19 @@ __host__ __device__ constexpr size_t attn_smem(int D, int P)
 // positions 0..pos (max subtracted); the weighted sum of v with the same
 // thread layout, the row groups' partial sums combined in a fixed order.
 // When this kernel appends (decode), row pos is this token's k, v (from the
-// shares, kept in shared memory) and the cache supplies rows 0..pos-1.
-template <int D>
+// shares, kept in shared memory as the cache holds them) and the cache
+// supplies rows 0..pos-1.  KT: the cache's element type (fp32, or bf16 with
+// k and v rounded to nearest even when written).
+template <int D, typename KT>
 __global__ void __launch_bounds__(kBT) k_b_attn(const BAttnArgs a)
 {
     constexpr int LPR = D / 4;               // threads per row
     constexpr int RPP = kBT / LPR;           // rows per pass
+    constexpr uint32_t kRowB = D * sizeof(KT), kStageB = kAttnStageB;
+    constexpr int kAttnRows = kStageB / kRowB;          // cache rows per stage
     constexpr int NPS = kAttnRows / RPP;     // passes per stage
-    constexpr uint32_t kRowB = D * 4, kStageB = kAttnRows * kRowB;
-    static_assert(kAttnRows % RPP == 0 && LPR <= 32, "thread layout");
-    extern __shared__ __align__(128) uint8_t dyn[];   // [stages][kAttnRows][D], then scores [P]
+    static_assert(kAttnRows % RPP == 0 && kAttnRows * kRowB == kStageB && LPR <= 32, "thread layout");
+    extern __shared__ __align__(128) uint8_t dyn[];   // [stages][kAttnRows][D] KT, then scores [P] fp32
     float *sc = reinterpret_cast<float *>(dyn + size_t(kAttnStages) * kStageB);
     __shared__ __align__(8) uint64_t full[kAttnStages];
     __shared__ float red[kBT / 32];
@@ -210,8 +234,8 @@ __global__ void __launch_bounds__(kBT) k_b_attn(const BAttnArgs a)
         return;
     }
     const int slot = a.slots == 1 ? 0 : b;
-    float *kh = a.kc + (size_t(slot) * a.H + h) * a.P * D;
-    float *vh = a.vc + (size_t(slot) * a.H + h) * a.P * D;
+    KT *kh = static_cast<KT *>(a.kc) + (size_t(slot) * a.H + h) * a.P * D;
+    KT *vh = static_cast<KT *>(a.vc) + (size_t(slot) * a.H + h) * a.P * D;
     const int n = pos + 1;
     const int nk = a.append ? pos : n;                    // rows read from the cache
     const int m = (nk + kAttnRows - 1) / kAttnRows;        // stages of K, then as many of V
@@ -239,9 +263,9 @@ __global__ void __launch_bounds__(kBT) k_b_attn(const BAttnArgs a)
         const int part_ = t / D, d = t % D;
         const int j = part_ * E + h * D + d;
         const float v = sum_shares(a.parts, a.splits, a.rows, 3 * E, b, j) + a.bias[j];
-        qkv[t] = v;
-        if (part_ == 1) kh[size_t(pos) * D + d] = v;
-        if (part_ == 2) vh[size_t(pos) * D + d] = v;
+        qkv[t] = part_ == 0 ? v : kv_round(v, kh);
+        if (part_ == 1) kv_put(kh + size_t(pos) * D + d, v);
+        if (part_ == 2) kv_put(vh + size_t(pos) * D + d, v);
     }
     __syncthreads();
     const float4 q4 = reinterpret_cast<const float4 *>(qkv)[l];
@@ -253,11 +277,11 @@ __global__ void __launch_bounds__(kBT) k_b_attn(const BAttnArgs a)
     };
     for (int c = 0; c < m; ++c) {
         wait_chunk(c);
-        const float *stg = reinterpret_cast<const float *>(dyn + size_t(c % kAttnStages) * kStageB);
+        const KT *stg = reinterpret_cast<const KT *>(dyn + size_t(c % kAttnStages) * kStageB);
 #pragma unroll
         for (int u = 0; u < NPS; ++u) {
             const int r = u * RPP + g, j = c * kAttnRows + r;
-            const float d = dot_row(reinterpret_cast<const float4 *>(stg + r * D)[l]);
+            const float d = dot_row(kv_load4(stg + r * D, l));
             if (l == 0 && j < nk) sc[j] = d * a.scale;
         }
         __syncthreads();   // the stage is free again
@@ -282,13 +306,13 @@ __global__ void __launch_bounds__(kBT) k_b_attn(const BAttnArgs a)
     for (int c = 0; c < m; ++c) {
         const int q = m + c;
         wait_chunk(q);
-        const float *stg = reinterpret_cast<const float *>(dyn + size_t(q % kAttnStages) * kStageB);
+        const KT *stg = reinterpret_cast<const KT *>(dyn + size_t(q % kAttnStages) * kStageB);
 #pragma unroll
         for (int u = 0; u < NPS; ++u) {
             const int r = u * RPP + g, j = c * kAttnRows + r;
             if (j < nk) {
                 const float p = sc[j];
-                const float4 v4 = reinterpret_cast<const float4 *>(stg + r * D)[l];
+                const float4 v4 = kv_load4(stg + r * D, l);
                 acc.x = fmaf(p, v4.x, acc.x);
                 acc.y = fmaf(p, v4.y, acc.y);
                 acc.z = fmaf(p, v4.z, acc.z);
@@ -345,7 +369,7 @@ __global__ void __launch_bounds__(kBT) k_b_append(const BAttnArgs a, int D)
         for (int t = blockIdx.y * kBT + threadIdx.x; t < 2 * E; t += gridDim.y * kBT) {
             const int part_ = 1 + t / E, hd = t % E, h = hd / D, d = hd % D, j = part_ * E + hd;
             const float v = sum_shares(a.parts, a.splits, a.rows, 3 * E, b, j) + a.bias[j];
-            (part_ == 1 ? a.kc : a.vc)[((size_t(slot) * a.H + h) * a.P + pos) * D + d] = v;
+            static_cast<float *>(part_ == 1 ? a.kc : a.vc)[((size_t(slot) * a.H + h) * a.P + pos) * D + d] = v;
         }
     }
     pdl_launch_dependents();
@@ -472,7 +496,8 @@ struct gpt2_batch {
     void *head = nullptr;           // bf16 planes of the head [planes][Vp][E] (rows V..Vp zero)
     Linear head_lin{};
     // work
-    float *kc = nullptr, *vc = nullptr;                   // [L][slots][H][P][D]
+    void *kc = nullptr, *vc = nullptr;                    // [L][slots][H][P][D] fp32, or bf16 (kv_bf16)
+    bool kv_bf16 = false;
     float *x = nullptr;                                   // [64][E]
     __nv_bfloat16 *b_e = nullptr, *b_a = nullptr, *b_f = nullptr;   // [128][E], [128][E], [128][F]
     CUtensorMap map_e{}, map_a{}, map_f{};
@@ -532,6 +557,17 @@ cudaError_t run_linear(const gpt2_batch *m, const Linear &L, const CUtensorMap &
     return tc_gemm_launch(L.a_map, b_map, a, L.splits, s, pdl);
 }
 
+const void *attn_kernel(int D, bool bf16)
+{
+    if (bf16)
+        return D == 32 ? reinterpret_cast<const void *>(k_b_attn<32, __nv_bfloat16>)
+               : D == 64 ? reinterpret_cast<const void *>(k_b_attn<64, __nv_bfloat16>)
+                         : reinterpret_cast<const void *>(k_b_attn<128, __nv_bfloat16>);
+    return D == 32 ? reinterpret_cast<const void *>(k_b_attn<32, float>)
+           : D == 64 ? reinterpret_cast<const void *>(k_b_attn<64, float>)
+                     : reinterpret_cast<const void *>(k_b_attn<128, float>);
+}
+
 // Records one batched step on stream s (under capture).
 int record_step(gpt2_batch *m, cudaStream_t s)
 {
@@ -578,8 +614,9 @@ int record_step(gpt2_batch *m, cudaStream_t s)
         at.parts = m->p_qkv;
         at.splits = Ly.lin[0].splits;
         at.bias = Ly.attn_b;
-        at.kc = m->kc + size_t(l) * slots * H * P * D;
-        at.vc = m->vc + size_t(l) * slots * H * P * D;
+        const size_t layer_bytes = size_t(slots) * H * P * D * (m->kv_bf16 ? 2 : 4);
+        at.kc = static_cast<uint8_t *>(m->kc) + size_t(l) * layer_bytes;
+        at.vc = static_cast<uint8_t *>(m->vc) + size_t(l) * layer_bytes;
         at.pos = m->pos;
         at.E = E;
         at.H = H;
@@ -597,10 +634,8 @@ int record_step(gpt2_batch *m, cudaStream_t s)
             ++kernels;
         }
         void *a2[] = {&at};
-        const void *afn = D == 32 ? reinterpret_cast<const void *>(k_b_attn<32>)
-                          : D == 64 ? reinterpret_cast<const void *>(k_b_attn<64>)
-                                    : reinterpret_cast<const void *>(k_b_attn<128>);
-        BTRY(launch_pdl(afn, dim3(R, H), dim3(kBT), attn_smem(D, P), s, pdl(), a2));
+        BTRY(launch_pdl(attn_kernel(D, m->kv_bf16), dim3(R, H), dim3(kBT), attn_smem(D, P, m->kv_bf16 ? 2 : 4), s,
+                        pdl(), a2));
         BTRY(run_linear(m, Ly.lin[1], m->map_a, m->p_o, s, pdl()));
         ln.mode = 1;
         ln.parts = m->p_o;
@@ -730,7 +765,8 @@ struct EngineSrc {
     std::vector<Layer> layers;
     bool hf = true;
     bool borrow = false;
-    float *kc = nullptr, *vc = nullptr;
+    float *kc = nullptr, *vc = nullptr;   // an fp32 cache of the caller's
+    bool kv_bf16 = false;                 // an own cache of bf16 k, v (RNE)
     int planes = 1, slots = 1, rows = kTcMaxRows;
     // in place of w[] / head: write the fp32 [out][in] matrix (or the [V][E]
     // head) into dst
@@ -744,16 +780,16 @@ int engine_build(gpt2_batch *m, const gpt2_config &cfg, const EngineSrc &src, cu
     const int D = E / H, F = 4 * E;
     BTRY(tc_gemm_init());
     {
-        const void *afn = D == 32 ? reinterpret_cast<const void *>(k_b_attn<32>)
-                          : D == 64 ? reinterpret_cast<const void *>(k_b_attn<64>)
-                                    : reinterpret_cast<const void *>(k_b_attn<128>);
-        BTRY(cudaFuncSetAttribute(afn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(attn_smem(D, P))));
+        const bool kb = src.kv_bf16 && src.kc == nullptr;
+        BTRY(cudaFuncSetAttribute(attn_kernel(D, kb), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  int(attn_smem(D, P, kb ? 2 : 4))));
     }
     m->cfg = cfg;
     m->max_batch = src.rows;
     m->planes = src.planes;
     m->slots = src.slots;
     m->own_cache = src.kc == nullptr;
+    m->kv_bf16 = src.kv_bf16 && m->own_cache;
     m->stream = stream;
     m->num_sms = sms;
     m->cached.assign(src.rows, 0);
@@ -785,7 +821,7 @@ int engine_build(gpt2_batch *m, const gpt2_config &cfg, const EngineSrc &src, cu
     const size_t arena_bytes = off;
     // ---- work ----
     off = 0;
-    const size_t kv = m->own_cache ? size_t(L) * src.slots * H * P * D * 4 : 0;
+    const size_t kv = m->own_cache ? size_t(L) * src.slots * H * P * D * (m->kv_bf16 ? 2 : 4) : 0;
     const size_t o_k = m->own_cache ? take(kv) : 0, o_v = m->own_cache ? take(kv) : 0;
     const size_t o_x = take(size_t(kTcMaxRows) * E * 4);
     const size_t o_be = take(size_t(2 * kTcMaxRows) * E * 2), o_ba = take(size_t(2 * kTcMaxRows) * E * 2);
@@ -880,8 +916,8 @@ int engine_build(gpt2_batch *m, const gpt2_config &cfg, const EngineSrc &src, cu
     if (rc != GPT2_OK) goto done;
     m->head_lin.splits = 1;                       // whole logits from one pass over K
     m->head_lin.cps = E / kTcK;
-    m->kc = m->own_cache ? reinterpret_cast<float *>(W + o_k) : src.kc;
-    m->vc = m->own_cache ? reinterpret_cast<float *>(W + o_v) : src.vc;
+    m->kc = m->own_cache ? static_cast<void *>(W + o_k) : static_cast<void *>(src.kc);
+    m->vc = m->own_cache ? static_cast<void *>(W + o_v) : static_cast<void *>(src.vc);
     m->x = reinterpret_cast<float *>(W + o_x);
     m->b_e = reinterpret_cast<__nv_bfloat16 *>(W + o_be);
     m->b_a = reinterpret_cast<__nv_bfloat16 *>(W + o_ba);
@@ -1016,8 +1052,15 @@ extern "C" {
 int gpt2_create_batch(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype, int32_t max_batch, void *stream,
                       gpt2_batch **out)
 {
+    return gpt2_create_batch_ex(cfg, w, wdtype, max_batch, 0u, stream, out);
+}
+
+int gpt2_create_batch_ex(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype, int32_t max_batch,
+                         uint32_t flags, void *stream, gpt2_batch **out)
+{
     if (!out) return GPT2_ERR_INVALID_ARG;
     *out = nullptr;
+    if (flags & ~uint32_t(GPT2_BATCH_KV_BF16)) return GPT2_ERR_INVALID_ARG;
     if (!cfg || !w || !w->layers) return GPT2_ERR_INVALID_ARG;
     if (wdtype != GPT2_BF16) return GPT2_ERR_INVALID_ARG;
     if (max_batch < 1 || max_batch > kTcMaxRows) return GPT2_ERR_INVALID_ARG;
@@ -1056,6 +1099,7 @@ int gpt2_create_batch(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdt
     src.planes = 1;
     src.slots = max_batch;
     src.rows = max_batch;
+    src.kv_bf16 = (flags & GPT2_BATCH_KV_BF16) != 0;
     gpt2_batch *m = new (std::nothrow) gpt2_batch();
     if (!m) return GPT2_ERR_OUT_OF_MEMORY;
     rc = engine_build(m, *cfg, src, static_cast<cudaStream_t>(stream), prop.multiProcessorCount);
@@ -1182,11 +1226,29 @@ int gpt2_export_kv_batch(gpt2_batch *m, int32_t layer, int32_t seq, int32_t n_ro
     if (!m || layer < 0 || layer >= m->cfg.n_layer || seq < 0 || seq >= m->max_batch) return GPT2_ERR_INVALID_ARG;
     const int H = m->cfg.n_head, D = m->cfg.n_embd / H, P = m->cfg.n_positions;
     if (n_rows < 0 || n_rows > P) return GPT2_ERR_INVALID_ARG;
+    const size_t es = m->kv_bf16 ? 2 : 4, row_elems = size_t(n_rows) * D;
+    // bf16 rows are widened to fp32 on the host on their way out
+    std::vector<uint16_t> tmp16(m->kv_bf16 ? row_elems : 0);
+    std::vector<float> tmp32(m->kv_bf16 ? row_elems : 0);
     for (int h = 0; h < H; ++h) {
-        const size_t src = ((size_t(layer) * m->max_batch + seq) * H + h) * P * D;
-        const size_t bytes = size_t(n_rows) * D * 4;
-        if (dst_k) BTRY(cudaMemcpyAsync(dst_k + size_t(h) * n_rows * D, m->kc + src, bytes, cudaMemcpyDefault, m->stream));
-        if (dst_v) BTRY(cudaMemcpyAsync(dst_v + size_t(h) * n_rows * D, m->vc + src, bytes, cudaMemcpyDefault, m->stream));
+        const size_t src = ((size_t(layer) * m->max_batch + seq) * H + h) * P * D * es;
+        for (int part = 0; part < 2; ++part) {
+            float *dst = part == 0 ? dst_k : dst_v;
+            if (!dst) continue;
+            const uint8_t *from = static_cast<const uint8_t *>(part == 0 ? m->kc : m->vc) + src;
+            dst += size_t(h) * row_elems;
+            if (!m->kv_bf16) {
+                BTRY(cudaMemcpyAsync(dst, from, row_elems * 4, cudaMemcpyDefault, m->stream));
+                continue;
+            }
+            BTRY(cudaMemcpyAsync(tmp16.data(), from, row_elems * 2, cudaMemcpyDeviceToHost, m->stream));
+            BTRY(cudaStreamSynchronize(m->stream));
+            for (size_t i = 0; i < row_elems; ++i) {
+                const uint32_t bits = uint32_t(tmp16[i]) << 16;
+                std::memcpy(&tmp32[i], &bits, 4);
+            }
+            BTRY(cudaMemcpy(dst, tmp32.data(), row_elems * 4, cudaMemcpyDefault));
+        }
     }
     BTRY(cudaStreamSynchronize(m->stream));
     return GPT2_OK;

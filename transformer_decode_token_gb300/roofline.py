@@ -43,11 +43,11 @@ def bytes_per_token(cfg, wdtype: str, pos: int, head: str = "f32") -> dict:
     return parts
 
 
-def batched_bytes_per_step(cfg, positions, wdtype: str = "bf16", head: str = "bf16") -> dict:
+def batched_bytes_per_step(cfg, positions, wdtype: str = "bf16", head: str = "bf16", kv: str = "f32") -> dict:
     """Bytes one step of the batched path must move: every stored weight once
     for the whole batch (block matrices and head), the small fp32 parameters,
     and per sequence at position p its embedding rows, its logits row and
-    its KV rows (read 0..p, write p)."""
+    its KV rows (read 0..p, write p; fp32 or bf16 elements)."""
     E, V, L = cfg.n_embd, cfg.vocab_size, cfg.n_layer
     positions = list(positions)
     n = len(positions)
@@ -58,7 +58,7 @@ def batched_bytes_per_step(cfg, positions, wdtype: str = "bf16", head: str = "bf
         "biases_ln": L * 13 * E * 4 + 2 * E * 4,
         "embedding_rows": n * 2 * E * 4,
         "logits": n * V * 4,
-        "kv": sum(L * 2 * E * 4 * (p + 2) for p in positions),
+        "kv": sum(L * 2 * E * {"f32": 4, "bf16": 2}[kv] * (p + 2) for p in positions),
     }
     parts["total"] = sum(parts.values())
     return parts
