@@ -10,7 +10,9 @@
 // head become dense contractions of the stored weights with 64 activation
 // rows (tc_gemm.cu); attention stays per sequence over that sequence's own
 // (ragged) KV cache.  One step is a CUDA graph of 8 kernels per block + 4,
-// chained by programmatic dependent launch:
+// chained by programmatic dependent launch (each kernel lets the next one
+// launch once it has passed its own wait, so the next one's CTAs are resident
+// and the linears' weight tiles in flight before its input exists):
 //   k_b_ln     residual add (the previous linear's split-K shares summed in a
 //              fixed order, + bias), or the embedding; LayerNorm; the bf16
 //              hi/lo B operand of the next linear
@@ -116,6 +118,7 @@ __global__ void __launch_bounds__(kBT) k_b_ln(const BLnArgs a)
     __shared__ float red[kBT / 32];
     const int b = blockIdx.x, E = a.E;
     pdl_wait();
+    pdl_launch_dependents();   // the next kernel's CTAs may start and park on their wait
     if (a.mode == 0) {
         int t = a.tok[b], p = a.pos[b];
         if (t < 0 || t >= a.V || p >= a.P) {
@@ -147,7 +150,6 @@ __global__ void __launch_bounds__(kBT) k_b_ln(const BLnArgs a)
     const float rstd = 1.0f / sqrtf(var + a.eps);
     for (int i = threadIdx.x; i < E; i += kBT)
         put_hi_lo(a.out, b, E, i, (xs[i] - mean) * rstd * a.gamma[i] + a.beta[i]);
-    pdl_launch_dependents();
 }
 
 struct BAttnArgs {
@@ -163,8 +165,8 @@ struct BAttnArgs {
     DeviceState *st;
 };
 
-constexpr int kAttnStageB = 8192;   // bytes per stage (32 fp32 or 64 bf16 rows of 64 dimensions)
-constexpr int kAttnStages = 3;
+constexpr int kAttnStageB = 16384;  // bytes per stage (64 fp32 or 128 bf16 rows of 64 dimensions)
+constexpr int kAttnStages = 2;
 
 // Dynamic shared memory of k_b_attn: the stages, then the scores [P];
 // es = bytes per cache element.
@@ -227,10 +229,10 @@ __global__ void __launch_bounds__(kBT) k_b_attn(const BAttnArgs a)
     }
     __syncthreads();
     pdl_wait();
+    pdl_launch_dependents();   // the next kernel's CTAs may start and park on their wait
     const int pos = a.pos[b];
     if (pos < 0 || pos >= a.P) {             // inactive row: zero output
         for (int d = tid; d < D; d += kBT) put_hi_lo(a.out, b, E, h * D + d, 0.f);
-        pdl_launch_dependents();
         return;
     }
     const int slot = a.slots == 1 ? 0 : b;
@@ -337,7 +339,6 @@ __global__ void __launch_bounds__(kBT) k_b_attn(const BAttnArgs a)
         for (int r = 0; r < RPP; ++r) o += part[r][d];
         put_hi_lo(a.out, b, E, h * D + d, o / sum);
     }
-    pdl_launch_dependents();
 }
 
 struct BGeluArgs {
@@ -352,8 +353,8 @@ __global__ void __launch_bounds__(kBT) k_b_gelu(const BGeluArgs a)
 {
     const int b = blockIdx.x, f = blockIdx.y * kBT + threadIdx.x;
     pdl_wait();
+    pdl_launch_dependents();   // the next kernel's CTAs may start and park on their wait
     if (f < a.F) put_hi_lo(a.out, b, a.F, f, gelu_new(sum_shares(a.parts, a.splits, a.rows, a.F, b, f) + a.bias[f]));
-    pdl_launch_dependents();
 }
 
 // k and v of every row (QKV shares + bias) into the cache at the row's
@@ -363,6 +364,7 @@ __global__ void __launch_bounds__(kBT) k_b_append(const BAttnArgs a, int D)
 {
     const int b = blockIdx.x, E = a.E;
     pdl_wait();
+    pdl_launch_dependents();   // the next kernel's CTAs may start and park on their wait
     const int pos = a.pos[b];
     if (pos >= 0 && pos < a.P) {
         const int slot = a.slots == 1 ? 0 : b;
@@ -372,7 +374,6 @@ __global__ void __launch_bounds__(kBT) k_b_append(const BAttnArgs a, int D)
             static_cast<float *>(part_ == 1 ? a.kc : a.vc)[((size_t(slot) * a.H + h) * a.P + pos) * D + d] = v;
         }
     }
-    pdl_launch_dependents();
 }
 
 struct BArgmaxArgs {
@@ -388,6 +389,7 @@ __global__ void __launch_bounds__(1024) k_b_argmax(const BArgmaxArgs a)
     __shared__ unsigned long long keys[32];
     const int b = blockIdx.x;
     pdl_wait();
+    pdl_launch_dependents();   // the next kernel's CTAs may start and park on their wait
     unsigned long long best = 0ull;
     for (int i = threadIdx.x; i < a.V; i += 1024) {
         const unsigned long long k = argmax_key(a.logits[size_t(b) * a.V + i], uint32_t(i));
@@ -406,13 +408,13 @@ __global__ void __launch_bounds__(1024) k_b_argmax(const BArgmaxArgs a)
             a.out_ids[size_t(p) * a.rows + b] = tok;
         }
     }
-    pdl_launch_dependents();
 }
 
 // Feeds each active row's choice to the next step, one position further.
 __global__ void k_b_advance(int32_t *tok, int32_t *pos, const int32_t *next_tok, int rows, int P, DeviceState *st)
 {
     pdl_wait();
+    pdl_launch_dependents();   // the next kernel's CTAs may start and park on their wait
     const int b = threadIdx.x;
     if (b < rows && pos[b] >= 0) {
         tok[b] = next_tok[b];
