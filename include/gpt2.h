@@ -393,9 +393,14 @@ int gpt2_decode_batch(gpt2_batch *m, const int32_t *tokens, const int32_t *posit
                       int32_t n, const float **dev_logits);
 
 /* Resets every sequence, then consumes the ragged prompts: sequence b's
- * lens[b] ids follow one another in the host array ids (sequence 0 first),
- * one position per step; afterwards each sequence's greedy choice after its
- * last prompt token is available (gpt2_argmax_batch). */
+ * lens[b] ids follow one another in the host array ids (sequence 0 first).
+ * Every position but each sequence's last runs in prompt steps of max_batch
+ * (sequence, position) rows packed sequence by sequence (the blocks only:
+ * they fill the cache); the last positions then run as one decode step, so
+ * each sequence's greedy choice after its prompt (gpt2_argmax_batch) and
+ * its logits (gpt2_copy_logits_batch) are available afterwards.  The ids
+ * chosen at prompt positions other than the last are not recorded
+ * (gpt2_batch_ids). */
 int gpt2_prefill_batch(gpt2_batch *m, const int32_t *ids, const int32_t *lens, int32_t n);
 
 /* n_steps device-resident greedy steps for every sequence with a cached

@@ -130,6 +130,21 @@ def test_tiny_batch_full_and_kv_cache():
         m.close()
 
 
+def test_tiny_batch_prompt_steps_packing():
+    """Prompts of 1, 2, 63, 64, 65 and 3 tokens: the prompt steps pack
+    max_batch (here 6) (sequence, position) rows at a time, so sequences
+    start and end inside a step and run across step boundaries; one-token
+    prompts have no prompt step at all (only the final decode step).  Every
+    sequence checked."""
+    import dataclasses
+    cfg = dataclasses.replace(synth.TINY, n_positions=128)
+    base = synth.make_batch_prompts(cfg, 6, 63, 63, seed=9)
+    lens = [1, 2, 63, 64, 65, 3]
+    prompts = [[int(t) for t in np.resize(np.asarray(q), L)] for q, L in zip(base, lens)]
+    m, _ = run_batch(cfg, prompts, 5, list(range(6)))
+    m.close()
+
+
 @pytest.mark.parametrize("kv", ["f32", "bf16"])
 def test_tiny_batch_long_contexts_span_attention_chunks(kv):
     """Tiny model with 256 positions: prompts of 40..230 tokens, so a

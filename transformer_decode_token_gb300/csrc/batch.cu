@@ -163,7 +163,13 @@ struct BAttnArgs {
     float scale;
     __nv_bfloat16 *out;             // [128][E] hi/lo B operand of the output projection
     DeviceState *st;
+    const int32_t *slot_of;         // [rows] cache slot of each row, or null: slot = row (or 0, one slot)
 };
+
+__device__ __forceinline__ int row_slot(const BAttnArgs &a, int b)
+{
+    return a.slot_of ? a.slot_of[b] : (a.slots == 1 ? 0 : b);
+}
 
 constexpr int kAttnStageB = 16384;  // bytes per stage (64 fp32 or 128 bf16 rows of 64 dimensions)
 constexpr int kAttnStages = 2;
@@ -235,7 +241,7 @@ __global__ void __launch_bounds__(kBT) k_b_attn(const BAttnArgs a)
         for (int d = tid; d < D; d += kBT) put_hi_lo(a.out, b, E, h * D + d, 0.f);
         return;
     }
-    const int slot = a.slots == 1 ? 0 : b;
+    const int slot = row_slot(a, b);
     KT *kh = static_cast<KT *>(a.kc) + (size_t(slot) * a.H + h) * a.P * D;
     KT *vh = static_cast<KT *>(a.vc) + (size_t(slot) * a.H + h) * a.P * D;
     const int n = pos + 1;
@@ -359,7 +365,8 @@ __global__ void __launch_bounds__(kBT) k_b_gelu(const BGeluArgs a)
 
 // k and v of every row (QKV shares + bias) into the cache at the row's
 // position, before any row's attention reads them: the rows of one step are
-// then positions of one sequence (slot 0).
+// then positions of sequences, consecutive within each (prompts).
+template <typename KT>
 __global__ void __launch_bounds__(kBT) k_b_append(const BAttnArgs a, int D)
 {
     const int b = blockIdx.x, E = a.E;
@@ -367,11 +374,11 @@ __global__ void __launch_bounds__(kBT) k_b_append(const BAttnArgs a, int D)
     pdl_launch_dependents();   // the next kernel's CTAs may start and park on their wait
     const int pos = a.pos[b];
     if (pos >= 0 && pos < a.P) {
-        const int slot = a.slots == 1 ? 0 : b;
+        const int slot = row_slot(a, b);
         for (int t = blockIdx.y * kBT + threadIdx.x; t < 2 * E; t += gridDim.y * kBT) {
             const int part_ = 1 + t / E, hd = t % E, h = hd / D, d = hd % D, j = part_ * E + hd;
             const float v = sum_shares(a.parts, a.splits, a.rows, 3 * E, b, j) + a.bias[j];
-            static_cast<float *>(part_ == 1 ? a.kc : a.vc)[((size_t(slot) * a.H + h) * a.P + pos) * D + d] = v;
+            kv_put(static_cast<KT *>(part_ == 1 ? a.kc : a.vc) + ((size_t(slot) * a.H + h) * a.P + pos) * D + d, v);
         }
     }
 }
@@ -510,6 +517,10 @@ struct gpt2_batch {
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
     int kernels_per_step = 0;
+    cudaGraph_t graph_p = nullptr;  // prompt steps of a batched model (packed rows)
+    cudaGraphExec_t exec_p = nullptr;
+    int kernels_per_prompt_step = 0;
+    int32_t *slot_of = nullptr;     // [kTcMaxRows] cache slot of each row in a prompt step
     std::vector<int> cached;        // host view: cached length of each sequence
     bool has_step = false;
     unsigned long long launches = 0;
@@ -571,7 +582,10 @@ const void *attn_kernel(int D, bool bf16)
 }
 
 // Records one batched step on stream s (under capture).
-int record_step(gpt2_batch *m, cudaStream_t s)
+// packed: a prompt step of the batched model: rows are (sequence, position)
+// pairs (slot_of), every row's k, v appended first; only the blocks run (the
+// cache is what a prompt step is for: no head, no choice).
+int record_step(gpt2_batch *m, cudaStream_t s, bool packed = false)
 {
     const gpt2_config &c = m->cfg;
     const int E = c.n_embd, H = c.n_head, D = E / H, F = 4 * E, R = m->max_batch, P = c.n_positions;
@@ -625,14 +639,18 @@ int record_step(gpt2_batch *m, cudaStream_t s)
         at.P = P;
         at.rows = R;
         at.slots = slots;
-        at.append = slots == 1 ? 0 : 1;   // one sequence: every row's k, v first (k_b_append)
+        const bool pre = slots == 1 || packed;   // rows of prompts: every row's k, v first (k_b_append)
+        at.append = pre ? 0 : 1;
+        at.slot_of = packed ? m->slot_of : nullptr;
         at.scale = float(1.0 / std::sqrt(double(D)));
         at.out = m->b_a;
         at.st = m->st;
-        if (slots == 1) {
+        if (pre) {
             int dd = D;
             void *ap[] = {&at, &dd};
-            BTRY(launch_pdl(reinterpret_cast<const void *>(k_b_append), dim3(R, 2), dim3(kBT), 0, s, pdl(), ap));
+            const void *fn = m->kv_bf16 ? reinterpret_cast<const void *>(k_b_append<__nv_bfloat16>)
+                                        : reinterpret_cast<const void *>(k_b_append<float>);
+            BTRY(launch_pdl(fn, dim3(R, 2), dim3(kBT), 0, s, pdl(), ap));
             ++kernels;
         }
         void *a2[] = {&at};
@@ -660,6 +678,10 @@ int record_step(gpt2_batch *m, cudaStream_t s)
                         pdl(), a4));
         BTRY(run_linear(m, Ly.lin[3], m->map_f, m->p_p, s, pdl()));
         kernels += 8;
+    }
+    if (packed) {
+        m->kernels_per_prompt_step = kernels;
+        return GPT2_OK;
     }
     BLnArgs ln{};
     ln.x = m->x;
@@ -699,7 +721,7 @@ int record_step(gpt2_batch *m, cudaStream_t s)
     return GPT2_OK;
 }
 
-int build_step_graph(gpt2_batch *m)
+int capture_step(gpt2_batch *m, bool packed, cudaGraph_t *graph, cudaGraphExec_t *exec)
 {
     cudaStream_t cs;
     BTRY(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
@@ -708,7 +730,7 @@ int build_step_graph(gpt2_batch *m)
         cudaStreamDestroy(cs);
         return cuda_rc(e);
     }
-    const int rc = record_step(m, cs);
+    const int rc = record_step(m, cs, packed);
     cudaGraph_t g = nullptr;
     e = cudaStreamEndCapture(cs, &g);
     cudaStreamDestroy(cs);
@@ -717,9 +739,18 @@ int build_step_graph(gpt2_batch *m)
         return rc;
     }
     if (e != cudaSuccess) return cuda_rc(e);
-    m->graph = g;
-    BTRY(cudaGraphInstantiate(&m->exec, g, 0));
+    *graph = g;
+    BTRY(cudaGraphInstantiate(exec, g, 0));
     return GPT2_OK;
+}
+
+// The decode step's graph, and for a batched model (one cache slot per
+// sequence) the prompt step's.
+int build_step_graph(gpt2_batch *m)
+{
+    int rc = capture_step(m, false, &m->graph, &m->exec);
+    if (rc == GPT2_OK && m->slots > 1) rc = capture_step(m, true, &m->graph_p, &m->exec_p);
+    return rc;
 }
 
 void free_batch(gpt2_batch *m)
@@ -727,6 +758,8 @@ void free_batch(gpt2_batch *m)
     if (!m) return;
     if (m->exec) cudaGraphExecDestroy(m->exec);
     if (m->graph) cudaGraphDestroy(m->graph);
+    if (m->exec_p) cudaGraphExecDestroy(m->exec_p);
+    if (m->graph_p) cudaGraphDestroy(m->graph_p);
     if (m->arena) cudaFree(m->arena);
     if (m->work) cudaFree(m->work);
     delete m;
@@ -835,6 +868,7 @@ int engine_build(gpt2_batch *m, const gpt2_config &cfg, const EngineSrc &src, cu
     const size_t o_lg = take(size_t(src.rows) * V * 4);
     const size_t o_tok = take(size_t(kTcMaxRows) * 4), o_pos = take(size_t(kTcMaxRows) * 4);
     const size_t o_nt = take(size_t(kTcMaxRows) * 4), o_ids = take(size_t(P) * src.rows * 4);
+    const size_t o_slot = take(size_t(kTcMaxRows) * 4);
     const size_t o_st = take(sizeof(DeviceState));
     const size_t work_bytes = off;
     const size_t tmp_elems = size_t(F) * E > size_t(Vp) * E ? size_t(F) * E : size_t(Vp) * E;
@@ -933,6 +967,7 @@ int engine_build(gpt2_batch *m, const gpt2_config &cfg, const EngineSrc &src, cu
     m->pos = reinterpret_cast<int32_t *>(W + o_pos);
     m->next_tok = reinterpret_cast<int32_t *>(W + o_nt);
     m->out_ids = reinterpret_cast<int32_t *>(W + o_ids);
+    m->slot_of = reinterpret_cast<int32_t *>(W + o_slot);
     m->st = reinterpret_cast<DeviceState *>(W + o_st);
     if (tc_make_tmap(&m->map_e, m->b_e, 2 * kTcMaxRows, uint64_t(E)) ||
         tc_make_tmap(&m->map_a, m->b_a, 2 * kTcMaxRows, uint64_t(E)) ||
@@ -1148,11 +1183,9 @@ int gpt2_decode_batch(gpt2_batch *m, const int32_t *tokens, const int32_t *posit
 int gpt2_prefill_batch(gpt2_batch *m, const int32_t *ids, const int32_t *lens, int32_t n)
 {
     if (!m || !ids || !lens || n < 1 || n > m->max_batch) return GPT2_ERR_INVALID_ARG;
-    int max_len = 0;
     size_t total = 0;
     for (int b = 0; b < n; ++b) {
         if (lens[b] < 1 || lens[b] > m->cfg.n_positions) return GPT2_ERR_POSITION_RANGE;
-        max_len = std::max(max_len, int(lens[b]));
         total += size_t(lens[b]);
     }
     for (size_t i = 0; i < total; ++i)
@@ -1160,17 +1193,49 @@ int gpt2_prefill_batch(gpt2_batch *m, const int32_t *ids, const int32_t *lens, i
     std::fill(m->cached.begin(), m->cached.end(), 0);
     std::vector<size_t> start(n, 0);
     for (int b = 1; b < n; ++b) start[b] = start[b - 1] + size_t(lens[b - 1]);
-    std::vector<int32_t> t(n), p(n);
-    for (int step = 0; step < max_len; ++step) {
-        for (int b = 0; b < n; ++b) {
-            const bool on = step < lens[b];
-            t[b] = on ? ids[start[b] + step] : 0;
-            p[b] = on ? step : -1;
+    // prompt steps: every position but each sequence's last, max_batch rows
+    // per step (the rows a step's kernels process) taken sequence by sequence
+    // (a sequence's rows in a step are consecutive positions; the step appends
+    // all their k, v before any attention reads the cache)
+    std::vector<int32_t> t(kTcMaxRows), p(kTcMaxRows), sl(kTcMaxRows);
+    const int rows = m->max_batch;
+    int r = 0;
+    auto flush = [&]() -> int {
+        if (r == 0) return GPT2_OK;
+        for (int i = r; i < kTcMaxRows; ++i) {
+            t[i] = 0;
+            p[i] = -1;
+            sl[i] = 0;
         }
-        const int rc = gpt2_decode_batch(m, t.data(), p.data(), n, nullptr);
-        if (rc != GPT2_OK) return rc;
+        BTRY(cudaMemcpyAsync(m->tok, t.data(), t.size() * 4, cudaMemcpyHostToDevice, m->stream));
+        BTRY(cudaMemcpyAsync(m->pos, p.data(), p.size() * 4, cudaMemcpyHostToDevice, m->stream));
+        BTRY(cudaMemcpyAsync(m->slot_of, sl.data(), sl.size() * 4, cudaMemcpyHostToDevice, m->stream));
+        BTRY(cudaGraphLaunch(m->exec_p, m->stream));
+        m->launches += m->kernels_per_prompt_step;
+        r = 0;
+        return GPT2_OK;
+    };
+    for (int b = 0; b < n; ++b)
+        for (int q = 0; q + 1 < lens[b]; ++q) {
+            t[r] = ids[start[b] + q];
+            p[r] = q;
+            sl[r] = b;
+            if (++r == rows) {
+                const int rc = flush();
+                if (rc != GPT2_OK) return rc;
+            }
+        }
+    int rc = flush();
+    if (rc != GPT2_OK) return rc;
+    // each sequence's last prompt token: one decode step, which leaves the
+    // choice after the prompt and its logits by sequence
+    std::vector<int32_t> tl(n), pl(n);
+    for (int b = 0; b < n; ++b) {
+        m->cached[b] = lens[b] - 1;
+        tl[b] = ids[start[b] + lens[b] - 1];
+        pl[b] = lens[b] - 1;
     }
-    return GPT2_OK;
+    return gpt2_decode_batch(m, tl.data(), pl.data(), n, nullptr);
 }
 
 int gpt2_decode_batch_greedy(gpt2_batch *m, int32_t n_steps)
