@@ -189,29 +189,37 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def kernel_source_sha() -> str:
-    """sha256 prefix of the decode kernel's sources: a traffic figure taken on
-    other sources no longer describes the kernel."""
+SOURCES = {"cluster": ("cluster.cu", "cluster.h", "common.cuh"),
+           "batched": ("batch.cu", "batch.h", "tc_gemm.cu", "tc_gemm.h", "common.cuh")}
+
+
+def kernel_source_sha(path: str = "cluster") -> str:
+    """sha256 prefix of a decode path's kernel sources: a traffic figure taken
+    on other sources no longer describes the kernels."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "transformer_decode_token_gb300", "csrc")
-    for name in ("cluster.cu", "cluster.h", "common.cuh"):
+    for name in SOURCES[path]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def load_traffic(path: str, key: str):
-    """DRAM bytes per decode pass from the committed ncu summaries
-    (profiles/traffic.json: {path: {key: {"bytes": B, "sources": sha}}}), or
-    None if there is none for the current kernel sources."""
+def load_traffic(path: str, key: str, alg=None):
+    """DRAM bytes per decode pass (batched: per step) from the committed ncu
+    summaries (profiles/traffic.json: {path: {key: {"bytes": B, "sources":
+    sha}}}), or None if there is none for the current kernel sources.  An
+    entry captured on a step with other positions ("algorithmic": its
+    algorithmic bytes) is scaled to `alg` by the algorithmic bytes."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             t = json.load(f).get(path, {}).get(key)
     except OSError:
         return None
-    if not isinstance(t, dict) or t.get("sources") != kernel_source_sha():
+    if not isinstance(t, dict) or t.get("sources") != kernel_source_sha(path if path in SOURCES else "cluster"):
         return None
+    if alg is not None and t.get("algorithmic"):
+        return t["bytes"] * alg / t["algorithmic"]
     return t.get("bytes")
 
 
@@ -551,7 +559,7 @@ def measure_batch(torch, cfg, w, steps, warmup, world, local, barrier, max_over_
                                                "ragged attention, LayerNorm/gelu/argmax), PDL-chained",
                      "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "peak_kind": f"{peak_kind} copy bandwidth",
-                     "traffic": None, "algorithmic_bytes_per_launch": alg,
+                     "traffic": load_traffic("batched", kv, alg), "algorithmic_bytes_per_launch": alg,
                      "tensor_tflops": flops / step_s / 1e12,
                      "tensor_frac": flops / step_s / 1e12 / peaks.get("bf16_tflops", 1900.0),
                      "note": f"bytes: weights once per step + each sequence's KV rows 0..p ({kv}), embedding and "
