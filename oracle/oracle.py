@@ -66,57 +66,83 @@ class _Weights(ctypes.Structure):
                 ("layers", ctypes.POINTER(_Layer)), ("head", _FP)]
 
 
+def build_variant(src_text: str, out_path: str) -> str:
+    """Compile another oracle source (e.g. one with a planted mistake, for the
+    tests that check the pins reject it) into out_path, same flags."""
+    src = out_path + ".c"
+    with open(src, "w") as f:
+        f.write(src_text)
+    subprocess.check_call(["gcc", *CFLAGS, "-I", _HERE, "-o", out_path, src, "-lm"])
+    return out_path
+
+
+def source() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
+def load(path: str):
+    """A ctypes handle on an oracle library at path, its calls typed."""
+    L = ctypes.CDLL(path)
+    _type_calls(L)
+    return L
+
+
 def lib(omp: bool = False):
     """The oracle library; omp=True: its multi-core build (OMP_NUM_THREADS,
     default all host cores)."""
     global _lib, _lib_omp
     with _lock:
         if (_lib_omp if omp else _lib) is None:
-            L = ctypes.CDLL(build(omp=omp))
-            c_sz, c_i32, c_f = ctypes.c_size_t, ctypes.c_int32, ctypes.c_float
-            vp = ctypes.c_void_p
-            L.orc_expf.restype = c_f; L.orc_expf.argtypes = [c_f]
-            L.orc_tanhf.restype = c_f; L.orc_tanhf.argtypes = [c_f]
-            L.orc_gelu_new.restype = c_f; L.orc_gelu_new.argtypes = [c_f]
-            L.orc_expf_reduce.argtypes = [c_f, ctypes.POINTER(c_i32), ctypes.POINTER(c_f)]
-            L.orc_gelu_new_vec.argtypes = [vp, vp, c_sz]
-            L.orc_expf_vec.argtypes = [vp, vp, c_sz]
-            L.orc_layernorm.argtypes = [vp, vp, vp, c_i32, c_f, vp]
-            L.orc_softmax.argtypes = [vp, c_i32]
-            L.orc_linear.argtypes = [vp, vp, vp, c_i32, c_i32, vp]
-            L.orc_linear_t.argtypes = [vp, vp, c_i32, c_i32, vp]
-            L.orc_attn_decode.argtypes = [vp, c_i32, c_i32, c_i32, c_i32, vp, vp, vp]
-            L.orc_argmax.restype = c_i32; L.orc_argmax.argtypes = [vp, c_i32]
-            c_u64 = ctypes.c_uint64
-            L.orc_splitmix64.restype = c_u64; L.orc_splitmix64.argtypes = [c_u64, c_u64]
-            L.orc_uniform.restype = c_f; L.orc_uniform.argtypes = [c_u64, c_u64]
-            L.orc_uniform_bits.restype = c_f; L.orc_uniform_bits.argtypes = [c_u64]
-            L.orc_sample_scores.argtypes = [vp, c_i32, c_f, c_u64, c_i32, vp]
-            L.orc_sample.restype = c_i32; L.orc_sample.argtypes = [vp, c_i32, c_f, c_u64, c_i32]
-            L.orc_create.restype = vp
-            L.orc_create.argtypes = [ctypes.POINTER(_Cfg), ctypes.POINTER(_Weights)]
-            L.orc_destroy.argtypes = [vp]
-            L.orc_reset.argtypes = [vp]
-            L.orc_set_kv_bf16.restype = None
-            L.orc_set_kv_bf16.argtypes = [vp, c_i32]
-            L.orc_forward.restype = c_i32
-            L.orc_forward.argtypes = [vp, c_i32, c_i32, vp]
-            L.orc_export_kv.restype = c_i32
-            L.orc_export_kv.argtypes = [vp, c_i32, c_i32, vp, vp]
-            L.orc_forward_full.restype = c_i32
-            L.orc_forward_full.argtypes = [ctypes.POINTER(_Cfg), ctypes.POINTER(_Weights),
-                                           vp, c_i32, vp]
-            for n in ("orc_f32_to_f16", "orc_f16_to_f32", "orc_f32_to_bf16", "orc_bf16_to_f32"):
-                getattr(L, n).argtypes = [vp, vp, c_sz]
-            L.orc_quant_int4.argtypes = [vp, c_i32, c_i32, vp, vp, vp]
-            L.orc_dequant_int4.argtypes = [vp, vp, vp, c_i32, c_i32, vp]
-            L.orc_pack_nibbles.argtypes = [vp, c_sz, vp]
-            L.orc_unpack_nibbles.argtypes = [vp, c_sz, vp]
+            L = load(build(omp=omp))
             if omp:
                 _lib_omp = L
             else:
                 _lib = L
     return _lib_omp if omp else _lib
+
+
+def _type_calls(L):
+    """Argument and result types of the oracle's C calls."""
+    c_sz, c_i32, c_f = ctypes.c_size_t, ctypes.c_int32, ctypes.c_float
+    vp = ctypes.c_void_p
+    L.orc_expf.restype = c_f; L.orc_expf.argtypes = [c_f]
+    L.orc_tanhf.restype = c_f; L.orc_tanhf.argtypes = [c_f]
+    L.orc_gelu_new.restype = c_f; L.orc_gelu_new.argtypes = [c_f]
+    L.orc_expf_reduce.argtypes = [c_f, ctypes.POINTER(c_i32), ctypes.POINTER(c_f)]
+    L.orc_gelu_new_vec.argtypes = [vp, vp, c_sz]
+    L.orc_expf_vec.argtypes = [vp, vp, c_sz]
+    L.orc_layernorm.argtypes = [vp, vp, vp, c_i32, c_f, vp]
+    L.orc_softmax.argtypes = [vp, c_i32]
+    L.orc_linear.argtypes = [vp, vp, vp, c_i32, c_i32, vp]
+    L.orc_linear_t.argtypes = [vp, vp, c_i32, c_i32, vp]
+    L.orc_attn_decode.argtypes = [vp, c_i32, c_i32, c_i32, c_i32, vp, vp, vp]
+    L.orc_argmax.restype = c_i32; L.orc_argmax.argtypes = [vp, c_i32]
+    c_u64 = ctypes.c_uint64
+    L.orc_splitmix64.restype = c_u64; L.orc_splitmix64.argtypes = [c_u64, c_u64]
+    L.orc_uniform.restype = c_f; L.orc_uniform.argtypes = [c_u64, c_u64]
+    L.orc_uniform_bits.restype = c_f; L.orc_uniform_bits.argtypes = [c_u64]
+    L.orc_sample_scores.argtypes = [vp, c_i32, c_f, c_u64, c_i32, vp]
+    L.orc_sample.restype = c_i32; L.orc_sample.argtypes = [vp, c_i32, c_f, c_u64, c_i32]
+    L.orc_create.restype = vp
+    L.orc_create.argtypes = [ctypes.POINTER(_Cfg), ctypes.POINTER(_Weights)]
+    L.orc_destroy.argtypes = [vp]
+    L.orc_reset.argtypes = [vp]
+    L.orc_set_kv_bf16.restype = None
+    L.orc_set_kv_bf16.argtypes = [vp, c_i32]
+    L.orc_forward.restype = c_i32
+    L.orc_forward.argtypes = [vp, c_i32, c_i32, vp]
+    L.orc_export_kv.restype = c_i32
+    L.orc_export_kv.argtypes = [vp, c_i32, c_i32, vp, vp]
+    L.orc_forward_full.restype = c_i32
+    L.orc_forward_full.argtypes = [ctypes.POINTER(_Cfg), ctypes.POINTER(_Weights),
+                                   vp, c_i32, vp]
+    for n in ("orc_f32_to_f16", "orc_f16_to_f32", "orc_f32_to_bf16", "orc_bf16_to_f32"):
+        getattr(L, n).argtypes = [vp, vp, c_sz]
+    L.orc_quant_int4.argtypes = [vp, c_i32, c_i32, vp, vp, vp]
+    L.orc_dequant_int4.argtypes = [vp, vp, vp, c_i32, c_i32, vp]
+    L.orc_pack_nibbles.argtypes = [vp, c_sz, vp]
+    L.orc_unpack_nibbles.argtypes = [vp, c_sz, vp]
 
 
 def _p(a: np.ndarray):
@@ -389,11 +415,11 @@ class OracleModel:
     multi-core build, for the CPU baseline's timing; kv="bf16": the cache
     holds k and v rounded to bf16, the batched configuration's KV variant)."""
 
-    def __init__(self, cfg, weights: dict, omp: bool = False, kv: str = "f32"):
+    def __init__(self, cfg, weights: dict, omp: bool = False, kv: str = "f32", library=None):
         if kv not in ("f32", "bf16"):
             raise ValueError(f"unknown KV cache type {kv!r}")
         self.cfg = cfg
-        self._lib = lib(omp)
+        self._lib = library if library is not None else lib(omp)
         self._c = _cfg_struct(cfg)
         self._h = _WeightsHolder(cfg, weights)
         self._m = self._lib.orc_create(ctypes.byref(self._c), ctypes.byref(self._h.w))
