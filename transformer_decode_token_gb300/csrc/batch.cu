@@ -397,11 +397,28 @@ __global__ void __launch_bounds__(1024) k_b_argmax(const BArgmaxArgs a)
     const int b = blockIdx.x;
     pdl_wait();
     pdl_launch_dependents();   // the next kernel's CTAs may start and park on their wait
-    unsigned long long best = 0ull;
-    for (int i = threadIdx.x; i < a.V; i += 1024) {
-        const unsigned long long k = argmax_key(a.logits[size_t(b) * a.V + i], uint32_t(i));
-        best = k > best ? k : best;
+    // four loads in flight per thread (the maximum of the keys does not
+    // depend on the order they are taken in)
+    const float *row = a.logits + size_t(b) * a.V;
+    unsigned long long bk[4] = {0ull, 0ull, 0ull, 0ull};
+    int i = threadIdx.x;
+    for (; i + 3 * 1024 < a.V; i += 4 * 1024) {
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = row[i + u * 1024];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const unsigned long long k = argmax_key(v[u], uint32_t(i + u * 1024));
+            bk[u] = k > bk[u] ? k : bk[u];
+        }
     }
+    for (; i < a.V; i += 1024) {
+        const unsigned long long k = argmax_key(row[i], uint32_t(i));
+        bk[0] = k > bk[0] ? k : bk[0];
+    }
+    unsigned long long best = bk[0] > bk[1] ? bk[0] : bk[1];
+    best = bk[2] > best ? bk[2] : best;
+    best = bk[3] > best ? bk[3] : best;
     best = warp_max_u64(best);
     if ((threadIdx.x & 31) == 0) keys[threadIdx.x >> 5] = best;
     __syncthreads();

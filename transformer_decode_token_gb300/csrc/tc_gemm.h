@@ -19,7 +19,7 @@ constexpr int kTcM = 128;
 constexpr int kTcN = 128;
 constexpr int kTcK = 64;
 constexpr int kTcMaxRows = 64;          // activation rows (sequences or positions) per call
-constexpr int kTcStages = 4;            // shared-memory pipeline depth
+constexpr int kTcStages = 3;            // shared-memory pipeline depth (97 KB: two CTAs fit an SM)
 constexpr int kTcThreads = 128;         // 4 warps: TMA producer, MMA issuer, then all four read TMEM
 constexpr int kTcMaxSplits = 8;         // K splits of one linear (the consumers sum at most this many shares)
 
