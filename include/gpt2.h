@@ -368,7 +368,8 @@ typedef struct gpt2_batch gpt2_batch;
 
 /* max_batch in [1, 64].  Same weights argument and ownership as gpt2_create.
  * Errors: INVALID_ARG (wdtype other than GPT2_BF16, shapes: n_embd % 64,
- * head_dim in {32, 64, 128}), UNSUPPORTED_DEVICE, OUT_OF_MEMORY, CUDA. */
+ * n_embd <= 1024, head_dim in {32, 64, 128}), UNSUPPORTED_DEVICE,
+ * OUT_OF_MEMORY, CUDA. */
 int gpt2_create_batch(const gpt2_config *cfg, const gpt2_weights *w, int32_t wdtype,
                       int32_t max_batch, void *stream, gpt2_batch **out);
 /* GPT2_BATCH_KV_BF16: the cache holds k and v rounded to bf16 (round to

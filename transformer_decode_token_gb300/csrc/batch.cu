@@ -111,45 +111,78 @@ struct BLnArgs {
 
 // One CTA per row: the residual stream update, then LayerNorm ("model.fir"
 // kernel g2.layernorm: mean, biased variance, (x - mean) / sqrt(var + eps) *
-// gamma + beta) into the next linear's B operand.
+// gamma + beta) into the next linear's B operand.  The row stays in
+// registers (E <= kLnPer * kBT) and the statistics take one block reduction:
+// s and q, the sums of v - K and (v - K)^2 with K a value near the row (the
+// first element of the row's previous residual, or of its embedding), give
+// mean = K + s/E and var = q/E - (s/E)^2 without cancelling when the row has
+// a large common offset.  The residual is stored after the reduction (K was
+// read by every thread before it).
+constexpr int kLnPer = 4;
 __global__ void __launch_bounds__(kBT) k_b_ln(const BLnArgs a)
 {
-    extern __shared__ float xs[];   // [E]
-    __shared__ float red[kBT / 32];
-    const int b = blockIdx.x, E = a.E;
+    __shared__ float red[2][kBT / 32];
+    const int b = blockIdx.x, E = a.E, tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
     pdl_wait();
     pdl_launch_dependents();   // the next kernel's CTAs may start and park on their wait
+    float v[kLnPer];
+    float K;
+    float *xr = a.x + size_t(b) * E;
     if (a.mode == 0) {
         int t = a.tok[b], p = a.pos[b];
         if (t < 0 || t >= a.V || p >= a.P) {
-            if (threadIdx.x == 0 && p >= 0) record_error(a.st, t < 0 || t >= a.V ? kDevErrBadToken : kDevErrBadPosition, b);
+            if (tid == 0 && p >= 0) record_error(a.st, t < 0 || t >= a.V ? kDevErrBadToken : kDevErrBadPosition, b);
             t = min(max(t, 0), a.V - 1);
         }
         p = min(max(p, 0), a.P - 1);
-        for (int i = threadIdx.x; i < E; i += kBT) {
-            const float v = a.wte[size_t(t) * E + i] + a.wpe[size_t(p) * E + i];
-            xs[i] = v;
-            a.x[size_t(b) * E + i] = v;
+        const float *we = a.wte + size_t(t) * E, *wp = a.wpe + size_t(p) * E;
+        K = we[0] + wp[0];
+#pragma unroll
+        for (int j = 0; j < kLnPer; ++j) {
+            const int i = tid + j * kBT;
+            v[j] = i < E ? we[i] + wp[i] : 0.f;
         }
     } else {
-        for (int i = threadIdx.x; i < E; i += kBT) {
-            const float v = a.x[size_t(b) * E + i] + (sum_shares(a.parts, a.splits, a.rows, E, b, i) + a.bias[i]);
-            xs[i] = v;
-            a.x[size_t(b) * E + i] = v;
+        K = xr[0];
+#pragma unroll
+        for (int j = 0; j < kLnPer; ++j) {
+            const int i = tid + j * kBT;
+            v[j] = i < E ? xr[i] + (sum_shares(a.parts, a.splits, a.rows, E, b, i) + a.bias[i]) : 0.f;
         }
     }
-    float s = 0.f;
-    for (int i = threadIdx.x; i < E; i += kBT) s += xs[i];
-    const float mean = block_sum(s, red) / float(E);
-    float q = 0.f;
-    for (int i = threadIdx.x; i < E; i += kBT) {
-        const float d = xs[i] - mean;
-        q = fmaf(d, d, q);
+    float s = 0.f, q = 0.f;
+#pragma unroll
+    for (int j = 0; j < kLnPer; ++j)
+        if (tid + j * kBT < E) {
+            const float d = v[j] - K;
+            s += d;
+            q = fmaf(d, d, q);
+        }
+    s = warp_sum(s);
+    q = warp_sum(q);
+    if (lane == 0) {
+        red[0][warp] = s;
+        red[1][warp] = q;
     }
-    const float var = block_sum(q, red) / float(E);
+    __syncthreads();
+    float S = 0.f, Q = 0.f;
+    for (int w = 0; w < kBT / 32; ++w) {
+        S += red[0][w];
+        Q += red[1][w];
+    }
+    const float ds = S / float(E);
+    const float mean = K + ds;
+    const float var = fmaxf(Q / float(E) - ds * ds, 0.f);
     const float rstd = 1.0f / sqrtf(var + a.eps);
-    for (int i = threadIdx.x; i < E; i += kBT)
-        put_hi_lo(a.out, b, E, i, (xs[i] - mean) * rstd * a.gamma[i] + a.beta[i]);
+#pragma unroll
+    for (int j = 0; j < kLnPer; ++j) {
+        const int i = tid + j * kBT;
+        if (i < E) {
+            xr[i] = v[j];
+            put_hi_lo(a.out, b, E, i, (v[j] - mean) * rstd * a.gamma[i] + a.beta[i]);
+        }
+    }
 }
 
 struct BAttnArgs {
@@ -614,7 +647,7 @@ int record_step(gpt2_batch *m, cudaStream_t s, bool packed = false)
         first = false;
         return p;
     };
-    const size_t ln_smem = size_t(E) * 4;
+    const size_t ln_smem = 0;
     for (int l = 0; l < L; ++l) {
         const gpt2_batch::Layer &Ly = m->layers[l];
         BLnArgs ln{};
@@ -1010,6 +1043,7 @@ int engine_shape_ok(const gpt2_config *cfg)
 {
     const int L = cfg->n_layer, E = cfg->n_embd, H = cfg->n_head, P = cfg->n_positions, V = cfg->vocab_size;
     if (L < 1 || H < 1 || P < 1 || V < 1 || E < 64 || E % 64 || E % H) return GPT2_ERR_INVALID_ARG;
+    if (E > kLnPer * kBT) return GPT2_ERR_INVALID_ARG;   // a LayerNorm row in one CTA's registers
     const int D = E / H;
     if (D != 32 && D != 64 && D != 128) return GPT2_ERR_INVALID_ARG;
     if (!(cfg->ln_eps > 0.f) || !std::isfinite(cfg->ln_eps)) return GPT2_ERR_INVALID_ARG;
