@@ -130,6 +130,16 @@ def test_tiny_batch_full_and_kv_cache():
         m.close()
 
 
+@pytest.mark.parametrize("kv", ["f32", "bf16"])
+def test_tiny_batch_of_one(kv):
+    """max_batch 1: one cache slot, so prompts run a decode step per position
+    (nothing to pack) and decode steps append before attending."""
+    cfg = synth.TINY
+    prompts = synth.make_batch_prompts(cfg, 1, 9, 9, seed=11)
+    m, _ = run_batch(cfg, prompts, 6, [0], kv=kv)
+    m.close()
+
+
 def test_tiny_batch_prompt_steps_packing():
     """Prompts of 1, 2, 63, 64, 65 and 3 tokens: the prompt steps pack
     max_batch (here 6) (sequence, position) rows at a time, so sequences

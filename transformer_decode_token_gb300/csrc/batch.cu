@@ -1266,18 +1266,28 @@ int gpt2_prefill_batch(gpt2_batch *m, const int32_t *ids, const int32_t *lens, i
         r = 0;
         return GPT2_OK;
     };
-    for (int b = 0; b < n; ++b)
-        for (int q = 0; q + 1 < lens[b]; ++q) {
-            t[r] = ids[start[b] + q];
-            p[r] = q;
-            sl[r] = b;
-            if (++r == rows) {
-                const int rc = flush();
-                if (rc != GPT2_OK) return rc;
-            }
+    if (!m->exec_p) {
+        // a model of one sequence (no prompt-step graph): a decode step per position
+        for (int q = 0; q + 1 < lens[0]; ++q) {
+            const int32_t tq = ids[q], pq = q;
+            m->cached[0] = q;
+            const int rc = gpt2_decode_batch(m, &tq, &pq, 1, nullptr);
+            if (rc != GPT2_OK) return rc;
         }
-    int rc = flush();
-    if (rc != GPT2_OK) return rc;
+    } else {
+        for (int b = 0; b < n; ++b)
+            for (int q = 0; q + 1 < lens[b]; ++q) {
+                t[r] = ids[start[b] + q];
+                p[r] = q;
+                sl[r] = b;
+                if (++r == rows) {
+                    const int rc = flush();
+                    if (rc != GPT2_OK) return rc;
+                }
+            }
+        const int rc = flush();
+        if (rc != GPT2_OK) return rc;
+    }
     // each sequence's last prompt token: one decode step, which leaves the
     // choice after the prompt and its logits by sequence
     std::vector<int32_t> tl(n), pl(n);
