@@ -197,6 +197,7 @@ struct BAttnArgs {
     __nv_bfloat16 *out;             // [128][E] hi/lo B operand of the output projection
     DeviceState *st;
     const int32_t *slot_of;         // [rows] cache slot of each row, or null: slot = row (or 0, one slot)
+    const int32_t *order;           // [rows] rows by decreasing position: CTA x takes row order[x]
 };
 
 __device__ __forceinline__ int row_slot(const BAttnArgs &a, int b)
@@ -260,7 +261,7 @@ __global__ void __launch_bounds__(kBT) k_b_attn(const BAttnArgs a)
     __shared__ float red[kBT / 32];
     __shared__ __align__(16) float qkv[3 * D];
     __shared__ __align__(16) float part[RPP][D];
-    const int b = blockIdx.x, h = blockIdx.y, E = a.E;
+    const int b = a.order[blockIdx.x], h = blockIdx.y, E = a.E;
     const int tid = threadIdx.x, g = tid / LPR, l = tid % LPR;
     if (tid == 0) {
         for (int i = 0; i < kAttnStages; ++i) mbar_init(&full[i], 1);
@@ -571,6 +572,7 @@ struct gpt2_batch {
     cudaGraphExec_t exec_p = nullptr;
     int kernels_per_prompt_step = 0;
     int32_t *slot_of = nullptr;     // [kTcMaxRows] cache slot of each row in a prompt step
+    int32_t *order = nullptr;       // [kTcMaxRows] rows by decreasing position (the attention's CTA order)
     std::vector<int> cached;        // host view: cached length of each sequence
     bool has_step = false;
     unsigned long long launches = 0;
@@ -692,6 +694,7 @@ int record_step(gpt2_batch *m, cudaStream_t s, bool packed = false)
         const bool pre = slots == 1 || packed;   // rows of prompts: every row's k, v first (k_b_append)
         at.append = pre ? 0 : 1;
         at.slot_of = packed ? m->slot_of : nullptr;
+        at.order = m->order;
         at.scale = float(1.0 / std::sqrt(double(D)));
         at.out = m->b_a;
         at.st = m->st;
@@ -859,6 +862,17 @@ struct EngineSrc {
     std::function<cudaError_t(float *, cudaStream_t)> head_fn;
 };
 
+// The attention's CTA order for a step's positions pos[kTcMaxRows]: rows by
+// decreasing position (inactive rows, -1, last; ties by row), so that the
+// longest rows start first and every SM gets a mix of lengths.
+cudaError_t upload_order(gpt2_batch *m, const int32_t *pos, cudaStream_t s)
+{
+    int32_t ord[kTcMaxRows];
+    for (int r = 0; r < kTcMaxRows; ++r) ord[r] = r;
+    std::stable_sort(ord, ord + kTcMaxRows, [&](int x, int y) { return pos[x] > pos[y]; });
+    return cudaMemcpyAsync(m->order, ord, sizeof ord, cudaMemcpyHostToDevice, s);
+}
+
 int engine_build(gpt2_batch *m, const gpt2_config &cfg, const EngineSrc &src, cudaStream_t stream, int sms)
 {
     const int L = cfg.n_layer, E = cfg.n_embd, H = cfg.n_head, P = cfg.n_positions, V = cfg.vocab_size;
@@ -918,7 +932,7 @@ int engine_build(gpt2_batch *m, const gpt2_config &cfg, const EngineSrc &src, cu
     const size_t o_lg = take(size_t(src.rows) * V * 4);
     const size_t o_tok = take(size_t(kTcMaxRows) * 4), o_pos = take(size_t(kTcMaxRows) * 4);
     const size_t o_nt = take(size_t(kTcMaxRows) * 4), o_ids = take(size_t(P) * src.rows * 4);
-    const size_t o_slot = take(size_t(kTcMaxRows) * 4);
+    const size_t o_slot = take(size_t(kTcMaxRows) * 4), o_order = take(size_t(kTcMaxRows) * 4);
     const size_t o_st = take(sizeof(DeviceState));
     const size_t work_bytes = off;
     const size_t tmp_elems = size_t(F) * E > size_t(Vp) * E ? size_t(F) * E : size_t(Vp) * E;
@@ -1018,6 +1032,7 @@ int engine_build(gpt2_batch *m, const gpt2_config &cfg, const EngineSrc &src, cu
     m->next_tok = reinterpret_cast<int32_t *>(W + o_nt);
     m->out_ids = reinterpret_cast<int32_t *>(W + o_ids);
     m->slot_of = reinterpret_cast<int32_t *>(W + o_slot);
+    m->order = reinterpret_cast<int32_t *>(W + o_order);
     m->st = reinterpret_cast<DeviceState *>(W + o_st);
     if (tc_make_tmap(&m->map_e, m->b_e, 2 * kTcMaxRows, uint64_t(E)) ||
         tc_make_tmap(&m->map_a, m->b_a, 2 * kTcMaxRows, uint64_t(E)) ||
@@ -1028,6 +1043,7 @@ int engine_build(gpt2_batch *m, const gpt2_config &cfg, const EngineSrc &src, cu
     {
         std::vector<int32_t> neg(kTcMaxRows, -1);   // every row inactive until a call feeds it
         ECK(cudaMemcpyAsync(m->pos, neg.data(), neg.size() * 4, cudaMemcpyHostToDevice, s));
+        ECK(upload_order(m, neg.data(), s));
         ECK(cudaStreamSynchronize(s));
     }
     rc = build_step_graph(m);
@@ -1118,6 +1134,7 @@ int prefill_engine_run(gpt2_batch *e, const int32_t *ids, int n, DeviceState *st
         }
         BTRY(cudaMemcpyAsync(e->tok, t.data(), t.size() * 4, cudaMemcpyHostToDevice, s));
         BTRY(cudaMemcpyAsync(e->pos, p.data(), p.size() * 4, cudaMemcpyHostToDevice, s));
+        BTRY(upload_order(e, p.data(), s));
         BTRY(cudaGraphLaunch(e->exec, s));
         e->launches += e->kernels_per_step;
         if (launches) *launches += e->kernels_per_step;
@@ -1222,6 +1239,7 @@ int gpt2_decode_batch(gpt2_batch *m, const int32_t *tokens, const int32_t *posit
     }
     BTRY(cudaMemcpyAsync(m->tok, t.data(), t.size() * 4, cudaMemcpyHostToDevice, m->stream));
     BTRY(cudaMemcpyAsync(m->pos, p.data(), p.size() * 4, cudaMemcpyHostToDevice, m->stream));
+    BTRY(upload_order(m, p.data(), m->stream));
     BTRY(cudaGraphLaunch(m->exec, m->stream));
     m->launches += m->kernels_per_step;
     for (int b = 0; b < n; ++b)
@@ -1261,6 +1279,7 @@ int gpt2_prefill_batch(gpt2_batch *m, const int32_t *ids, const int32_t *lens, i
         BTRY(cudaMemcpyAsync(m->tok, t.data(), t.size() * 4, cudaMemcpyHostToDevice, m->stream));
         BTRY(cudaMemcpyAsync(m->pos, p.data(), p.size() * 4, cudaMemcpyHostToDevice, m->stream));
         BTRY(cudaMemcpyAsync(m->slot_of, sl.data(), sl.size() * 4, cudaMemcpyHostToDevice, m->stream));
+        BTRY(upload_order(m, p.data(), m->stream));
         BTRY(cudaGraphLaunch(m->exec_p, m->stream));
         m->launches += m->kernels_per_prompt_step;
         r = 0;
@@ -1312,6 +1331,7 @@ int gpt2_decode_batch_greedy(gpt2_batch *m, int32_t n_steps)
     for (int b = 0; b < m->max_batch; ++b)
         if (m->cached[b] > 0) p[b] = m->cached[b];
     BTRY(cudaMemcpyAsync(m->pos, p.data(), p.size() * 4, cudaMemcpyHostToDevice, m->stream));
+    BTRY(upload_order(m, p.data(), m->stream));
     BTRY(cudaMemcpyAsync(m->tok, m->next_tok, size_t(kTcMaxRows) * 4, cudaMemcpyDeviceToDevice, m->stream));
     for (int i = 0; i < n_steps; ++i) BTRY(cudaGraphLaunch(m->exec, m->stream));
     m->launches += (unsigned long long)n_steps * m->kernels_per_step;
