@@ -8,7 +8,8 @@
 // K runs over 64-input chunks (one 128-byte swizzle atom).  One CTA per
 // (128-row tile, K split):
 //   warp 0, one lane: TMA loads of the weight and activation tiles into a
-//       4-stage shared-memory ring (cp.async.bulk.tensor, 128-byte swizzle,
+//       3-stage shared-memory ring (97 KB, so two CTAs share an SM;
+//       cp.async.bulk.tensor, 128-byte swizzle,
 //       mbarrier completion; the weight tiles of the first stages are issued
 //       before the wait for the previous kernel, which writes the activations);
 //   warp 1, one lane: tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M = 128,
