@@ -124,6 +124,16 @@ __global__ void __launch_bounds__(kBT) k_b_ln(const BLnArgs a)
     __shared__ float red[2][kBT / 32];
     const int b = blockIdx.x, E = a.E, tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
+    // gamma, beta and the bias are weights (no kernel of the step writes
+    // them): loaded before the wait for the previous kernel
+    float gm[kLnPer], bt[kLnPer], bi[kLnPer];
+#pragma unroll
+    for (int j = 0; j < kLnPer; ++j) {
+        const int i = tid + j * kBT;
+        gm[j] = i < E ? a.gamma[i] : 0.f;
+        bt[j] = i < E ? a.beta[i] : 0.f;
+        bi[j] = i < E && a.mode != 0 ? a.bias[i] : 0.f;
+    }
     pdl_wait();
     pdl_launch_dependents();   // the next kernel's CTAs may start and park on their wait
     float v[kLnPer];
@@ -148,7 +158,7 @@ __global__ void __launch_bounds__(kBT) k_b_ln(const BLnArgs a)
 #pragma unroll
         for (int j = 0; j < kLnPer; ++j) {
             const int i = tid + j * kBT;
-            v[j] = i < E ? xr[i] + (sum_shares(a.parts, a.splits, a.rows, E, b, i) + a.bias[i]) : 0.f;
+            v[j] = i < E ? xr[i] + (sum_shares(a.parts, a.splits, a.rows, E, b, i) + bi[j]) : 0.f;
         }
     }
     float s = 0.f, q = 0.f;
@@ -180,7 +190,7 @@ __global__ void __launch_bounds__(kBT) k_b_ln(const BLnArgs a)
         const int i = tid + j * kBT;
         if (i < E) {
             xr[i] = v[j];
-            put_hi_lo(a.out, b, E, i, (v[j] - mean) * rstd * a.gamma[i] + a.beta[i]);
+            put_hi_lo(a.out, b, E, i, (v[j] - mean) * rstd * gm[j] + bt[j]);
         }
     }
 }
@@ -267,20 +277,26 @@ __global__ void __launch_bounds__(kBT) k_b_attn(const BAttnArgs a)
         for (int i = 0; i < kAttnStages; ++i) mbar_init(&full[i], 1);
         mbar_init_fence();
     }
-    __syncthreads();
-    pdl_wait();
-    pdl_launch_dependents();   // the next kernel's CTAs may start and park on their wait
-    const int pos = a.pos[b];
-    if (pos < 0 || pos >= a.P) {             // inactive row: zero output
-        for (int d = tid; d < D; d += kBT) put_hi_lo(a.out, b, E, h * D + d, 0.f);
-        return;
+    // this thread's q, k, v bias elements (weights: loaded before the wait)
+    constexpr int kQ = (3 * D + kBT - 1) / kBT;
+    const int nq = a.append ? 3 * D : D;
+    float bq[kQ];
+#pragma unroll
+    for (int u = 0; u < kQ; ++u) {
+        const int t = tid + u * kBT;
+        bq[u] = t < nq ? a.bias[(t / D) * E + h * D + t % D] : 0.f;
     }
-    const int slot = row_slot(a, b);
+    // the row's position is fixed for the whole step (uploaded by the host,
+    // or advanced by the last kernel of the previous step, which has finished
+    // before the kernel ahead of this one started)
+    const int pos = a.pos[b];
+    const bool active = pos >= 0 && pos < a.P;
+    const int slot = active ? row_slot(a, b) : 0;
     KT *kh = static_cast<KT *>(a.kc) + (size_t(slot) * a.H + h) * a.P * D;
     KT *vh = static_cast<KT *>(a.vc) + (size_t(slot) * a.H + h) * a.P * D;
     const int n = pos + 1;
-    const int nk = a.append ? pos : n;                    // rows read from the cache
-    const int m = (nk + kAttnRows - 1) / kAttnRows;        // stages of K, then as many of V
+    const int nk = a.append ? pos : n;                                   // rows read from the cache
+    const int m = active ? (nk + kAttnRows - 1) / kAttnRows : 0;         // stages of K, then as many of V
     // chunk q of the stream (K chunks 0..m-1, then V chunks) into stage q % kAttnStages
     auto issue = [&](int q) {
         const bool isv = q >= m;
@@ -291,7 +307,20 @@ __global__ void __launch_bounds__(kBT) k_b_attn(const BAttnArgs a)
         bulk_g2s(dyn + size_t(q % kAttnStages) * kStageB, (isv ? vh : kh) + size_t(r0) * D, uint32_t(rows) * kRowB,
                  bar);
     };
-    if (tid == 0)
+    // decode steps (append): rows 0..pos-1 were written by earlier steps, so
+    // the first copies go out before the wait and stream while the QKV linear
+    // runs; a prompt step's rows come from the append kernel just before this
+    // one, so its copies wait for it
+    if (a.append && tid == 0)
+        for (int q = 0; q < min(kAttnStages, 2 * m); ++q) issue(q);
+    __syncthreads();
+    pdl_wait();
+    pdl_launch_dependents();   // the next kernel's CTAs may start and park on their wait
+    if (!active) {             // inactive row: zero output
+        for (int d = tid; d < D; d += kBT) put_hi_lo(a.out, b, E, h * D + d, 0.f);
+        return;
+    }
+    if (!a.append && tid == 0)
         for (int q = 0; q < min(kAttnStages, 2 * m); ++q) issue(q);
     bool good = true;   // (the copies always land; a wait that runs out is recorded)
     auto wait_chunk = [&](int q) {
@@ -301,10 +330,13 @@ __global__ void __launch_bounds__(kBT) k_b_attn(const BAttnArgs a)
         }
     };
     // q, k, v from the QKV shares; k and v appended to the cache
-    for (int t = tid; t < (a.append ? 3 * D : D); t += kBT) {
+#pragma unroll
+    for (int u = 0; u < kQ; ++u) {
+        const int t = tid + u * kBT;
+        if (t >= nq) break;
         const int part_ = t / D, d = t % D;
         const int j = part_ * E + h * D + d;
-        const float v = sum_shares(a.parts, a.splits, a.rows, 3 * E, b, j) + a.bias[j];
+        const float v = sum_shares(a.parts, a.splits, a.rows, 3 * E, b, j) + bq[u];
         qkv[t] = part_ == 0 ? v : kv_round(v, kh);
         if (part_ == 1) kv_put(kh + size_t(pos) * D + d, v);
         if (part_ == 2) kv_put(vh + size_t(pos) * D + d, v);
@@ -392,9 +424,10 @@ struct BGeluArgs {
 __global__ void __launch_bounds__(kBT) k_b_gelu(const BGeluArgs a)
 {
     const int b = blockIdx.x, f = blockIdx.y * kBT + threadIdx.x;
+    const float bf = f < a.F ? a.bias[f] : 0.f;   // a weight: loaded before the wait
     pdl_wait();
     pdl_launch_dependents();   // the next kernel's CTAs may start and park on their wait
-    if (f < a.F) put_hi_lo(a.out, b, a.F, f, gelu_new(sum_shares(a.parts, a.splits, a.rows, a.F, b, f) + a.bias[f]));
+    if (f < a.F) put_hi_lo(a.out, b, a.F, f, gelu_new(sum_shares(a.parts, a.splits, a.rows, a.F, b, f) + bf));
 }
 
 // k and v of every row (QKV shares + bias) into the cache at the row's
