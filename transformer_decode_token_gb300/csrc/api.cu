@@ -84,8 +84,9 @@ namespace {
 constexpr size_t kAlign = 256;
 // Prompts of at least this many tokens run on the tensor cores (the
 // prefill engine), shorter ones as single-token passes of the cluster kernel
-// (measured on GB300, GPT-2 small fp32: one engine step takes ~0.62 ms for up
-// to 64 positions, a pass ~0.148 ms, so the engine wins from 5 tokens).
+// (measured on GB300, GPT-2 small fp32: one engine step takes 0.51-0.55 ms
+// for up to 64 positions, a pass ~0.145 ms: the engine wins clearly from 5
+// tokens; at 4 the two are within 0.07 ms).
 constexpr int kTcPrefillMin = 5;
 // Per-kernel graph path: shared-memory stage budget and stages in flight of
 // each GEMV launch (measured on GB300: 96 KB in up to 4 stages).
