@@ -464,28 +464,28 @@ __global__ void __launch_bounds__(1024) k_b_argmax(const BArgmaxArgs a)
     const int b = blockIdx.x;
     pdl_wait();
     pdl_launch_dependents();   // the next kernel's CTAs may start and park on their wait
-    // four loads in flight per thread (the maximum of the keys does not
-    // depend on the order they are taken in)
+    // kArgLoads loads in flight per thread, so a row of 50,257 logits takes
+    // two rounds (the maximum of the keys does not depend on the order they
+    // are taken in)
+    constexpr int kArgLoads = 25;
     const float *row = a.logits + size_t(b) * a.V;
-    unsigned long long bk[4] = {0ull, 0ull, 0ull, 0ull};
-    int i = threadIdx.x;
-    for (; i + 3 * 1024 < a.V; i += 4 * 1024) {
-        float v[4];
+    unsigned long long best = 0ull;
+    for (int i0 = threadIdx.x; i0 < a.V; i0 += kArgLoads * 1024) {
+        float v[kArgLoads];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = row[i + u * 1024];
+        for (int u = 0; u < kArgLoads; ++u) {
+            const int i = i0 + u * 1024;
+            v[u] = i < a.V ? row[i] : 0.f;
+        }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const unsigned long long k = argmax_key(v[u], uint32_t(i + u * 1024));
-            bk[u] = k > bk[u] ? k : bk[u];
+        for (int u = 0; u < kArgLoads; ++u) {
+            const int i = i0 + u * 1024;
+            if (i < a.V) {
+                const unsigned long long k = argmax_key(v[u], uint32_t(i));
+                best = k > best ? k : best;
+            }
         }
     }
-    for (; i < a.V; i += 1024) {
-        const unsigned long long k = argmax_key(row[i], uint32_t(i));
-        bk[0] = k > bk[0] ? k : bk[0];
-    }
-    unsigned long long best = bk[0] > bk[1] ? bk[0] : bk[1];
-    best = bk[2] > best ? bk[2] : best;
-    best = bk[3] > best ? bk[3] : best;
     best = warp_max_u64(best);
     if ((threadIdx.x & 31) == 0) keys[threadIdx.x >> 5] = best;
     __syncthreads();
